@@ -1,0 +1,160 @@
+/*
+ * moe_gb300.h -- C ABI of a single-GPU (GB300, sm_103a) library that runs the forward pass of
+ * a mixture-of-experts (MoE) layer whose expert weights are stored quantized.
+ *
+ * The pass: top-k routing with a renormalised softmax, permutation of (token, slot) rows by
+ * expert, a grouped gate/up GEMM over packed weights, SiLU(gate) * up, a grouped down GEMM,
+ * and the routing-weighted combine back to token order.
+ *
+ * Weight formats (model-card pages, cited by page title and section):
+ *   MOE_FMT_FP8_B128_W8A16  clef-omni-fp8, "What was quantized" / "Recipe": E4M3 weights, one
+ *                           fp32 scale per 128x128 tile (scale = 448/amax, stored inverted as
+ *                           weight_scale_inv); bf16 activations.
+ *   MOE_FMT_INT4_G128_W4A16 clef-omni-int4, "What was quantized": symmetric INT4, group 128
+ *                           along K, auto_gptq packing; bf16 activations.
+ *   MOE_FMT_NVFP4_W4A16     clef-omni-NVFP4, "How it was made": E2M1 codes two per byte, one
+ *                           E4M3 scale per 16 weights, one fp32 global scale 448*6/amax per
+ *                           expert matrix; bf16 activations.
+ *   MOE_FMT_NVFP4_W4A4      the same weights with activations quantized to NVFP4 at run time
+ *                           (clef-flash-NVFP4-Hybrid, layer table: 16-element groups, FP8 group
+ *                           scales, one fp32 global scale), here one global scale per row.
+ *
+ * Conventions for every call:
+ *   - Pointers marked (dev) are device pointers; (host) are host pointers.  All memory is owned
+ *     by the caller: the library never allocates, frees or synchronises inside the forward
+ *     pass, and enqueues work only on the stream it is given.
+ *   - Argument errors are reported synchronously by the return value and nothing is enqueued.
+ *     MOE_ERR_CUDA means a CUDA launch or copy failed; cudaGetLastError() has the reason.
+ *   - Device-side failures (a bounded wait that ran out, an index out of range) set an error
+ *     word inside the workspace; moe_get_device_error() reads it.
+ *   - Shapes: H and I are multiples of 128; 1 <= top_k <= min(E, 8); E <= 256; T >= 0.
+ *   - bf16 tensors are passed as void* holding IEEE bfloat16 values.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t; NULL = the legacy default stream */
+
+typedef enum {
+  MOE_FMT_FP8_B128_W8A16 = 1,
+  MOE_FMT_INT4_G128_W4A16 = 2,
+  MOE_FMT_NVFP4_W4A16 = 3,
+  MOE_FMT_NVFP4_W4A4 = 4
+} moe_format_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer, bad shape, bad format, k out of range */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run (e.g. no sm_103a device) */
+  MOE_ERR_WORKSPACE = 3,    /* workspace smaller than moe_workspace_size() asked for */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime call failed */
+  MOE_ERR_DEVICE_TIMEOUT = 5, /* a bounded device wait gave up (reported by moe_get_device_error) */
+  MOE_ERR_DEVICE_FAULT = 6  /* a device-side bounds check fired (reported by moe_get_device_error) */
+} moe_status_t;
+
+/* Canonical tensors inside a packed-expert buffer (index into moe_packed_desc_t arrays).
+ * Per format, for all E experts back to back ("gu" = fused gate/up [2I, H] with gate rows
+ * 0..I-1 then up rows I..2I-1, "d" = down [H, I]; torch Linear orientation [out, in]):
+ *   FP8:   GU_A = codes u8 [E, 2I, H]      GU_B = scale_inv f32 [E, 2I/128, H/128]
+ *          D_A  = codes u8 [E, H, I]       D_B  = scale_inv f32 [E, H/128, I/128]
+ *   INT4:  GU_A = qweight i32 [E, H/8, 2I] GU_B = scales f16 [E, H/128, 2I]
+ *          D_A  = qweight i32 [E, I/8, H]  D_B  = scales f16 [E, I/128, H]
+ *          (nibble j of qweight word (kr, n) holds k = 8*kr + j; code = q + 8)
+ *   NVFP4: GU_A = weight_packed u8 [E, 2I, H/2] (element 2i in the low nibble)
+ *          GU_B = weight_scale E4M3 [E, 2I, H/16]
+ *          D_A  = weight_packed u8 [E, H, I/2]  D_B = weight_scale E4M3 [E, H, I/16]
+ *          GU_GS / D_GS = weight_global_scale f32 [E] (the quantize multiplier 2688/amax)
+ * Every tensor starts on a 256-byte boundary of the packed buffer. */
+enum {
+  MOE_T_GU_A = 0,
+  MOE_T_GU_B = 1,
+  MOE_T_D_A = 2,
+  MOE_T_D_B = 3,
+  MOE_T_GU_GS = 4,
+  MOE_T_D_GS = 5,
+  MOE_T_COUNT = 8
+};
+
+typedef struct {
+  int32_t fmt;                   /* moe_format_t */
+  int32_t E, H, I;               /* experts, hidden size, expert intermediate size */
+  uint64_t bytes;                /* total size of the packed buffer */
+  uint64_t offset[MOE_T_COUNT];  /* byte offset of each canonical tensor (0 if absent) */
+  uint64_t size[MOE_T_COUNT];    /* byte size of each canonical tensor (0 if absent) */
+} moe_packed_desc_t;
+
+/* Fill *desc with the packed layout for (fmt, E, H, I).  Host only; no CUDA calls. */
+moe_status_t moe_packed_size(int fmt, int E, int H, int I, moe_packed_desc_t* desc);
+
+/* Quantize and pack bf16 expert weights on the GPU (stream-ordered, asynchronous).
+ *   w_gate_up (dev) bf16 [E, 2I, H]; w_down (dev) bf16 [E, H, I]; packed (dev) desc->bytes.
+ * Results are bit-identical to the quantizers defined above (per-tile / per-group / per-block
+ * amax scaling, round-to-nearest-even).  Pages: see the format list at the top. */
+moe_status_t moe_pack_experts(const moe_packed_desc_t* desc, const void* w_gate_up, const void* w_down,
+                              void* packed, moe_stream_t stream);
+
+/* Bytes of device workspace moe_layer_forward needs for T tokens and top_k (host only).
+ * The same size also serves moe_debug_route and moe_get_device_error. */
+moe_status_t moe_workspace_size(const moe_packed_desc_t* desc, int T, int top_k, size_t* bytes);
+
+/* The forward pass on `stream` (asynchronous; no host synchronisation, no allocation):
+ *   x (dev) bf16 [T, H]; router_logits (dev) f32 [T, E]; packed (dev) from moe_pack_experts;
+ *   out (dev) bf16 [T, H], must not alias x; workspace (dev) >= moe_workspace_size bytes,
+ *   256-byte aligned, contents need not be initialised and are overwritten.
+ * out[t] = sum_j w_tj * Wd_e (silu(Wg_e a_t) * (Wu_e a_t)), e = j-th routed expert of t,
+ * w = softmax over the top-k logits, a_t = x_t (W*A16) or its NVFP4 quantization (W4A4). */
+moe_status_t moe_layer_forward(const void* x, const float* router_logits, int T, const moe_packed_desc_t* desc,
+                               const void* packed, int top_k, void* out, void* workspace, size_t ws_bytes,
+                               moe_stream_t stream);
+
+/* Bytes of workspace moe_layer_forward_host needs: moe_workspace_size plus device staging for
+ * x, the logits and out (host only). */
+moe_status_t moe_workspace_size_host_io(const moe_packed_desc_t* desc, int T, int top_k, size_t* bytes);
+
+/* moe_layer_forward with HOST activations: copies x_host bf16 [T, H] and logits_host f32 [T, E]
+ * into the workspace, runs the layer, copies the result to out_host bf16 [T, H], all on
+ * `stream` and asynchronously (use pinned host memory for overlap; the caller synchronises
+ * before reading out_host).  packed stays on the device. */
+moe_status_t moe_layer_forward_host(const void* x_host, const float* logits_host, int T,
+                                    const moe_packed_desc_t* desc, const void* packed, int top_k,
+                                    void* out_host, void* workspace, size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the device error word kept in `workspace`.
+ * *code receives MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_FAULT. */
+moe_status_t moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* code);
+
+/* A static English description of a status code. */
+const char* moe_status_string(int status);
+
+/* ---- inspection views of individual steps (same kernels as the forward pass) ---------- */
+
+/* Routing and permutation alone: topk_idx i32 [T, k] (descending logits, ties to the lower
+ * expert), topk_w f32 [T, k] (renormalised softmax), offsets i32 [E+1], perm i32 [T*k]
+ * (row r holds t*k + j, rows sorted by expert, token, slot), inv i32 [T*k] (row of t*k + j).
+ * All (dev).  workspace as for moe_layer_forward. */
+moe_status_t moe_debug_route(const float* router_logits, int T, int E, int top_k, int32_t* topk_idx,
+                             float* topk_w, int32_t* offsets, int32_t* perm, int32_t* inv, void* workspace,
+                             size_t ws_bytes, moe_stream_t stream);
+
+/* Dequantize one packed matrix to f32 (dev) [N, K]: which = 0 fused gate/up, 1 down.
+ * Values are bit-identical to the format's dequantization rule:
+ *   FP8 code * scale_inv; INT4 (code - 8) * scale; NVFP4 (e2m1 * e4m3) / global_scale. */
+moe_status_t moe_debug_dequant(const moe_packed_desc_t* desc, const void* packed, int expert, int which,
+                               float* out, moe_stream_t stream);
+
+/* Dynamic NVFP4 quantization of bf16 rows x (dev) [T, H]: codes u8 [T, H/2], scales E4M3
+ * [T, H/16], gs f32 [T] = 2688 / max(amax(row), 1e-12).  Bit-identical to the W4A4 rule. */
+moe_status_t moe_debug_quant_act(const void* x, int T, int H, uint8_t* codes, uint8_t* scales, float* gs,
+                                 moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,267 @@
+// Host side of the C ABI declared in include/moe_gb300.h: argument checks, the packed and
+// workspace layouts, and the launch sequence of the forward pass.
+#include <string.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
+  WsLayout L;
+  memset(&L, 0, sizeof(L));
+  size_t cur = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = cur;
+    cur += align256(bytes);
+    return o;
+  };
+  const size_t R = (size_t)T * k;
+  L.nb = T > 0 ? (T + kRouteTB - 1) / kRouteTB : 1;
+  L.max_tiles = (int)(R / kMinRowBlock + (R < (size_t)E ? R : (size_t)E) + 1);
+  L.err = take(256);
+  L.topk_idx = take(4 * R);
+  L.topk_w = take(4 * R);
+  L.blkcnt = take(4 * (size_t)L.nb * E);
+  L.blkbase = take(4 * (size_t)L.nb * E);
+  L.offsets = take(4 * (size_t)(E + 1));
+  L.perm = take(4 * R);
+  L.inv = take(4 * R);
+  L.tiles = take(sizeof(TileEntry) * (size_t)(L.max_tiles + 1));
+  L.h = take(2 * R * I);
+  L.out_acc = take(4 * (size_t)T * H);
+  if (fmt == MOE_FMT_NVFP4_W4A4) {
+    L.xq = take((size_t)T * H / 2);
+    L.xs = take((size_t)T * H / 16);
+    L.xg = take(4 * (size_t)T);
+    L.hq = take(R * I / 2);
+    L.hs = take(R * I / 16);
+    L.hg = take(4 * R);
+  }
+  if (host_io) {
+    L.x_stage = take(2 * (size_t)T * H);
+    L.lg_stage = take(4 * (size_t)T * E);
+    L.out_stage = take(2 * (size_t)T * H);
+  }
+  L.total = cur;
+  return L;
+}
+
+static bool fmt_ok(int f) { return f >= MOE_FMT_FP8_B128_W8A16 && f <= MOE_FMT_NVFP4_W4A4; }
+
+static bool desc_ok(const moe_packed_desc_t* d) {
+  return d && fmt_ok(d->fmt) && d->E >= 1 && d->E <= kMaxE && d->H >= 128 && d->I >= 128 && d->H % 128 == 0 &&
+         d->I % 128 == 0;
+}
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// The kernels are built for sm_103a only; refuse other devices before launching anything.
+static moe_status_t device_ok() {
+  static int checked[64];  // 0 unknown, 1 ok, 2 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev >= 0 && dev < 64 && checked[dev]) return checked[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const bool ok = major == 10 && minor == 3;
+  if (dev >= 0 && dev < 64) checked[dev] = ok ? 1 : 2;
+  return ok ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+static moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+static moe_status_t forward_checked(const void* x, const float* logits, int T, const moe_packed_desc_t* d,
+                                    const void* packed, int k, void* out, void* ws, size_t ws_bytes,
+                                    cudaStream_t s, bool host_io_layout) {
+  if (!desc_ok(d) || T < 0 || k < 1 || k > kMaxTopK || k > d->E) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !logits || !packed || !out || !ws)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256) || !aligned(x, 16) || !aligned(out, 16) || !aligned(packed, 256))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && x == out) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(d->fmt, d->E, d->H, d->I, T, k, host_io_layout);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  const moe_status_t dv = device_ok();
+  if (dv != MOE_OK) return dv;
+  char* w = (char*)ws;
+  const int rb = simt_row_block();
+  if (launch_route(logits, T, d->E, k, rb, L, w, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_experts(*d, (const char*)packed, (const __nv_bfloat16*)x, T, k, rb, L, w,
+                                    (__nv_bfloat16*)out, s));
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status_t moe_packed_size(int fmt, int E, int H, int I, moe_packed_desc_t* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  memset(d, 0, sizeof(*d));
+  d->fmt = fmt;
+  d->E = E;
+  d->H = H;
+  d->I = I;
+  if (!desc_ok(d)) return MOE_ERR_INVALID_ARG;
+  const size_t e = (size_t)E, gu = (size_t)2 * I * H, dn = (size_t)H * I;
+  size_t sz[MOE_T_COUNT] = {0};
+  switch (fmt) {
+    case MOE_FMT_FP8_B128_W8A16:
+      sz[MOE_T_GU_A] = e * gu;
+      sz[MOE_T_GU_B] = e * gu / (128 * 128) * 4;
+      sz[MOE_T_D_A] = e * dn;
+      sz[MOE_T_D_B] = e * dn / (128 * 128) * 4;
+      break;
+    case MOE_FMT_INT4_G128_W4A16:
+      sz[MOE_T_GU_A] = e * gu / 2;
+      sz[MOE_T_GU_B] = e * gu / 128 * 2;
+      sz[MOE_T_D_A] = e * dn / 2;
+      sz[MOE_T_D_B] = e * dn / 128 * 2;
+      break;
+    default:
+      sz[MOE_T_GU_A] = e * gu / 2;
+      sz[MOE_T_GU_B] = e * gu / 16;
+      sz[MOE_T_D_A] = e * dn / 2;
+      sz[MOE_T_D_B] = e * dn / 16;
+      sz[MOE_T_GU_GS] = e * 4;
+      sz[MOE_T_D_GS] = e * 4;
+      break;
+  }
+  size_t cur = 0;
+  for (int i = 0; i < MOE_T_COUNT; ++i) {
+    if (!sz[i]) continue;
+    d->offset[i] = cur;
+    d->size[i] = sz[i];
+    cur += align256(sz[i]);
+  }
+  d->bytes = cur;
+  return MOE_OK;
+}
+
+moe_status_t moe_pack_experts(const moe_packed_desc_t* d, const void* w_gate_up, const void* w_down, void* packed,
+                              moe_stream_t stream) {
+  if (!desc_ok(d) || !w_gate_up || !w_down || !packed || !aligned(packed, 256)) return MOE_ERR_INVALID_ARG;
+  moe_packed_desc_t ref;
+  if (moe_packed_size(d->fmt, d->E, d->H, d->I, &ref) != MOE_OK || ref.bytes != d->bytes) return MOE_ERR_INVALID_ARG;
+  const moe_status_t dv = device_ok();
+  if (dv != MOE_OK) return dv;
+  return cuda_status(launch_pack(*d, (const __nv_bfloat16*)w_gate_up, (const __nv_bfloat16*)w_down, (char*)packed,
+                                 (cudaStream_t)stream));
+}
+
+moe_status_t moe_workspace_size(const moe_packed_desc_t* d, int T, int top_k, size_t* bytes) {
+  if (!desc_ok(d) || !bytes || T < 0 || top_k < 1 || top_k > kMaxTopK || top_k > d->E) return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(d->fmt, d->E, d->H, d->I, T, top_k, false).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_size_host_io(const moe_packed_desc_t* d, int T, int top_k, size_t* bytes) {
+  if (!desc_ok(d) || !bytes || T < 0 || top_k < 1 || top_k > kMaxTopK || top_k > d->E) return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(d->fmt, d->E, d->H, d->I, T, top_k, true).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_forward(const void* x, const float* router_logits, int T, const moe_packed_desc_t* d,
+                               const void* packed, int top_k, void* out, void* workspace, size_t ws_bytes,
+                               moe_stream_t stream) {
+  return forward_checked(x, router_logits, T, d, packed, top_k, out, workspace, ws_bytes, (cudaStream_t)stream,
+                         false);
+}
+
+moe_status_t moe_layer_forward_host(const void* x_host, const float* logits_host, int T, const moe_packed_desc_t* d,
+                                    const void* packed, int top_k, void* out_host, void* workspace, size_t ws_bytes,
+                                    moe_stream_t stream) {
+  if (!desc_ok(d) || T < 0 || top_k < 1 || top_k > kMaxTopK || top_k > d->E) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x_host || !logits_host || !out_host || !workspace)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(d->fmt, d->E, d->H, d->I, T, top_k, true);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = (char*)workspace;
+  if (T > 0) {
+    if (cudaMemcpyAsync(w + L.x_stage, x_host, 2 * (size_t)T * d->H, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(w + L.lg_stage, logits_host, 4 * (size_t)T * d->E, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  const moe_status_t st = forward_checked(w + L.x_stage, (const float*)(w + L.lg_stage), T, d, packed, top_k,
+                                          w + L.out_stage, workspace, ws_bytes, s, true);
+  if (st != MOE_OK) return st;
+  if (T > 0 && cudaMemcpyAsync(out_host, w + L.out_stage, 2 * (size_t)T * d->H, cudaMemcpyDeviceToHost, s) !=
+                   cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* code) {
+  if (!workspace || !code) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+  *code = v;
+  return MOE_OK;
+}
+
+const char* moe_status_string(int st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported device or request";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_FAULT: return "device-side bounds check failed";
+    default: return "unknown status";
+  }
+}
+
+moe_status_t moe_debug_route(const float* logits, int T, int E, int top_k, int32_t* topk_idx, float* topk_w,
+                             int32_t* offsets, int32_t* perm, int32_t* inv, void* workspace, size_t ws_bytes,
+                             moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > kMaxE || top_k < 1 || top_k > kMaxTopK || top_k > E || !workspace || !offsets)
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !topk_idx || !topk_w || !perm || !inv)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(MOE_FMT_FP8_B128_W8A16, E, 128, 128, T, top_k, false);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  const moe_status_t dv = device_ok();
+  if (dv != MOE_OK) return dv;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = (char*)workspace;
+  if (launch_route(logits, T, E, top_k, simt_row_block(), L, w, s) != cudaSuccess) return MOE_ERR_CUDA;
+  const size_t R = (size_t)T * top_k;
+  cudaError_t e = cudaMemcpyAsync(offsets, w + L.offsets, 4 * (size_t)(E + 1), cudaMemcpyDeviceToDevice, s);
+  if (R) {
+    if (e == cudaSuccess) e = cudaMemcpyAsync(topk_idx, w + L.topk_idx, 4 * R, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(topk_w, w + L.topk_w, 4 * R, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(perm, w + L.perm, 4 * R, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(inv, w + L.inv, 4 * R, cudaMemcpyDeviceToDevice, s);
+  }
+  return cuda_status(e);
+}
+
+moe_status_t moe_debug_dequant(const moe_packed_desc_t* d, const void* packed, int expert, int which, float* out,
+                               moe_stream_t stream) {
+  if (!desc_ok(d) || !packed || !out || expert < 0 || expert >= d->E || (which != 0 && which != 1))
+    return MOE_ERR_INVALID_ARG;
+  const moe_status_t dv = device_ok();
+  if (dv != MOE_OK) return dv;
+  return cuda_status(launch_dequant(*d, (const char*)packed, expert, which, out, (cudaStream_t)stream));
+}
+
+moe_status_t moe_debug_quant_act(const void* x, int T, int H, uint8_t* codes, uint8_t* scales, float* gs,
+                                 moe_stream_t stream) {
+  if (T < 0 || H < 16 || H % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !codes || !scales || !gs || !aligned(x, 16))) return MOE_ERR_INVALID_ARG;
+  const moe_status_t dv = device_ok();
+  if (dv != MOE_OK) return dv;
+  return cuda_status(launch_quant_rows((const __nv_bfloat16*)x, T, H, codes, scales, gs, (cudaStream_t)stream));
+}
+
+}  // extern "C"

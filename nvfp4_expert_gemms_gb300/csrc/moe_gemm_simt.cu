@@ -1,0 +1,200 @@
+// Grouped expert GEMMs on CUDA cores (fp32 FMA), one CTA per (row block of one expert,
+// column block).  Dequantization uses each format's rule on the fly; SiLU(gate)*up is fused
+// into the gate/up GEMM, and the routing-weighted combine into the down GEMM (fp32 atomics
+// into an fp32 accumulator, then one rounding to bf16).
+//
+// The pages dequantize the selected experts to bf16 and call a grouped matmul
+// (clef-omni-NVFP4, "How it was made"; clef-omni-fp8, "How this checkpoint runs"); here the
+// dequantization happens inside the GEMM and the bf16 copy of the weights never exists.
+#include "moe_formats.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kSimtRB = 8;   // rows (token slots) per CTA
+constexpr int kSimtNB = 16;  // output columns per CTA (4 per warp)
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// Activation row r of the tile into shared memory as fp32: bf16 x / h, or the NVFP4
+// dequantization (e2m1 * e4m3) / gs of the W4A4 codes.
+template <bool A4>
+__device__ __forceinline__ void stage_rows(float* xs, int K, int rows, const uint16_t* __restrict__ src,
+                                           const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf,
+                                           const float* __restrict__ gs, const int* src_row) {
+  for (int i = threadIdx.x; i < kSimtRB * K; i += blockDim.x) {
+    const int r = i / K, c = i % K;
+    float v = 0.f;
+    if (r < rows) {
+      const size_t sr = (size_t)src_row[r];
+      if constexpr (A4) {
+        const uint8_t byte = q[sr * (K / 2) + c / 2];
+        const float bs = e4m3_to_f32(sf[sr * (K / 16) + c / 16]);
+        v = __fdiv_rn(e2m1_to_f32((c & 1) ? (byte >> 4) : (byte & 0xF)) * bs, gs[sr]);
+      } else {
+        v = bf16_to_f32(src[sr * K + c]);
+      }
+    }
+    xs[i] = v;
+  }
+}
+
+template <int FMT, bool A4>
+__global__ void __launch_bounds__(128) gateup_simt_kernel(MatView gu, const uint16_t* __restrict__ x,
+                                                          const uint8_t* __restrict__ xq,
+                                                          const uint8_t* __restrict__ xsf,
+                                                          const float* __restrict__ xgs,
+                                                          const int32_t* __restrict__ perm, int k, int I,
+                                                          const TileEntry* __restrict__ tiles,
+                                                          uint16_t* __restrict__ h) {
+  extern __shared__ float xs[];
+  __shared__ int src_row[kSimtRB];
+  if ((int)blockIdx.x >= tiles[0].expert) return;
+  const TileEntry te = tiles[1 + blockIdx.x];
+  const int H = gu.K, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x < kSimtRB) src_row[threadIdx.x] = threadIdx.x < te.rows ? perm[te.row0 + threadIdx.x] / k : 0;
+  __syncthreads();
+  stage_rows<A4>(xs, H, te.rows, x, xq, xsf, xgs, src_row);
+  __syncthreads();
+  for (int i = 0; i < 4; ++i) {
+    const int n = blockIdx.y * kSimtNB + warp * 4 + i;
+    float ag[kSimtRB], au[kSimtRB];
+#pragma unroll
+    for (int r = 0; r < kSimtRB; ++r) ag[r] = au[r] = 0.f;
+    for (int k0 = lane * 8; k0 < H; k0 += 256) {
+      float wg[8], wu[8];
+      load_w8<FMT>(gu, te.expert, n, k0, wg);
+      load_w8<FMT>(gu, te.expert, I + n, k0, wu);
+#pragma unroll
+      for (int r = 0; r < kSimtRB; ++r) {
+        const float* xr = xs + r * H + k0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          ag[r] = fmaf(wg[j], xr[j], ag[r]);
+          au[r] = fmaf(wu[j], xr[j], au[r]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kSimtRB; ++r)
+      for (int off = 16; off > 0; off >>= 1) {
+        ag[r] += __shfl_xor_sync(0xffffffffu, ag[r], off);
+        au[r] += __shfl_xor_sync(0xffffffffu, au[r], off);
+      }
+    if (lane == 0)
+      for (int r = 0; r < te.rows; ++r) {
+        const float v = silu_f(ag[r]) * au[r];
+        h[(size_t)(te.row0 + r) * I + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      }
+  }
+}
+
+template <int FMT, bool A4>
+__global__ void __launch_bounds__(128) down_simt_kernel(MatView dn, const uint16_t* __restrict__ h,
+                                                        const uint8_t* __restrict__ hq,
+                                                        const uint8_t* __restrict__ hsf,
+                                                        const float* __restrict__ hgs,
+                                                        const int32_t* __restrict__ perm,
+                                                        const float* __restrict__ topk_w, int k,
+                                                        const TileEntry* __restrict__ tiles,
+                                                        float* __restrict__ out_acc) {
+  extern __shared__ float hs[];
+  __shared__ int src_row[kSimtRB];
+  if ((int)blockIdx.x >= tiles[0].expert) return;
+  const TileEntry te = tiles[1 + blockIdx.x];
+  const int I = dn.K, H = dn.N, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x < kSimtRB) src_row[threadIdx.x] = te.row0 + min((int)threadIdx.x, te.rows - 1);
+  __syncthreads();
+  stage_rows<A4>(hs, I, te.rows, h, hq, hsf, hgs, src_row);
+  __syncthreads();
+  for (int i = 0; i < 4; ++i) {
+    const int c = blockIdx.y * kSimtNB + warp * 4 + i;
+    float acc[kSimtRB];
+#pragma unroll
+    for (int r = 0; r < kSimtRB; ++r) acc[r] = 0.f;
+    for (int k0 = lane * 8; k0 < I; k0 += 256) {
+      float w[8];
+      load_w8<FMT>(dn, te.expert, c, k0, w);
+#pragma unroll
+      for (int r = 0; r < kSimtRB; ++r) {
+        const float* hr = hs + r * I + k0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[r] = fmaf(w[j], hr[j], acc[r]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kSimtRB; ++r)
+      for (int off = 16; off > 0; off >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
+    if (lane == 0)
+      for (int r = 0; r < te.rows; ++r) {
+        const int p = perm[te.row0 + r];
+        atomicAdd(&out_acc[(size_t)(p / k) * H + c], topk_w[p] * acc[r]);
+      }
+  }
+}
+
+__global__ void finalize_kernel(const float* __restrict__ acc, uint16_t* __restrict__ out, size_t n) {
+  const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i >= n) return;
+  if (i + 3 < n) {
+    const float4 v = *(const float4*)(acc + i);
+    uint2 o;
+    o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x)) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y)) << 16);
+    o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.z)) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.w)) << 16);
+    *(uint2*)(out + i) = o;
+  } else {
+    for (size_t j = i; j < n; ++j) out[j] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+  }
+}
+
+template <int FMT, bool A4>
+cudaError_t run_simt(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
+                     const WsLayout& L, char* ws, cudaStream_t s) {
+  const int H = d.H, I = d.I;
+  const MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
+  const TileEntry* tiles = (const TileEntry*)(ws + L.tiles);
+  const int32_t* perm = (const int32_t*)(ws + L.perm);
+  const size_t smem_gu = sizeof(float) * kSimtRB * H, smem_d = sizeof(float) * kSimtRB * I;
+  cudaFuncSetAttribute(gateup_simt_kernel<FMT, A4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_gu);
+  cudaFuncSetAttribute(down_simt_kernel<FMT, A4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_d);
+  gateup_simt_kernel<FMT, A4><<<dim3(L.max_tiles, I / kSimtNB), 128, smem_gu, s>>>(
+      gu, (const uint16_t*)x, (const uint8_t*)(ws + L.xq), (const uint8_t*)(ws + L.xs),
+      (const float*)(ws + L.xg), perm, k, I, tiles, (uint16_t*)(ws + L.h));
+  if (A4)
+    launch_quant_rows((const __nv_bfloat16*)(ws + L.h), T * k, I, (uint8_t*)(ws + L.hq), (uint8_t*)(ws + L.hs),
+                      (float*)(ws + L.hg), s);
+  down_simt_kernel<FMT, A4><<<dim3(L.max_tiles, H / kSimtNB), 128, smem_d, s>>>(
+      dn, (const uint16_t*)(ws + L.h), (const uint8_t*)(ws + L.hq), (const uint8_t*)(ws + L.hs),
+      (const float*)(ws + L.hg), perm, (const float*)(ws + L.topk_w), k, tiles, (float*)(ws + L.out_acc));
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
+                           int row_block, const WsLayout& L, char* ws, __nv_bfloat16* out, cudaStream_t s) {
+  (void)row_block;
+  const size_t n_out = (size_t)T * d.H;
+  if (T == 0) return cudaGetLastError();
+  cudaMemsetAsync(ws + L.out_acc, 0, sizeof(float) * n_out, s);
+  if (d.fmt == MOE_FMT_NVFP4_W4A4)
+    launch_quant_rows(x, T, d.H, (uint8_t*)(ws + L.xq), (uint8_t*)(ws + L.xs), (float*)(ws + L.xg), s);
+  cudaError_t e;
+  switch (d.fmt) {
+    case MOE_FMT_FP8_B128_W8A16: e = run_simt<MOE_FMT_FP8_B128_W8A16, false>(d, packed, x, T, k, L, ws, s); break;
+    case MOE_FMT_INT4_G128_W4A16: e = run_simt<MOE_FMT_INT4_G128_W4A16, false>(d, packed, x, T, k, L, ws, s); break;
+    case MOE_FMT_NVFP4_W4A16: e = run_simt<MOE_FMT_NVFP4_W4A16, false>(d, packed, x, T, k, L, ws, s); break;
+    default: e = run_simt<MOE_FMT_NVFP4_W4A16, true>(d, packed, x, T, k, L, ws, s); break;
+  }
+  if (e != cudaSuccess) return e;
+  const unsigned blocks = (unsigned)((n_out / 4 + 255) / 256 + 1);
+  finalize_kernel<<<blocks, 256, 0, s>>>((const float*)(ws + L.out_acc), (uint16_t*)out, n_out);
+  return cudaGetLastError();
+}
+
+int simt_row_block() { return kSimtRB; }
+
+}  // namespace moe

@@ -1,0 +1,90 @@
+// Internal declarations shared by the library's translation units (not installed).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_gb300.h"
+
+namespace moe {
+
+constexpr int kMaxE = 256;      // router width supported by the warp top-k (8 logits per lane)
+constexpr int kMaxTopK = 8;     // slots per token
+constexpr int kRouteTB = 128;   // tokens per routing block (histogram granularity)
+constexpr int kMinRowBlock = 8; // smallest GEMM row block; bounds the tile table
+
+// Device error word values (written with atomicCAS so the first failure is kept).
+enum : int { kDevOk = 0, kDevTimeout = MOE_ERR_DEVICE_TIMEOUT, kDevFault = MOE_ERR_DEVICE_FAULT };
+
+__device__ __forceinline__ void set_dev_error(int* err, int code) { atomicCAS(err, 0, code); }
+
+// ---- scalar codecs (device) --------------------------------------------------------------
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// E4M3 ("e4m3fn") code -> float; exact.
+__device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+  return __half2float(__half(h));
+}
+// float -> E4M3, round to nearest even, saturating at +-448 (hardware conversion).
+__device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
+  return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+// E2M1 magnitude table {0, .5, 1, 1.5, 2, 3, 4, 6}; bit 3 is the sign.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+  const float m[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+  float v = m[c & 7];
+  return (c & 8) ? -v : v;
+}
+// float -> E2M1: nearest grid point, a tie goes to the even code, saturating at 6; the sign
+// bit is kept even when the magnitude rounds to zero.
+__device__ __forceinline__ uint32_t f32_to_e2m1(float v) {
+  float a = fabsf(v);
+  uint32_t m;
+  if (a <= 0.25f) m = 0;
+  else if (a < 0.75f) m = 1;
+  else if (a <= 1.25f) m = 2;
+  else if (a < 1.75f) m = 3;
+  else if (a <= 2.5f) m = 4;
+  else if (a < 3.5f) m = 5;
+  else if (a <= 5.0f) m = 6;
+  else m = 7;
+  return m | (signbit(v) ? 8u : 0u);
+}
+
+// ---- routing tile table ------------------------------------------------------------------
+// One entry per GEMM row block: rows [row0, row0 + rows) of the permuted order, all routed
+// to `expert`.  Entry 0 of the table is a header whose .expert field holds the tile count.
+struct TileEntry {
+  int32_t expert, row0, rows, pad;
+};
+
+// ---- workspace layout ----------------------------------------------------------------------
+struct WsLayout {
+  size_t err, topk_idx, topk_w, blkcnt, blkbase, offsets, perm, inv, tiles;
+  size_t h, out_acc, xq, xs, xg, hq, hs, hg;
+  size_t x_stage, lg_stage, out_stage;
+  size_t total;
+  int nb;         // routing blocks
+  int max_tiles;  // capacity of the tile table (excluding the header)
+};
+
+WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io);
+
+// ---- launches (each returns cudaGetLastError() after enqueueing) -------------------------
+cudaError_t launch_route(const float* logits, int T, int E, int k, int row_block, const WsLayout& L,
+                         char* ws, cudaStream_t s);
+cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, const __nv_bfloat16* wd,
+                        char* packed, cudaStream_t s);
+cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e, int which, float* out,
+                           cudaStream_t s);
+cudaError_t launch_quant_rows(const __nv_bfloat16* x, int rows, int K, uint8_t* q, uint8_t* sf, float* gs,
+                              cudaStream_t s);
+cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,
+                           int k, int row_block, const WsLayout& L, char* ws, __nv_bfloat16* out,
+                           cudaStream_t s);
+int simt_row_block();
+
+}  // namespace moe

@@ -1,0 +1,222 @@
+// Quantize-and-pack kernels (off the hot path) and the dequantization view.
+// Every quantizer step is one IEEE fp32 operation with an explicit rounding intrinsic, so the
+// packed bytes are reproducible bit for bit:
+//   FP8   (clef-omni-fp8, "Recipe"): per 128x128 tile s = 448/amax, code = E4M3(w*s),
+//         scale_inv = 1/s.
+//   INT4  (clef-omni-int4, "What was quantized"): per (row, 128-group) s16 = fp16(amax/7),
+//         q = clamp(rint(w/s16), -8, 7), code = q + 8, auto_gptq word order along K.
+//   NVFP4 (clef-omni-NVFP4, "How it was made"): gs = 2688/amax(matrix); per 16-block
+//         bs = E4M3((amax_b/6)*gs), q = E2M1(w/(bs/gs)).
+// A zero amax is clamped to 1e-12 (FP8 tiles, NVFP4 matrices); an INT4 group with a zero
+// scale stores the zero code 8.
+#include "moe_formats.cuh"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = 0.f;
+  for (int i = 0; i < nw; ++i) r = fmaxf(r, red[i]);
+  return r;
+}
+
+// grid (K/128, N/128, E), 256 threads: thread t covers row t/2, columns (t%2)*64 .. +63.
+__global__ void __launch_bounds__(256) pack_fp8_kernel(const uint16_t* __restrict__ w, int N, int K,
+                                                       uint8_t* __restrict__ codes,
+                                                       float* __restrict__ scale_inv) {
+  __shared__ float red[8];
+  const int tk = blockIdx.x, tn = blockIdx.y, e = blockIdx.z;
+  const int r = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 64;
+  const size_t base = ((size_t)e * N + tn * 128 + r) * K + tk * 128 + c0;
+  float amax = 0.f;
+  for (int c = 0; c < 64; ++c) amax = fmaxf(amax, fabsf(bf16_to_f32(w[base + c])));
+  amax = block_max(amax, red);
+  if (amax < 1e-12f) amax = 1e-12f;
+  const float s = __fdiv_rn(448.0f, amax);
+  for (int c = 0; c < 64; c += 4) {
+    uint32_t word = 0;
+    for (int i = 0; i < 4; ++i) word |= (uint32_t)f32_to_e4m3(__fmul_rn(bf16_to_f32(w[base + c + i]), s)) << (8 * i);
+    *(uint32_t*)(codes + base + c) = word;
+  }
+  if (threadIdx.x == 0) scale_inv[((size_t)e * (N / 128) + tn) * (K / 128) + tk] = __fdiv_rn(1.0f, s);
+}
+
+// grid (N/128, K/128, E), 128 threads: thread = output row n of one 128-group.
+__global__ void __launch_bounds__(128) pack_int4_kernel(const uint16_t* __restrict__ w, int N, int K,
+                                                        uint32_t* __restrict__ qweight,
+                                                        __half* __restrict__ scales) {
+  const int n = blockIdx.x * 128 + threadIdx.x, g = blockIdx.y, e = blockIdx.z;
+  const uint16_t* row = w + ((size_t)e * N + n) * K + g * 128;
+  float amax = 0.f;
+  for (int c = 0; c < 128; ++c) amax = fmaxf(amax, fabsf(bf16_to_f32(row[c])));
+  const __half s16 = __float2half_rn(__fdiv_rn(amax, 7.0f));
+  const float sf = __half2float(s16);
+  scales[((size_t)e * (K / 128) + g) * N + n] = s16;
+  for (int kr = 0; kr < 16; ++kr) {
+    uint32_t word = 0;
+    for (int j = 0; j < 8; ++j) {
+      int code = 8;
+      if (sf != 0.0f) {
+        float q = rintf(__fdiv_rn(bf16_to_f32(row[kr * 8 + j]), sf));
+        q = fminf(fmaxf(q, -8.0f), 7.0f);
+        code = (int)q + 8;
+      }
+      word |= (uint32_t)code << (4 * j);
+    }
+    qweight[((size_t)e * (K / 8) + g * 16 + kr) * N + n] = word;
+  }
+}
+
+// Matrix amax into the global-scale slot (as float bits; non-negative floats order like uints).
+__global__ void __launch_bounds__(256) nvfp4_amax_kernel(const uint16_t* __restrict__ w, size_t per_expert,
+                                                         unsigned* __restrict__ slot) {
+  __shared__ float red[8];
+  const int e = blockIdx.y;
+  const uint16_t* m = w + (size_t)e * per_expert;
+  float amax = 0.f;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < per_expert; i += (size_t)gridDim.x * blockDim.x)
+    amax = fmaxf(amax, fabsf(bf16_to_f32(m[i])));
+  amax = block_max(amax, red);
+  if (threadIdx.x == 0) atomicMax(&slot[e], __float_as_uint(amax));
+}
+
+// One NVFP4 16-block of a row with global scale gs: 8 code bytes and 1 scale byte.
+__device__ __forceinline__ void nvfp4_block(const float v[16], float gs, uint2* codes8, uint8_t* scale) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const uint8_t bsc = f32_to_e4m3(__fmul_rn(__fdiv_rn(amax, 6.0f), gs));
+  const float bs = e4m3_to_f32(bsc);
+  uint32_t lo = 0, hi = 0;
+  if (bs != 0.0f) {
+    const float eff = __fdiv_rn(bs, gs);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) lo |= f32_to_e2m1(__fdiv_rn(v[i], eff)) << (4 * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hi |= f32_to_e2m1(__fdiv_rn(v[8 + i], eff)) << (4 * i);
+  }
+  *codes8 = make_uint2(lo, hi);
+  *scale = bsc;
+}
+
+// thread = one (row, 16-block) of one expert matrix.
+__global__ void __launch_bounds__(256) nvfp4_pack_kernel(const uint16_t* __restrict__ w, int N, int K,
+                                                         const unsigned* __restrict__ amax_slot,
+                                                         uint8_t* __restrict__ packed,
+                                                         uint8_t* __restrict__ scales) {
+  const int e = blockIdx.y;
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;  // block index within the expert
+  const size_t nblk = (size_t)N * K / 16;
+  if (i >= nblk) return;
+  float amax_m = __uint_as_float(amax_slot[e]);
+  if (amax_m < 1e-12f) amax_m = 1e-12f;
+  const float gs = __fdiv_rn(2688.0f, amax_m);
+  const uint16_t* src = w + (size_t)e * N * K + i * 16;
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = bf16_to_f32(src[j]);
+  nvfp4_block(v, gs, (uint2*)(packed + (size_t)e * N * K / 2 + i * 8), scales + (size_t)e * nblk + i);
+}
+
+__global__ void nvfp4_finish_kernel(unsigned* slot, int E) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e < E) {
+    float a = __uint_as_float(slot[e]);
+    if (a < 1e-12f) a = 1e-12f;
+    ((float*)slot)[e] = __fdiv_rn(2688.0f, a);
+  }
+}
+
+// Dynamic NVFP4 quantization of bf16 rows (W4A4 activations): one warp per row;
+// gs_row = 2688 / max(amax_row, 1e-12), then blocks exactly as for weights.
+__global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restrict__ x, int rows, int K,
+                                                         uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                                         float* __restrict__ gs_out) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const uint16_t* row = x + (size_t)r * K;
+  float amax = 0.f;
+  for (int c = lane * 8; c < K; c += 256) {
+    const uint4 u = *(const uint4*)(row + c);
+    const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(ww[i] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(ww[i] & 0xFFFF0000u)));
+    }
+  }
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if (amax < 1e-12f) amax = 1e-12f;
+  const float gs = __fdiv_rn(2688.0f, amax);
+  if (lane == 0) gs_out[r] = gs;
+  for (int b = lane; b < K / 16; b += 32) {
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = bf16_to_f32(row[b * 16 + j]);
+    nvfp4_block(v, gs, (uint2*)(q + (size_t)r * (K / 2) + b * 8), sf + (size_t)r * (K / 16) + b);
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(256) dequant_kernel(MatView m, int e, float* __restrict__ out) {
+  const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (i >= (size_t)m.N * m.K) return;
+  const int n = (int)(i / m.K), k0 = (int)(i % m.K);
+  float w[8];
+  load_w8<FMT>(m, e, n, k0, w);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) out[i + j] = w[j];
+}
+
+}  // namespace
+
+cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, const __nv_bfloat16* wd, char* packed,
+                        cudaStream_t s) {
+  const int E = d.E, H = d.H, I = d.I;
+  for (int which = 0; which < 2; ++which) {
+    const uint16_t* w = (const uint16_t*)(which == 0 ? wgu : wd);
+    const int N = which == 0 ? 2 * I : H, K = which == 0 ? H : I;
+    uint8_t* a = (uint8_t*)(packed + d.offset[which == 0 ? MOE_T_GU_A : MOE_T_D_A]);
+    uint8_t* b = (uint8_t*)(packed + d.offset[which == 0 ? MOE_T_GU_B : MOE_T_D_B]);
+    if (d.fmt == MOE_FMT_FP8_B128_W8A16) {
+      pack_fp8_kernel<<<dim3(K / 128, N / 128, E), 256, 0, s>>>(w, N, K, a, (float*)b);
+    } else if (d.fmt == MOE_FMT_INT4_G128_W4A16) {
+      pack_int4_kernel<<<dim3(N / 128, K / 128, E), 128, 0, s>>>(w, N, K, (uint32_t*)a, (__half*)b);
+    } else {
+      unsigned* slot = (unsigned*)(packed + d.offset[which == 0 ? MOE_T_GU_GS : MOE_T_D_GS]);
+      cudaMemsetAsync(slot, 0, sizeof(float) * E, s);
+      const size_t per = (size_t)N * K;
+      nvfp4_amax_kernel<<<dim3(64, E), 256, 0, s>>>(w, per, slot);
+      const size_t nblk = per / 16;
+      nvfp4_pack_kernel<<<dim3((unsigned)((nblk + 255) / 256), E), 256, 0, s>>>(w, N, K, slot, a, b);
+      nvfp4_finish_kernel<<<(E + 127) / 128, 128, 0, s>>>(slot, E);
+    }
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e, int which, float* out,
+                           cudaStream_t s) {
+  const MatView m = mat_view(d, packed, which);
+  const unsigned blocks = (unsigned)(((size_t)m.N * m.K / 8 + 255) / 256);
+  if (d.fmt == MOE_FMT_FP8_B128_W8A16) dequant_kernel<MOE_FMT_FP8_B128_W8A16><<<blocks, 256, 0, s>>>(m, e, out);
+  else if (d.fmt == MOE_FMT_INT4_G128_W4A16) dequant_kernel<MOE_FMT_INT4_G128_W4A16><<<blocks, 256, 0, s>>>(m, e, out);
+  else dequant_kernel<MOE_FMT_NVFP4_W4A16><<<blocks, 256, 0, s>>>(m, e, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows(const __nv_bfloat16* x, int rows, int K, uint8_t* q, uint8_t* sf, float* gs,
+                              cudaStream_t s) {
+  if (rows <= 0) return cudaGetLastError();
+  quant_rows_kernel<<<(rows + 7) / 8, 256, 0, s>>>((const uint16_t*)x, rows, K, q, sf, gs);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,205 @@
+// Routing: warp-level top-k with a renormalised softmax, per-expert histogram, exclusive
+// scan, and a deterministic permutation of (token, slot) rows by (expert, token, slot).
+//
+// The pages route with the model's BF16 router (clef-omni-fp8, page header: "router ... stay
+// BF16") and run the experts as one grouped matmul per layer (clef-omni-fp8, "How this
+// checkpoint runs"; clef-omni-int4, same section); grouping rows by expert is what a grouped
+// matmul consumes.  Three launches, no atomics whose order reaches the output:
+//   1. route_topk_kernel   one warp per token; per-block expert histogram in shared memory
+//   2. route_scan_kernel   one block: expert totals, offsets, per-block bases, GEMM tile table
+//   3. route_scatter_kernel rank of each row inside its block from per-warp ballot masks
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+struct Cand {
+  float v;
+  int i;
+};
+// a beats b: larger logit, or equal logit and lower expert index; i == INT_MAX is "none".
+__device__ __forceinline__ bool beats(float av, int ai, float bv, int bi) {
+  if (bi == INT_MAX) return ai != INT_MAX;
+  if (ai == INT_MAX) return false;
+  return av > bv || (av == bv && ai < bi);
+}
+
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                         int32_t* __restrict__ topk_idx,
+                                                         float* __restrict__ topk_w,
+                                                         int32_t* __restrict__ blkcnt, int* err) {
+  __shared__ int cnt[kMaxE];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  if (blockIdx.x == 0 && tid == 0) *err = kDevOk;  // each forward pass reports its own errors
+  __syncthreads();
+  const int per_warp = kRouteTB / 8;
+  for (int it = 0; it < per_warp; ++it) {
+    const int t = blockIdx.x * kRouteTB + warp * per_warp + it;
+    if (t >= T) break;
+    float v[kMaxE / 32];
+#pragma unroll
+    for (int m = 0; m < kMaxE / 32; ++m) {
+      const int e = lane + 32 * m;
+      float x = e < E ? logits[(size_t)t * E + e] : -INFINITY;
+      v[m] = isnan(x) ? -INFINITY : x;
+    }
+    uint32_t taken = 0;  // bit m: candidate lane + 32m already selected
+    float selv[kMaxTopK];
+    int seli[kMaxTopK];
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int m = 0; m < kMaxE / 32; ++m) {
+        const int e = lane + 32 * m;
+        if (e < E && !((taken >> m) & 1u) && beats(v[m], e, bv, bi)) {
+          bv = v[m];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (beats(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      selv[j] = bv;
+      seli[j] = bi;
+    }
+    // renormalised softmax over the selected logits (descending: selv[0] is the max)
+    float den = 0.f;
+    for (int j = 0; j < k; ++j) den += expf(selv[j] - selv[0]);
+    if (lane < k) {
+      float mine = selv[0];
+      int mi = seli[0];
+      for (int j = 1; j < k; ++j)
+        if (j == lane) {
+          mine = selv[j];
+          mi = seli[j];
+        }
+      topk_idx[(size_t)t * k + lane] = mi;
+      topk_w[(size_t)t * k + lane] = expf(mine - selv[0]) / den;
+      atomicAdd(&cnt[mi], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) blkcnt[(size_t)blockIdx.x * E + e] = cnt[e];
+}
+
+// One block of 1024 threads.  Thread e < E owns expert e.
+__global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restrict__ blkcnt, int nb, int E,
+                                                          int row_block, int max_tiles,
+                                                          int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ blkbase,
+                                                          TileEntry* __restrict__ tiles, int* err) {
+  __shared__ int tot[kMaxE], ntl[kMaxE], off_s[kMaxE + 1], toff_s[kMaxE + 1];
+  const int e = threadIdx.x;
+  if (e < E) {
+    int s = 0;
+    for (int b = 0; b < nb; ++b) s += blkcnt[(size_t)b * E + e];
+    tot[e] = s;
+    ntl[e] = (s + row_block - 1) / row_block;
+  }
+  __syncthreads();
+  if (e == 0) {  // E <= 256: a serial scan is a few hundred cycles
+    int a = 0, b = 0;
+    for (int i = 0; i < E; ++i) {
+      off_s[i] = a;
+      toff_s[i] = b;
+      a += tot[i];
+      b += ntl[i];
+    }
+    off_s[E] = a;
+    toff_s[E] = b;
+  }
+  __syncthreads();
+  if (e <= E) offsets[e] = off_s[e];
+  if (e < E) {
+    int run = off_s[e];
+    for (int b = 0; b < nb; ++b) {
+      blkbase[(size_t)b * E + e] = run;
+      run += blkcnt[(size_t)b * E + e];
+    }
+    const int t0 = toff_s[e];
+    for (int i = 0; i < ntl[e]; ++i) {
+      if (t0 + i >= max_tiles) {
+        set_dev_error(err, kDevFault);
+        break;
+      }
+      TileEntry te;
+      te.expert = e;
+      te.row0 = off_s[e] + i * row_block;
+      te.rows = min(row_block, tot[e] - i * row_block);
+      te.pad = 0;
+      tiles[1 + t0 + i] = te;
+    }
+  }
+  if (e == 0) {
+    TileEntry h;
+    h.expert = min(toff_s[E], max_tiles);
+    h.row0 = off_s[E];
+    h.rows = row_block;
+    h.pad = 0;
+    tiles[0] = h;
+  }
+}
+
+__global__ void __launch_bounds__(kRouteTB) route_scatter_kernel(const int32_t* __restrict__ topk_idx, int T,
+                                                                 int E, int k,
+                                                                 const int32_t* __restrict__ blkbase,
+                                                                 int32_t* __restrict__ perm,
+                                                                 int32_t* __restrict__ inv) {
+  __shared__ uint32_t mask[kRouteTB / 32][kMaxE];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < (kRouteTB / 32) * kMaxE; i += blockDim.x) (&mask[0][0])[i] = 0u;
+  __syncthreads();
+  const int t = blockIdx.x * kRouteTB + tid;
+  int ex[kMaxTopK];
+  if (t < T)
+    for (int j = 0; j < k; ++j) {
+      ex[j] = topk_idx[(size_t)t * k + j];
+      atomicOr(&mask[warp][ex[j]], 1u << lane);
+    }
+  __syncthreads();
+  if (t < T) {
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int j = 0; j < k; ++j) {
+      const int e = ex[j];
+      int rank = __popc(mask[warp][e] & lt);
+      for (int w = 0; w < warp; ++w) rank += __popc(mask[w][e]);
+      const int pos = blkbase[(size_t)blockIdx.x * E + e] + rank;
+      perm[pos] = t * k + j;
+      inv[(size_t)t * k + j] = pos;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int row_block, const WsLayout& L, char* ws,
+                         cudaStream_t s) {
+  int* err = (int*)(ws + L.err);
+  int32_t* idx = (int32_t*)(ws + L.topk_idx);
+  float* w = (float*)(ws + L.topk_w);
+  int32_t* blkcnt = (int32_t*)(ws + L.blkcnt);
+  int32_t* blkbase = (int32_t*)(ws + L.blkbase);
+  int32_t* off = (int32_t*)(ws + L.offsets);
+  int32_t* perm = (int32_t*)(ws + L.perm);
+  int32_t* inv = (int32_t*)(ws + L.inv);
+  TileEntry* tiles = (TileEntry*)(ws + L.tiles);
+  const int nb = L.nb;
+  if (T > 0) route_topk_kernel<<<nb, 256, 0, s>>>(logits, T, E, k, idx, w, blkcnt, err);
+  else cudaMemsetAsync(err, 0, sizeof(int), s);
+  route_scan_kernel<<<1, 1024, 0, s>>>(blkcnt, T > 0 ? nb : 0, E, row_block, L.max_tiles, off, blkbase, tiles,
+                                       err);
+  if (T > 0) route_scatter_kernel<<<nb, kRouteTB, 0, s>>>(idx, T, E, k, blkbase, perm, inv);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,87 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every function that
+include/*.h declares, and the host-only calls (layouts, sizes, argument checks) behave."""
+import ctypes as C
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+import nvfp4_expert_gemms_gb300 as M
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_library_exports_every_declared_function():
+    lib = M.lib()
+    names = declared_functions()
+    assert {"moe_layer_forward", "moe_pack_experts", "moe_packed_size"} <= names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(M.EXPORTS) <= names
+
+
+def test_packed_sizes_match_canonical_shapes(orc):
+    H, I, E = 2048, 768, 128
+    per_expert = {"fp8": 4_719_744, "int4": 2_433_024, "nvfp4_w4a16": 2_654_216}
+    for fmt, want in per_expert.items():
+        d = M.moe_packed_size(fmt, E, H, I)
+        got = sum(int(d.size[i]) for i in range(8))
+        assert got == E * want, (fmt, got)
+        assert all(int(d.offset[i]) % 256 == 0 for i in range(8))
+        assert d.bytes >= got
+    # the NVFP4 layer is the 0.32 GiB the page quotes
+    d = M.moe_packed_size("nvfp4_w4a4", E, H, I)
+    assert round(sum(int(d.size[i]) for i in range(8)) / 2 ** 30, 2) == 0.32
+
+
+def test_packed_tensor_sizes_equal_oracle_outputs(orc):
+    import synth
+
+    wgu, wd = synth.gen_expert_weights(2, 256, 128, seed=0)
+    for fmt_name, fid in (("fp8", 1), ("int4", 2), ("nvfp4_w4a16", 3)):
+        p = orc.pack_experts(fid, wgu, wd)
+        d = M.moe_packed_size(fmt_name, 2, 256, 128)
+        assert int(d.size[M.MOE_T_GU_A]) == p["gu"][0].nbytes
+        assert int(d.size[M.MOE_T_GU_B]) == p["gu"][1].nbytes
+        assert int(d.size[M.MOE_T_D_A]) == p["d"][0].nbytes
+        assert int(d.size[M.MOE_T_D_B]) == p["d"][1].nbytes
+
+
+def test_argument_errors_are_synchronous():
+    lib = M.lib()
+    d = M.PackedDesc()
+    assert lib.moe_packed_size(9, 8, 256, 128, C.byref(d)) == 1
+    assert lib.moe_packed_size(1, 8, 200, 128, C.byref(d)) == 1
+    assert lib.moe_packed_size(1, 300, 256, 128, C.byref(d)) == 1
+    assert lib.moe_packed_size(1, 8, 256, 128, C.byref(d)) == 0
+    n = C.c_size_t()
+    assert lib.moe_workspace_size(C.byref(d), 16, 0, C.byref(n)) == 1
+    assert lib.moe_workspace_size(C.byref(d), 16, 9, C.byref(n)) == 1
+    assert lib.moe_workspace_size(C.byref(d), 16, 2, C.byref(n)) == 0 and n.value > 0
+    # forward with a too-small workspace is refused before any CUDA call
+    st = lib.moe_layer_forward(C.c_void_p(256), C.c_void_p(256), 16, C.byref(d), C.c_void_p(256), 2,
+                               C.c_void_p(512), C.c_void_p(1024), 16, None)
+    assert st == 3
+    assert lib.moe_layer_forward(C.c_void_p(256), C.c_void_p(256), 16, C.byref(d), C.c_void_p(256), 2,
+                                 C.c_void_p(256), C.c_void_p(1024), 1 << 30, None) == 1  # x aliases out
+    assert M.moe_status_string(3) == "workspace too small"
+
+
+def test_workspace_grows_with_tokens():
+    d = M.moe_packed_size("nvfp4_w4a4", 128, 2048, 768)
+    a = M.moe_workspace_size(d, 1, 8)
+    b = M.moe_workspace_size(d, 16384, 8)
+    assert b > a > 0
+    assert M.moe_workspace_size_host_io(d, 16, 8) > M.moe_workspace_size(d, 16, 8)

@@ -1,0 +1,198 @@
+"""GPU parity: the CUDA library against the CPU oracle on the same seeded inputs.
+
+Integer work (packed codes, routing indices, permutation, activation codes) must be
+bit-exact; dequantized weights bit-exact; routing weights within 1e-6 relative (expf is
+not correctly rounded); layer outputs within relative Frobenius 1e-2 and per-element
+2e-2 * max|ref| of the oracle's fp64 result.
+"""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_expert_gemms_gb300 as M
+import synth
+
+pytestmark = pytest.mark.gpu
+
+FMTS = ["fp8", "int4", "nvfp4_w4a16", "nvfp4_w4a4"]
+FID = {"fp8": 1, "int4": 2, "nvfp4_w4a16": 3, "nvfp4_w4a4": 4}
+REL_FRO, REL_MAX = 1e-2, 2e-2
+
+
+def dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def host_bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def check_close(got, ref, what=""):
+    ref = np.asarray(ref, np.float64)
+    got = np.asarray(got, np.float64)
+    assert np.all(np.isfinite(got)), what
+    fro = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    mx = np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30)
+    assert fro <= REL_FRO and mx <= REL_MAX, f"{what}: rel fro {fro:.3e}, rel max {mx:.3e}"
+    return fro, mx
+
+
+class Case:
+    def __init__(self, fmt, T, H, I, E, k, seed=0, zipf=None, experts_for_oracle="routed"):
+        self.fmt, self.T, self.H, self.I, self.E, self.k = fmt, T, H, I, E, k
+        self.x = synth.gen_x(T, H, seed)
+        self.lg = synth.gen_logits(T, E, seed, zipf_alpha=zipf)
+        self.wgu, self.wd = synth.gen_expert_weights(E, H, I, seed)
+        self.layer = M.MoELayer(fmt, dev_bf16(self.wgu), dev_bf16(self.wd))
+
+    def run(self):
+        x = dev_bf16(self.x)
+        lg = torch.from_numpy(self.lg).cuda()
+        out = self.layer.forward(x, lg, self.k)
+        torch.cuda.synchronize()
+        assert M.moe_get_device_error(self.layer.workspace) == 0
+        return host_bits(out)
+
+    def oracle(self, orc, tokens=None):
+        idx, _ = orc.route(self.lg if tokens is None else self.lg[tokens], self.k)
+        p = orc.pack_experts(FID[self.fmt], self.wgu, self.wd, experts=np.unique(idx))
+        return orc.moe_layer(FID[self.fmt], self.x, self.lg, p, self.k, tokens=tokens)
+
+
+# ------------------------------------------------------------------ packing and dequant
+@pytest.mark.parametrize("fmt", ["fp8", "int4", "nvfp4_w4a16"])
+def test_pack_bit_exact(orc, fmt):
+    E, H, I = 3, 384, 256
+    wgu, wd = synth.gen_expert_weights(E, H, I, seed=5)
+    wgu[1, 7, :] = 0  # a zero row: INT4 zero scale, NVFP4 zero blocks
+    wd[2, :128, :128] = 0  # a zero FP8 tile
+    layer = M.MoELayer(fmt, dev_bf16(wgu), dev_bf16(wd))
+    torch.cuda.synchronize()
+    ref = orc.pack_experts(FID[fmt], wgu, wd)
+    d = layer.desc
+    for which, name in ((M.MOE_T_GU_A, ("gu", 0)), (M.MOE_T_GU_B, ("gu", 1)), (M.MOE_T_D_A, ("d", 0)),
+                        (M.MOE_T_D_B, ("d", 1))):
+        got = M.packed_view(d, layer.packed, which).cpu().numpy()
+        want = ref[name[0]][name[1]]
+        assert got.tobytes() == np.ascontiguousarray(want).tobytes(), (fmt, which)
+    if fmt.startswith("nvfp4"):
+        for which, name in ((M.MOE_T_GU_GS, "gu"), (M.MOE_T_D_GS, "d")):
+            got = M.packed_view(d, layer.packed, which).cpu().numpy()
+            assert got.tobytes() == ref[name][2].tobytes()
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int4", "nvfp4_w4a16"])
+def test_dequant_view_bit_exact(orc, fmt):
+    E, H, I = 2, 256, 128
+    wgu, wd = synth.gen_expert_weights(E, H, I, seed=6)
+    layer = M.MoELayer(fmt, dev_bf16(wgu), dev_bf16(wd))
+    ref = orc.pack_experts(FID[fmt], wgu, wd)
+    for e in range(E):
+        for which, key in ((0, "gu"), (1, "d")):
+            got = M.moe_debug_dequant(layer.desc, layer.packed, e, which).cpu().numpy()
+            a, b, g = ref[key]
+            if fmt == "fp8":
+                want = orc.dequant_fp8(a[e], b[e])
+            elif fmt == "int4":
+                want = orc.dequant_int4(a[e], b[e])
+            else:
+                want = orc.dequant_nvfp4(a[e], b[e], g[e])
+            assert got.tobytes() == want.tobytes()
+
+
+def test_quant_act_bit_exact(orc):
+    x = synth.gen_x(33, 2048, seed=7)
+    x[5] = 0  # an all-zero row: amax clamp
+    q, s, g = M.moe_debug_quant_act(dev_bf16(x))
+    rq, rs, rg = orc.quant_act_nvfp4(x)
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert g.cpu().numpy().tobytes() == rg.tobytes()
+
+
+# ------------------------------------------------------------------ routing
+@pytest.mark.parametrize("T,E,k,zipf", [(64, 8, 2, None), (1, 128, 8, None), (300, 128, 8, 1.1), (257, 256, 8, None),
+                                        (5, 6, 6, None), (1000, 37, 3, None)])
+def test_route_bit_exact(orc, T, E, k, zipf):
+    lg = synth.gen_logits(T, E, seed=T + E, zipf_alpha=zipf)
+    d = M.moe_packed_size("fp8", E, 128, 128)
+    ws = torch.empty(M.moe_workspace_size(d, T, k), dtype=torch.uint8, device="cuda")
+    idx, w, off, perm, inv = M.moe_debug_route(torch.from_numpy(lg).cuda(), k, ws)
+    ridx, rw = orc.route(lg, k)
+    roff, rperm, rinv = orc.permute(ridx, E)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    assert np.array_equal(off.cpu().numpy(), roff)
+    assert np.array_equal(perm.cpu().numpy(), rperm)
+    assert np.array_equal(inv.cpu().numpy(), rinv)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-6, atol=0)
+
+
+def test_route_ties_lower_index(orc):
+    lg = np.array([[0.5, 2.0, 2.0, 1.0, 2.0, -1.0, 1.0, 1.0]], np.float32)
+    d = M.moe_packed_size("fp8", 8, 128, 128)
+    ws = torch.empty(M.moe_workspace_size(d, 1, 5), dtype=torch.uint8, device="cuda")
+    idx, w, off, perm, inv = M.moe_debug_route(torch.from_numpy(lg).cuda(), 5, ws)
+    assert idx.cpu().numpy().tolist() == [[1, 2, 4, 3, 6]] == orc.route(lg, 5)[0].tolist()
+
+
+# ------------------------------------------------------------------ the layer
+@pytest.mark.parametrize("fmt", FMTS)
+def test_layer_tiny_config(orc, fmt):
+    """64 tokens, hidden 256, intermediate 128, 8 experts, top-2 (seed 0)."""
+    c = Case(fmt, 64, 256, 128, 8, 2)
+    check_close(synth.bf16_bits_to_f32(c.run()), c.oracle(orc), fmt)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_layer_ragged_multi_tile(orc, fmt):
+    """Several row blocks per expert with ragged tails, several column and K tiles."""
+    c = Case(fmt, 45, 384, 256, 16, 4, seed=3)
+    check_close(synth.bf16_bits_to_f32(c.run()), c.oracle(orc), fmt)
+
+
+@pytest.mark.parametrize("fmt,T,E,k", [("fp8", 1, 8, 1), ("nvfp4_w4a4", 3, 4, 4), ("int4", 9, 1, 1),
+                                       ("nvfp4_w4a16", 17, 8, 8)])
+def test_layer_edge_cases(orc, fmt, T, E, k):
+    c = Case(fmt, T, 256, 128, E, k, seed=11)
+    check_close(synth.bf16_bits_to_f32(c.run()), c.oracle(orc), fmt)
+
+
+def test_layer_zero_tokens_is_a_no_op():
+    c = Case("fp8", 4, 256, 128, 8, 2)
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    lg = torch.empty((0, 8), dtype=torch.float32, device="cuda")
+    out = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    ws = c.layer.ensure_workspace(0, 2)
+    M.moe_layer_forward(x, lg, c.layer.desc, c.layer.packed, 2, out, ws)
+    torch.cuda.synchronize()
+    assert M.moe_get_device_error(ws) == 0
+
+
+def test_layer_forward_host_matches_device_path(orc):
+    c = Case("nvfp4_w4a16", 20, 256, 128, 8, 2, seed=4)
+    dev_out = c.run()
+    ws = c.layer.ensure_workspace(c.T, c.k, host_io=True)
+    xh = torch.from_numpy(c.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    lh = torch.from_numpy(c.lg).pin_memory()
+    oh = torch.empty((c.T, c.H), dtype=torch.bfloat16).pin_memory()
+    M.moe_layer_forward_host(xh, lh, c.layer.desc, c.layer.packed, c.k, oh, ws)
+    torch.cuda.synchronize()
+    check_close(synth.bf16_bits_to_f32(host_bits(oh)), c.oracle(orc), "host io")
+    check_close(synth.bf16_bits_to_f32(host_bits(oh)), synth.bf16_bits_to_f32(dev_out), "host vs device")
+
+
+# ------------------------------------------------------------------ full-size workloads
+FULL = dict(H=2048, I=768, E=128, k=8)
+
+
+@pytest.mark.parametrize("fmt,T,zipf,sample", [("fp8", 16, None, None), ("int4", 256, None, 24),
+                                               ("nvfp4_w4a16", 4096, 1.1, 24), ("nvfp4_w4a4", 16384, 1.1, 16)])
+def test_layer_full_size_sampled(orc, fmt, T, zipf, sample):
+    c = Case(fmt, T, FULL["H"], FULL["I"], FULL["E"], FULL["k"], seed=0, zipf=zipf)
+    got = synth.bf16_bits_to_f32(c.run())
+    toks = None
+    if sample:
+        g = np.random.default_rng(T)
+        toks = np.sort(g.choice(T, size=sample, replace=False)).astype(np.int32)
+        got = got[toks]
+    check_close(got, c.oracle(orc, tokens=toks), f"{fmt} T={T}")
