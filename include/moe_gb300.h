@@ -154,6 +154,18 @@ moe_status_t moe_debug_dequant(const moe_packed_desc_t* desc, const void* packed
 moe_status_t moe_debug_quant_act(const void* x, int T, int H, uint8_t* codes, uint8_t* scales, float* gs,
                                  moe_stream_t stream);
 
+/* ---- measurement hooks ------------------------------------------------------------------ */
+
+/* Total number of CUDA kernels this library has enqueued in the calling process (all threads,
+ * all devices) since it was loaded.  Memsets and copies are not counted. */
+uint64_t moe_kernel_launch_count(void);
+
+/* Ask the next moe_layer_forward / moe_layer_forward_host call made by this host thread to
+ * record `start` right before and `stop` right after the launches of one step, on the call's
+ * stream (step 0 = grouped gate/up GEMM, 1 = grouped down GEMM).  The request is consumed by
+ * that one call.  Events are cudaEvent_t passed as void*; pass NULL to cancel. */
+moe_status_t moe_time_next_step(int step, void* start, void* stop);
+
 #ifdef __cplusplus
 }
 #endif

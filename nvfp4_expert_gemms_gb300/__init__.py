@@ -26,7 +26,8 @@ MOE_T_GU_A, MOE_T_GU_B, MOE_T_D_A, MOE_T_D_B, MOE_T_GU_GS, MOE_T_D_GS = range(6)
 
 EXPORTS = ("moe_packed_size", "moe_pack_experts", "moe_workspace_size", "moe_layer_forward",
            "moe_workspace_size_host_io", "moe_layer_forward_host", "moe_get_device_error", "moe_status_string",
-           "moe_debug_route", "moe_debug_dequant", "moe_debug_quant_act")
+           "moe_debug_route", "moe_debug_dequant", "moe_debug_quant_act", "moe_kernel_launch_count",
+           "moe_time_next_step")
 
 
 class PackedDesc(C.Structure):
@@ -69,6 +70,9 @@ def lib() -> C.CDLL:
         L.moe_debug_route.argtypes = [P, I32, I32, I32, P, P, P, P, P, P, SZ, P]
         L.moe_debug_dequant.argtypes = [PD, P, I32, I32, P, P]
         L.moe_debug_quant_act.argtypes = [P, I32, I32, P, P, P, P]
+        L.moe_kernel_launch_count.restype = C.c_uint64
+        L.moe_kernel_launch_count.argtypes = []
+        L.moe_time_next_step.argtypes = [I32, P, P]
         _lib = L
     return _lib
 
@@ -140,6 +144,18 @@ def moe_get_device_error(workspace, stream=None) -> int:
     code = C.c_int32()
     _check(lib().moe_get_device_error(_ptr(workspace), _stream(stream), C.byref(code)), "moe_get_device_error")
     return code.value
+
+
+def moe_kernel_launch_count() -> int:
+    return int(lib().moe_kernel_launch_count())
+
+
+def moe_time_next_step(step: int, start_event=None, stop_event=None):
+    """Record torch.cuda.Event pair around GEMM step `step` (0 gate/up, 1 down) of the next
+    forward call made by this thread."""
+    s = C.c_void_p(start_event.cuda_event if start_event is not None else 0)
+    e = C.c_void_p(stop_event.cuda_event if stop_event is not None else 0)
+    _check(lib().moe_time_next_step(step, s, e), "moe_time_next_step")
 
 
 def moe_debug_route(router_logits, top_k: int, workspace, stream=None):

@@ -2,9 +2,15 @@
 // workspace layouts, and the launch sequence of the forward pass.
 #include <string.h>
 
+#include <atomic>
+
 #include "moe_internal.cuh"
 
 namespace moe {
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+static thread_local StepEvents g_pending_events;
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -89,8 +95,10 @@ static moe_status_t forward_checked(const void* x, const float* logits, int T, c
   char* w = (char*)ws;
   const int rb = simt_row_block();
   if (launch_route(logits, T, d->E, k, rb, L, w, s) != cudaSuccess) return MOE_ERR_CUDA;
+  const StepEvents ev = g_pending_events;
+  g_pending_events = StepEvents();
   return cuda_status(launch_experts(*d, (const char*)packed, (const __nv_bfloat16*)x, T, k, rb, L, w,
-                                    (__nv_bfloat16*)out, s));
+                                    (__nv_bfloat16*)out, ev, s));
 }
 
 }  // namespace moe
@@ -205,6 +213,16 @@ moe_status_t moe_get_device_error(void* workspace, moe_stream_t stream, int32_t*
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
   *code = v;
+  return MOE_OK;
+}
+
+uint64_t moe_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+moe_status_t moe_time_next_step(int step, void* start, void* stop) {
+  if (step != 0 && step != 1) return MOE_ERR_INVALID_ARG;
+  if ((start == nullptr) != (stop == nullptr)) return MOE_ERR_INVALID_ARG;
+  g_pending_events.start[step] = (cudaEvent_t)start;
+  g_pending_events.stop[step] = (cudaEvent_t)stop;
   return MOE_OK;
 }
 

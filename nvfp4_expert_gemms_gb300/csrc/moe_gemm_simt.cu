@@ -152,7 +152,7 @@ __global__ void finalize_kernel(const float* __restrict__ acc, uint16_t* __restr
 
 template <int FMT, bool A4>
 cudaError_t run_simt(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
-                     const WsLayout& L, char* ws, cudaStream_t s) {
+                     const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s) {
   const int H = d.H, I = d.I;
   const MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
   const TileEntry* tiles = (const TileEntry*)(ws + L.tiles);
@@ -160,22 +160,28 @@ cudaError_t run_simt(const moe_packed_desc_t& d, const char* packed, const __nv_
   const size_t smem_gu = sizeof(float) * kSimtRB * H, smem_d = sizeof(float) * kSimtRB * I;
   cudaFuncSetAttribute(gateup_simt_kernel<FMT, A4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_gu);
   cudaFuncSetAttribute(down_simt_kernel<FMT, A4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_d);
+  if (ev.start[0]) cudaEventRecord(ev.start[0], s);
   gateup_simt_kernel<FMT, A4><<<dim3(L.max_tiles, I / kSimtNB), 128, smem_gu, s>>>(
       gu, (const uint16_t*)x, (const uint8_t*)(ws + L.xq), (const uint8_t*)(ws + L.xs),
       (const float*)(ws + L.xg), perm, k, I, tiles, (uint16_t*)(ws + L.h));
+  if (ev.stop[0]) cudaEventRecord(ev.stop[0], s);
   if (A4)
     launch_quant_rows((const __nv_bfloat16*)(ws + L.h), T * k, I, (uint8_t*)(ws + L.hq), (uint8_t*)(ws + L.hs),
                       (float*)(ws + L.hg), s);
+  if (ev.start[1]) cudaEventRecord(ev.start[1], s);
   down_simt_kernel<FMT, A4><<<dim3(L.max_tiles, H / kSimtNB), 128, smem_d, s>>>(
       dn, (const uint16_t*)(ws + L.h), (const uint8_t*)(ws + L.hq), (const uint8_t*)(ws + L.hs),
       (const float*)(ws + L.hg), perm, (const float*)(ws + L.topk_w), k, tiles, (float*)(ws + L.out_acc));
+  if (ev.stop[1]) cudaEventRecord(ev.stop[1], s);
+  note_launches(2);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
-                           int row_block, const WsLayout& L, char* ws, __nv_bfloat16* out, cudaStream_t s) {
+                           int row_block, const WsLayout& L, char* ws, __nv_bfloat16* out, const StepEvents& ev,
+                           cudaStream_t s) {
   (void)row_block;
   const size_t n_out = (size_t)T * d.H;
   if (T == 0) return cudaGetLastError();
@@ -184,14 +190,15 @@ cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const
     launch_quant_rows(x, T, d.H, (uint8_t*)(ws + L.xq), (uint8_t*)(ws + L.xs), (float*)(ws + L.xg), s);
   cudaError_t e;
   switch (d.fmt) {
-    case MOE_FMT_FP8_B128_W8A16: e = run_simt<MOE_FMT_FP8_B128_W8A16, false>(d, packed, x, T, k, L, ws, s); break;
-    case MOE_FMT_INT4_G128_W4A16: e = run_simt<MOE_FMT_INT4_G128_W4A16, false>(d, packed, x, T, k, L, ws, s); break;
-    case MOE_FMT_NVFP4_W4A16: e = run_simt<MOE_FMT_NVFP4_W4A16, false>(d, packed, x, T, k, L, ws, s); break;
-    default: e = run_simt<MOE_FMT_NVFP4_W4A16, true>(d, packed, x, T, k, L, ws, s); break;
+    case MOE_FMT_FP8_B128_W8A16: e = run_simt<MOE_FMT_FP8_B128_W8A16, false>(d, packed, x, T, k, L, ws, ev, s); break;
+    case MOE_FMT_INT4_G128_W4A16: e = run_simt<MOE_FMT_INT4_G128_W4A16, false>(d, packed, x, T, k, L, ws, ev, s); break;
+    case MOE_FMT_NVFP4_W4A16: e = run_simt<MOE_FMT_NVFP4_W4A16, false>(d, packed, x, T, k, L, ws, ev, s); break;
+    default: e = run_simt<MOE_FMT_NVFP4_W4A16, true>(d, packed, x, T, k, L, ws, ev, s); break;
   }
   if (e != cudaSuccess) return e;
   const unsigned blocks = (unsigned)((n_out / 4 + 255) / 256 + 1);
   finalize_kernel<<<blocks, 256, 0, s>>>((const float*)(ws + L.out_acc), (uint16_t*)out, n_out);
+  note_launches(1);
   return cudaGetLastError();
 }
 

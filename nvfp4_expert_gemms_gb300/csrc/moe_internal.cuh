@@ -82,9 +82,15 @@ cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e
                            cudaStream_t s);
 cudaError_t launch_quant_rows(const __nv_bfloat16* x, int rows, int K, uint8_t* q, uint8_t* sf, float* gs,
                               cudaStream_t s);
+// Optional events around the two GEMM steps (0 = gate/up, 1 = down); null entries are skipped.
+struct StepEvents {
+  cudaEvent_t start[2] = {nullptr, nullptr}, stop[2] = {nullptr, nullptr};
+};
 cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,
                            int k, int row_block, const WsLayout& L, char* ws, __nv_bfloat16* out,
-                           cudaStream_t s);
+                           const StepEvents& ev, cudaStream_t s);
+// Running count of kernels enqueued by the library (moe_kernel_launch_count).
+void note_launches(int n);
 int simt_row_block();
 
 }  // namespace moe

@@ -197,7 +197,9 @@ cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, co
       const size_t nblk = per / 16;
       nvfp4_pack_kernel<<<dim3((unsigned)((nblk + 255) / 256), E), 256, 0, s>>>(w, N, K, slot, a, b);
       nvfp4_finish_kernel<<<(E + 127) / 128, 128, 0, s>>>(slot, E);
+      note_launches(2);
     }
+    note_launches(1);
   }
   return cudaGetLastError();
 }
@@ -209,6 +211,7 @@ cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e
   if (d.fmt == MOE_FMT_FP8_B128_W8A16) dequant_kernel<MOE_FMT_FP8_B128_W8A16><<<blocks, 256, 0, s>>>(m, e, out);
   else if (d.fmt == MOE_FMT_INT4_G128_W4A16) dequant_kernel<MOE_FMT_INT4_G128_W4A16><<<blocks, 256, 0, s>>>(m, e, out);
   else dequant_kernel<MOE_FMT_NVFP4_W4A16><<<blocks, 256, 0, s>>>(m, e, out);
+  note_launches(1);
   return cudaGetLastError();
 }
 
@@ -216,6 +219,7 @@ cudaError_t launch_quant_rows(const __nv_bfloat16* x, int rows, int K, uint8_t* 
                               cudaStream_t s) {
   if (rows <= 0) return cudaGetLastError();
   quant_rows_kernel<<<(rows + 7) / 8, 256, 0, s>>>((const uint16_t*)x, rows, K, q, sf, gs);
+  note_launches(1);
   return cudaGetLastError();
 }
 

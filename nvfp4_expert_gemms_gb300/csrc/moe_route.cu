@@ -199,6 +199,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int row_block
   route_scan_kernel<<<1, 1024, 0, s>>>(blkcnt, T > 0 ? nb : 0, E, row_block, L.max_tiles, off, blkbase, tiles,
                                        err);
   if (T > 0) route_scatter_kernel<<<nb, kRouteTB, 0, s>>>(idx, T, E, k, blkbase, perm, inv);
+  note_launches(T > 0 ? 3 : 1);
   return cudaGetLastError();
 }
 

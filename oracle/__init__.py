@@ -206,30 +206,34 @@ def pack_experts(fmt: int, wgu: np.ndarray, wd: np.ndarray, experts=None) -> dic
     Experts not in ``experts`` (when given) are left zero-filled: cheaper for full-size
     checks that only touch routed experts.
     """
+    from concurrent.futures import ThreadPoolExecutor
+
     E, N2, H = wgu.shape
     I = N2 // 2
     sel = range(E) if experts is None else sorted(set(int(e) for e in experts))
+    pool = ThreadPoolExecutor(max_workers=os.cpu_count() or 1)  # ctypes calls release the GIL
     out = {}
     for name, W, N, K in (("gu", wgu, 2 * I, H), ("d", wd, H, I)):
         if fmt == FMT_FP8:
             a = np.zeros((E, N, K), np.uint8)
             b = np.zeros((E, N // 128, K // 128), np.float32)
             g = None
-            for e in sel:
-                a[e], b[e] = pack_fp8(W[e])
+            for e, r in zip(sel, pool.map(lambda e: pack_fp8(W[e]), sel)):
+                a[e], b[e] = r
         elif fmt == FMT_INT4:
             a = np.zeros((E, K // 8, N), np.int32)
             b = np.zeros((E, K // 128, N), np.uint16)
             g = None
-            for e in sel:
-                a[e], b[e] = pack_int4(W[e])
+            for e, r in zip(sel, pool.map(lambda e: pack_int4(W[e]), sel)):
+                a[e], b[e] = r
         else:
             a = np.zeros((E, N, K // 2), np.uint8)
             b = np.zeros((E, N, K // 16), np.uint8)
             g = np.ones(E, np.float32)
-            for e in sel:
-                a[e], b[e], g[e] = pack_nvfp4(W[e])
+            for e, r in zip(sel, pool.map(lambda e: pack_nvfp4(W[e]), sel)):
+                a[e], b[e], g[e] = r
         out[name] = (a, b, g)
+    pool.shutdown()
     return out
 
 

@@ -63,7 +63,9 @@ def gen_logits(T: int, E: int, seed: int, layer: int = 0, zipf_alpha: float | No
     lg = g.standard_normal((T, E), dtype=np.float32)
     if zipf_alpha is not None:
         lg = (lg + zipf_bias(E, seed, layer, zipf_alpha)[None, :]).astype(np.float32)
-    for t in range(T):
+    srt = np.sort(lg, axis=1)
+    tied = np.flatnonzero((np.diff(srt, axis=1) == 0).any(axis=1))
+    for t in tied:
         while len(np.unique(lg[t])) != E:
             lg[t] = g.standard_normal(E, dtype=np.float32)
             if zipf_alpha is not None:
@@ -76,13 +78,21 @@ def gen_expert_weights(E: int, H: int, I: int, seed: int, layer: int = 0, expert
 
     When ``experts`` is given only those experts are drawn; the rest stay zero.
     """
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
     wgu = np.zeros((E, 2 * I, H), dtype=np.uint16)
     wd = np.zeros((E, H, I), dtype=np.uint16)
-    for e in range(E) if experts is None else experts:
+
+    def one(e):  # each expert has its own streams, so drawing order across threads is irrelevant
         g1 = _rng(seed, layer, STREAM_WGU, e)
         g2 = _rng(seed, layer, STREAM_WD, e)
         wgu[e] = f32_to_bf16_bits(g1.standard_normal((2 * I, H), dtype=np.float32) * np.float32(WEIGHT_STD))
         wd[e] = f32_to_bf16_bits(g2.standard_normal((H, I), dtype=np.float32) * np.float32(WEIGHT_STD))
+
+    sel = list(range(E) if experts is None else experts)
+    with ThreadPoolExecutor(max_workers=min(len(sel), os.cpu_count() or 1) or 1) as pool:
+        list(pool.map(one, sel))
     return wgu, wd
 
 
