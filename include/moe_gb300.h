@@ -154,6 +154,29 @@ moe_status_t moe_debug_dequant(const moe_packed_desc_t* desc, const void* packed
 moe_status_t moe_debug_quant_act(const void* x, int T, int H, uint8_t* codes, uint8_t* scales, float* gs,
                                  moe_stream_t stream);
 
+/* ---- routing without any caller workspace ----------------------------------------------- */
+
+/* The pages have no counterpart to this entry point; it exists for callers that cannot obtain
+ * device memory at this point: a plugin or callback run by a host engine that owns every device
+ * allocation and gives it no scratch, or a serving loop with a memory pool fixed at start-up
+ * where a cudaMalloc (and the device-wide synchronisation it brings) would stall other streams.
+ *
+ * Same results as moe_debug_route (same kernels), but the routing scratch lives in a static
+ * device array inside the library (MOE_ROUTE_NOALLOC_SCRATCH_BYTES, held on every GPU that
+ * loads the library until the process exits).  The call allocates nothing and frees nothing.
+ *   router_logits (dev) f32 [T, E]; topk_idx (dev) i32 [T, k]; topk_w (dev) f32 [T, k];
+ *   offsets (dev) i32 [E+1]; perm (dev) i32 [T*k]; inv (dev) i32 [T*k]; all caller-owned.
+ * Limits: T <= MOE_ROUTE_NOALLOC_MAX_TOKENS, E <= 256, top_k <= 8.  Larger T returns
+ * MOE_ERR_WORKSPACE ("workspace too small") before anything is enqueued.
+ * The first call on each device resolves the array's device address (cudaGetSymbolAddress with
+ * that device current) and caches it: make that first call before any stream capture begins.
+ * All calls share the one array, which keeps the last call's contents (each call writes all it
+ * reads); calls whose work overlaps on the GPU, e.g. on two streams, race on it. */
+#define MOE_ROUTE_NOALLOC_MAX_TOKENS 2048
+#define MOE_ROUTE_NOALLOC_SCRATCH_BYTES (512u * 1024u)
+moe_status_t moe_route_noalloc(const float* router_logits, int T, int E, int top_k, int32_t* topk_idx,
+                               float* topk_w, int32_t* offsets, int32_t* perm, int32_t* inv, moe_stream_t stream);
+
 /* ---- measurement hooks ------------------------------------------------------------------ */
 
 /* Total number of CUDA kernels this library has enqueued in the calling process (all threads,
