@@ -93,7 +93,7 @@ static moe_status_t forward_checked(const void* x, const float* logits, int T, c
   const moe_status_t dv = device_ok();
   if (dv != MOE_OK) return dv;
   char* w = (char*)ws;
-  const int rb = simt_row_block();
+  const int rb = d->fmt == MOE_FMT_NVFP4_W4A4 ? simt_row_block() : tc_row_block(T, k, d->E);
   if (launch_route(logits, T, d->E, k, rb, L, w, s) != cudaSuccess) return MOE_ERR_CUDA;
   const StepEvents ev = g_pending_events;
   g_pending_events = StepEvents();

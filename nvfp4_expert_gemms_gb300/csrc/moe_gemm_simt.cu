@@ -182,18 +182,15 @@ cudaError_t run_simt(const moe_packed_desc_t& d, const char* packed, const __nv_
 cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
                            int row_block, const WsLayout& L, char* ws, __nv_bfloat16* out, const StepEvents& ev,
                            cudaStream_t s) {
-  (void)row_block;
   const size_t n_out = (size_t)T * d.H;
   if (T == 0) return cudaGetLastError();
   cudaMemsetAsync(ws + L.out_acc, 0, sizeof(float) * n_out, s);
-  if (d.fmt == MOE_FMT_NVFP4_W4A4)
-    launch_quant_rows(x, T, d.H, (uint8_t*)(ws + L.xq), (uint8_t*)(ws + L.xs), (float*)(ws + L.xg), s);
   cudaError_t e;
-  switch (d.fmt) {
-    case MOE_FMT_FP8_B128_W8A16: e = run_simt<MOE_FMT_FP8_B128_W8A16, false>(d, packed, x, T, k, L, ws, ev, s); break;
-    case MOE_FMT_INT4_G128_W4A16: e = run_simt<MOE_FMT_INT4_G128_W4A16, false>(d, packed, x, T, k, L, ws, ev, s); break;
-    case MOE_FMT_NVFP4_W4A16: e = run_simt<MOE_FMT_NVFP4_W4A16, false>(d, packed, x, T, k, L, ws, ev, s); break;
-    default: e = run_simt<MOE_FMT_NVFP4_W4A16, true>(d, packed, x, T, k, L, ws, ev, s); break;
+  if (d.fmt == MOE_FMT_NVFP4_W4A4) {
+    launch_quant_rows(x, T, d.H, (uint8_t*)(ws + L.xq), (uint8_t*)(ws + L.xs), (float*)(ws + L.xg), s);
+    e = run_simt<MOE_FMT_NVFP4_W4A16, true>(d, packed, x, T, k, L, ws, ev, s);
+  } else {
+    e = launch_experts_tc(d, packed, x, T, k, row_block, L, ws, ev, s);
   }
   if (e != cudaSuccess) return e;
   const unsigned blocks = (unsigned)((n_out / 4 + 255) / 256 + 1);

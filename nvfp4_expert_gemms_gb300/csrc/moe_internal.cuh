@@ -92,5 +92,9 @@ cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const
 // Running count of kernels enqueued by the library (moe_kernel_launch_count).
 void note_launches(int n);
 int simt_row_block();
+// Tensor-core path (FP8 W8A16, INT4 W4A16, NVFP4 W4A16): row block per tile, and the two GEMMs.
+int tc_row_block(int T, int k, int E);
+cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
+                              int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);
 
 }  // namespace moe
