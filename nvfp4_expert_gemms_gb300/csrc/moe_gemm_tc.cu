@@ -34,11 +34,15 @@ namespace {
 using namespace tc;
 
 constexpr int kKC = 128;          // K elements per pipeline chunk
-constexpr int kThreads = 320;
+constexpr int kConvWarps = 16;    // warps 0-15: converters + epilogue
+constexpr int kProdWarp = 16;     // TMA producer
+constexpr int kMmaWarp = 17;      // TMEM owner and MMA issuer
+constexpr int kThreads = 18 * 32;
 constexpr int kStagesW = 4;       // weight chunks in flight (shared memory)
-constexpr int kStagesA = 2;       // converted A chunks (TMEM)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kACol = 256;   // TMEM columns [256, 512): A ring; [0, 2*BN): accumulators
+// TMEM columns: [0, 2*BN) accumulators (two sub-tiles), then a ring of converted A chunks of 128
+// columns (both sub-tiles, 64 columns each): three stages from column 128 when BN <= 64, two from
+// column 256 when BN = 128.
 
 template <int FMT>
 struct WFmt;
@@ -69,109 +73,172 @@ struct TcArgs {
   int k, N, K, I, H;
 };
 
+// Packed bf16 helpers on plain 32-bit registers (no address-taken temporaries).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
 }
 
-// ---- converters: raw chunk of one weight row (128 K) -> 64 bf16x2 words ------------------
-// FP8: e4m3 bits re-based into an fp32 exponent (value * 2^-120, exact incl. subnormals), an
-// exact multiply by 2^120, then one fp32 multiply by scale_inv and one rounding to bf16.
-__device__ __forceinline__ void conv_fp8(const char* sub, int r, float sc, uint32_t* out) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
+// ---- converters: half a chunk (64 K) of one weight row -> 32 bf16x2 words -------------------
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// FP8: each e4m3 byte becomes bf16 bits of (value * 2^-120) by moving its magnitude bits under
+// the bf16 exponent (exact, with e4m3 subnormals landing on bf16 subnormals), then one packed
+// bf16 multiply by bf16(scale_inv * 2^120) gives the dequantized weight rounded once to bf16.
+// When scale_inv * 2^120 does not fit bf16 (|w| > ~1e5) the exact fp32 route is taken instead.
+// (The shared-memory loads are issued first and the path choice sits outside the loops: both
+// matter several-fold for the converter's issue rate.)
+__device__ __forceinline__ void conv_fp8_exact(const char* sub, int r, int kh, float scale, uint32_t* out) {
+  for (int cc = 0; cc < 4; ++cc) {
+    const int c = kh * 4 + cc;
     const uint4 q = *(const uint4*)(sub + r * 128 + ((c ^ (r & 7)) * 16));
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
     for (int i = 0; i < 4; ++i) {
       float f[4];
-#pragma unroll
       for (int b = 0; b < 4; ++b) {
         const uint32_t byte = (w[i] >> (8 * b)) & 0xFFu;
-        f[b] = (__uint_as_float(((byte & 0x7Fu) << 20) | ((byte & 0x80u) << 24)) * 0x1p120f) * sc;
+        f[b] = (__uint_as_float(((byte & 0x7Fu) << 20) | ((byte & 0x80u) << 24)) * 0x1p120f) * scale;
       }
-      out[c * 8 + i * 2] = pack_bf16x2(f[0], f[1]);
-      out[c * 8 + i * 2 + 1] = pack_bf16x2(f[2], f[3]);
+      out[cc * 8 + i * 2] = pack_bf16x2(f[0], f[1]);
+      out[cc * 8 + i * 2 + 1] = pack_bf16x2(f[2], f[3]);
     }
   }
 }
 
-// INT4: 16 qweight words of column r (rows kr = 0..15 of the chunk), (code - 8) * scale.
-__device__ __forceinline__ void conv_int4(const char* sub, int r, float s, uint32_t* out) {
+__device__ __forceinline__ void conv_fp8(const char* sub, int r, int kh, float scale, uint32_t* out) {
+  const float big = scale * 0x1p120f;
+  if (!(big < 3.0e38f)) {
+    conv_fp8_exact(sub, r, kh, scale, out);
+    return;
+  }
+  const uint32_t sc = pack_bf16x2(big, big);
+  uint4 q[4];
 #pragma unroll
-  for (int kr = 0; kr < 16; ++kr) {
-    const uint32_t q = *(const uint32_t*)(sub + kr * 512 + r * 4);
+  for (int cc = 0; cc < 4; ++cc) q[cc] = *(const uint4*)(sub + r * 128 + (((kh * 4 + cc) ^ (r & 7)) * 16));
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    const uint32_t w[4] = {q[cc].x, q[cc].y, q[cc].z, q[cc].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float lo = (float)((int)((q >> (8 * i)) & 0xF) - 8) * s;
-      const float hi = (float)((int)((q >> (8 * i + 4)) & 0xF) - 8) * s;
-      out[kr * 4 + i] = pack_bf16x2(lo, hi);
+      const uint32_t m = w[i] & 0x7F7F7F7Fu, sg = w[i] & 0x80808080u;
+      out[cc * 8 + i * 2] = bmul2((prmt(m, 0u, 0x4140u) << 4) | prmt(sg, 0u, 0x1404u), sc);
+      out[cc * 8 + i * 2 + 1] = bmul2((prmt(m, 0u, 0x4342u) << 4) | prmt(sg, 0u, 0x3424u), sc);
     }
   }
 }
 
-// NVFP4: e2m1 * e4m3 block scale is exact in bf16; the global scale is applied in the epilogue.
-__device__ __forceinline__ void conv_nvfp4(const char* sub, int r, uint2 bs8, uint32_t* out) {
-  const uint32_t bsw[2] = {bs8.x, bs8.y};
+// INT4: nibble pair (k, k+1) of byte i -> bf16x2 (128 + n) by placing the nibbles under the
+// exponent of 128, minus 136 (exact), times the bf16-rounded group scale.
+__device__ __forceinline__ void conv_int4(const char* sub, int r, int kh, float scale, uint32_t* out) {
+  const uint32_t sc = pack_bf16x2(scale, scale);
+  const uint32_t off = 0x43084308u;  // bf16x2 (136, 136)
+  uint32_t qs[8];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {  // 16-byte chunk c = 32 codes = two 16-element blocks
-    const uint4 q = *(const uint4*)(sub + r * 64 + ((c ^ ((r >> 1) & 3)) * 16));
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  for (int j = 0; j < 8; ++j) qs[j] = *(const uint32_t*)(sub + (kh * 8 + j) * 512 + r * 4);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t q = qs[j], q4 = q >> 4;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int blk = c * 2 + (i >> 1);
-      const float bs = e4m3_to_f32((bsw[blk >> 2] >> (8 * (blk & 3))) & 0xFF);
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const uint32_t byte = (w[i] >> (8 * p)) & 0xFFu;
-        out[c * 16 + i * 4 + p] = pack_bf16x2(e2m1_to_f32(byte & 0xF) * bs, e2m1_to_f32(byte >> 4) * bs);
-      }
+      // out byte 0 = byte i of q (low nibble = k 2i), out byte 2 = byte i of q >> 4 (low nibble = k 2i+1)
+      const uint32_t t = prmt(q, q4, 0x4040u | (uint32_t)i | ((uint32_t)(4 + i) << 8));
+      const uint32_t v = (t & 0x000F000Fu) | 0x43004300u;
+      out[j * 4 + i] = bmul2(bsub2(v, off), sc);
     }
   }
 }
 
+// NVFP4: four E2M1 codes at a time become bf16 through byte-permute lookups of the bf16 bytes of
+// {0, .5, 1, 1.5, 2, 3, 4, 6}, the sign bits are merged, and one packed multiply by the E4M3 block
+// scale (exact: the product has at most 6 significant bits).  The global scale is applied in the
+// epilogue.
+__device__ __forceinline__ void e2m1x4_to_bf16x2(uint32_t w16, uint32_t& p0, uint32_t& p1) {
+  const uint32_t sel = w16 & 0x7777u;
+  const uint32_t lo = prmt(0xC0800000u, 0xC0804000u, sel);  // low bytes of the bf16 values
+  const uint32_t hi = prmt(0x3F3F3F00u, 0x40404040u, sel);  // high bytes
+  p0 = prmt(lo, hi, 0x5140u) | ((w16 << 12) & 0x8000u) | ((w16 << 24) & 0x80000000u);
+  p1 = prmt(lo, hi, 0x7362u) | ((w16 << 4) & 0x8000u) | ((w16 << 16) & 0x80000000u);
+}
+
+__device__ __forceinline__ void conv_nvfp4(const char* sub, int r, int kh, uint32_t bs4, uint32_t* out) {
+  uint4 q[2];
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) q[cc] = *(const uint4*)(sub + r * 64 + (((kh * 2 + cc) ^ ((r >> 1) & 3)) * 16));
+  uint32_t bs2[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const float f = e4m3_to_f32((bs4 >> (8 * b)) & 0xFF);
+    bs2[b] = pack_bf16x2(f, f);
+  }
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {  // 16-byte chunk = 32 codes = two 16-element blocks
+    const uint32_t w[4] = {q[cc].x, q[cc].y, q[cc].z, q[cc].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t bs = bs2[cc * 2 + (i >> 1)];
+      uint32_t p0, p1, p2, p3;
+      e2m1x4_to_bf16x2(w[i] & 0xFFFFu, p0, p1);
+      e2m1x4_to_bf16x2(w[i] >> 16, p2, p3);
+      out[cc * 16 + i * 4 + 0] = bmul2(p0, bs);
+      out[cc * 16 + i * 4 + 1] = bmul2(p1, bs);
+      out[cc * 16 + i * 4 + 2] = bmul2(p2, bs);
+      out[cc * 16 + i * 4 + 3] = bmul2(p3, bs);
+    }
+  }
+}
+
+// Persistent kernel: one CTA per SM walks the work items (row tile of one expert x column block)
+// with a stride of gridDim.x; the pipeline rings keep their phases across items, so the TMA for
+// the next item runs while the current item's epilogue executes.
 // MODE 0: gate/up GEMM + SiLU(gate)*up -> h (bf16, permuted row order).
 // MODE 1: down GEMM + routing weight -> fp32 red.add into the token-order accumulator.
 template <int FMT, int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __grid_constant__ TcArgs a) {
   constexpr int SB = BN >= 64 ? 2 : 4;  // activation stages
+  constexpr int kStagesA = BN <= 64 ? 3 : 2;
+  constexpr uint32_t kACol = BN <= 64 ? 128 : 256;
   constexpr int WSUB = WFmt<FMT>::kSubBytes;
   constexpr int WSTAGE = 2 * WSUB;
   constexpr int BSTAGE = BN * 256;  // BN rows x 128 K bf16, two 128-byte swizzle atoms
+  constexpr int TPL = (BN + 31) / 32;
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = (char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   char* sW = smem;
   char* sB = smem + kStagesW * WSTAGE;
   __shared__ uint64_t w_full[kStagesW], w_empty[kStagesW], a_full[kStagesA], a_empty[kStagesA], b_full[SB],
-      b_empty[SB], acc_full;
+      b_empty[SB], acc_full, drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_tok[BN];
-  __shared__ float s_w[BN];
 
-  if ((int)blockIdx.x >= a.tiles[0].expert) return;  // header entry holds the tile count
-  const TileEntry te = a.tiles[1 + blockIdx.x];
+  const int ntiles = a.tiles[0].expert;  // header entry holds the tile count
+  const int ncb = MODE == 0 ? a.I / 128 : (a.H + 255) / 256;
+  const int nwork = ntiles * ncb;
+  if ((int)blockIdx.x >= nwork) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = te.expert, row0 = te.row0, rows = te.rows;
-  int nbase0, nbase1, nsub;
-  if (MODE == 0) {
-    nbase0 = blockIdx.y * 128;
-    nbase1 = a.I + nbase0;
-    nsub = 2;
-  } else {
-    nbase0 = blockIdx.y * 256;
-    nbase1 = nbase0 + 128;
-    nsub = (a.H - nbase0) >= 256 ? 2 : 1;
-  }
   const int nK = a.K / kKC;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStagesW; ++i) {
       mbar_init(&w_full[i], 1);
-      mbar_init(&w_empty[i], 4 * nsub);
+      mbar_init(&w_empty[i], kConvWarps);
     }
     for (int i = 0; i < kStagesA; ++i) {
-      mbar_init(&a_full[i], 4 * nsub);
+      mbar_init(&a_full[i], kConvWarps);
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < SB; ++i) {
@@ -179,20 +246,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       mbar_init(&b_empty[i], 1);
     }
     mbar_init(&acc_full, 1);
+    mbar_init(&drain, 1);
     s_abort = 0;
     fence_barrier_init();
   }
-  if (threadIdx.x < BN) {
-    const int j = threadIdx.x;
-    const int p = a.perm[row0 + (j < rows ? j : rows - 1)];
-    s_tok[j] = p / a.k;
-    s_w[j] = j < rows ? a.topk_w[p] : 0.f;
-  }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&s_tmem, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kProdWarp && lane == 0) {
     prefetch_tmap(&a.wmap);
     prefetch_tmap(&a.bmap);
   }
@@ -201,162 +263,248 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   fence_after_sync();
   const uint32_t tmem = s_tmem;
 
-  if (warp == 8) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      int armed_w[kStagesW] = {0}, armed_b[SB] = {0};
-      for (int kc = 0; kc < nK && !s_abort; ++kc) {
-        const int sw = kc % kStagesW;
-        if (!mbar_wait(&w_empty[sw], ((kc / kStagesW) & 1) ^ 1, &s_abort)) break;
-        mbar_arrive_expect_tx(&w_full[sw], nsub * WSUB);
-        ++armed_w[sw];
-        for (int g = 0; g < nsub; ++g) {
-          char* dst = sW + sw * WSTAGE + g * WSUB;
-          const int nb = g == 0 ? nbase0 : nbase1;
-          if (FMT == MOE_FMT_FP8_B128_W8A16) tma_load_2d(dst, &a.wmap, &w_full[sw], kc * kKC, e * a.N + nb);
-          else if (FMT == MOE_FMT_INT4_G128_W4A16) tma_load_2d(dst, &a.wmap, &w_full[sw], nb, e * (a.K / 8) + kc * 16);
-          else tma_load_2d(dst, &a.wmap, &w_full[sw], kc * (kKC / 2), e * a.N + nb);
+  // per-item geometry
+  auto item = [&](int wk, TileEntry& te, int& nb0, int& nb1, int& nsub) {
+    const int tile = wk / ncb, cb = wk % ncb;
+    te = a.tiles[1 + tile];
+    if (MODE == 0) {
+      nb0 = cb * 128;
+      nb1 = a.I + nb0;
+      nsub = 2;
+    } else {
+      nb0 = cb * 256;
+      nb1 = nb0 + 128;
+      nsub = (a.H - nb0) >= 256 ? 2 : 1;
+    }
+  };
+
+  if (warp == kProdWarp) {
+    // ---------------- TMA producer (lane 0 issues; the warp holds the gather row indices) ----
+    int it = 0;
+    int armed_w[kStagesW] = {0}, armed_b[SB] = {0};
+    for (int wk = blockIdx.x; wk < nwork; wk += gridDim.x) {
+      TileEntry te;
+      int nb0, nb1, nsub;
+      item(wk, te, nb0, nb1, nsub);
+      int tk[TPL];
+#pragma unroll
+      for (int m = 0; m < TPL; ++m) {
+        const int j = lane + 32 * m;
+        tk[m] = (MODE == 0 && j < BN) ? a.perm[te.row0 + (j < te.rows ? j : te.rows - 1)] / a.k : 0;
+      }
+      bool ok = true;
+      for (int kc = 0; kc < nK; ++kc, ++it) {
+        const int sw = it % kStagesW, sb = it % SB;
+        if (lane == 0) {
+          ok = mbar_wait(&w_empty[sw], ((it / kStagesW) & 1) ^ 1, &s_abort);
+          if (ok) {
+            mbar_arrive_expect_tx(&w_full[sw], nsub * WSUB);
+            ++armed_w[sw];
+            for (int g = 0; g < nsub; ++g) {
+              char* dst = sW + sw * WSTAGE + g * WSUB;
+              const int nb = g == 0 ? nb0 : nb1;
+              if (FMT == MOE_FMT_FP8_B128_W8A16)
+                tma_load_2d(dst, &a.wmap, &w_full[sw], kc * kKC, te.expert * a.N + nb);
+              else if (FMT == MOE_FMT_INT4_G128_W4A16)
+                tma_load_2d(dst, &a.wmap, &w_full[sw], nb, te.expert * (a.K / 8) + kc * 16);
+              else
+                tma_load_2d(dst, &a.wmap, &w_full[sw], kc * (kKC / 2), te.expert * a.N + nb);
+            }
+            ok = mbar_wait(&b_empty[sb], ((it / SB) & 1) ^ 1, &s_abort);
+          }
+          if (ok) {
+            mbar_arrive_expect_tx(&b_full[sb], BSTAGE);
+            ++armed_b[sb];
+          }
         }
-        const int sb = kc % SB;
-        if (!mbar_wait(&b_empty[sb], ((kc / SB) & 1) ^ 1, &s_abort)) break;
-        mbar_arrive_expect_tx(&b_full[sb], BSTAGE);
-        ++armed_b[sb];
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
         char* bd = sB + sb * BSTAGE;
+        if (MODE == 0) {
 #pragma unroll
-        for (int at = 0; at < 2; ++at) {
-          if (MODE == 0) {
-            for (int j = 0; j < BN; j += 4)
-              tma_gather4(bd + at * BN * 128 + j * 128, &a.bmap, &b_full[sb], kc * kKC + at * 64, s_tok[j],
-                          s_tok[j + 1], s_tok[j + 2], s_tok[j + 3]);
-          } else {
-            tma_load_2d(bd + at * BN * 128, &a.bmap, &b_full[sb], kc * kKC + at * 64, row0);
+          for (int j = 0; j < BN; j += 4) {
+            const int r0 = __shfl_sync(0xffffffffu, tk[j >> 5], (j & 31) + 0);
+            const int r1 = __shfl_sync(0xffffffffu, tk[j >> 5], (j & 31) + 1);
+            const int r2 = __shfl_sync(0xffffffffu, tk[j >> 5], (j & 31) + 2);
+            const int r3 = __shfl_sync(0xffffffffu, tk[j >> 5], (j & 31) + 3);
+            if (lane == 0) {
+              tma_gather4(bd + j * 128, &a.bmap, &b_full[sb], kc * kKC, r0, r1, r2, r3);
+              tma_gather4(bd + BN * 128 + j * 128, &a.bmap, &b_full[sb], kc * kKC + 64, r0, r1, r2, r3);
+            }
           }
+        } else if (lane == 0) {
+          tma_load_2d(bd, &a.bmap, &b_full[sb], kc * kKC, te.row0);
+          tma_load_2d(bd + BN * 128, &a.bmap, &b_full[sb], kc * kKC + 64, te.row0);
         }
       }
-      if (s_abort) {  // let every issued copy land before the CTA's shared memory goes away
-        volatile int no_abort = 0;
-        for (int i = 0; i < kStagesW; ++i)
-          if (armed_w[i]) mbar_wait(&w_full[i], (armed_w[i] - 1) & 1, &no_abort);
-        for (int i = 0; i < SB; ++i)
-          if (armed_b[i]) mbar_wait(&b_full[i], (armed_b[i] - 1) & 1, &no_abort);
-      }
+      if (!ok) break;
     }
-  } else if (warp == 9) {
+    if (lane == 0 && s_abort) {  // let every issued copy land before shared memory goes away
+      volatile int no_abort = 0;
+      for (int i = 0; i < kStagesW; ++i)
+        if (armed_w[i]) mbar_wait(&w_full[i], (armed_w[i] - 1) & 1, &no_abort);
+      for (int i = 0; i < SB; ++i)
+        if (armed_b[i]) mbar_wait(&b_full[i], (armed_b[i] - 1) & 1, &no_abort);
+    }
+  } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, BN);
-      for (int kc = 0; kc < nK && !s_abort; ++kc) {
-        const int sa = kc % kStagesA, sb = kc % SB;
-        if (!mbar_wait(&a_full[sa], (kc / kStagesA) & 1, &s_abort)) break;
-        if (!mbar_wait(&b_full[sb], (kc / SB) & 1, &s_abort)) break;
+    // The whole warp walks the loop and waits together (lane 0 issues): a lane left idling in a
+    // barrier wait would hold the diverged warp, and with it the issuing lane, asleep.
+    const uint32_t idesc = idesc_bf16_f32(128, BN);
+    int it = 0;
+    bool ok = true;
+    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x) {
+      TileEntry te;
+      int nb0, nb1, nsub;
+      item(wk, te, nb0, nb1, nsub);
+      for (int kc = 0; kc < nK; ++kc, ++it) {
+        const int sa = it % kStagesA, sb = it % SB;
+        ok = mbar_wait(&a_full[sa], (it / kStagesA) & 1, &s_abort) &&
+             mbar_wait(&b_full[sb], (it / SB) & 1, &s_abort);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
         fence_after_sync();
-        const uint32_t b0 = smem_u32(sB + sb * BSTAGE);
-        for (int g = 0; g < nsub; ++g)
+        if (lane == 0) {
+          const uint32_t b0 = smem_u32(sB + sb * BSTAGE);
+          for (int g = 0; g < nsub; ++g)
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t bdsc = sdesc_k_sw128(b0 + (ks >> 2) * BN * 128 + (ks & 3) * 32);
-            mma_f16_ts(tmem + g * BN, tmem + kACol + sa * 128 + g * 64 + ks * 8, bdsc, idesc, (kc | ks) != 0);
-          }
-        mma_commit(&a_empty[sa]);
-        mma_commit(&b_empty[sb]);
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint64_t bdsc = sdesc_k_sw128(b0 + (ks >> 2) * BN * 128 + (ks & 3) * 32);
+              mma_f16_ts(tmem + g * BN, tmem + kACol + sa * 128 + g * 64 + ks * 8, bdsc, idesc, (kc | ks) != 0);
+            }
+          mma_commit(&a_empty[sa]);
+          mma_commit(&b_empty[sb]);
+        }
+        __syncwarp();
       }
-      mma_commit(&acc_full);  // always committed, so the epilogue can drain even after an abort
+      if (ok && lane == 0) mma_commit(&acc_full);
+      __syncwarp();
     }
+    if (lane == 0) mma_commit(&drain);  // completes once every MMA issued by this thread has finished
+    __syncwarp();
   } else {
-    // ---------------- converters: packed weights -> bf16 A in TMEM ----------------
-    const int g = warp >> 2, q = warp & 3, r = q * 32 + lane;
-    const int nb = g == 0 ? nbase0 : nbase1;
-    if (g < nsub) {
-      for (int kc = 0; kc < nK && !s_abort; ++kc) {
-        const int sw = kc % kStagesW, sa = kc % kStagesA;
-        float sc = 1.f;
-        uint2 bs8 = make_uint2(0, 0);
+    // ---------------- converters (16 warps) and epilogue ----------------
+    const int g = (warp >> 2) & 1, kh = warp >> 3, q = warp & 3, r = q * 32 + lane;
+    int it = 0, nitem = 0;
+    bool ok = true;
+    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x, ++nitem) {
+      TileEntry te;
+      int nb0, nb1, nsub;
+      item(wk, te, nb0, nb1, nsub);
+      const int e = te.expert;
+      const bool active = g < nsub;
+      const int nb = g == 0 ? nb0 : nb1;
+      // per-chunk scales, fetched one chunk ahead so their latency hides behind a conversion
+      auto scale_of = [&](int kc) -> uint32_t {
+        if (!active) return 0u;
         if (FMT == MOE_FMT_FP8_B128_W8A16)
-          sc = ((const float*)a.wscale)[((size_t)e * (a.N / 128) + nb / 128) * (a.K / 128) + kc];
-        else if (FMT == MOE_FMT_INT4_G128_W4A16)
-          sc = __half2float(((const __half*)a.wscale)[((size_t)e * (a.K / 128) + kc) * a.N + nb + r]);
-        else
-          bs8 = *(const uint2*)((const uint8_t*)a.wscale + ((size_t)e * a.N + nb + r) * (a.K / 16) + kc * 8);
-        if (!mbar_wait(&w_full[sw], (kc / kStagesW) & 1, &s_abort)) break;
-        uint32_t v[64];
-        const char* sub = sW + sw * WSTAGE + g * WSUB;
-        if (FMT == MOE_FMT_FP8_B128_W8A16) conv_fp8(sub, r, sc, v);
-        else if (FMT == MOE_FMT_INT4_G128_W4A16) conv_int4(sub, r, sc, v);
-        else conv_nvfp4(sub, r, bs8, v);
+          return __float_as_uint(((const float*)a.wscale)[((size_t)e * (a.N / 128) + nb / 128) * (a.K / 128) + kc]);
+        if (FMT == MOE_FMT_INT4_G128_W4A16)
+          return __float_as_uint(__half2float(((const __half*)a.wscale)[((size_t)e * (a.K / 128) + kc) * a.N + nb + r]));
+        return *(const uint32_t*)((const uint8_t*)a.wscale + ((size_t)e * a.N + nb + r) * (a.K / 16) + kc * 8 + kh * 4);
+      };
+      uint32_t sc_next = scale_of(0);
+      for (int kc = 0; kc < nK; ++kc, ++it) {
+        const int sw = it % kStagesW, sa = it % kStagesA;
+        const uint32_t sc_raw = sc_next;
+        if (kc + 1 < nK) sc_next = scale_of(kc + 1);
+        const float sc = __uint_as_float(sc_raw);
+        const uint32_t bs4 = sc_raw;
+        ok = mbar_wait(&w_full[sw], (it / kStagesW) & 1, &s_abort);
+        if (!ok) break;
+        uint32_t v[32];
+        if (active) {
+          const char* sub = sW + sw * WSTAGE + g * WSUB;
+          if (FMT == MOE_FMT_FP8_B128_W8A16) conv_fp8(sub, r, kh, sc, v);
+          else if (FMT == MOE_FMT_INT4_G128_W4A16) conv_int4(sub, r, kh, sc, v);
+          else conv_nvfp4(sub, r, kh, bs4, v);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&w_empty[sw]);
-        if (!mbar_wait(&a_empty[sa], ((kc / kStagesA) & 1) ^ 1, &s_abort)) break;
+        ok = mbar_wait(&a_empty[sa], ((it / kStagesA) & 1) ^ 1, &s_abort);
+        if (!ok) break;
         fence_after_sync();
-        const uint32_t ta = taddr(tmem, q * 32, kACol + sa * 128 + g * 64);
-        tmem_st_32x32(ta, v);
-        tmem_st_32x32(ta + 32, v + 32);
-        tmem_st_wait();
+        if (active) {
+          tmem_st_32x32(taddr(tmem, q * 32, kACol + sa * 128 + g * 64 + kh * 32), v);
+          tmem_st_wait();
+        }
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[sa]);
       }
+      if (!ok) break;
+      // epilogue of this item
+      ok = mbar_wait(&acc_full, nitem & 1, &s_abort);
+      if (!ok) break;
+      fence_after_sync();
+      const float gs = FMT == MOE_FMT_NVFP4_W4A16 ? a.wgs[e] : 1.f;
+      if (MODE == 0) {
+        const int part = warp >> 2;  // 0..3: 16-column chunks part, part+4, ...
+        const int n = nb0 + r;
+        for (int c0 = part * 16; c0 < BN; c0 += 64) {
+          uint32_t G[16], U[16];
+          tmem_ld_32x16(taddr(tmem, q * 32, c0), G);
+          tmem_ld_32x16(taddr(tmem, q * 32, BN + c0), U);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            if (col < te.rows) {
+              float gv = __uint_as_float(G[j]), uv = __uint_as_float(U[j]);
+              if (FMT == MOE_FMT_NVFP4_W4A16) {
+                gv = __fdiv_rn(gv, gs);
+                uv = __fdiv_rn(uv, gs);
+              }
+              const float hv = gv / (1.0f + expf(-gv)) * uv;
+              a.h_out[(size_t)(te.row0 + col) * a.I + n] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+            }
+          }
+        }
+      } else if (active) {
+        const int c = nb + r;
+        for (int c0 = kh * 16; c0 < BN; c0 += 32) {
+          uint32_t Y[16];
+          tmem_ld_32x16(taddr(tmem, q * 32, g * BN + c0), Y);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            if (col < te.rows) {
+              const int p = a.perm[te.row0 + col];
+              float y = __uint_as_float(Y[j]);
+              if (FMT == MOE_FMT_NVFP4_W4A16) y = __fdiv_rn(y, gs);
+              atomicAdd(&a.out_acc[(size_t)(p / a.k) * a.H + c], a.topk_w[p] * y);
+            }
+          }
+        }
+      }
+      fence_before_sync();  // accumulator reads are ordered before the next item's MMAs
     }
   }
 
-  // ---------------- epilogue ----------------
   {
     volatile int no_abort = 0;
-    mbar_wait(&acc_full, 0, &no_abort);  // bounded; drains outstanding MMAs in every case
-  }
-  fence_after_sync();
-  if (warp < 8 && !s_abort) {
-    const int q = warp & 3, half = warp >> 2, r = q * 32 + lane;
-    const float gs = FMT == MOE_FMT_NVFP4_W4A16 ? a.wgs[e] : 1.f;
-    if (MODE == 0) {
-      const int cbeg = BN == 16 ? 0 : half * (BN / 2);
-      const int cend = BN == 16 ? (half == 0 ? 16 : 0) : cbeg + BN / 2;
-      const int n = nbase0 + r;
-      for (int c0 = cbeg; c0 < cend; c0 += 16) {
-        uint32_t G[16], U[16];
-        tmem_ld_32x16(taddr(tmem, q * 32, c0), G);
-        tmem_ld_32x16(taddr(tmem, q * 32, BN + c0), U);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int col = c0 + j;
-          if (col < rows) {
-            float gv = __uint_as_float(G[j]), uv = __uint_as_float(U[j]);
-            if (FMT == MOE_FMT_NVFP4_W4A16) {
-              gv = __fdiv_rn(gv, gs);
-              uv = __fdiv_rn(uv, gs);
-            }
-            const float hv = gv / (1.0f + expf(-gv)) * uv;
-            a.h_out[(size_t)(row0 + col) * a.I + n] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
-          }
-        }
-      }
-    } else if (half < nsub) {
-      const int c = (half == 0 ? nbase0 : nbase1) + r;
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t Y[16];
-        tmem_ld_32x16(taddr(tmem, q * 32, half * BN + c0), Y);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int col = c0 + j;
-          if (col < rows) {
-            float y = __uint_as_float(Y[j]);
-            if (FMT == MOE_FMT_NVFP4_W4A16) y = __fdiv_rn(y, gs);
-            atomicAdd(&a.out_acc[(size_t)s_tok[col] * a.H + c], s_w[col] * y);
-          }
-        }
-      }
-    }
+    mbar_wait(&drain, 0, &no_abort);  // bounded; every MMA of this CTA has completed
   }
   fence_before_sync();
   __syncthreads();
-  if (warp == 9) tmem_dealloc(tmem, kTmemCols);
+  fence_after_sync();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0 && s_abort) set_dev_error(a.err, kDevTimeout);
 }
 
 // ---------------------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------------------
+int num_sms() {
+  static int n[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!n[dev]) cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev);
+  return n[dev] > 0 ? n[dev] : 148;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -405,7 +553,8 @@ cudaError_t launch_one(const TcArgs& args, int grid_x, int grid_y, cudaStream_t 
     cudaFuncSetAttribute(tc_expert_gemm_kernel<FMT, MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     attr = true;
   }
-  tc_expert_gemm_kernel<FMT, MODE, BN><<<dim3(grid_x, grid_y), kThreads, smem, s>>>(args);
+  tc_expert_gemm_kernel<FMT, MODE, BN><<<dim3(grid_x * grid_y < num_sms() ? grid_x * grid_y : num_sms()), kThreads,
+                                          smem, s>>>(args);
   return cudaGetLastError();
 }
 

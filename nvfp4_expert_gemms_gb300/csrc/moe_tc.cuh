@@ -1,8 +1,8 @@
 // Blackwell (sm_103a) building blocks written as inline PTX: mbarriers with bounded waits,
 // TMA tensor loads, tensor-memory (TMEM) allocation / loads / stores, and tcgen05.mma.
 //
-// Every wait is bounded by the global nanosecond timer; a wait that runs out reports false and
-// the caller records MOE_ERR_DEVICE_TIMEOUT and unwinds, so no kernel can spin forever.
+// Every wait is bounded by the SM cycle counter (about one second); a wait that runs out reports
+// false and the caller records MOE_ERR_DEVICE_TIMEOUT and unwinds, so no kernel spins forever.
 #pragma once
 #include <cuda.h>
 #include <stdint.h>
@@ -10,15 +10,9 @@
 namespace moe {
 namespace tc {
 
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
+constexpr long long kWaitLimitCycles = 2000000000ll;  // about 1 s at the GB300 SM clock
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ unsigned long long now_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 // ---- mbarrier -------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -45,16 +39,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase with the given parity to complete; false after kWaitLimitNs or when another
-// thread of the CTA has raised *abort.
+// Wait for the phase with the given parity to complete; false after kWaitLimitCycles SM cycles
+// or when another thread of the CTA has raised *abort.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = now_ns();
+  const long long t0 = clock64();
   for (;;) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (now_ns() - t0 > kWaitLimitNs) {
+    if (clock64() - t0 > kWaitLimitCycles) {
       *abort = 1;
       return false;
     }
