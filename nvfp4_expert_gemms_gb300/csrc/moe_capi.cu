@@ -37,6 +37,8 @@ WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
   L.tiles = take(sizeof(TileEntry) * (size_t)(L.max_tiles + 1));
   L.h = take(2 * R * I);
   L.out_acc = take(4 * (size_t)T * H);
+  L.xmax = take(4 * (size_t)T);
+  L.hmax = take(4 * R);
   if (fmt == MOE_FMT_NVFP4_W4A4) {
     L.xq = take((size_t)T * H / 2);
     L.xs = take((size_t)T * H / 16);

@@ -1,0 +1,480 @@
+// FP8 W8A16 grouped GEMMs for decode-sized tiles (16 token rows per tile) on tcgen05 kind::f8f6f4.
+//
+// At decode the layer streams weights: each routed expert sees one or two tokens, so the kernel's
+// job is to move 4.7 MB of E4M3 codes per expert through the tensor cores at HBM speed.  Here the
+// packed weights (clef-omni-fp8, "What was quantized": E4M3 codes, one fp32 scale per 128x128
+// tile) go from HBM to shared memory by TMA and straight into the MMA as the B operand -- there is
+// no dequantization pass at all.  The activations become the A operand instead:
+//
+//   v = x * scale_inv(tile) * u_row          (u_row: a power of two putting max|v| <= 448)
+//   v = hi + lo,  hi = E4M3(v),  lo = E4M3(v - hi)
+//
+// A bf16 value has 8 significant bits; hi keeps the top 4 and the rounding residual v - hi has at
+// most 4 more, so hi + lo equals v exactly unless lo falls below the E4M3 subnormal step (elements
+// under ~1/1800 of the row maximum, whose products are then off by at most 2^-4 of themselves).
+// The hi and lo rows of each token are two N columns of one MMA (columns j and 16 + j), and the
+// epilogue adds them and divides by u_row.  The tile scale is folded in per 128-K chunk because
+// it changes along K; the fp32 product x * scale is rounded once, to about bf16 precision, by the
+// split (the same rounding a bf16 copy of the dequantized weights would carry).
+//
+//   D[weight row, act row] += A[weight row, k] * B[act row, k]   (M = 128 weight rows per
+//                            sub-tile, N = 32 activation rows, K = 32 per instruction, fp32)
+//
+// Warps (448 threads): 0-3 build the B chunk (split activations), 4-11 run the epilogue (warp w:
+// sub-tile (w-4)/4, TMEM lanes 32*(w%4).., one thread per weight row), 12 issues TMA, 13 owns
+// TMEM and issues the MMAs.  Persistent CTAs walk (row tile, column block) work items; two TMEM
+// accumulator buffers let the epilogue of one item overlap the MMAs of the next.
+#include <cudaTypedefs.h>
+
+#include "moe_formats.cuh"
+#include "moe_tc.cuh"
+
+namespace moe {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kRows = 16;        // token rows per tile (decode)
+constexpr int kKC = 128;         // K per chunk = one FP8 scale block
+constexpr int kStagesW = 5;      // weight chunks in flight
+constexpr int kStagesA = 2;      // split-activation chunks
+constexpr int kStagesX = 4;      // gathered activation chunks
+constexpr int kPrepWarps = 4, kEpiWarp0 = 4, kEpiWarps = 8, kProdWarp = 12, kMmaWarp = 13;
+constexpr int kThreads = 14 * 32;
+constexpr int kWSub = 128 * 128;       // one 128x128 E4M3 tile (128-byte swizzle)
+constexpr int kASub = 32 * 128;        // split-activation tile: 32 rows (hi, lo) x 128 K of E4M3
+constexpr int kXStage = kRows * 256;   // 16 rows x 128 K bf16 (two swizzle atoms)
+constexpr uint32_t kTmemCols = 128;    // two accumulator buffers x two sub-tiles x 32 columns
+constexpr size_t kSmem = 1024 + (size_t)kStagesW * 2 * kWSub + (size_t)kStagesA * 2 * kASub +
+                         (size_t)kStagesX * kXStage;
+
+struct Fp8Args {
+  CUtensorMap wmap;    // E4M3 codes [E*N, K]
+  CUtensorMap xmap;    // activations: x [T, H] (one-row box, gathered) or h [R, I] (16-row box)
+  const float* scale_inv;  // [E, N/128, K/128]
+  const float* rowmax;     // max |activation| per source row (x: per token, h: per permuted row)
+  const int32_t* perm;
+  const float* topk_w;
+  const TileEntry* tiles;
+  uint16_t* h_out;         // MODE 0 output [R, I] bf16
+  unsigned* h_rowmax;      // MODE 0: running max |h| per permuted row (fp32 bits)
+  float* out_acc;          // MODE 1 output [T, H] fp32
+  int* err;
+  int k, N, K, I, H;
+};
+
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);  // A, B = E4M3 (0)
+}
+
+__device__ __forceinline__ void mma_f8_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t v) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
+  return __half22float2(__half2(h));
+}
+
+// Largest power of two u with amax * smax * u <= 448 (1 when the row is all zeros).
+__device__ __forceinline__ float pow2_norm(float amax, float smax) {
+  const float m = amax * smax;
+  if (!(m > 0.f)) return 1.f;
+  int e;
+  frexpf(448.0f / m, &e);  // 448/m = f * 2^e, f in [0.5, 1); inf / denormal ranges clamp below
+  e = e - 1 < -126 ? -126 : (e - 1 > 126 ? 126 : e - 1);
+  return ldexpf(1.0f, e);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_constant__ Fp8Args a) {
+  extern __shared__ __align__(1024) char smem_raw[];
+  char* smem = (char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  char* sW = smem;
+  char* sA = sW + kStagesW * 2 * kWSub;
+  char* sX = sA + kStagesA * 2 * kASub;
+  __shared__ uint64_t w_full[kStagesW], w_empty[kStagesW], a_full[kStagesA], a_empty[kStagesA], x_full[kStagesX],
+      x_empty[kStagesX], acc_full[2], acc_empty[2], drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int ntiles = a.tiles[0].expert;
+  const int ncb = MODE == 0 ? a.I / 128 : (a.H + 255) / 256;
+  const int nwork = ntiles * ncb;
+  if ((int)blockIdx.x >= nwork) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nK = a.K / kKC;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStagesW; ++i) {
+      mbar_init(&w_full[i], 1);
+      mbar_init(&w_empty[i], 1);
+    }
+    for (int i = 0; i < kStagesA; ++i) {
+      mbar_init(&a_full[i], kPrepWarps);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < kStagesX; ++i) {
+      mbar_init(&x_full[i], 1);
+      mbar_init(&x_empty[i], kPrepWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpiWarps);
+    }
+    mbar_init(&drain, 1);
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProdWarp && lane == 0) {
+    prefetch_tmap(&a.wmap);
+    prefetch_tmap(&a.xmap);
+  }
+  fence_proxy_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = s_tmem;
+
+  auto item = [&](int wk, TileEntry& te, int& nb0, int& nb1, int& nsub) {
+    te = a.tiles[1 + wk / ncb];
+    const int cb = wk % ncb;
+    if (MODE == 0) {
+      nb0 = cb * 128;
+      nb1 = a.I + nb0;
+      nsub = 2;
+    } else {
+      nb0 = cb * 256;
+      nb1 = nb0 + 128;
+      nsub = (a.H - nb0) >= 256 ? 2 : 1;
+    }
+  };
+  auto scale_at = [&](const TileEntry& te, int nb, int kc) {
+    return a.scale_inv[((size_t)te.expert * (a.N / 128) + nb / 128) * (a.K / 128) + kc];
+  };
+  // The item's largest tile scale over both sub-tiles and all K chunks (one warp, no block sync),
+  // and the power-of-two normalizer of tile row j; builders and epilogue compute them alike.
+  auto item_smax = [&](const TileEntry& te, int nb0, int nb1, int nsub) {
+    float m = 0.f;
+    for (int i = lane; i < nsub * nK; i += 32) m = fmaxf(m, scale_at(te, i < nK ? nb0 : nb1, i % nK));
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    return m;
+  };
+  auto row_norm = [&](const TileEntry& te, int j, float smax) {
+    if (j >= te.rows) return 1.f;
+    const int src = MODE == 0 ? a.perm[te.row0 + j] / a.k : te.row0 + j;
+    return pow2_norm(a.rowmax[src], smax);
+  };
+
+  if (warp == kProdWarp) {
+    // ---------------- TMA producer ----------------
+    int it = 0;
+    bool ok = true;
+    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x) {
+      TileEntry te;
+      int nb0, nb1, nsub;
+      item(wk, te, nb0, nb1, nsub);
+      int tok = 0;
+      if (MODE == 0 && lane < kRows) tok = a.perm[te.row0 + (lane < te.rows ? lane : te.rows - 1)] / a.k;
+      for (int kc = 0; kc < nK; ++kc, ++it) {
+        const int sw = it % kStagesW, sx = it % kStagesX;
+        if (lane == 0) {
+          ok = mbar_wait(&w_empty[sw], ((it / kStagesW) & 1) ^ 1, &s_abort);
+          if (ok) {
+            mbar_arrive_expect_tx(&w_full[sw], nsub * kWSub);
+            tma_load_2d(sW + sw * 2 * kWSub, &a.wmap, &w_full[sw], kc * kKC, te.expert * a.N + nb0);
+            if (nsub == 2) tma_load_2d(sW + sw * 2 * kWSub + kWSub, &a.wmap, &w_full[sw], kc * kKC, te.expert * a.N + nb1);
+            ok = mbar_wait(&x_empty[sx], ((it / kStagesX) & 1) ^ 1, &s_abort);
+          }
+          if (ok) mbar_arrive_expect_tx(&x_full[sx], kXStage);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        char* xd = sX + sx * kXStage;
+        if (MODE == 0) {
+#pragma unroll
+          for (int j = 0; j < kRows; j += 4) {
+            const int r0 = __shfl_sync(0xffffffffu, tok, j), r1 = __shfl_sync(0xffffffffu, tok, j + 1);
+            const int r2 = __shfl_sync(0xffffffffu, tok, j + 2), r3 = __shfl_sync(0xffffffffu, tok, j + 3);
+            if (lane == 0) {
+              tma_gather4(xd + j * 128, &a.xmap, &x_full[sx], kc * kKC, r0, r1, r2, r3);
+              tma_gather4(xd + kRows * 128 + j * 128, &a.xmap, &x_full[sx], kc * kKC + 64, r0, r1, r2, r3);
+            }
+          }
+        } else if (lane == 0) {
+          tma_load_2d(xd, &a.xmap, &x_full[sx], kc * kKC, te.row0);
+          tma_load_2d(xd + kRows * 128, &a.xmap, &x_full[sx], kc * kKC + 64, te.row0);
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issuer (whole warp waits, lane 0 issues) ----------------
+    const uint32_t idesc = idesc_e4m3_f32(128, 32);
+    int it = 0, nitem = 0;
+    bool ok = true;
+    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x, ++nitem) {
+      TileEntry te;
+      int nb0, nb1, nsub;
+      item(wk, te, nb0, nb1, nsub);
+      const int ab = nitem & 1;
+      ok = mbar_wait(&acc_empty[ab], ((nitem >> 1) & 1) ^ 1, &s_abort);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      fence_after_sync();
+      for (int kc = 0; kc < nK; ++kc, ++it) {
+        const int sw = it % kStagesW, sa = it % kStagesA;
+        ok = mbar_wait(&w_full[sw], (it / kStagesW) & 1, &s_abort) &&
+             mbar_wait(&a_full[sa], (it / kStagesA) & 1, &s_abort);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        fence_after_sync();
+        if (lane == 0) {
+          for (int g = 0; g < nsub; ++g) {
+            const uint32_t wa = smem_u32(sW + sw * 2 * kWSub + g * kWSub), aa = smem_u32(sA + (sa * 2 + g) * kASub);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_f8_ss(tmem + ab * 64 + g * 32, sdesc_k_sw128(wa + ks * 32), sdesc_k_sw128(aa + ks * 32), idesc,
+                        (kc | ks) != 0);
+          }
+          mma_commit(&w_empty[sw]);
+          mma_commit(&a_empty[sa]);
+        }
+        __syncwarp();
+      }
+      if (ok && lane == 0) mma_commit(&acc_full[ab]);
+      __syncwarp();
+    }
+    if (lane == 0) mma_commit(&drain);
+    __syncwarp();
+  } else if (warp < kPrepWarps) {
+    // ---------------- A builders: split activations into E4M3 hi/lo rows ----------------
+    const int t = threadIdx.x, j = t >> 3, q = t & 7;  // row j, 16-element group q of the chunk
+    int it = 0, nitem = 0;
+    bool ok = true;
+    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x, ++nitem) {
+      TileEntry te;
+      int nb0, nb1, nsub;
+      item(wk, te, nb0, nb1, nsub);
+      const bool real = j < te.rows;
+      const float u = row_norm(te, j, item_smax(te, nb0, nb1, nsub));
+      float sc_next0 = scale_at(te, nb0, 0), sc_next1 = nsub == 2 ? scale_at(te, nb1, 0) : 0.f;
+      for (int kc = 0; kc < nK; ++kc, ++it) {
+        const int sx = it % kStagesX, sa = it % kStagesA;
+        const float f0 = sc_next0 * u, f1 = sc_next1 * u;
+        if (kc + 1 < nK) {
+          sc_next0 = scale_at(te, nb0, kc + 1);
+          if (nsub == 2) sc_next1 = scale_at(te, nb1, kc + 1);
+        }
+        ok = mbar_wait(&x_full[sx], (it / kStagesX) & 1, &s_abort) &&
+             mbar_wait(&a_empty[sa], ((it / kStagesA) & 1) ^ 1, &s_abort);
+        if (!ok) break;
+        // 16 bf16 of row j at K = 16q .. 16q+15: atom q/4, 16-byte chunks 2(q%4) and 2(q%4)+1
+        const char* xr = sX + sx * kXStage + (q >> 2) * (kRows * 128) + j * 128;
+        const int c0 = 2 * (q & 3);
+        const uint4 x0 = *(const uint4*)(xr + ((c0 ^ (j & 7)) * 16));
+        const uint4 x1 = *(const uint4*)(xr + (((c0 + 1) ^ (j & 7)) * 16));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&x_empty[sx]);
+        const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        for (int g = 0; g < nsub; ++g) {
+          const float f = g == 0 ? f0 : f1;
+          uint32_t hiw[4], low[4];
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            float v[4];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const uint32_t w = xw[p * 2 + h2];
+              v[h2 * 2] = real ? __uint_as_float(w << 16) * f : 0.f;
+              v[h2 * 2 + 1] = real ? __uint_as_float(w & 0xFFFF0000u) * f : 0.f;
+            }
+            const uint16_t h01 = e4m3x2(v[0], v[1]), h23 = e4m3x2(v[2], v[3]);
+            const float2 d01 = e4m3x2_to_f2(h01), d23 = e4m3x2_to_f2(h23);
+            const uint16_t l01 = e4m3x2(v[0] - d01.x, v[1] - d01.y), l23 = e4m3x2(v[2] - d23.x, v[3] - d23.y);
+            hiw[p] = (uint32_t)h01 | ((uint32_t)h23 << 16);
+            low[p] = (uint32_t)l01 | ((uint32_t)l23 << 16);
+          }
+          char* at = sA + (sa * 2 + g) * kASub;
+          *(uint4*)(at + j * 128 + ((q ^ (j & 7)) * 16)) = make_uint4(hiw[0], hiw[1], hiw[2], hiw[3]);
+          const int jl = kRows + j;
+          *(uint4*)(at + jl * 128 + ((q ^ (jl & 7)) * 16)) = make_uint4(low[0], low[1], low[2], low[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[sa]);
+      }
+    }
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
+    // ---------------- epilogue: thread = weight row, columns = activation rows ----------------
+    const int g = (warp - kEpiWarp0) >> 2, q = warp & 3, r = q * 32 + lane;
+    int nitem = 0;
+    bool ok = true;
+    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x, ++nitem) {
+      TileEntry te;
+      int nb0, nb1, nsub;
+      item(wk, te, nb0, nb1, nsub);
+      const int ab = nitem & 1;
+      ok = mbar_wait(&acc_full[ab], (nitem >> 1) & 1, &s_abort);
+      if (!ok) break;
+      fence_after_sync();
+      // normalizers of the tile's rows: lane j < 16 computes row j's, then broadcast
+      const float smax = item_smax(te, nb0, nb1, nsub);
+      const float u_l = row_norm(te, lane & 15, smax);
+      if (MODE == 0) {
+        if (g == 0) {  // sub-tile 0 threads own gate row r and up row r of the column block
+          uint32_t G[32], U[32];
+          tmem_ld_32x16(taddr(tmem, q * 32, ab * 64), G);
+          tmem_ld_32x16(taddr(tmem, q * 32, ab * 64 + 16), G + 16);
+          tmem_ld_32x16(taddr(tmem, q * 32, ab * 64 + 32), U);
+          tmem_ld_32x16(taddr(tmem, q * 32, ab * 64 + 48), U + 16);
+          tmem_ld_wait();
+          const int n = nb0 + r;
+#pragma unroll
+          for (int j = 0; j < kRows; ++j) {
+            const float inv_u = 1.0f / __shfl_sync(0xffffffffu, u_l, j);  // exact: a power of two
+            if (j < te.rows) {
+              const float gv = (__uint_as_float(G[j]) + __uint_as_float(G[16 + j])) * inv_u;
+              const float uv = (__uint_as_float(U[j]) + __uint_as_float(U[16 + j])) * inv_u;
+              const __nv_bfloat16 hb = __float2bfloat16_rn(gv * __frcp_rn(1.0f + __expf(-gv)) * uv);
+              a.h_out[(size_t)(te.row0 + j) * a.I + n] = __bfloat16_as_ushort(hb);
+              float m = fabsf(__bfloat162float(hb));
+              for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+              if (lane == 0) atomicMax(&a.h_rowmax[te.row0 + j], __float_as_uint(m));
+            }
+          }
+        }
+      } else if (g < nsub) {
+        uint32_t Y[32];
+        tmem_ld_32x16(taddr(tmem, q * 32, ab * 64 + g * 32), Y);
+        tmem_ld_32x16(taddr(tmem, q * 32, ab * 64 + g * 32 + 16), Y + 16);
+        tmem_ld_wait();
+        const int c = (g == 0 ? nb0 : nb1) + r;
+        int p_l = 0;
+        float w_l = 0.f;
+        if (lane < te.rows && lane < kRows) {
+          p_l = a.perm[te.row0 + lane];
+          w_l = a.topk_w[p_l];
+        }
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+          const float inv_u = 1.0f / __shfl_sync(0xffffffffu, u_l, j);
+          const int p = __shfl_sync(0xffffffffu, p_l, j);
+          const float w = __shfl_sync(0xffffffffu, w_l, j);
+          if (j < te.rows) {
+            const float y = (__uint_as_float(Y[j]) + __uint_as_float(Y[16 + j])) * inv_u * w;
+            atomicAdd(&a.out_acc[(size_t)(p / a.k) * a.H + c], y);
+          }
+        }
+      }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
+    }
+  }
+
+  {
+    volatile int no_abort = 0;
+    mbar_wait(&drain, 0, &no_abort);  // bounded; every MMA of this CTA has completed
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0 && s_abort) set_dev_error(a.err, kDevTimeout);
+}
+
+// max |x| of each bf16 row (warp per row)
+__global__ void __launch_bounds__(256) row_absmax_kernel(const uint16_t* __restrict__ x, int rows, int K,
+                                                         float* __restrict__ out) {
+  const int lane = threadIdx.x & 31, r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  float m = 0.f;
+  for (int c = lane * 8; c < K; c += 256) {
+    const uint4 v = *(const uint4*)(x + (size_t)r * K + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+  }
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane == 0) out[r] = m;
+}
+
+}  // namespace
+
+
+int fp8dec_row_block() { return kRows; }
+
+cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,
+                                  int k, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s) {
+  const int E = d.E, H = d.H, I = d.I;
+  const size_t R = (size_t)T * k;
+  const MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(fp8dec_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    cudaFuncSetAttribute(fp8dec_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    attr = true;
+  }
+  Fp8Args a;
+  memset(&a, 0, sizeof(a));
+  a.perm = (const int32_t*)(ws + L.perm);
+  a.topk_w = (const float*)(ws + L.topk_w);
+  a.tiles = (const TileEntry*)(ws + L.tiles);
+  a.h_out = (uint16_t*)(ws + L.h);
+  a.h_rowmax = (unsigned*)(ws + L.hmax);
+  a.out_acc = (float*)(ws + L.out_acc);
+  a.err = (int*)(ws + L.err);
+  a.k = k;
+  a.I = I;
+  a.H = H;
+  const int sms = tc_num_sms();
+  const int max_tiles = (int)(R / kRows + (R < (size_t)E ? R : (size_t)E) + 1);
+
+  row_absmax_kernel<<<(T + 7) / 8, 256, 0, s>>>((const uint16_t*)x, T, H, (float*)(ws + L.xmax));
+  cudaMemsetAsync(ws + L.hmax, 0, sizeof(unsigned) * R, s);
+
+  if (!tc_make_map(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, gu.a, H, (uint64_t)E * 2 * I, H, 128, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc_make_map(&a.xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, H, (uint64_t)T, (uint64_t)H * 2, 64, 1,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  a.scale_inv = (const float*)gu.b;
+  a.rowmax = (const float*)(ws + L.xmax);
+  a.N = 2 * I;
+  a.K = H;
+  int grid = max_tiles * (I / 128);
+  if (ev.start[0]) cudaEventRecord(ev.start[0], s);
+  fp8dec_kernel<0><<<grid < sms ? grid : sms, kThreads, kSmem, s>>>(a);
+  if (ev.stop[0]) cudaEventRecord(ev.stop[0], s);
+
+  if (!tc_make_map(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, dn.a, I, (uint64_t)E * H, I, 128, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc_make_map(&a.xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws + L.h, I, (uint64_t)R, (uint64_t)I * 2, 64, kRows,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  a.scale_inv = (const float*)dn.b;
+  a.rowmax = (const float*)(ws + L.hmax);
+  a.N = H;
+  a.K = I;
+  grid = max_tiles * ((H + 255) / 256);
+  if (ev.start[1]) cudaEventRecord(ev.start[1], s);
+  fp8dec_kernel<1><<<grid < sms ? grid : sms, kThreads, kSmem, s>>>(a);
+  if (ev.stop[1]) cudaEventRecord(ev.stop[1], s);
+  note_launches(3);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

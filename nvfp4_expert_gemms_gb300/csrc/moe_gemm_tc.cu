@@ -577,6 +577,12 @@ cudaError_t launch_fmt(int fmt, int bn, const TcArgs& args, int gx, int gy, cuda
 
 }  // namespace
 
+bool tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1, uint64_t pitch,
+                 uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw) {
+  return make_map(m, dt, base, d0, d1, pitch, b0, b1, sw);
+}
+int tc_num_sms() { return num_sms(); }
+
 // Token rows per GEMM tile: the next power of two >= the mean rows per active expert, 16..128.
 int tc_row_block(int T, int k, int E) {
   const long R = (long)T * k;

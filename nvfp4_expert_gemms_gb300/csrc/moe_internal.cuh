@@ -3,6 +3,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -65,6 +66,7 @@ struct TileEntry {
 struct WsLayout {
   size_t err, topk_idx, topk_w, blkcnt, blkbase, offsets, perm, inv, tiles;
   size_t h, out_acc, xq, xs, xg, hq, hs, hg;
+  size_t xmax, hmax;  // per-row max |activation| (FP8 decode path)
   size_t x_stage, lg_stage, out_stage;
   size_t total;
   int nb;         // routing blocks
@@ -94,6 +96,13 @@ void note_launches(int n);
 int simt_row_block();
 // Tensor-core path (FP8 W8A16, INT4 W4A16, NVFP4 W4A16): row block per tile, and the two GEMMs.
 int tc_row_block(int T, int k, int E);
+bool tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1, uint64_t pitch,
+                 uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw);
+int tc_num_sms();
+// FP8 decode path (16-row tiles, weights straight into kind::f8f6f4 MMAs).
+int fp8dec_row_block();
+cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,
+                                  int k, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);
 cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
                               int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);
 
