@@ -51,6 +51,7 @@ def parse_args():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-sweep", action="store_true")
+    p.add_argument("--no-graph", action="store_true", help="launch layer by layer instead of replaying a CUDA graph")
     return p.parse_args()
 
 
@@ -242,19 +243,33 @@ def run_ours(args, c, rank, world, local_rank):
         for l in range(L):
             if timed_events is not None:
                 M.moe_time_next_step(0, *timed_events[l])
-            M.moe_layer_forward(x, lg[l], layers[l].desc, layers[l].packed, k, outs[l], ws, stream)
+            M.moe_layer_forward(x, lg[l], layers[l].desc, layers[l].packed, k, outs[l], ws)
 
+    def as_runner(fn):
+        """The step as a CUDA graph (captured after an eager warm-up call) or as eager launches.
+        Returns (run, kernels per step)."""
+        fn()  # eager call: one-time set-up (function attributes) happens outside any capture
+        torch.cuda.synchronize()
+        n0 = M.moe_kernel_launch_count()
+        if args.no_graph:
+            fn()
+            torch.cuda.synchronize()
+            return fn, M.moe_kernel_launch_count() - n0
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g.replay, M.moe_kernel_launch_count() - n0
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+    for a_, b_ in ev:  # torch creates the CUDA event on first record; the library re-records it
+        a_.record()
+        b_.record()
+    run, launches_per_step = as_runner(lambda: step(ev))
     for _ in range(args.warmup):
-        step()
+        run()
     torch.cuda.synchronize()
     assert M.moe_get_device_error(ws) == 0, "device error flag set during warm-up"
 
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
-          for _ in range(args.steps)]
-    for pairs in ev:  # torch creates the CUDA event on first record; the library re-records it
-        for a, b in pairs:
-            a.record(stream)
-            b.record(stream)
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     uuid = getattr(torch.cuda.get_device_properties(local_rank), "uuid", None)
     clocks = Clocks(f"GPU-{uuid}" if uuid is not None else local_rank)
@@ -262,18 +277,18 @@ def run_ours(args, c, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    n0 = M.moe_kernel_launch_count()
-    t_start.record(stream)
+    t_start.record()
     for s in range(args.steps):
-        step(ev[s])
-    t_stop.record(stream)
+        run()
+    t_stop.record()
     torch.cuda.synchronize()
-    n_launch = M.moe_kernel_launch_count() - n0
+    n_launch = launches_per_step * args.steps
     clk = clocks.stop()
+    assert M.moe_get_device_error(ws) == 0, "device error flag set during the timed steps"
     if world > 1:
         torch.distributed.barrier()
     ms_total = t_start.elapsed_time(t_stop)
-    gu_ms = [ev[s][l][0].elapsed_time(ev[s][l][1]) for s in range(args.steps) for l in range(L)]
+    gu_ms = [ev[l][0].elapsed_time(ev[l][1]) for l in range(L)]  # the last timed step's launches
     mt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
     if world > 1:
         torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
@@ -295,7 +310,7 @@ def run_ours(args, c, rank, world, local_rank):
                 "frac": round(achieved / peak, 4)}
     roof.update({"traffic": recorded_traffic(fmt, T), "kernel": "grouped gate/up GEMM",
                  "launch_ms": round(gu_avg_s * 1e3, 4), "peak_source": peak_src,
-                 "step_fraction": round(sum(gu_ms) / ms_total, 3)})
+                 "step_fraction": round(sum(gu_ms) / ms_step, 3)})
     layer_s = ms_step / 1e3 / L
     whole = {"hbm_gbs": round(statistics.mean(layer_bytes) / layer_s / 1e9, 1),
              "tflops": round(flops_layer / layer_s / 1e12, 2),
@@ -312,16 +327,17 @@ def run_ours(args, c, rank, world, local_rank):
 
     def step_host():
         for l in range(L):
-            M.moe_layer_forward_host(x_h, lg_h[l], layers[l].desc, layers[l].packed, k, out_h[l], ws_io, stream)
+            M.moe_layer_forward_host(x_h, lg_h[l], layers[l].desc, layers[l].packed, k, out_h[l], ws_io)
 
+    run_host, _ = as_runner(step_host)
     for _ in range(args.warmup):
-        step_host()
+        run_host()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step_host()
+        run_host()
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / args.steps
     me = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
@@ -329,7 +345,7 @@ def run_ours(args, c, rank, world, local_rank):
         torch.distributed.all_reduce(me, op=torch.distributed.ReduceOp.MAX)
     e2e = {"value": round(world * T * L / float(me.item()), 1), "unit": "tokens/s",
            "h2d_bytes_per_step": L * (x_b + lg_b), "d2h_bytes_per_step": L * out_b,
-           "api": "moe_layer_forward_host (pinned host buffers)"}
+           "api": "moe_layer_forward_host (pinned host buffers)" + ("" if args.no_graph else ", CUDA graph")}
 
     sweep = None
     if not args.no_sweep and rank == 0 and len(synth.CONFIGS[args.config]["T"]) > 1:
@@ -341,14 +357,15 @@ def run_ours(args, c, rank, world, local_rank):
             xs = x[:Ts].contiguous()
             lgs = [lg[l, :Ts].contiguous() for l in range(L)]
             wss = torch.empty(M.moe_workspace_size(layers[0].desc, Ts, k), dtype=torch.uint8, device=dev)
-            for it in range(2 + 3):
-                if it == 2:
-                    torch.cuda.synchronize()
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                for l in range(L):
-                    M.moe_layer_forward(xs, lgs[l], layers[l].desc, layers[l].packed, k, outs[l, :Ts], wss, stream)
-            b.record(stream)
+            run_s, _ = as_runner(lambda: [M.moe_layer_forward(xs, lgs[l], layers[l].desc, layers[l].packed, k,
+                                                              outs[l, :Ts], wss) for l in range(L)])
+            for _ in range(2):
+                run_s()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(3):
+                run_s()
+            b.record()
             torch.cuda.synchronize()
             sweep[str(Ts)] = round(Ts * L / (a.elapsed_time(b) / 3 / 1e3), 1)
 
@@ -368,7 +385,8 @@ def main():
             "config": {"workload": describe(c), "format": c["fmt"], "tokens": c["T"], "layers": c["L"],
                        "hidden": c["H"], "intermediate": c["I"], "experts": c["E"], "top_k": c["k"],
                        "l2": "inputs larger than L2: each step streams the distinct weights of all layers",
-                       "parallelism": f"replicas x{world}"}}
+                       "parallelism": f"replicas x{world}",
+                       "launch": "eager" if args.no_graph else "CUDA graph of the whole step (replayed)"}}
 
     if args.impl == "reference":
         if rank != 0:

@@ -96,7 +96,17 @@ static moe_status_t forward_checked(const void* x, const float* logits, int T, c
   if (dv != MOE_OK) return dv;
   char* w = (char*)ws;
   const int rb = d->fmt == MOE_FMT_NVFP4_W4A4 ? simt_row_block() : tc_row_block(T, k, d->E);
-  if (launch_route(logits, T, d->E, k, rb, L, w, s) != cudaSuccess) return MOE_ERR_CUDA;
+  RoutePrelude pre;
+  pre.zero_f32 = (float*)(w + L.out_acc);
+  pre.n_f32 = (size_t)T * d->H;
+  if (d->fmt == MOE_FMT_FP8_B128_W8A16 && rb == fp8dec_row_block()) {  // FP8 decode path needs row maxima
+    pre.zero_u32 = (unsigned*)(w + L.hmax);
+    pre.n_u32 = (size_t)T * k;
+    pre.x = (const uint16_t*)x;
+    pre.H = d->H;
+    pre.xmax = (float*)(w + L.xmax);
+  }
+  if (launch_route(logits, T, d->E, k, rb, L, w, pre, s) != cudaSuccess) return MOE_ERR_CUDA;
   const StepEvents ev = g_pending_events;
   g_pending_events = StepEvents();
   return cuda_status(launch_experts(*d, (const char*)packed, (const __nv_bfloat16*)x, T, k, rb, L, w,
@@ -254,7 +264,7 @@ moe_status_t moe_debug_route(const float* logits, int T, int E, int top_k, int32
   if (dv != MOE_OK) return dv;
   cudaStream_t s = (cudaStream_t)stream;
   char* w = (char*)workspace;
-  if (launch_route(logits, T, E, top_k, simt_row_block(), L, w, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_route(logits, T, E, top_k, simt_row_block(), L, w, RoutePrelude(), s) != cudaSuccess) return MOE_ERR_CUDA;
   const size_t R = (size_t)T * top_k;
   cudaError_t e = cudaMemcpyAsync(offsets, w + L.offsets, 4 * (size_t)(E + 1), cudaMemcpyDeviceToDevice, s);
   if (R) {

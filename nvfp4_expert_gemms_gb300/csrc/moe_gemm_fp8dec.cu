@@ -395,23 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
   if (threadIdx.x == 0 && s_abort) set_dev_error(a.err, kDevTimeout);
 }
 
-// max |x| of each bf16 row (warp per row)
-__global__ void __launch_bounds__(256) row_absmax_kernel(const uint16_t* __restrict__ x, int rows, int K,
-                                                         float* __restrict__ out) {
-  const int lane = threadIdx.x & 31, r = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (r >= rows) return;
-  float m = 0.f;
-  for (int c = lane * 8; c < K; c += 256) {
-    const uint4 v = *(const uint4*)(x + (size_t)r * K + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
-  }
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  if (lane == 0) out[r] = m;
-}
-
 }  // namespace
 
 
@@ -443,8 +426,7 @@ cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed
   const int sms = tc_num_sms();
   const int max_tiles = (int)(R / kRows + (R < (size_t)E ? R : (size_t)E) + 1);
 
-  row_absmax_kernel<<<(T + 7) / 8, 256, 0, s>>>((const uint16_t*)x, T, H, (float*)(ws + L.xmax));
-  cudaMemsetAsync(ws + L.hmax, 0, sizeof(unsigned) * R, s);
+  // x row maxima and the zeroed h row maxima come from the routing launch (RoutePrelude)
 
   if (!tc_make_map(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, gu.a, H, (uint64_t)E * 2 * I, H, 128, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -456,9 +438,9 @@ cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed
   a.N = 2 * I;
   a.K = H;
   int grid = max_tiles * (I / 128);
-  if (ev.start[0]) cudaEventRecord(ev.start[0], s);
+  record_event(ev.start[0], s);
   fp8dec_kernel<0><<<grid < sms ? grid : sms, kThreads, kSmem, s>>>(a);
-  if (ev.stop[0]) cudaEventRecord(ev.stop[0], s);
+  record_event(ev.stop[0], s);
 
   if (!tc_make_map(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, dn.a, I, (uint64_t)E * H, I, 128, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -470,10 +452,10 @@ cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed
   a.N = H;
   a.K = I;
   grid = max_tiles * ((H + 255) / 256);
-  if (ev.start[1]) cudaEventRecord(ev.start[1], s);
+  record_event(ev.start[1], s);
   fp8dec_kernel<1><<<grid < sms ? grid : sms, kThreads, kSmem, s>>>(a);
-  if (ev.stop[1]) cudaEventRecord(ev.stop[1], s);
-  note_launches(3);
+  record_event(ev.stop[1], s);
+  note_launches(2);
   return cudaGetLastError();
 }
 

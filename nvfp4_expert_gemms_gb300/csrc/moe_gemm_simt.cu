@@ -160,19 +160,19 @@ cudaError_t run_simt(const moe_packed_desc_t& d, const char* packed, const __nv_
   const size_t smem_gu = sizeof(float) * kSimtRB * H, smem_d = sizeof(float) * kSimtRB * I;
   cudaFuncSetAttribute(gateup_simt_kernel<FMT, A4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_gu);
   cudaFuncSetAttribute(down_simt_kernel<FMT, A4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_d);
-  if (ev.start[0]) cudaEventRecord(ev.start[0], s);
+  record_event(ev.start[0], s);
   gateup_simt_kernel<FMT, A4><<<dim3(L.max_tiles, I / kSimtNB), 128, smem_gu, s>>>(
       gu, (const uint16_t*)x, (const uint8_t*)(ws + L.xq), (const uint8_t*)(ws + L.xs),
       (const float*)(ws + L.xg), perm, k, I, tiles, (uint16_t*)(ws + L.h));
-  if (ev.stop[0]) cudaEventRecord(ev.stop[0], s);
+  record_event(ev.stop[0], s);
   if (A4)
     launch_quant_rows((const __nv_bfloat16*)(ws + L.h), T * k, I, (uint8_t*)(ws + L.hq), (uint8_t*)(ws + L.hs),
                       (float*)(ws + L.hg), s);
-  if (ev.start[1]) cudaEventRecord(ev.start[1], s);
+  record_event(ev.start[1], s);
   down_simt_kernel<FMT, A4><<<dim3(L.max_tiles, H / kSimtNB), 128, smem_d, s>>>(
       dn, (const uint16_t*)(ws + L.h), (const uint8_t*)(ws + L.hq), (const uint8_t*)(ws + L.hs),
       (const float*)(ws + L.hg), perm, (const float*)(ws + L.topk_w), k, tiles, (float*)(ws + L.out_acc));
-  if (ev.stop[1]) cudaEventRecord(ev.stop[1], s);
+  record_event(ev.stop[1], s);
   note_launches(2);
   return cudaGetLastError();
 }
@@ -183,8 +183,7 @@ cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const
                            int row_block, const WsLayout& L, char* ws, __nv_bfloat16* out, const StepEvents& ev,
                            cudaStream_t s) {
   const size_t n_out = (size_t)T * d.H;
-  if (T == 0) return cudaGetLastError();
-  cudaMemsetAsync(ws + L.out_acc, 0, sizeof(float) * n_out, s);
+  if (T == 0) return cudaGetLastError();  // the routing launch has zeroed the fp32 accumulator
   cudaError_t e;
   if (d.fmt == MOE_FMT_NVFP4_W4A4) {
     launch_quant_rows(x, T, d.H, (uint8_t*)(ws + L.xq), (uint8_t*)(ws + L.xs), (float*)(ws + L.xg), s);

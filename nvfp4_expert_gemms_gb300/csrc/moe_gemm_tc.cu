@@ -620,9 +620,9 @@ cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, co
   a.wgs = gu.gs;
   a.N = 2 * I;
   a.K = H;
-  if (ev.start[0]) cudaEventRecord(ev.start[0], s);
+  record_event(ev.start[0], s);
   cudaError_t err = launch_fmt<0>(d.fmt, bn, a, gx, I / 128, s);
-  if (ev.stop[0]) cudaEventRecord(ev.stop[0], s);
+  record_event(ev.stop[0], s);
   if (err != cudaSuccess) return err;
 
   // down: A = [H, I] weights, B = rows of h (already in permuted order)
@@ -634,9 +634,9 @@ cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, co
   a.wgs = dn.gs;
   a.N = H;
   a.K = I;
-  if (ev.start[1]) cudaEventRecord(ev.start[1], s);
+  record_event(ev.start[1], s);
   err = launch_fmt<1>(d.fmt, bn, a, gx, (H + 255) / 256, s);
-  if (ev.stop[1]) cudaEventRecord(ev.stop[1], s);
+  record_event(ev.stop[1], s);
   note_launches(2);
   return err;
 }

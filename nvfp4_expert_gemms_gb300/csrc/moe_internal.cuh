@@ -76,8 +76,19 @@ struct WsLayout {
 WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io);
 
 // ---- launches (each returns cudaGetLastError() after enqueueing) -------------------------
+// Work folded into the first routing launch: zero two accumulators and (optionally) record the
+// max |x| of every activation row.
+struct RoutePrelude {
+  float* zero_f32 = nullptr;
+  size_t n_f32 = 0;  // multiple of 4
+  unsigned* zero_u32 = nullptr;
+  size_t n_u32 = 0;
+  const uint16_t* x = nullptr;  // bf16 [T, H] or null
+  int H = 0;
+  float* xmax = nullptr;
+};
 cudaError_t launch_route(const float* logits, int T, int E, int k, int row_block, const WsLayout& L,
-                         char* ws, cudaStream_t s);
+                         char* ws, const RoutePrelude& pre, cudaStream_t s);
 cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, const __nv_bfloat16* wd,
                         char* packed, cudaStream_t s);
 cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e, int which, float* out,
@@ -91,6 +102,14 @@ struct StepEvents {
 cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,
                            int k, int row_block, const WsLayout& L, char* ws, __nv_bfloat16* out,
                            const StepEvents& ev, cudaStream_t s);
+// Record a timing event on s; under stream capture it becomes an event-record node of the graph.
+inline void record_event(cudaEvent_t ev, cudaStream_t s) {
+  if (!ev) return;
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &st);
+  if (st == cudaStreamCaptureStatusActive) cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else cudaEventRecord(ev, s);
+}
 // Running count of kernels enqueued by the library (moe_kernel_launch_count).
 void note_launches(int n);
 int simt_row_block();

@@ -28,16 +28,37 @@ __device__ __forceinline__ bool beats(float av, int ai, float bv, int bi) {
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int32_t* __restrict__ topk_idx,
                                                          float* __restrict__ topk_w,
-                                                         int32_t* __restrict__ blkcnt, int* err) {
+                                                         int32_t* __restrict__ blkcnt, int* err, RoutePrelude pre) {
   __shared__ int cnt[kMaxE];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  {  // zero the accumulators of this forward pass (grid-stride)
+    const size_t g = (size_t)blockIdx.x * blockDim.x + tid, stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = g; i < pre.n_f32 / 4; i += stride) ((float4*)pre.zero_f32)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (size_t i = g; i < pre.n_u32; i += stride) pre.zero_u32[i] = 0u;
+  }
   if (blockIdx.x == 0 && tid == 0) *err = kDevOk;  // each forward pass reports its own errors
   __syncthreads();
-  const int per_warp = kRouteTB / 8;
-  for (int it = 0; it < per_warp; ++it) {
-    const int t = blockIdx.x * kRouteTB + warp * per_warp + it;
-    if (t >= T) break;
+  const int t_end = min(T, (int)(blockIdx.x + 1) * kRouteTB);
+  for (int t = blockIdx.x * kRouteTB + warp; t < t_end; t += 8) {  // tokens round-robin over the warps
+    if (pre.x) {  // max |x| of the token's activation row; all loads issued before use
+      float m = 0.f;
+      const uint16_t* row = pre.x + (size_t)t * pre.H;
+      for (int c0 = lane * 8; c0 < pre.H; c0 += 256 * 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = c0 + u * 256 < pre.H ? *(const uint4*)(row + c0 + u * 256) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[i] << 16)), fabsf(__uint_as_float(w4[i] & 0xFFFF0000u))));
+        }
+      }
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      if (lane == 0) pre.xmax[t] = m;
+    }
     float v[kMaxE / 32];
 #pragma unroll
     for (int m = 0; m < kMaxE / 32; ++m) {
@@ -183,7 +204,7 @@ __global__ void __launch_bounds__(kRouteTB) route_scatter_kernel(const int32_t* 
 }  // namespace
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int row_block, const WsLayout& L, char* ws,
-                         cudaStream_t s) {
+                         const RoutePrelude& pre, cudaStream_t s) {
   int* err = (int*)(ws + L.err);
   int32_t* idx = (int32_t*)(ws + L.topk_idx);
   float* w = (float*)(ws + L.topk_w);
@@ -194,7 +215,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int row_block
   int32_t* inv = (int32_t*)(ws + L.inv);
   TileEntry* tiles = (TileEntry*)(ws + L.tiles);
   const int nb = L.nb;
-  if (T > 0) route_topk_kernel<<<nb, 256, 0, s>>>(logits, T, E, k, idx, w, blkcnt, err);
+  if (T > 0) route_topk_kernel<<<nb, 256, 0, s>>>(logits, T, E, k, idx, w, blkcnt, err, pre);
   else cudaMemsetAsync(err, 0, sizeof(int), s);
   route_scan_kernel<<<1, 1024, 0, s>>>(blkcnt, T > 0 ? nb : 0, E, row_block, L.max_tiles, off, blkbase, tiles,
                                        err);

@@ -90,7 +90,7 @@ extern "C" moe_status_t moe_route_noalloc(const float* logits, int T, int E, int
   const moe_status_t st = scratch_address(&w);
   if (st != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  if (launch_route(logits, T, E, top_k, kMinRowBlock, L, w, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_route(logits, T, E, top_k, kMinRowBlock, L, w, RoutePrelude(), s) != cudaSuccess) return MOE_ERR_CUDA;
   const size_t R = (size_t)T * top_k;
   cudaError_t e = cudaMemcpyAsync(offsets, w + L.offsets, 4 * (size_t)(E + 1), cudaMemcpyDeviceToDevice, s);
   if (R) {
