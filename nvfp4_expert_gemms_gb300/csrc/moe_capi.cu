@@ -95,7 +95,8 @@ static moe_status_t forward_checked(const void* x, const float* logits, int T, c
   const moe_status_t dv = device_ok();
   if (dv != MOE_OK) return dv;
   char* w = (char*)ws;
-  const int rb = d->fmt == MOE_FMT_NVFP4_W4A4 ? simt_row_block() : tc_row_block(T, k, d->E);
+  const int rb =
+      d->fmt == MOE_FMT_NVFP4_W4A4 && !fp4_supported(*d) ? simt_row_block() : tc_row_block(T, k, d->E);
   RoutePrelude pre;
   pre.zero_f32 = (float*)(w + L.out_acc);
   pre.n_f32 = (size_t)T * d->H;

@@ -196,3 +196,12 @@ def test_layer_full_size_sampled(orc, fmt, T, zipf, sample):
         toks = np.sort(g.choice(T, size=sample, replace=False)).astype(np.int32)
         got = got[toks]
     check_close(got, c.oracle(orc, tokens=toks), f"{fmt} T={T}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("T,E,k", [(64, 8, 2), (45, 16, 4), (300, 32, 8)])
+def test_layer_k256_shapes(orc, fmt, T, E, k):
+    """Hidden and intermediate sizes that are multiples of 256 (the block-scaled FP4 path's
+    K chunk): several tiles per expert, ragged tails, and row blocks from 16 to 128."""
+    c = Case(fmt, T, 512, 256, E, k, seed=T + E)
+    check_close(synth.bf16_bits_to_f32(c.run()), c.oracle(orc), f"{fmt} T={T}")
