@@ -13,12 +13,15 @@
 // memory by the four scale warps (16 bytes per row and chunk, fetched one chunk ahead), which
 // place both in tensor memory in the layout the MMA reads (per K = 64 step and 128 rows:
 // 4 columns; lane l, column j = the four scales of row l + 32 j, repeated in every lane quarter).
+// The gate/up GEMM's token rows are gathered by four warps of 16-byte cp.async copies into the
+// same swizzled layout a TMA tile load produces (a gather4 per four rows ran at about one
+// 128-byte row per 35 SM cycles and starved the MMA).
 //
 //   D[weight row, act row] += A[weight row, k] * B[act row, k]     M = 128, N = BN <= 128, K = 64
 //
-// Warps (448 threads): 0-3 stage scale factors, 4-11 run the epilogue (thread = weight row),
-// 12 issues TMA, 13 owns TMEM and issues the MMAs.  Persistent CTAs walk (row tile, column
-// block) work items.
+// Warps (576 threads): 0-3 stage scale factors, 4-11 run the epilogue (thread = weight row),
+// 12 issues TMA, 13 owns TMEM and issues the MMAs, 14-17 gather activation rows (gate/up).
+// Persistent CTAs walk (row tile, column block) work items.
 #include <cudaTypedefs.h>
 
 #include "moe_formats.cuh"
@@ -31,9 +34,11 @@ namespace {
 using namespace tc;
 
 constexpr int kKC = 256;                  // K per chunk: 128 bytes of codes per row
-constexpr int kStagesW = 4, kStagesX = 3, kStagesS = 2;
+constexpr int kStagesW = 4, kStagesX = 4, kStagesS = 2;
+constexpr int kLag = kStagesX - 2;        // gathered chunks a gather thread leaves in flight
 constexpr int kSfWarps = 4, kEpiWarp0 = 4, kEpiWarps = 8, kProdWarp = 12, kMmaWarp = 13;
-constexpr int kThreads = 14 * 32;
+constexpr int kGathWarp0 = 14, kGathWarps = 4;
+constexpr int kThreads = 18 * 32;
 constexpr int kWCodes = 128 * 128;        // 128 rows x 128 B (256 codes), 128-byte swizzle
 constexpr int kWSf = 128 * 16;            // 128 rows x 16 scales
 constexpr int kWStage = 2 * kWCodes + 2 * kWSf;
@@ -49,7 +54,8 @@ struct Fp4Cfg {
 
 struct Fp4Args {
   CUtensorMap wcode, wsf;   // weight codes [E*N, K/2], scales [E*N, K/16]
-  CUtensorMap xcode;        // activation codes: x rows (gathered) or h rows (tiles)
+  CUtensorMap xcode;        // activation codes of h rows (down GEMM tiles)
+  const uint8_t* xq;        // activation codes of x [T, K/2] (gate/up rows, gathered by token)
   const uint8_t* asf;       // activation block scales [rows, K/16] (x: per token, h: per permuted row)
   const float* wgs;         // weight global scales [E]
   const float* ags;         // activation global scales per source row
@@ -110,6 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
       s_empty[kStagesS], acc_full, acc_empty, drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  // per output column of the current item (double-buffered by item parity): the scale that
+  // undoes both global scales (times the routing weight for the down GEMM) and the token row
+  __shared__ float s_cs[2][BN];
+  __shared__ int s_ct[2][BN];
 
   const int ntiles = a.tiles[0].expert;
   const int ncb = MODE == 0 ? a.I / 128 : (a.H + 255) / 256;
@@ -124,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
       mbar_init(&w_empty[i], 1);
     }
     for (int i = 0; i < kStagesX; ++i) {
-      mbar_init(&x_full[i], 1);
+      mbar_init(&x_full[i], MODE == 0 ? kGathWarps : 1);
       mbar_init(&x_empty[i], 1);
     }
     for (int i = 0; i < kStagesS; ++i) {
@@ -166,20 +176,14 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   };
 
   if (warp == kProdWarp) {
-    // ---------------- TMA producer ----------------
-    constexpr int TPL = (BN + 31) / 32;
+    // ---------------- TMA producer (whole warp walks the loop, lane 0 issues) ----------------
     int it = 0;
     bool ok = true;
+    int armed_w[kStagesW] = {0}, armed_x[kStagesX] = {0};
     for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x) {
       TileEntry te;
       int nb0, nb1, nsub;
       item(wk, te, nb0, nb1, nsub);
-      int tk[TPL];
-#pragma unroll
-      for (int m = 0; m < TPL; ++m) {
-        const int j = lane + 32 * m;
-        tk[m] = (MODE == 0 && j < BN) ? a.perm[te.row0 + (j < te.rows ? j : te.rows - 1)] / a.k : 0;
-      }
       for (int kc = 0; kc < nK; ++kc, ++it) {
         const int sw = it % kStagesW, sx = it % kStagesX;
         if (lane == 0) {
@@ -187,32 +191,34 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
           if (ok) {
             char* ws = sW + sw * kWStage;
             mbar_arrive_expect_tx(&w_full[sw], nsub * (kWCodes + kWSf));
+            ++armed_w[sw];
             for (int g = 0; g < nsub; ++g) {
               const int row = te.expert * a.N + (g == 0 ? nb0 : nb1);
               tma_load_2d(ws + g * kWCodes, &a.wcode, &w_full[sw], kc * (kKC / 2), row);
               tma_load_2d(ws + 2 * kWCodes + g * kWSf, &a.wsf, &w_full[sw], kc * (kKC / 16), row);
             }
-            ok = mbar_wait(&x_empty[sx], ((it / kStagesX) & 1) ^ 1, &s_abort);
           }
-          if (ok) mbar_arrive_expect_tx(&x_full[sx], Fp4Cfg<BN>::kXBytes);
+          if (ok && MODE == 1) {
+            ok = mbar_wait(&x_empty[sx], ((it / kStagesX) & 1) ^ 1, &s_abort);
+            if (ok) {
+              mbar_arrive_expect_tx(&x_full[sx], Fp4Cfg<BN>::kXBytes);
+              ++armed_x[sx];
+              tma_load_2d(sX + sx * kXStage, &a.xcode, &x_full[sx], kc * (kKC / 2), te.row0);
+            }
+          }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        char* xs = sX + sx * kXStage;
-        if (MODE == 0) {
-#pragma unroll
-          for (int j = 0; j < BN; j += 4) {
-            const int r0 = __shfl_sync(0xffffffffu, tk[j >> 5], (j & 31) + 0);
-            const int r1 = __shfl_sync(0xffffffffu, tk[j >> 5], (j & 31) + 1);
-            const int r2 = __shfl_sync(0xffffffffu, tk[j >> 5], (j & 31) + 2);
-            const int r3 = __shfl_sync(0xffffffffu, tk[j >> 5], (j & 31) + 3);
-            if (lane == 0) tma_gather4(xs + j * 128, &a.xcode, &x_full[sx], kc * (kKC / 2), r0, r1, r2, r3);
-          }
-        } else if (lane == 0) {
-          tma_load_2d(xs, &a.xcode, &x_full[sx], kc * (kKC / 2), te.row0);
-        }
       }
     }
+    if (lane == 0 && s_abort) {  // let every issued copy land before shared memory goes away
+      volatile int no_abort = 0;
+      for (int i = 0; i < kStagesW; ++i)
+        if (armed_w[i]) mbar_wait(&w_full[i], (armed_w[i] - 1) & 1, &no_abort);
+      for (int i = 0; i < kStagesX; ++i)
+        if (armed_x[i]) mbar_wait(&x_full[i], (armed_x[i] - 1) & 1, &no_abort);
+    }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer (whole warp waits, lane 0 issues) ----------------
     const uint32_t idesc = idesc_nvf4(128, BN);
@@ -286,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
           cur[j] = nxt[j];
           if (kc + 1 < nK) nxt[j] = src[j] ? *(const uint4*)(src[j] + (kc + 1) * 16) : make_uint4(0, 0, 0, 0);
         }
-        ok = mbar_wait(&w_full[sw], (it / kStagesW) & 1, &s_abort) &&
-             mbar_wait(&s_empty[ss], ((it / kStagesS) & 1) ^ 1, &s_abort);
+        ok = __all_sync(0xffffffffu, mbar_wait(&w_full[sw], (it / kStagesW) & 1, &s_abort) &&
+                                         mbar_wait(&s_empty[ss], ((it / kStagesS) & 1) ^ 1, &s_abort));
         if (!ok) break;
         fence_after_sync();
         const uint32_t col = kSfCol + ss * kSfStageCols;
@@ -313,16 +319,37 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
     // ---------------- epilogue: thread = weight row, columns = activation rows ----------------
     const int ge = (warp - kEpiWarp0) >> 2, q = warp & 3, r = q * 32 + lane;
+    const int et = threadIdx.x - kEpiWarp0 * 32;
     int nitem = 0;
     bool ok = true;
-    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x, ++nitem) {
+    for (int wk = blockIdx.x; wk < nwork; wk += gridDim.x, ++nitem) {
       TileEntry te;
       int nb0, nb1, nsub;
       item(wk, te, nb0, nb1, nsub);
+      const int buf = nitem & 1;
+      // column table of this item, filled while its MMAs run
+      if (et < BN) {
+        float cs = 0.f;
+        int ct = 0;
+        if (et < te.rows) {
+          const float gw = a.wgs[te.expert];
+          if (MODE == 0) {
+            cs = 1.0f / (gw * a.ags[a.perm[te.row0 + et] / a.k]);
+          } else {
+            const int p = a.perm[te.row0 + et];
+            cs = a.topk_w[p] / (gw * a.ags[te.row0 + et]);
+            ct = p / a.k;
+          }
+        }
+        s_cs[buf][et] = cs;
+        s_ct[buf][et] = ct;
+      }
       ok = mbar_wait(&acc_full, nitem & 1, &s_abort);
+      // every epilogue thread takes the same branch: the table is complete and no one has aborted
+      ok = named_bar_and(1, kEpiWarps * 32, ok);
       if (!ok) break;
       fence_after_sync();
-      const float gw = a.wgs[te.expert];
+      const float* cs = s_cs[buf];
       if (MODE == 0) {
         // both warp groups own the same weight rows (gate in sub-tile 0, up in sub-tile 1) and
         // split the token columns
@@ -338,9 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
           for (int j = 0; j < 16; ++j) {
             const int col = c0 + j;
             if (col < te.rows) {
-              const int tok = a.perm[te.row0 + col] / a.k;
-              const float inv = 1.0f / (gw * a.ags[tok]);
-              const float gv = __uint_as_float(G[j]) * inv, uv = __uint_as_float(U[j]) * inv;
+              const float gv = __uint_as_float(G[j]) * cs[col], uv = __uint_as_float(U[j]) * cs[col];
               const float hv = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
               a.h_out[(size_t)(te.row0 + col) * a.I + n] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
             }
@@ -348,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
         }
       } else if (ge < nsub) {
         const int c = (ge == 0 ? nb0 : nb1) + r;
+        const int* ct = s_ct[buf];
         for (int c0 = 0; c0 < BN; c0 += 16) {
           uint32_t Y[16];
           tmem_ld_32x16(taddr(tmem, q * 32, ge * BN + c0), Y);
@@ -355,11 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c0 + j;
-            if (col < te.rows) {
-              const int p = a.perm[te.row0 + col];
-              const float y = __uint_as_float(Y[j]) / (gw * a.ags[te.row0 + col]);
-              atomicAdd(&a.out_acc[(size_t)(p / a.k) * a.H + c], a.topk_w[p] * y);
-            }
+            if (col < te.rows) atomicAdd(&a.out_acc[(size_t)ct[col] * a.H + c], cs[col] * __uint_as_float(Y[j]));
           }
         }
       }
@@ -367,6 +389,54 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty);
     }
+  } else if (MODE == 0 && warp >= kGathWarp0) {
+    // ---------------- gate/up activation rows: token rows of x -> shared memory ----------------
+    // 8 threads per 128-byte row slice, 16 rows per pass; the 16-byte piece p of row j goes to
+    // piece p ^ (j % 8) of that row (the 128-byte swizzle the MMA descriptor expects).
+    constexpr int RP = BN / 16;
+    const int gt = (warp - kGathWarp0) * 32 + lane;
+    const int piece = gt & 7, rsub = gt >> 3;
+    int it = 0, pend = 0;
+    bool ok = true;
+    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x) {
+      TileEntry te;
+      int nb0, nb1, nsub;
+      item(wk, te, nb0, nb1, nsub);
+      const uint8_t* src[RP];
+#pragma unroll
+      for (int i = 0; i < RP; ++i) {
+        const int j = rsub + 16 * i;
+        src[i] = a.xq + (size_t)(a.perm[te.row0 + (j < te.rows ? j : te.rows - 1)] / a.k) * (a.K / 2) + piece * 16;
+      }
+      for (int kc = 0; kc < nK; ++kc, ++it) {
+        const int sx = it % kStagesX;
+        ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[sx], ((it / kStagesX) & 1) ^ 1, &s_abort));
+        if (!ok) break;
+        const uint32_t xs = smem_u32(sX + sx * kXStage);
+#pragma unroll
+        for (int i = 0; i < RP; ++i) {
+          const int j = rsub + 16 * i;
+          cp_async_16(xs + j * 128 + ((piece ^ (j & 7)) << 4), src[i] + kc * (kKC / 2));
+        }
+        cp_async_commit();
+        if (pend == kLag) {  // the chunk kLag behind this one has landed: publish it
+          cp_async_wait<kLag>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&x_full[(it - kLag) % kStagesX]);
+        } else {
+          ++pend;
+        }
+      }
+    }
+    cp_async_wait<0>();
+    if (ok) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0)
+        for (int p = pend; p > 0; --p) mbar_arrive(&x_full[(it - p) % kStagesX]);
+    }
+    __syncwarp();
   }
 
   {
@@ -437,6 +507,7 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
       !tc_make_map(&a.wsf, u8, gu.b, H / 16, (uint64_t)E * 2 * I, H / 16, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !tc_make_map(&a.xcode, u8, xq, H / 2, (uint64_t)T, H / 2, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  a.xq = xq;
   a.asf = xsf;
   a.wgs = gu.gs;
   a.ags = (const float*)(ws + L.xg);

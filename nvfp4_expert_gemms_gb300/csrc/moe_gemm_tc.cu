@@ -6,7 +6,7 @@
 // dequantization is fused into the GEMM and never reaches HBM:
 //
 //   weights (packed, HBM) --TMA--> shared memory --converter warps--> bf16 A operand in TMEM
-//   activations (bf16)    --TMA gather4 / tile--> shared memory (128-byte swizzle) = B operand
+//   activations (bf16)    --cp.async gather / TMA tile--> shared memory (128-byte swizzle) = B operand
 //   tcgen05.mma kind::f16: D[weight row, token] += A[weight row, k] * B[token, k]   (fp32, TMEM)
 //
 // Weight rows are the MMA's M side (128 per sub-tile) and tokens its N side (BN = 16..128), so a
@@ -17,8 +17,11 @@
 // consecutive output features for the down GEMM (whose epilogue scales by the routing weight
 // and adds into the fp32 token-order accumulator).
 //
-// Warp roles (320 threads): warps 0-7 convert (warp w: sub-tile w/4, TMEM lanes 32*(w%4)..) and
-// later run the epilogue; warp 8 issues TMA; warp 9 owns TMEM and issues the MMAs.
+// Warp roles (640 threads): warps 0-15 convert (warp w: sub-tile (w/4)%2, K half w/8, TMEM lanes
+// 32*(w%4)..) and later run the epilogue; warp 16 issues TMA; warp 17 owns TMEM and issues the
+// MMAs; warps 18-19 gather the gate/up GEMM's token rows of x with 16-byte cp.async copies (a
+// TMA gather4 per four 128-byte rows moved about one row per 35 SM cycles, well below what the
+// MMAs consume at 128 tokens per tile).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -37,8 +40,8 @@ constexpr int kKC = 128;          // K elements per pipeline chunk
 constexpr int kConvWarps = 16;    // warps 0-15: converters + epilogue
 constexpr int kProdWarp = 16;     // TMA producer
 constexpr int kMmaWarp = 17;      // TMEM owner and MMA issuer
-constexpr int kThreads = 18 * 32;
-constexpr int kStagesW = 4;       // weight chunks in flight (shared memory)
+constexpr int kGathWarp0 = 18, kGathWarps = 2;  // activation row gather (gate/up)
+constexpr int kThreads = 20 * 32;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: [0, 2*BN) accumulators (two sub-tiles), then a ring of converted A chunks of 128
 // columns (both sub-tiles, 64 columns each): three stages from column 128 when BN <= 64, two from
@@ -59,9 +62,22 @@ struct WFmt<MOE_FMT_NVFP4_W4A16> {
   static constexpr int kSubBytes = 128 * 64;  // 128 rows x 64 bytes (128 codes), 64-byte swizzle
 };
 
+// Shared-memory rings: weight chunks (kStagesW) and activation chunks (SB, each BN rows x 128 K
+// bf16 as two 128-byte swizzle atoms); the gather threads keep LAG chunks in flight.
+template <int FMT, int BN>
+struct TcCfg {
+  static constexpr int kWSub = WFmt<FMT>::kSubBytes;
+  static constexpr int kStagesW = (FMT == MOE_FMT_FP8_B128_W8A16 && BN == 128) ? 3 : 4;
+  static constexpr int kBStage = BN * 256;
+  static constexpr int SB = BN <= 32 ? 4 : (1024 + kStagesW * 2 * kWSub + 4 * kBStage <= 200 * 1024 ? 4 : 3);
+  static constexpr int LAG = SB - 2;
+  static constexpr size_t kSmem = 1024 + (size_t)kStagesW * 2 * kWSub + (size_t)SB * kBStage;
+};
+
 struct TcArgs {
   CUtensorMap wmap;  // packed weight codes of the matrix
-  CUtensorMap bmap;  // activations: x (gate/up, one-row box for gather4) or h (down, BN-row box)
+  CUtensorMap bmap;  // activations of the down GEMM: h rows (BN-row box)
+  const __nv_bfloat16* x;  // activations of the gate/up GEMM [T, K], gathered by token
   const void* wscale;
   const float* wgs;
   const int32_t* perm;
@@ -209,13 +225,14 @@ __device__ __forceinline__ void conv_nvfp4(const char* sub, int r, int kh, uint3
 // MODE 1: down GEMM + routing weight -> fp32 red.add into the token-order accumulator.
 template <int FMT, int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __grid_constant__ TcArgs a) {
-  constexpr int SB = BN >= 64 ? 2 : 4;  // activation stages
+  using Cfg = TcCfg<FMT, BN>;
+  constexpr int kStagesW = Cfg::kStagesW;
+  constexpr int SB = Cfg::SB;  // activation stages
   constexpr int kStagesA = BN <= 64 ? 3 : 2;
   constexpr uint32_t kACol = BN <= 64 ? 128 : 256;
   constexpr int WSUB = WFmt<FMT>::kSubBytes;
   constexpr int WSTAGE = 2 * WSUB;
-  constexpr int BSTAGE = BN * 256;  // BN rows x 128 K bf16, two 128-byte swizzle atoms
-  constexpr int TPL = (BN + 31) / 32;
+  constexpr int BSTAGE = Cfg::kBStage;  // BN rows x 128 K bf16, two 128-byte swizzle atoms
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = (char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   char* sW = smem;
@@ -224,6 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       b_empty[SB], acc_full, drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_tok[2][BN];     // gather: token of each row of the item (double-buffered)
+  __shared__ int s_ct[2][BN];      // down epilogue: token of each column
+  __shared__ float s_cw[2][BN];    // down epilogue: routing weight / global scale of each column
 
   const int ntiles = a.tiles[0].expert;  // header entry holds the tile count
   const int ncb = MODE == 0 ? a.I / 128 : (a.H + 255) / 256;
@@ -242,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < SB; ++i) {
-      mbar_init(&b_full[i], 1);
+      mbar_init(&b_full[i], MODE == 0 ? kGathWarps : 1);
       mbar_init(&b_empty[i], 1);
     }
     mbar_init(&acc_full, 1);
@@ -279,19 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   };
 
   if (warp == kProdWarp) {
-    // ---------------- TMA producer (lane 0 issues; the warp holds the gather row indices) ----
+    // ---------------- TMA producer (the whole warp walks the loop, lane 0 issues) ----------------
     int it = 0;
     int armed_w[kStagesW] = {0}, armed_b[SB] = {0};
     for (int wk = blockIdx.x; wk < nwork; wk += gridDim.x) {
       TileEntry te;
       int nb0, nb1, nsub;
       item(wk, te, nb0, nb1, nsub);
-      int tk[TPL];
-#pragma unroll
-      for (int m = 0; m < TPL; ++m) {
-        const int j = lane + 32 * m;
-        tk[m] = (MODE == 0 && j < BN) ? a.perm[te.row0 + (j < te.rows ? j : te.rows - 1)] / a.k : 0;
-      }
       bool ok = true;
       for (int kc = 0; kc < nK; ++kc, ++it) {
         const int sw = it % kStagesW, sb = it % SB;
@@ -310,32 +324,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
               else
                 tma_load_2d(dst, &a.wmap, &w_full[sw], kc * (kKC / 2), te.expert * a.N + nb);
             }
-            ok = mbar_wait(&b_empty[sb], ((it / SB) & 1) ^ 1, &s_abort);
           }
-          if (ok) {
-            mbar_arrive_expect_tx(&b_full[sb], BSTAGE);
-            ++armed_b[sb];
+          if (ok && MODE == 1) {
+            ok = mbar_wait(&b_empty[sb], ((it / SB) & 1) ^ 1, &s_abort);
+            if (ok) {
+              char* bd = sB + sb * BSTAGE;
+              mbar_arrive_expect_tx(&b_full[sb], BSTAGE);
+              ++armed_b[sb];
+              tma_load_2d(bd, &a.bmap, &b_full[sb], kc * kKC, te.row0);
+              tma_load_2d(bd + BN * 128, &a.bmap, &b_full[sb], kc * kKC + 64, te.row0);
+            }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        char* bd = sB + sb * BSTAGE;
-        if (MODE == 0) {
-#pragma unroll
-          for (int j = 0; j < BN; j += 4) {
-            const int r0 = __shfl_sync(0xffffffffu, tk[j >> 5], (j & 31) + 0);
-            const int r1 = __shfl_sync(0xffffffffu, tk[j >> 5], (j & 31) + 1);
-            const int r2 = __shfl_sync(0xffffffffu, tk[j >> 5], (j & 31) + 2);
-            const int r3 = __shfl_sync(0xffffffffu, tk[j >> 5], (j & 31) + 3);
-            if (lane == 0) {
-              tma_gather4(bd + j * 128, &a.bmap, &b_full[sb], kc * kKC, r0, r1, r2, r3);
-              tma_gather4(bd + BN * 128 + j * 128, &a.bmap, &b_full[sb], kc * kKC + 64, r0, r1, r2, r3);
-            }
-          }
-        } else if (lane == 0) {
-          tma_load_2d(bd, &a.bmap, &b_full[sb], kc * kKC, te.row0);
-          tma_load_2d(bd + BN * 128, &a.bmap, &b_full[sb], kc * kKC + 64, te.row0);
-        }
       }
       if (!ok) break;
     }
@@ -346,6 +348,59 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       for (int i = 0; i < SB; ++i)
         if (armed_b[i]) mbar_wait(&b_full[i], (armed_b[i] - 1) & 1, &no_abort);
     }
+    __syncwarp();
+  } else if (MODE == 0 && warp >= kGathWarp0) {
+    // ---------------- gate/up activation rows: token rows of x -> shared memory ----------------
+    // 16 threads per row (16-byte pieces of the 256-byte chunk row), 4 rows per pass.  Piece p of
+    // row j lands in swizzle atom p / 8 (K 0-63 or 64-127) at piece (p % 8) ^ (j % 8).
+    constexpr int LAG = Cfg::LAG;
+    constexpr int RP = BN / 4;
+    const int gt = (warp - kGathWarp0) * 32 + lane;
+    const int piece = gt & 15, rsub = gt >> 4;
+    const uint32_t dpiece = (uint32_t)(piece >> 3) * BN * 128;
+    int it = 0, pend = 0, nitem = 0;
+    bool ok = true;
+    for (int wk = blockIdx.x; wk < nwork; wk += gridDim.x, ++nitem) {
+      TileEntry te;
+      int nb0, nb1, nsub;
+      item(wk, te, nb0, nb1, nsub);
+      int* tb = s_tok[nitem & 1];
+      if (ok)
+        for (int j = gt; j < BN; j += kGathWarps * 32) tb[j] = a.perm[te.row0 + (j < te.rows ? j : te.rows - 1)] / a.k;
+      ok = named_bar_and(2, kGathWarps * 32, ok);
+      if (!ok) break;
+      const char* xrow = (const char*)a.x + piece * 16;
+      for (int kc = 0; kc < nK; ++kc, ++it) {
+        const int sb = it % SB;
+        ok = __all_sync(0xffffffffu, mbar_wait(&b_empty[sb], ((it / SB) & 1) ^ 1, &s_abort));
+        if (!ok) break;
+        const uint32_t bs = smem_u32(sB + sb * BSTAGE) + dpiece;
+        const char* xk = xrow + kc * (kKC * 2);
+#pragma unroll 8
+        for (int i = 0; i < RP; ++i) {
+          const int j = rsub + 4 * i;
+          cp_async_16(bs + j * 128 + ((((uint32_t)piece & 7u) ^ (uint32_t)(j & 7)) << 4),
+                      xk + (size_t)tb[j] * (a.K * 2));
+        }
+        cp_async_commit();
+        if (pend == LAG) {  // the chunk LAG behind this one has landed: publish it
+          cp_async_wait<LAG>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&b_full[(it - LAG) % SB]);
+        } else {
+          ++pend;
+        }
+      }
+    }
+    cp_async_wait<0>();
+    if (ok) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0)
+        for (int p = pend; p > 0; --p) mbar_arrive(&b_full[(it - p) % SB]);
+    }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer ----------------
     // The whole warp walks the loop and waits together (lane 0 issues): a lane left idling in a
@@ -382,18 +437,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     }
     if (lane == 0) mma_commit(&drain);  // completes once every MMA issued by this thread has finished
     __syncwarp();
-  } else {
+  } else if (warp < kConvWarps) {
     // ---------------- converters (16 warps) and epilogue ----------------
     const int g = (warp >> 2) & 1, kh = warp >> 3, q = warp & 3, r = q * 32 + lane;
     int it = 0, nitem = 0;
     bool ok = true;
-    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x, ++nitem) {
+    for (int wk = blockIdx.x; wk < nwork; wk += gridDim.x, ++nitem) {
       TileEntry te;
       int nb0, nb1, nsub;
       item(wk, te, nb0, nb1, nsub);
       const int e = te.expert;
       const bool active = g < nsub;
       const int nb = g == 0 ? nb0 : nb1;
+      const int buf = nitem & 1;
+      const float inv_gs = FMT == MOE_FMT_NVFP4_W4A16 ? 1.0f / a.wgs[e] : 1.f;
+      if (MODE == 1 && threadIdx.x < BN) {  // column table of the down epilogue
+        const int col = threadIdx.x;
+        int ct = 0;
+        float cw = 0.f;
+        if (col < te.rows) {
+          const int p = a.perm[te.row0 + col];
+          ct = p / a.k;
+          cw = a.topk_w[p] * inv_gs;
+        }
+        s_ct[buf][col] = ct;
+        s_cw[buf][col] = cw;
+      }
       // per-chunk scales, fetched one chunk ahead so their latency hides behind a conversion
       auto scale_of = [&](int kc) -> uint32_t {
         if (!active) return 0u;
@@ -410,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         if (kc + 1 < nK) sc_next = scale_of(kc + 1);
         const float sc = __uint_as_float(sc_raw);
         const uint32_t bs4 = sc_raw;
-        ok = mbar_wait(&w_full[sw], (it / kStagesW) & 1, &s_abort);
+        ok = __all_sync(0xffffffffu, mbar_wait(&w_full[sw], (it / kStagesW) & 1, &s_abort));
         if (!ok) break;
         uint32_t v[32];
         if (active) {
@@ -421,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&w_empty[sw]);
-        ok = mbar_wait(&a_empty[sa], ((it / kStagesA) & 1) ^ 1, &s_abort);
+        ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[sa], ((it / kStagesA) & 1) ^ 1, &s_abort));
         if (!ok) break;
         fence_after_sync();
         if (active) {
@@ -432,12 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[sa]);
       }
-      if (!ok) break;
-      // epilogue of this item
-      ok = mbar_wait(&acc_full, nitem & 1, &s_abort);
+      // epilogue of this item; every converter thread takes the same branch here
+      if (ok) ok = mbar_wait(&acc_full, nitem & 1, &s_abort);
+      ok = named_bar_and(1, kConvWarps * 32, ok);
       if (!ok) break;
       fence_after_sync();
-      const float gs = FMT == MOE_FMT_NVFP4_W4A16 ? a.wgs[e] : 1.f;
       if (MODE == 0) {
         const int part = warp >> 2;  // 0..3: 16-column chunks part, part+4, ...
         const int n = nb0 + r;
@@ -450,18 +518,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
           for (int j = 0; j < 16; ++j) {
             const int col = c0 + j;
             if (col < te.rows) {
-              float gv = __uint_as_float(G[j]), uv = __uint_as_float(U[j]);
-              if (FMT == MOE_FMT_NVFP4_W4A16) {
-                gv = __fdiv_rn(gv, gs);
-                uv = __fdiv_rn(uv, gs);
-              }
-              const float hv = gv / (1.0f + expf(-gv)) * uv;
+              const float gv = __uint_as_float(G[j]) * inv_gs, uv = __uint_as_float(U[j]) * inv_gs;
+              const float hv = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
               a.h_out[(size_t)(te.row0 + col) * a.I + n] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
             }
           }
         }
       } else if (active) {
         const int c = nb + r;
+        const int* ct = s_ct[buf];
+        const float* cw = s_cw[buf];
         for (int c0 = kh * 16; c0 < BN; c0 += 32) {
           uint32_t Y[16];
           tmem_ld_32x16(taddr(tmem, q * 32, g * BN + c0), Y);
@@ -469,12 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c0 + j;
-            if (col < te.rows) {
-              const int p = a.perm[te.row0 + col];
-              float y = __uint_as_float(Y[j]);
-              if (FMT == MOE_FMT_NVFP4_W4A16) y = __fdiv_rn(y, gs);
-              atomicAdd(&a.out_acc[(size_t)(p / a.k) * a.H + c], a.topk_w[p] * y);
-            }
+            if (col < te.rows) atomicAdd(&a.out_acc[(size_t)ct[col] * a.H + c], cw[col] * __uint_as_float(Y[j]));
           }
         }
       }
@@ -544,8 +605,7 @@ bool weight_map(CUtensorMap* m, int fmt, const MatView& v, int E) {
 
 template <int FMT, int MODE, int BN>
 cudaError_t launch_one(const TcArgs& args, int grid_x, int grid_y, cudaStream_t s) {
-  constexpr int SB = BN >= 64 ? 2 : 4;
-  constexpr size_t need = 1024 + (size_t)kStagesW * 2 * WFmt<FMT>::kSubBytes + (size_t)SB * BN * 256;
+  constexpr size_t need = TcCfg<FMT, BN>::kSmem;
   // at least 116 KB so that a single CTA (owning all 512 TMEM columns) runs per SM
   constexpr size_t smem = need > 116 * 1024 ? need : 116 * 1024;
   static bool attr = false;
@@ -612,10 +672,8 @@ cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, co
   const int gx = (int)(R / bn + (R < (size_t)E ? R : (size_t)E) + 1);
 
   // gate/up: A = fused [2I, H] weights, B = gathered rows of x
-  if (!weight_map(&a.wmap, d.fmt, gu, E) ||
-      !make_map(&a.bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, H, (uint64_t)T, (uint64_t)H * 2, 64, 1,
-                CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
+  if (!weight_map(&a.wmap, d.fmt, gu, E)) return cudaErrorInvalidValue;
+  a.x = x;
   a.wscale = gu.b;
   a.wgs = gu.gs;
   a.N = 2 * I;

@@ -80,6 +80,32 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// ---- cp.async: 16-byte global -> shared copies through L2, issued per thread -------------------
+// Used for row gathers: one TMA gather4 moves four 128-byte rows, and at that granularity the
+// tensor-memory-access unit issues far fewer bytes per cycle than a few warps of cp.async do.
+// The writing threads wait for their own groups, fence the generic-proxy writes against the
+// async proxy (the MMA reads shared memory through it) and only then arrive on the barrier.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Barrier over the first `nthreads` threads that use barrier `id` (1..15), returning the AND of
+// every participant's `v`; every participant must reach it the same number of times.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // ---- tensor memory --------------------------------------------------------------------------
 // Executed by one whole warp; the allocated base address is written to *dst (shared memory).
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
