@@ -39,14 +39,15 @@ WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
   L.out_acc = take(4 * (size_t)T * H);
   L.xmax = take(4 * (size_t)T);
   L.hmax = take(4 * R);
-  if (fmt == MOE_FMT_NVFP4_W4A4) {
-    L.xq = take((size_t)T * H / 2);
-    L.xs = take((size_t)T * H / 16);
-    L.xg = take(4 * (size_t)T);
+  if (fmt == MOE_FMT_NVFP4_W4A4) {  // activation codes per permuted row (first T rows: per token)
+    L.xq = take(R * H / 2);
+    L.xs = take(R * H / 16);
+    L.xg = take(4 * R);
     L.hq = take(R * I / 2);
     L.hs = take(R * I / 16);
     L.hg = take(4 * R);
   }
+  if (fmt != MOE_FMT_NVFP4_W4A4 && tc_row_block(T, k, E) >= kTcPermuteFromRows) L.xp = take(2 * R * H);
   if (host_io) {
     L.x_stage = take(2 * (size_t)T * H);
     L.lg_stage = take(4 * (size_t)T * E);
@@ -292,7 +293,7 @@ moe_status_t moe_debug_quant_act(const void* x, int T, int H, uint8_t* codes, ui
   if (T > 0 && (!x || !codes || !scales || !gs || !aligned(x, 16))) return MOE_ERR_INVALID_ARG;
   const moe_status_t dv = device_ok();
   if (dv != MOE_OK) return dv;
-  return cuda_status(launch_quant_rows((const __nv_bfloat16*)x, T, H, codes, scales, gs, (cudaStream_t)stream));
+  return cuda_status(launch_quant_rows((const __nv_bfloat16*)x, nullptr, 1, T, H, codes, scales, gs, (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -7,21 +7,19 @@
 //   weights      E2M1 codes [N, K/2] + E4M3 block scales [N, K/16] + global scale gs_w (per matrix)
 //   activations  E2M1 codes [rows, K/2] + E4M3 block scales [rows, K/16] + global scale gs_a (per row)
 // The MMA forms sum_k (q_w * bs_w)(q_a * bs_a) exactly in fp32, and the epilogue divides by
-// gs_w * gs_a.  Codes arrive by TMA (weights: 128-row tiles; activations: gather4 of token rows
-// for gate/up, tiles of permuted h rows for down) in the 128-byte swizzle.  The weight block
+// gs_w * gs_a.  Codes arrive by TMA tiles in the 128-byte swizzle: weights in 128-row tiles,
+// activations in BN-row tiles of their expert-permuted rows (x is quantized straight into that
+// order, one copy per routed token slot, so the gate/up GEMM needs no row gather).  The weight block
 // scales arrive by TMA next to their codes; the activation block scales are read from global
 // memory by the four scale warps (16 bytes per row and chunk, fetched one chunk ahead), which
 // place both in tensor memory in the layout the MMA reads (per K = 64 step and 128 rows:
 // 4 columns; lane l, column j = the four scales of row l + 32 j, repeated in every lane quarter).
-// The gate/up GEMM's token rows are gathered by four warps of 16-byte cp.async copies into the
-// same swizzled layout a TMA tile load produces (a gather4 per four rows ran at about one
-// 128-byte row per 35 SM cycles and starved the MMA).
 //
 //   D[weight row, act row] += A[weight row, k] * B[act row, k]     M = 128, N = BN <= 128, K = 64
 //
-// Warps (576 threads): 0-3 stage scale factors, 4-11 run the epilogue (thread = weight row),
-// 12 issues TMA, 13 owns TMEM and issues the MMAs, 14-17 gather activation rows (gate/up).
-// Persistent CTAs walk (row tile, column block) work items.
+// Warps (448 threads): 0-3 stage scale factors, 4-11 run the epilogue (thread = weight row),
+// 12 issues TMA, 13 owns TMEM and issues the MMAs.  Persistent CTAs walk (row tile, column
+// block) work items.
 #include <cudaTypedefs.h>
 
 #include "moe_formats.cuh"
@@ -34,31 +32,32 @@ namespace {
 using namespace tc;
 
 constexpr int kKC = 256;                  // K per chunk: 128 bytes of codes per row
-constexpr int kStagesW = 4, kStagesX = 4, kStagesS = 2;
-constexpr int kLag = kStagesX - 2;        // gathered chunks a gather thread leaves in flight
+constexpr int kStagesX = 4, kStagesS = 4;
 constexpr int kSfWarps = 4, kEpiWarp0 = 4, kEpiWarps = 8, kProdWarp = 12, kMmaWarp = 13;
-constexpr int kGathWarp0 = 14, kGathWarps = 4;
-constexpr int kThreads = 18 * 32;
+constexpr int kThreads = 14 * 32;
 constexpr int kWCodes = 128 * 128;        // 128 rows x 128 B (256 codes), 128-byte swizzle
 constexpr int kWSf = 128 * 16;            // 128 rows x 16 scales
 constexpr int kWStage = 2 * kWCodes + 2 * kWSf;
-constexpr uint32_t kSfCol = 256;          // TMEM: [0, 2*BN) accumulators, then scale-factor stages
+constexpr uint32_t kSfCol = 256;          // TMEM: [0, 2*BN) accumulators, then 4 x 48 scale-factor columns
 constexpr uint32_t kSfStageCols = 48;     // sub-tile 0 A scales (16), sub-tile 1 (16), B scales (16)
 
-template <int BN>
+// Shared memory: weight stages, activation stages, and (gate/up) the h tile staged for
+// coalesced stores: BN token rows x 128 intermediate columns of bf16.
+template <int MODE, int BN>
 struct Fp4Cfg {
+  static constexpr int kStagesW = MODE == 0 ? 3 : 4;
   static constexpr int kXBytes = BN * 128;                        // codes, 128-byte swizzle
   static constexpr int kXStage = (kXBytes + 1023) / 1024 * 1024;  // stages start 1024-aligned
-  static constexpr size_t kSmem = 1024 + (size_t)kStagesW * kWStage + (size_t)kStagesX * kXStage;
+  static constexpr int kHBytes = MODE == 0 ? BN * 256 : 0;
+  static constexpr size_t kSmem = 1024 + (size_t)kStagesW * kWStage + (size_t)kStagesX * kXStage + kHBytes;
 };
 
 struct Fp4Args {
   CUtensorMap wcode, wsf;   // weight codes [E*N, K/2], scales [E*N, K/16]
-  CUtensorMap xcode;        // activation codes of h rows (down GEMM tiles)
-  const uint8_t* xq;        // activation codes of x [T, K/2] (gate/up rows, gathered by token)
-  const uint8_t* asf;       // activation block scales [rows, K/16] (x: per token, h: per permuted row)
+  CUtensorMap xcode;        // activation codes [R, K/2] in permuted row order
+  const uint8_t* asf;       // activation block scales [R, K/16]
   const float* wgs;         // weight global scales [E]
-  const float* ags;         // activation global scales per source row
+  const float* ags;         // activation global scales [R]
   const int32_t* perm;
   const float* topk_w;
   const TileEntry* tiles;
@@ -107,19 +106,21 @@ __device__ __forceinline__ void sf_words(const char* tile, int l, int nrows, uin
 
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant__ Fp4Args a) {
-  constexpr int kXStage = Fp4Cfg<BN>::kXStage;
+  constexpr int kStagesW = Fp4Cfg<MODE, BN>::kStagesW;
+  constexpr int kXStage = Fp4Cfg<MODE, BN>::kXStage;
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = (char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   char* sW = smem;
   char* sX = sW + kStagesW * kWStage;
+  char* sH = sX + kStagesX * kXStage;
   __shared__ uint64_t w_full[kStagesW], w_empty[kStagesW], x_full[kStagesX], x_empty[kStagesX], s_full[kStagesS],
       s_empty[kStagesS], acc_full, acc_empty, drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   // per output column of the current item (double-buffered by item parity): the scale that
   // undoes both global scales (times the routing weight for the down GEMM) and the token row
-  __shared__ float s_cs[2][BN];
-  __shared__ int s_ct[2][BN];
+  __shared__ __align__(16) float s_cs[2][BN];
+  __shared__ __align__(16) int s_ct[2][BN];
 
   const int ntiles = a.tiles[0].expert;
   const int ncb = MODE == 0 ? a.I / 128 : (a.H + 255) / 256;
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
       mbar_init(&w_empty[i], 1);
     }
     for (int i = 0; i < kStagesX; ++i) {
-      mbar_init(&x_full[i], MODE == 0 ? kGathWarps : 1);
+      mbar_init(&x_full[i], 1);
       mbar_init(&x_empty[i], 1);
     }
     for (int i = 0; i < kStagesS; ++i) {
@@ -198,10 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
               tma_load_2d(ws + 2 * kWCodes + g * kWSf, &a.wsf, &w_full[sw], kc * (kKC / 16), row);
             }
           }
-          if (ok && MODE == 1) {
+          if (ok) {
             ok = mbar_wait(&x_empty[sx], ((it / kStagesX) & 1) ^ 1, &s_abort);
             if (ok) {
-              mbar_arrive_expect_tx(&x_full[sx], Fp4Cfg<BN>::kXBytes);
+              mbar_arrive_expect_tx(&x_full[sx], Fp4Cfg<MODE, BN>::kXBytes);
               ++armed_x[sx];
               tma_load_2d(sX + sx * kXStage, &a.xcode, &x_full[sx], kc * (kKC / 2), te.row0);
             }
@@ -276,10 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
       for (int j = 0; j < 4; ++j) {
         const int row = l + 32 * j;
         src[j] = nullptr;
-        if (row < te.rows && row < BN) {
-          const size_t sr = MODE == 0 ? (size_t)(a.perm[te.row0 + row] / a.k) : (size_t)(te.row0 + row);
-          src[j] = a.asf + sr * (a.K / 16);
-        }
+        if (row < te.rows && row < BN) src[j] = a.asf + (size_t)(te.row0 + row) * (a.K / 16);
       }
       uint4 nxt[4];
 #pragma unroll
@@ -334,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
         if (et < te.rows) {
           const float gw = a.wgs[te.expert];
           if (MODE == 0) {
-            cs = 1.0f / (gw * a.ags[a.perm[te.row0 + et] / a.k]);
+            cs = 1.0f / (gw * a.ags[te.row0 + et]);
           } else {
             const int p = a.perm[te.row0 + et];
             cs = a.topk_w[p] / (gw * a.ags[te.row0 + et]);
@@ -352,24 +350,32 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
       const float* cs = s_cs[buf];
       if (MODE == 0) {
         // both warp groups own the same weight rows (gate in sub-tile 0, up in sub-tile 1) and
-        // split the token columns
-        const int n = nb0 + r;
+        // split the token columns; h goes to the staged tile [token][weight row] first
         const int c_beg = BN <= 16 ? (ge == 0 ? 0 : BN) : ge * (BN / 2);
         const int c_end = BN <= 16 ? (ge == 0 ? BN : BN) : c_beg + BN / 2;
+        uint16_t* sh = (uint16_t*)sH;
         for (int c0 = c_beg; c0 < c_end; c0 += 16) {
           uint32_t G[16], U[16];
           tmem_ld_32x16(taddr(tmem, q * 32, c0), G);
           tmem_ld_32x16(taddr(tmem, q * 32, BN + c0), U);
+          float sc[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) *(float4*)(sc + 4 * i) = *(const float4*)(cs + c0 + 4 * i);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int col = c0 + j;
-            if (col < te.rows) {
-              const float gv = __uint_as_float(G[j]) * cs[col], uv = __uint_as_float(U[j]) * cs[col];
-              const float hv = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
-              a.h_out[(size_t)(te.row0 + col) * a.I + n] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
-            }
+            const float gv = __uint_as_float(G[j]) * sc[j], uv = __uint_as_float(U[j]) * sc[j];
+            const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+            sh[(c0 + j) * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
           }
+        }
+        // the tile's valid token rows leave as 256-byte row segments in 16-byte stores
+        named_bar_sync(2, kEpiWarps * 32);
+        const int nrows = te.rows < BN ? te.rows : BN;
+        for (int idx = et; idx < nrows * 16; idx += kEpiWarps * 32) {
+          const int row = idx >> 4, piece = idx & 15;
+          *(uint4*)(a.h_out + (size_t)(te.row0 + row) * a.I + nb0 + piece * 8) =
+              *(const uint4*)(sH + row * 256 + piece * 16);
         }
       } else if (ge < nsub) {
         const int c = (ge == 0 ? nb0 : nb1) + r;
@@ -377,66 +383,23 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
         for (int c0 = 0; c0 < BN; c0 += 16) {
           uint32_t Y[16];
           tmem_ld_32x16(taddr(tmem, q * 32, ge * BN + c0), Y);
+          float sc[16];
+          int tok[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            *(float4*)(sc + 4 * i) = *(const float4*)(cs + c0 + 4 * i);
+            *(int4*)(tok + 4 * i) = *(const int4*)(ct + c0 + 4 * i);
+          }
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c0 + j;
-            if (col < te.rows) atomicAdd(&a.out_acc[(size_t)ct[col] * a.H + c], cs[col] * __uint_as_float(Y[j]));
-          }
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < te.rows) atomicAdd(&a.out_acc[(size_t)tok[j] * a.H + c], sc[j] * __uint_as_float(Y[j]));
         }
       }
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty);
     }
-  } else if (MODE == 0 && warp >= kGathWarp0) {
-    // ---------------- gate/up activation rows: token rows of x -> shared memory ----------------
-    // 8 threads per 128-byte row slice, 16 rows per pass; the 16-byte piece p of row j goes to
-    // piece p ^ (j % 8) of that row (the 128-byte swizzle the MMA descriptor expects).
-    constexpr int RP = BN / 16;
-    const int gt = (warp - kGathWarp0) * 32 + lane;
-    const int piece = gt & 7, rsub = gt >> 3;
-    int it = 0, pend = 0;
-    bool ok = true;
-    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x) {
-      TileEntry te;
-      int nb0, nb1, nsub;
-      item(wk, te, nb0, nb1, nsub);
-      const uint8_t* src[RP];
-#pragma unroll
-      for (int i = 0; i < RP; ++i) {
-        const int j = rsub + 16 * i;
-        src[i] = a.xq + (size_t)(a.perm[te.row0 + (j < te.rows ? j : te.rows - 1)] / a.k) * (a.K / 2) + piece * 16;
-      }
-      for (int kc = 0; kc < nK; ++kc, ++it) {
-        const int sx = it % kStagesX;
-        ok = __all_sync(0xffffffffu, mbar_wait(&x_empty[sx], ((it / kStagesX) & 1) ^ 1, &s_abort));
-        if (!ok) break;
-        const uint32_t xs = smem_u32(sX + sx * kXStage);
-#pragma unroll
-        for (int i = 0; i < RP; ++i) {
-          const int j = rsub + 16 * i;
-          cp_async_16(xs + j * 128 + ((piece ^ (j & 7)) << 4), src[i] + kc * (kKC / 2));
-        }
-        cp_async_commit();
-        if (pend == kLag) {  // the chunk kLag behind this one has landed: publish it
-          cp_async_wait<kLag>();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&x_full[(it - kLag) % kStagesX]);
-        } else {
-          ++pend;
-        }
-      }
-    }
-    cp_async_wait<0>();
-    if (ok) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0)
-        for (int p = pend; p > 0; --p) mbar_arrive(&x_full[(it - p) % kStagesX]);
-    }
-    __syncwarp();
   }
 
   {
@@ -459,11 +422,12 @@ template <int MODE, int BN>
 static cudaError_t launch_fp4_one(const Fp4Args& a, int work, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(fp4_kernel<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Fp4Cfg<BN>::kSmem);
+    cudaFuncSetAttribute(fp4_kernel<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)Fp4Cfg<MODE, BN>::kSmem);
     attr = true;
   }
   const int sms = tc_num_sms();
-  fp4_kernel<MODE, BN><<<work < sms ? work : sms, kThreads, Fp4Cfg<BN>::kSmem, s>>>(a);
+  fp4_kernel<MODE, BN><<<work < sms ? work : sms, kThreads, Fp4Cfg<MODE, BN>::kSmem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -486,7 +450,7 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   uint8_t* xsf = (uint8_t*)(ws + L.xs);
   uint8_t* hq = (uint8_t*)(ws + L.hq);
   uint8_t* hsf = (uint8_t*)(ws + L.hs);
-  launch_quant_rows(x, T, H, xq, xsf, (float*)(ws + L.xg), s);
+  launch_quant_rows(x, (const int32_t*)(ws + L.inv), k, T, H, xq, xsf, (float*)(ws + L.xg), s);
 
   Fp4Args a;
   memset(&a, 0, sizeof(a));
@@ -502,12 +466,11 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   const int max_tiles = (int)(R / bn + (R < (size_t)E ? R : (size_t)E) + 1);
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 
-  // gate/up: A = fused [2I, H] NVFP4 weights, B = quantized x rows gathered by token
+  // gate/up: A = fused [2I, H] NVFP4 weights, B = quantized x in permuted row order
   if (!tc_make_map(&a.wcode, u8, gu.a, H / 2, (uint64_t)E * 2 * I, H / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tc_make_map(&a.wsf, u8, gu.b, H / 16, (uint64_t)E * 2 * I, H / 16, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !tc_make_map(&a.xcode, u8, xq, H / 2, (uint64_t)T, H / 2, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B))
+      !tc_make_map(&a.xcode, u8, xq, H / 2, (uint64_t)R, H / 2, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  a.xq = xq;
   a.asf = xsf;
   a.wgs = gu.gs;
   a.ags = (const float*)(ws + L.xg);
@@ -519,7 +482,7 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   if (err != cudaSuccess) return err;
 
   // h -> NVFP4 per permuted row (its own global scale), then down: A = [H, I] weights, B = h rows
-  launch_quant_rows((const __nv_bfloat16*)(ws + L.h), (int)R, I, hq, hsf, (float*)(ws + L.hg), s);
+  launch_quant_rows((const __nv_bfloat16*)(ws + L.h), nullptr, 1, (int)R, I, hq, hsf, (float*)(ws + L.hg), s);
   if (!tc_make_map(&a.wcode, u8, dn.a, I / 2, (uint64_t)E * H, I / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tc_make_map(&a.wsf, u8, dn.b, I / 16, (uint64_t)E * H, I / 16, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !tc_make_map(&a.xcode, u8, hq, I / 2, (uint64_t)R, I / 2, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B))

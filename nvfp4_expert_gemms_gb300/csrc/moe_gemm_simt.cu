@@ -166,7 +166,7 @@ cudaError_t run_simt(const moe_packed_desc_t& d, const char* packed, const __nv_
       (const float*)(ws + L.xg), perm, k, I, tiles, (uint16_t*)(ws + L.h));
   record_event(ev.stop[0], s);
   if (A4)
-    launch_quant_rows((const __nv_bfloat16*)(ws + L.h), T * k, I, (uint8_t*)(ws + L.hq), (uint8_t*)(ws + L.hs),
+    launch_quant_rows((const __nv_bfloat16*)(ws + L.h), nullptr, 1, T * k, I, (uint8_t*)(ws + L.hq), (uint8_t*)(ws + L.hs),
                       (float*)(ws + L.hg), s);
   record_event(ev.start[1], s);
   down_simt_kernel<FMT, A4><<<dim3(L.max_tiles, H / kSimtNB), 128, smem_d, s>>>(
@@ -188,7 +188,7 @@ cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const
   if (d.fmt == MOE_FMT_NVFP4_W4A4 && fp4_supported(d)) {
     e = launch_experts_fp4(d, packed, x, T, k, row_block, L, ws, ev, s);
   } else if (d.fmt == MOE_FMT_NVFP4_W4A4) {
-    launch_quant_rows(x, T, d.H, (uint8_t*)(ws + L.xq), (uint8_t*)(ws + L.xs), (float*)(ws + L.xg), s);
+    launch_quant_rows(x, nullptr, 1, T, d.H, (uint8_t*)(ws + L.xq), (uint8_t*)(ws + L.xs), (float*)(ws + L.xg), s);
     e = run_simt<MOE_FMT_NVFP4_W4A16, true>(d, packed, x, T, k, L, ws, ev, s);
   } else if (d.fmt == MOE_FMT_FP8_B128_W8A16 && row_block == fp8dec_row_block()) {
     e = launch_experts_fp8dec(d, packed, x, T, k, L, ws, ev, s);

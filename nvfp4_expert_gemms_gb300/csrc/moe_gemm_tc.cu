@@ -6,7 +6,7 @@
 // dequantization is fused into the GEMM and never reaches HBM:
 //
 //   weights (packed, HBM) --TMA--> shared memory --converter warps--> bf16 A operand in TMEM
-//   activations (bf16)    --cp.async gather / TMA tile--> shared memory (128-byte swizzle) = B operand
+//   activations (bf16)    --TMA tile / cp.async gather--> shared memory (128-byte swizzle) = B operand
 //   tcgen05.mma kind::f16: D[weight row, token] += A[weight row, k] * B[token, k]   (fp32, TMEM)
 //
 // Weight rows are the MMA's M side (128 per sub-tile) and tokens its N side (BN = 16..128), so a
@@ -19,9 +19,11 @@
 //
 // Warp roles (640 threads): warps 0-15 convert (warp w: sub-tile (w/4)%2, K half w/8, TMEM lanes
 // 32*(w%4)..) and later run the epilogue; warp 16 issues TMA; warp 17 owns TMEM and issues the
-// MMAs; warps 18-19 gather the gate/up GEMM's token rows of x with 16-byte cp.async copies (a
-// TMA gather4 per four 128-byte rows moved about one row per 35 SM cycles, well below what the
-// MMAs consume at 128 tokens per tile).
+// MMAs.  The gate/up GEMM reads x rows in expert-permuted order: for row blocks of 64 or more a
+// separate pass writes that permuted copy and the kernel loads it in TMA tiles; for smaller row
+// blocks warps 18-19 gather the token rows with 16-byte cp.async copies.  (A TMA gather4 per four
+// 128-byte rows moved about one row per 35 SM cycles, and a few cp.async warps reach only about
+// 20-40 GB/s per SM, both far below what the MMAs consume at 64-128 tokens per tile.)
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -76,8 +78,8 @@ struct TcCfg {
 
 struct TcArgs {
   CUtensorMap wmap;  // packed weight codes of the matrix
-  CUtensorMap bmap;  // activations of the down GEMM: h rows (BN-row box)
-  const __nv_bfloat16* x;  // activations of the gate/up GEMM [T, K], gathered by token
+  CUtensorMap bmap;  // activation rows in permuted order (BN-row box): x copy or h
+  const __nv_bfloat16* x;  // activations of the gate/up GEMM [T, K], gathered by token (small row blocks)
   const void* wscale;
   const float* wgs;
   const int32_t* perm;
@@ -226,6 +228,7 @@ __device__ __forceinline__ void conv_nvfp4(const char* sub, int r, int kh, uint3
 template <int FMT, int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __grid_constant__ TcArgs a) {
   using Cfg = TcCfg<FMT, BN>;
+  constexpr bool kGather = MODE == 0 && BN < kTcPermuteFromRows;
   constexpr int kStagesW = Cfg::kStagesW;
   constexpr int SB = Cfg::SB;  // activation stages
   constexpr int kStagesA = BN <= 64 ? 3 : 2;
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < SB; ++i) {
-      mbar_init(&b_full[i], MODE == 0 ? kGathWarps : 1);
+      mbar_init(&b_full[i], kGather ? kGathWarps : 1);
       mbar_init(&b_empty[i], 1);
     }
     mbar_init(&acc_full, 1);
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
                 tma_load_2d(dst, &a.wmap, &w_full[sw], kc * (kKC / 2), te.expert * a.N + nb);
             }
           }
-          if (ok && MODE == 1) {
+          if (ok && !kGather) {
             ok = mbar_wait(&b_empty[sb], ((it / SB) & 1) ^ 1, &s_abort);
             if (ok) {
               char* bd = sB + sb * BSTAGE;
@@ -349,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         if (armed_b[i]) mbar_wait(&b_full[i], (armed_b[i] - 1) & 1, &no_abort);
     }
     __syncwarp();
-  } else if (MODE == 0 && warp >= kGathWarp0) {
+  } else if (kGather && warp >= kGathWarp0) {
     // ---------------- gate/up activation rows: token rows of x -> shared memory ----------------
     // 16 threads per row (16-byte pieces of the 256-byte chunk row), 4 rows per pass.  Piece p of
     // row j lands in swizzle atom p / 8 (K 0-63 or 64-127) at piece (p % 8) ^ (j % 8).
@@ -519,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
             const int col = c0 + j;
             if (col < te.rows) {
               const float gv = __uint_as_float(G[j]) * inv_gs, uv = __uint_as_float(U[j]) * inv_gs;
-              const float hv = gv * __frcp_rn(1.0f + __expf(-gv)) * uv;
+              const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
               a.h_out[(size_t)(te.row0 + col) * a.I + n] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
             }
           }
@@ -674,6 +677,13 @@ cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, co
   // gate/up: A = fused [2I, H] weights, B = gathered rows of x
   if (!weight_map(&a.wmap, d.fmt, gu, E)) return cudaErrorInvalidValue;
   a.x = x;
+  if (bn >= kTcPermuteFromRows) {
+    __nv_bfloat16* xp = (__nv_bfloat16*)(ws + L.xp);
+    if (launch_gather_rows(x, a.perm, k, (int)R, H, xp, s) != cudaSuccess ||
+        !make_map(&a.bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xp, H, (uint64_t)R, (uint64_t)H * 2, 64, bn,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   a.wscale = gu.b;
   a.wgs = gu.gs;
   a.N = 2 * I;

@@ -66,6 +66,7 @@ struct TileEntry {
 struct WsLayout {
   size_t err, topk_idx, topk_w, blkcnt, blkbase, offsets, perm, inv, tiles;
   size_t h, out_acc, xq, xs, xg, hq, hs, hg;
+  size_t xp;          // expert-permuted bf16 copy of x (tensor-core path, row blocks >= 64)
   size_t xmax, hmax;  // per-row max |activation| (FP8 decode path)
   size_t x_stage, lg_stage, out_stage;
   size_t total;
@@ -93,8 +94,15 @@ cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, co
                         char* packed, cudaStream_t s);
 cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e, int which, float* out,
                            cudaStream_t s);
-cudaError_t launch_quant_rows(const __nv_bfloat16* x, int rows, int K, uint8_t* q, uint8_t* sf, float* gs,
-                              cudaStream_t s);
+// NVFP4 quantization of bf16 rows; row r's codes go to output row r, or (scatter != null) to
+// rows scatter[r*k .. r*k+k-1].
+cudaError_t launch_quant_rows(const __nv_bfloat16* x, const int32_t* scatter, int k, int rows, int K, uint8_t* q,
+                              uint8_t* sf, float* gs, cudaStream_t s);
+// out[r] = x[map[r] / k] for r < rows (rows of K bf16).
+cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* map, int k, int rows, int K, __nv_bfloat16* out,
+                               cudaStream_t s);
+// Row block from which the tensor-core path reads a permuted copy of x instead of gathering rows.
+constexpr int kTcPermuteFromRows = 64;
 // Optional events around the two GEMM steps (0 = gate/up, 1 = down); null entries are skipped.
 struct StepEvents {
   cudaEvent_t start[2] = {nullptr, nullptr}, stop[2] = {nullptr, nullptr};

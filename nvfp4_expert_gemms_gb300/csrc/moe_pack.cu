@@ -133,9 +133,12 @@ __global__ void nvfp4_finish_kernel(unsigned* slot, int E) {
   }
 }
 
-// Dynamic NVFP4 quantization of bf16 rows (W4A4 activations): one warp per row;
-// gs_row = 2688 / max(amax_row, 1e-12), then blocks exactly as for weights.
-__global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restrict__ x, int rows, int K,
+// Dynamic NVFP4 quantization of bf16 rows (W4A4 activations): one warp per input row r;
+// gs_row = 2688 / max(amax_row, 1e-12), then blocks exactly as for weights.  The codes, scales
+// and gs_row go to output row r, or, with a scatter map, to each of rows scatter[r*k .. r*k+k-1]
+// (the expert-permuted copies of a token: computed once, stored k times).
+__global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restrict__ x,
+                                                         const int32_t* __restrict__ scatter, int k, int rows, int K,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                          float* __restrict__ gs_out) {
   const int lane = threadIdx.x & 31;
@@ -155,13 +158,37 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   if (amax < 1e-12f) amax = 1e-12f;
   const float gs = __fdiv_rn(2688.0f, amax);
-  if (lane == 0) gs_out[r] = gs;
+  const int ncopy = scatter ? k : 1;
+  if (lane < ncopy) gs_out[scatter ? scatter[(size_t)r * k + lane] : r] = gs;
   for (int b = lane; b < K / 16; b += 32) {
+    const uint4 u0 = *(const uint4*)(row + b * 16), u1 = *(const uint4*)(row + b * 16 + 8);
+    const uint32_t ww[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
     float v[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = bf16_to_f32(row[b * 16 + j]);
-    nvfp4_block(v, gs, (uint2*)(q + (size_t)r * (K / 2) + b * 8), sf + (size_t)r * (K / 16) + b);
+    for (int j = 0; j < 8; ++j) {
+      v[2 * j] = __uint_as_float(ww[j] << 16);
+      v[2 * j + 1] = __uint_as_float(ww[j] & 0xFFFF0000u);
+    }
+    uint2 code;
+    uint8_t scale;
+    nvfp4_block(v, gs, &code, &scale);
+    for (int c = 0; c < ncopy; ++c) {
+      const size_t d = scatter ? (size_t)scatter[(size_t)r * k + c] : (size_t)r;
+      *(uint2*)(q + d * (K / 2) + b * 8) = code;
+      sf[d * (K / 16) + b] = scale;
+    }
   }
+}
+
+// out[r] = x[map[r] / k]: the expert-permuted copy of the activation rows (one warp per row).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ map,
+                                                          int k, int rows, int row_vec, uint4* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const uint4* src = x + (size_t)(map[r] / k) * row_vec;
+  uint4* dst = out + (size_t)r * row_vec;
+  for (int c = lane; c < row_vec; c += 32) dst[c] = src[c];
 }
 
 template <int FMT>
@@ -215,10 +242,18 @@ cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_rows(const __nv_bfloat16* x, int rows, int K, uint8_t* q, uint8_t* sf, float* gs,
-                              cudaStream_t s) {
+cudaError_t launch_quant_rows(const __nv_bfloat16* x, const int32_t* scatter, int k, int rows, int K, uint8_t* q,
+                              uint8_t* sf, float* gs, cudaStream_t s) {
   if (rows <= 0) return cudaGetLastError();
-  quant_rows_kernel<<<(rows + 7) / 8, 256, 0, s>>>((const uint16_t*)x, rows, K, q, sf, gs);
+  quant_rows_kernel<<<(rows + 7) / 8, 256, 0, s>>>((const uint16_t*)x, scatter, k, rows, K, q, sf, gs);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* map, int k, int rows, int K, __nv_bfloat16* out,
+                               cudaStream_t s) {
+  if (rows <= 0) return cudaGetLastError();
+  gather_rows_kernel<<<(rows + 7) / 8, 256, 0, s>>>((const uint4*)x, map, k, rows, K / 8, (uint4*)out);
   note_launches(1);
   return cudaGetLastError();
 }

@@ -94,6 +94,10 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Plain barrier over the `nthreads` threads that use barrier `id` (1..15).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 // Barrier over the first `nthreads` threads that use barrier `id` (1..15), returning the AND of
 // every participant's `v`; every participant must reach it the same number of times.
 __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
