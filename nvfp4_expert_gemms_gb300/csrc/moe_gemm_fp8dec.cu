@@ -21,8 +21,10 @@
 //                            sub-tile, N = 32 activation rows, K = 32 per instruction, fp32)
 //
 // Warps (448 threads): 0-3 build the B chunk (split activations), 4-11 run the epilogue (warp w:
-// sub-tile (w-4)/4, TMEM lanes 32*(w%4).., one thread per weight row), 12 issues TMA, 13 owns
-// TMEM and issues the MMAs.  Persistent CTAs walk (row tile, column block) work items; two TMEM
+// sub-tile (w-4)/4, TMEM lanes 32*(w%4).., one thread per weight row), 12 issues the weight TMA,
+// 13 owns TMEM and issues the MMAs.  The builders read their 32 bytes of activations per chunk
+// straight from global memory (two chunks ahead): staging the 16 rows through TMA gather4 took
+// the producer thread longer per chunk than the weight tiles take to stream.  Persistent CTAs walk (row tile, column block) work items; two TMEM
 // accumulator buffers let the epilogue of one item overlap the MMAs of the next.
 #include <cudaTypedefs.h>
 
@@ -38,20 +40,17 @@ using namespace tc;
 constexpr int kRows = 16;        // token rows per tile (decode)
 constexpr int kKC = 128;         // K per chunk = one FP8 scale block
 constexpr int kStagesW = 5;      // weight chunks in flight
-constexpr int kStagesA = 2;      // split-activation chunks
-constexpr int kStagesX = 4;      // gathered activation chunks
+constexpr int kStagesA = 4;      // split-activation chunks
 constexpr int kPrepWarps = 4, kEpiWarp0 = 4, kEpiWarps = 8, kProdWarp = 12, kMmaWarp = 13;
 constexpr int kThreads = 14 * 32;
 constexpr int kWSub = 128 * 128;       // one 128x128 E4M3 tile (128-byte swizzle)
 constexpr int kASub = 32 * 128;        // split-activation tile: 32 rows (hi, lo) x 128 K of E4M3
-constexpr int kXStage = kRows * 256;   // 16 rows x 128 K bf16 (two swizzle atoms)
 constexpr uint32_t kTmemCols = 128;    // two accumulator buffers x two sub-tiles x 32 columns
-constexpr size_t kSmem = 1024 + (size_t)kStagesW * 2 * kWSub + (size_t)kStagesA * 2 * kASub +
-                         (size_t)kStagesX * kXStage;
+constexpr size_t kSmem = 1024 + (size_t)kStagesW * 2 * kWSub + (size_t)kStagesA * 2 * kASub;
 
 struct Fp8Args {
   CUtensorMap wmap;    // E4M3 codes [E*N, K]
-  CUtensorMap xmap;    // activations: x [T, H] (one-row box, gathered) or h [R, I] (16-row box)
+  const uint16_t* act;     // activations (bf16): x [T, K] (rows by token) or h [R, K] (permuted rows)
   const float* scale_inv;  // [E, N/128, K/128]
   const float* rowmax;     // max |activation| per source row (x: per token, h: per permuted row)
   const int32_t* perm;
@@ -100,9 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
   char* smem = (char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   char* sW = smem;
   char* sA = sW + kStagesW * 2 * kWSub;
-  char* sX = sA + kStagesA * 2 * kASub;
-  __shared__ uint64_t w_full[kStagesW], w_empty[kStagesW], a_full[kStagesA], a_empty[kStagesA], x_full[kStagesX],
-      x_empty[kStagesX], acc_full[2], acc_empty[2], drain;
+  __shared__ uint64_t w_full[kStagesW], w_empty[kStagesW], a_full[kStagesA], a_empty[kStagesA], acc_full[2],
+      acc_empty[2], drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -122,10 +120,6 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
       mbar_init(&a_full[i], kPrepWarps);
       mbar_init(&a_empty[i], 1);
     }
-    for (int i = 0; i < kStagesX; ++i) {
-      mbar_init(&x_full[i], 1);
-      mbar_init(&x_empty[i], kPrepWarps);
-    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], kEpiWarps);
@@ -140,7 +134,6 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
   }
   if (warp == kProdWarp && lane == 0) {
     prefetch_tmap(&a.wmap);
-    prefetch_tmap(&a.xmap);
   }
   fence_proxy_async_smem();
   fence_before_sync();
@@ -179,46 +172,35 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
   };
 
   if (warp == kProdWarp) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer (weights only; whole warp walks the loop) ----------------
     int it = 0;
     bool ok = true;
+    int armed[kStagesW] = {0};
     for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x) {
       TileEntry te;
       int nb0, nb1, nsub;
       item(wk, te, nb0, nb1, nsub);
-      int tok = 0;
-      if (MODE == 0 && lane < kRows) tok = a.perm[te.row0 + (lane < te.rows ? lane : te.rows - 1)] / a.k;
       for (int kc = 0; kc < nK; ++kc, ++it) {
-        const int sw = it % kStagesW, sx = it % kStagesX;
+        const int sw = it % kStagesW;
         if (lane == 0) {
           ok = mbar_wait(&w_empty[sw], ((it / kStagesW) & 1) ^ 1, &s_abort);
           if (ok) {
             mbar_arrive_expect_tx(&w_full[sw], nsub * kWSub);
+            ++armed[sw];
             tma_load_2d(sW + sw * 2 * kWSub, &a.wmap, &w_full[sw], kc * kKC, te.expert * a.N + nb0);
             if (nsub == 2) tma_load_2d(sW + sw * 2 * kWSub + kWSub, &a.wmap, &w_full[sw], kc * kKC, te.expert * a.N + nb1);
-            ok = mbar_wait(&x_empty[sx], ((it / kStagesX) & 1) ^ 1, &s_abort);
           }
-          if (ok) mbar_arrive_expect_tx(&x_full[sx], kXStage);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        char* xd = sX + sx * kXStage;
-        if (MODE == 0) {
-#pragma unroll
-          for (int j = 0; j < kRows; j += 4) {
-            const int r0 = __shfl_sync(0xffffffffu, tok, j), r1 = __shfl_sync(0xffffffffu, tok, j + 1);
-            const int r2 = __shfl_sync(0xffffffffu, tok, j + 2), r3 = __shfl_sync(0xffffffffu, tok, j + 3);
-            if (lane == 0) {
-              tma_gather4(xd + j * 128, &a.xmap, &x_full[sx], kc * kKC, r0, r1, r2, r3);
-              tma_gather4(xd + kRows * 128 + j * 128, &a.xmap, &x_full[sx], kc * kKC + 64, r0, r1, r2, r3);
-            }
-          }
-        } else if (lane == 0) {
-          tma_load_2d(xd, &a.xmap, &x_full[sx], kc * kKC, te.row0);
-          tma_load_2d(xd + kRows * 128, &a.xmap, &x_full[sx], kc * kKC + 64, te.row0);
-        }
       }
     }
+    if (lane == 0 && s_abort) {  // let every issued copy land before shared memory goes away
+      volatile int no_abort = 0;
+      for (int i = 0; i < kStagesW; ++i)
+        if (armed[i]) mbar_wait(&w_full[i], (armed[i] - 1) & 1, &no_abort);
+    }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer (whole warp waits, lane 0 issues) ----------------
     const uint32_t idesc = idesc_e4m3_f32(128, 32);
@@ -268,25 +250,35 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
       int nb0, nb1, nsub;
       item(wk, te, nb0, nb1, nsub);
       const bool real = j < te.rows;
+      // 16 bf16 of row j at K = 128 kc + 16q .. +15, loaded two chunks ahead of their use
+      const uint16_t* xrow = nullptr;
+      if (real) xrow = a.act + (size_t)(MODE == 0 ? a.perm[te.row0 + j] / a.k : te.row0 + j) * a.K + q * 16;
+      auto load = [&](int kc, uint4& v0, uint4& v1) {
+        if (xrow != nullptr && kc < nK) {
+          v0 = __ldg((const uint4*)(xrow + kc * kKC));
+          v1 = __ldg((const uint4*)(xrow + kc * kKC + 8));
+        } else {
+          v0 = v1 = make_uint4(0u, 0u, 0u, 0u);
+        }
+      };
+      uint4 n0a, n0b, n1a, n1b;
+      load(0, n0a, n0b);
+      load(1, n1a, n1b);
       const float u = row_norm(te, j, item_smax(te, nb0, nb1, nsub));
       float sc_next0 = scale_at(te, nb0, 0), sc_next1 = nsub == 2 ? scale_at(te, nb1, 0) : 0.f;
       for (int kc = 0; kc < nK; ++kc, ++it) {
-        const int sx = it % kStagesX, sa = it % kStagesA;
+        const int sa = it % kStagesA;
         const float f0 = sc_next0 * u, f1 = sc_next1 * u;
         if (kc + 1 < nK) {
           sc_next0 = scale_at(te, nb0, kc + 1);
           if (nsub == 2) sc_next1 = scale_at(te, nb1, kc + 1);
         }
-        ok = mbar_wait(&x_full[sx], (it / kStagesX) & 1, &s_abort) &&
-             mbar_wait(&a_empty[sa], ((it / kStagesA) & 1) ^ 1, &s_abort);
+        const uint4 x0 = n0a, x1 = n0b;
+        n0a = n1a;
+        n0b = n1b;
+        load(kc + 2, n1a, n1b);
+        ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[sa], ((it / kStagesA) & 1) ^ 1, &s_abort));
         if (!ok) break;
-        // 16 bf16 of row j at K = 16q .. 16q+15: atom q/4, 16-byte chunks 2(q%4) and 2(q%4)+1
-        const char* xr = sX + sx * kXStage + (q >> 2) * (kRows * 128) + j * 128;
-        const int c0 = 2 * (q & 3);
-        const uint4 x0 = *(const uint4*)(xr + ((c0 ^ (j & 7)) * 16));
-        const uint4 x1 = *(const uint4*)(xr + (((c0 + 1) ^ (j & 7)) * 16));
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&x_empty[sx]);
         const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         for (int g = 0; g < nsub; ++g) {
           const float f = g == 0 ? f0 : f1;
@@ -429,10 +421,9 @@ cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed
   // x row maxima and the zeroed h row maxima come from the routing launch (RoutePrelude)
 
   if (!tc_make_map(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, gu.a, H, (uint64_t)E * 2 * I, H, 128, 128,
-                       CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc_make_map(&a.xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, H, (uint64_t)T, (uint64_t)H * 2, 64, 1,
-                       CU_TENSOR_MAP_SWIZZLE_128B))
+                   CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  a.act = (const uint16_t*)x;
   a.scale_inv = (const float*)gu.b;
   a.rowmax = (const float*)(ws + L.xmax);
   a.N = 2 * I;
@@ -443,10 +434,9 @@ cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed
   record_event(ev.stop[0], s);
 
   if (!tc_make_map(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, dn.a, I, (uint64_t)E * H, I, 128, 128,
-                       CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc_make_map(&a.xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws + L.h, I, (uint64_t)R, (uint64_t)I * 2, 64, kRows,
-                       CU_TENSOR_MAP_SWIZZLE_128B))
+                   CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  a.act = (const uint16_t*)(ws + L.h);
   a.scale_inv = (const float*)dn.b;
   a.rowmax = (const float*)(ws + L.hmax);
   a.N = H;
