@@ -104,6 +104,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
+  // The gate/up GEMM follows the routing launch that writes the tile table; the down GEMM
+  // follows the gate/up GEMM, whose own pdl_wait() came after routing had finished.
+  if (MODE == 0) pdl_wait();
   const int ntiles = a.tiles[0].expert;
   const int ncb = MODE == 0 ? a.I / 128 : (a.H + 255) / 256;
   const int nwork = ntiles * ncb;
@@ -140,6 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = s_tmem;
+  // Down GEMM: the weight producer starts streaming at once (packed weights and the tile table
+  // only); every other role waits for the gate/up GEMM's h and row maxima.
+  if (MODE == 1 && warp != kProdWarp) pdl_wait();
+  pdl_trigger();
 
   auto item = [&](int wk, TileEntry& te, int& nb0, int& nb1, int& nsub) {
     te = a.tiles[1 + wk / ncb];
@@ -430,7 +437,8 @@ cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed
   a.K = H;
   int grid = max_tiles * (I / 128);
   record_event(ev.start[0], s);
-  fp8dec_kernel<0><<<grid < sms ? grid : sms, kThreads, kSmem, s>>>(a);
+  cudaError_t err = launch_pdl(fp8dec_kernel<0>, dim3(grid < sms ? grid : sms), dim3(kThreads), kSmem, s, a);
+  if (err != cudaSuccess) return err;
   record_event(ev.stop[0], s);
 
   if (!tc_make_map(&a.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, dn.a, I, (uint64_t)E * H, I, 128, 128,
@@ -443,10 +451,10 @@ cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed
   a.K = I;
   grid = max_tiles * ((H + 255) / 256);
   record_event(ev.start[1], s);
-  fp8dec_kernel<1><<<grid < sms ? grid : sms, kThreads, kSmem, s>>>(a);
+  err = launch_pdl(fp8dec_kernel<1>, dim3(grid < sms ? grid : sms), dim3(kThreads), kSmem, s, a);
   record_event(ev.stop[1], s);
   note_launches(2);
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace moe

@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(128) down_simt_kernel(MatView dn, const uint16
 }
 
 __global__ void finalize_kernel(const float* __restrict__ acc, uint16_t* __restrict__ out, size_t n) {
+  pdl_wait();
   const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (i >= n) return;
   if (i + 3 < n) {
@@ -197,9 +198,9 @@ cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const
   }
   if (e != cudaSuccess) return e;
   const unsigned blocks = (unsigned)((n_out / 4 + 255) / 256 + 1);
-  finalize_kernel<<<blocks, 256, 0, s>>>((const float*)(ws + L.out_acc), (uint16_t*)out, n_out);
   note_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(finalize_kernel, dim3(blocks), dim3(256), 0, s, (const float*)(ws + L.out_acc), (uint16_t*)out,
+                    n_out);
 }
 
 int simt_row_block() { return kSimtRB; }

@@ -110,6 +110,28 @@ struct StepEvents {
 cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,
                            int k, int row_block, const WsLayout& L, char* ws, __nv_bfloat16* out,
                            const StepEvents& ev, cudaStream_t s);
+// Programmatic dependent launch.  A kernel started with launch_pdl may begin while the previous
+// kernel of the stream is still running (in a CUDA graph the edge becomes programmatic): it sets
+// up shared and tensor memory, then calls pdl_wait() before it touches memory that earlier
+// kernels write or read, and pdl_trigger() to let its own dependent start setting up.  Only
+// read-only data (packed weights) and the routing tile table, which is final before the
+// previous GEMM passed its own pdl_wait(), may be read before pdl_wait().
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 // Record a timing event on s; under stream capture it becomes an event-record node of the graph.
 inline void record_event(cudaEvent_t ev, cudaStream_t s) {
   if (!ev) return;

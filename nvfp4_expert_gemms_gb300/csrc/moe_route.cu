@@ -8,11 +8,15 @@
 //   1. route_topk_kernel   one warp per token; per-block expert histogram in shared memory
 //   2. route_scan_kernel   one block: expert totals, offsets, per-block bases, GEMM tile table
 //   3. route_scatter_kernel rank of each row inside its block from per-warp ballot masks
+// Up to kRouteTB tokens (decode) all three steps run in one block of one launch
+// (route_small_kernel), which produces the same outputs.
 #include "moe_internal.cuh"
 
 namespace moe {
 
 namespace {
+
+constexpr int kRouteSmallZeroMax = 1 << 18;  // fp32 accumulators one block zeroes quickly (1 MB)
 
 struct Cand {
   float v;
@@ -25,6 +29,88 @@ __device__ __forceinline__ bool beats(float av, int ai, float bv, int bi) {
   return av > bv || (av == bv && ai < bi);
 }
 
+// Zero the accumulators of this forward pass (grid-stride over all launched threads).
+__device__ __forceinline__ void zero_prelude(const RoutePrelude& pre) {
+  const size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = g; i < pre.n_f32 / 4; i += stride) ((float4*)pre.zero_f32)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (size_t i = g; i < pre.n_u32; i += stride) pre.zero_u32[i] = 0u;
+}
+
+// max |x| of token t's activation row (one warp); all loads are issued before use.
+__device__ __forceinline__ void row_absmax(const RoutePrelude& pre, int t, int lane) {
+  float m = 0.f;
+  const uint16_t* row = pre.x + (size_t)t * pre.H;
+  for (int c0 = lane * 8; c0 < pre.H; c0 += 256 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = c0 + u * 256 < pre.H ? *(const uint4*)(row + c0 + u * 256) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[i] << 16)), fabsf(__uint_as_float(w4[i] & 0xFFFF0000u))));
+    }
+  }
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane == 0) pre.xmax[t] = m;
+}
+
+// Top-k of token t (one warp): writes its k expert indices and renormalised softmax weights and
+// returns, in lane j < k, the j-th selected expert.
+__device__ __forceinline__ int route_token(const float* __restrict__ logits, int t, int E, int k, int lane,
+                                           int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  float v[kMaxE / 32];
+#pragma unroll
+  for (int m = 0; m < kMaxE / 32; ++m) {
+    const int e = lane + 32 * m;
+    float x = e < E ? logits[(size_t)t * E + e] : -INFINITY;
+    v[m] = isnan(x) ? -INFINITY : x;
+  }
+  uint32_t taken = 0;  // bit m: candidate lane + 32m already selected
+  float selv[kMaxTopK];
+  int seli[kMaxTopK];
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int m = 0; m < kMaxE / 32; ++m) {
+      const int e = lane + 32 * m;
+      if (e < E && !((taken >> m) & 1u) && beats(v[m], e, bv, bi)) {
+        bv = v[m];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (beats(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    selv[j] = bv;
+    seli[j] = bi;
+  }
+  // renormalised softmax over the selected logits (descending: selv[0] is the max)
+  float den = 0.f;
+  for (int j = 0; j < k; ++j) den += expf(selv[j] - selv[0]);
+  float mine = selv[0];
+  int mi = seli[0];
+  for (int j = 1; j < k; ++j)
+    if (j == lane) {
+      mine = selv[j];
+      mi = seli[j];
+    }
+  if (lane < k) {
+    topk_idx[(size_t)t * k + lane] = mi;
+    topk_w[(size_t)t * k + lane] = expf(mine - selv[0]) / den;
+  }
+  return mi;
+}
+
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int32_t* __restrict__ topk_idx,
                                                          float* __restrict__ topk_w,
@@ -32,82 +118,14 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   __shared__ int cnt[kMaxE];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
-  {  // zero the accumulators of this forward pass (grid-stride)
-    const size_t g = (size_t)blockIdx.x * blockDim.x + tid, stride = (size_t)gridDim.x * blockDim.x;
-    for (size_t i = g; i < pre.n_f32 / 4; i += stride) ((float4*)pre.zero_f32)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (size_t i = g; i < pre.n_u32; i += stride) pre.zero_u32[i] = 0u;
-  }
+  zero_prelude(pre);
   if (blockIdx.x == 0 && tid == 0) *err = kDevOk;  // each forward pass reports its own errors
   __syncthreads();
   const int t_end = min(T, (int)(blockIdx.x + 1) * kRouteTB);
   for (int t = blockIdx.x * kRouteTB + warp; t < t_end; t += 8) {  // tokens round-robin over the warps
-    if (pre.x) {  // max |x| of the token's activation row; all loads issued before use
-      float m = 0.f;
-      const uint16_t* row = pre.x + (size_t)t * pre.H;
-      for (int c0 = lane * 8; c0 < pre.H; c0 += 256 * 8) {
-        uint4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = c0 + u * 256 < pre.H ? *(const uint4*)(row + c0 + u * 256) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[i] << 16)), fabsf(__uint_as_float(w4[i] & 0xFFFF0000u))));
-        }
-      }
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      if (lane == 0) pre.xmax[t] = m;
-    }
-    float v[kMaxE / 32];
-#pragma unroll
-    for (int m = 0; m < kMaxE / 32; ++m) {
-      const int e = lane + 32 * m;
-      float x = e < E ? logits[(size_t)t * E + e] : -INFINITY;
-      v[m] = isnan(x) ? -INFINITY : x;
-    }
-    uint32_t taken = 0;  // bit m: candidate lane + 32m already selected
-    float selv[kMaxTopK];
-    int seli[kMaxTopK];
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
-#pragma unroll
-      for (int m = 0; m < kMaxE / 32; ++m) {
-        const int e = lane + 32 * m;
-        if (e < E && !((taken >> m) & 1u) && beats(v[m], e, bv, bi)) {
-          bv = v[m];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (beats(ov, oi, bv, bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      selv[j] = bv;
-      seli[j] = bi;
-    }
-    // renormalised softmax over the selected logits (descending: selv[0] is the max)
-    float den = 0.f;
-    for (int j = 0; j < k; ++j) den += expf(selv[j] - selv[0]);
-    if (lane < k) {
-      float mine = selv[0];
-      int mi = seli[0];
-      for (int j = 1; j < k; ++j)
-        if (j == lane) {
-          mine = selv[j];
-          mi = seli[j];
-        }
-      topk_idx[(size_t)t * k + lane] = mi;
-      topk_w[(size_t)t * k + lane] = expf(mine - selv[0]) / den;
-      atomicAdd(&cnt[mi], 1);
-    }
+    if (pre.x) row_absmax(pre, t, lane);
+    const int mi = route_token(logits, t, E, k, lane, topk_idx, topk_w);
+    if (lane < k) atomicAdd(&cnt[mi], 1);
   }
   __syncthreads();
   for (int e = tid; e < E; e += blockDim.x) blkcnt[(size_t)blockIdx.x * E + e] = cnt[e];
@@ -201,6 +219,85 @@ __global__ void __launch_bounds__(kRouteTB) route_scatter_kernel(const int32_t* 
   }
 }
 
+// All of routing in one block of 1024 threads (T <= kRouteTB): top-k by warps with the expert
+// histogram and per-32-token membership masks in shared memory, then the scan and tile table,
+// then each row's rank among the rows of its expert (tokens in order), as the three kernels
+// above compute them.
+__global__ void __launch_bounds__(1024) route_small_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                           int row_block, int max_tiles,
+                                                           int32_t* __restrict__ topk_idx,
+                                                           float* __restrict__ topk_w, int32_t* __restrict__ offsets,
+                                                           int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                                                           TileEntry* __restrict__ tiles, int* err, RoutePrelude pre) {
+  __shared__ int cnt[kMaxE], off_s[kMaxE + 1], toff_s[kMaxE + 1];
+  __shared__ uint32_t mask[kRouteTB / 32][kMaxE];
+  __shared__ uint8_t sel_e[kRouteTB][kMaxTopK];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  for (int i = tid; i < (kRouteTB / 32) * kMaxE; i += blockDim.x) (&mask[0][0])[i] = 0u;
+  pdl_wait();  // the previous kernel of the stream may still read the accumulators zeroed here
+  pdl_trigger();
+  zero_prelude(pre);
+  if (tid == 0) *err = kDevOk;
+  __syncthreads();
+  for (int t = warp; t < T; t += 32) {
+    if (pre.x) row_absmax(pre, t, lane);
+    const int mi = route_token(logits, t, E, k, lane, topk_idx, topk_w);
+    if (lane < k) {
+      atomicAdd(&cnt[mi], 1);
+      atomicOr(&mask[t >> 5][mi], 1u << (t & 31));
+      sel_e[t][lane] = (uint8_t)mi;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {  // E <= 256: a serial scan is a few hundred cycles
+    int a = 0, b = 0;
+    for (int i = 0; i < E; ++i) {
+      off_s[i] = a;
+      toff_s[i] = b;
+      a += cnt[i];
+      b += (cnt[i] + row_block - 1) / row_block;
+    }
+    off_s[E] = a;
+    toff_s[E] = b;
+    TileEntry h;
+    h.expert = min(b, max_tiles);
+    h.row0 = a;
+    h.rows = row_block;
+    h.pad = 0;
+    tiles[0] = h;
+  }
+  __syncthreads();
+  if (tid <= E) offsets[tid] = off_s[tid];
+  if (tid < E) {
+    const int ntl = (cnt[tid] + row_block - 1) / row_block, t0 = toff_s[tid];
+    for (int i = 0; i < ntl; ++i) {
+      if (t0 + i >= max_tiles) {
+        set_dev_error(err, kDevFault);
+        break;
+      }
+      TileEntry te;
+      te.expert = tid;
+      te.row0 = off_s[tid] + i * row_block;
+      te.rows = min(row_block, cnt[tid] - i * row_block);
+      te.pad = 0;
+      tiles[1 + t0 + i] = te;
+    }
+  }
+  if (tid < T) {
+    const int t = tid, g = t >> 5;
+    const uint32_t lt = (1u << (t & 31)) - 1u;
+    for (int j = 0; j < k; ++j) {
+      const int e = sel_e[t][j];
+      int rank = __popc(mask[g][e] & lt);
+      for (int w = 0; w < g; ++w) rank += __popc(mask[w][e]);
+      const int pos = off_s[e] + rank;
+      perm[pos] = t * k + j;
+      inv[(size_t)t * k + j] = pos;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int row_block, const WsLayout& L, char* ws,
@@ -215,6 +312,11 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int row_block
   int32_t* inv = (int32_t*)(ws + L.inv);
   TileEntry* tiles = (TileEntry*)(ws + L.tiles);
   const int nb = L.nb;
+  if (T > 0 && T <= kRouteTB && pre.n_f32 <= (size_t)kRouteSmallZeroMax) {
+    note_launches(1);
+    return launch_pdl(route_small_kernel, dim3(1), dim3(1024), 0, s, logits, T, E, k, row_block, L.max_tiles, idx,
+                      w, off, perm, inv, tiles, err, pre);
+  }
   if (T > 0) route_topk_kernel<<<nb, 256, 0, s>>>(logits, T, E, k, idx, w, blkcnt, err, pre);
   else cudaMemsetAsync(err, 0, sizeof(int), s);
   route_scan_kernel<<<1, 1024, 0, s>>>(blkcnt, T > 0 ? nb : 0, E, row_block, L.max_tiles, off, blkbase, tiles,
