@@ -122,6 +122,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   __shared__ __align__(16) float s_cs[2][BN];
   __shared__ __align__(16) int s_ct[2][BN];
 
+  // gate/up: wait for the activation quantization (and, before it, routing); down: the tile table
+  // was final before the gate/up GEMM passed its own pdl_wait(), so only the h codes need the wait
+  if (MODE == 0) pdl_wait();
   const int ntiles = a.tiles[0].expert;
   const int ncb = MODE == 0 ? a.I / 128 : (a.H + 255) / 256;
   const int nwork = ntiles * ncb;
@@ -161,6 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = s_tmem;
+  if (MODE == 1 && warp != kProdWarp) pdl_wait();  // the producer waits before its first h tile
+  pdl_trigger();
 
   auto item = [&](int wk, TileEntry& te, int& nb0, int& nb1, int& nsub) {
     te = a.tiles[1 + wk / ncb];
@@ -201,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
           }
           if (ok) {
             ok = mbar_wait(&x_empty[sx], ((it / kStagesX) & 1) ^ 1, &s_abort);
+            if (MODE == 1 && it == 0) pdl_wait();
             if (ok) {
               mbar_arrive_expect_tx(&x_full[sx], Fp4Cfg<MODE, BN>::kXBytes);
               ++armed_x[sx];
@@ -427,8 +433,8 @@ static cudaError_t launch_fp4_one(const Fp4Args& a, int work, cudaStream_t s) {
     attr = true;
   }
   const int sms = tc_num_sms();
-  fp4_kernel<MODE, BN><<<work < sms ? work : sms, kThreads, Fp4Cfg<MODE, BN>::kSmem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(fp4_kernel<MODE, BN>, dim3(work < sms ? work : sms), dim3(kThreads), Fp4Cfg<MODE, BN>::kSmem, s,
+                    a);
 }
 
 template <int MODE>

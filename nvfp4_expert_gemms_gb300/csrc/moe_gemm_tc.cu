@@ -248,6 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   __shared__ int s_ct[2][BN];      // down epilogue: token of each column
   __shared__ float s_cw[2][BN];    // down epilogue: routing weight / global scale of each column
 
+  // gate/up: the tile table may come from the launch right before this one; down: it was final
+  // before the gate/up GEMM passed its own pdl_wait(), so only the activations need the wait
+  if (MODE == 0) pdl_wait();
   const int ntiles = a.tiles[0].expert;  // header entry holds the tile count
   const int ncb = MODE == 0 ? a.I / 128 : (a.H + 255) / 256;
   const int nwork = ntiles * ncb;
@@ -285,6 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = s_tmem;
+  if (MODE == 1 && warp != kProdWarp) pdl_wait();  // the producer waits before its first h tile
+  pdl_trigger();
 
   // per-item geometry
   auto item = [&](int wk, TileEntry& te, int& nb0, int& nb1, int& nsub) {
@@ -330,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
           }
           if (ok && !kGather) {
             ok = mbar_wait(&b_empty[sb], ((it / SB) & 1) ^ 1, &s_abort);
+            if (MODE == 1 && it == 0) pdl_wait();
             if (ok) {
               char* bd = sB + sb * BSTAGE;
               mbar_arrive_expect_tx(&b_full[sb], BSTAGE);
@@ -616,9 +622,8 @@ cudaError_t launch_one(const TcArgs& args, int grid_x, int grid_y, cudaStream_t 
     cudaFuncSetAttribute(tc_expert_gemm_kernel<FMT, MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     attr = true;
   }
-  tc_expert_gemm_kernel<FMT, MODE, BN><<<dim3(grid_x * grid_y < num_sms() ? grid_x * grid_y : num_sms()), kThreads,
-                                          smem, s>>>(args);
-  return cudaGetLastError();
+  return launch_pdl(tc_expert_gemm_kernel<FMT, MODE, BN>,
+                    dim3(grid_x * grid_y < num_sms() ? grid_x * grid_y : num_sms()), dim3(kThreads), smem, s, args);
 }
 
 template <int FMT, int MODE>

@@ -143,6 +143,8 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
                                                          float* __restrict__ gs_out) {
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  pdl_wait();
+  pdl_trigger();
   if (r >= rows) return;
   const uint16_t* row = x + (size_t)r * K;
   float amax = 0.f;
@@ -185,6 +187,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           int k, int rows, int row_vec, uint4* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  pdl_wait();
+  pdl_trigger();
   if (r >= rows) return;
   const uint4* src = x + (size_t)(map[r] / k) * row_vec;
   uint4* dst = out + (size_t)r * row_vec;
@@ -245,17 +249,17 @@ cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e
 cudaError_t launch_quant_rows(const __nv_bfloat16* x, const int32_t* scatter, int k, int rows, int K, uint8_t* q,
                               uint8_t* sf, float* gs, cudaStream_t s) {
   if (rows <= 0) return cudaGetLastError();
-  quant_rows_kernel<<<(rows + 7) / 8, 256, 0, s>>>((const uint16_t*)x, scatter, k, rows, K, q, sf, gs);
   note_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(quant_rows_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, (const uint16_t*)x, scatter, k, rows, K,
+                    q, sf, gs);
 }
 
 cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* map, int k, int rows, int K, __nv_bfloat16* out,
                                cudaStream_t s) {
   if (rows <= 0) return cudaGetLastError();
-  gather_rows_kernel<<<(rows + 7) / 8, 256, 0, s>>>((const uint4*)x, map, k, rows, K / 8, (uint4*)out);
   note_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, (const uint4*)x, map, k, rows, K / 8,
+                    (uint4*)out);
 }
 
 }  // namespace moe

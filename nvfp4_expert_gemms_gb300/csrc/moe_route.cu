@@ -118,6 +118,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   __shared__ int cnt[kMaxE];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  pdl_wait();
+  pdl_trigger();
   zero_prelude(pre);
   if (blockIdx.x == 0 && tid == 0) *err = kDevOk;  // each forward pass reports its own errors
   __syncthreads();
@@ -139,6 +141,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
                                                           TileEntry* __restrict__ tiles, int* err) {
   __shared__ int tot[kMaxE], ntl[kMaxE], off_s[kMaxE + 1], toff_s[kMaxE + 1];
   const int e = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (e < E) {
     int s = 0;
     for (int b = 0; b < nb; ++b) s += blkcnt[(size_t)b * E + e];
@@ -197,6 +201,8 @@ __global__ void __launch_bounds__(kRouteTB) route_scatter_kernel(const int32_t* 
   __shared__ uint32_t mask[kRouteTB / 32][kMaxE];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < (kRouteTB / 32) * kMaxE; i += blockDim.x) (&mask[0][0])[i] = 0u;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   const int t = blockIdx.x * kRouteTB + tid;
   int ex[kMaxTopK];
@@ -317,13 +323,17 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int row_block
     return launch_pdl(route_small_kernel, dim3(1), dim3(1024), 0, s, logits, T, E, k, row_block, L.max_tiles, idx,
                       w, off, perm, inv, tiles, err, pre);
   }
-  if (T > 0) route_topk_kernel<<<nb, 256, 0, s>>>(logits, T, E, k, idx, w, blkcnt, err, pre);
-  else cudaMemsetAsync(err, 0, sizeof(int), s);
-  route_scan_kernel<<<1, 1024, 0, s>>>(blkcnt, T > 0 ? nb : 0, E, row_block, L.max_tiles, off, blkbase, tiles,
-                                       err);
-  if (T > 0) route_scatter_kernel<<<nb, kRouteTB, 0, s>>>(idx, T, E, k, blkbase, perm, inv);
+  cudaError_t e = cudaSuccess;
+  if (T > 0) e = launch_pdl(route_topk_kernel, dim3(nb), dim3(256), 0, s, logits, T, E, k, idx, w, blkcnt, err, pre);
+  else e = cudaMemsetAsync(err, 0, sizeof(int), s);
+  if (e == cudaSuccess)
+    e = launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)blkcnt, T > 0 ? nb : 0, E, row_block,
+                   L.max_tiles, off, blkbase, tiles, err);
+  if (e == cudaSuccess && T > 0)
+    e = launch_pdl(route_scatter_kernel, dim3(nb), dim3(kRouteTB), 0, s, (const int32_t*)idx, T, E, k,
+                   (const int32_t*)blkbase, perm, inv);
   note_launches(T > 0 ? 3 : 1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace moe
