@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   // gate/up: wait for the activation quantization (and, before it, routing); down: the tile table
   // was final before the gate/up GEMM passed its own pdl_wait(), so only the h codes need the wait
   if (MODE == 0) pdl_wait();
-  const int ntiles = a.tiles[0].expert;
+  const int ntiles = load_tile(a.tiles).expert;
   const int ncb = MODE == 0 ? a.I / 128 : (a.H + 255) / 256;
   const int nwork = ntiles * ncb;
   if ((int)blockIdx.x >= nwork) return;
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   pdl_trigger();
 
   auto item = [&](int wk, TileEntry& te, int& nb0, int& nb1, int& nsub) {
-    te = a.tiles[1 + wk / ncb];
+    te = load_tile(a.tiles + 1 + wk / ncb);
     const int cb = wk % ncb;
     if (MODE == 0) {
       nb0 = cb * 128;

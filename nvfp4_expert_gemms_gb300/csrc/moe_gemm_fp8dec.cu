@@ -28,6 +28,7 @@
 // accumulator buffers let the epilogue of one item overlap the MMAs of the next.
 #include <cudaTypedefs.h>
 
+#include "moe_dec.cuh"
 #include "moe_formats.cuh"
 #include "moe_tc.cuh"
 
@@ -36,8 +37,8 @@ namespace moe {
 namespace {
 
 using namespace tc;
+using namespace dec;
 
-constexpr int kRows = 16;        // token rows per tile (decode)
 constexpr int kKC = 128;         // K per chunk = one FP8 scale block
 constexpr int kStagesW = 5;      // weight chunks in flight
 constexpr int kStagesA = 4;      // split-activation chunks
@@ -63,36 +64,6 @@ struct Fp8Args {
   int k, N, K, I, H;
 };
 
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
-  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);  // A, B = E4M3 (0)
-}
-
-__device__ __forceinline__ void mma_f8_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
-  return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
-}
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t v) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
-  return __half22float2(__half2(h));
-}
-
-// Largest power of two u with amax * smax * u <= 448 (1 when the row is all zeros).
-__device__ __forceinline__ float pow2_norm(float amax, float smax) {
-  const float m = amax * smax;
-  if (!(m > 0.f)) return 1.f;
-  int e;
-  frexpf(448.0f / m, &e);  // 448/m = f * 2^e, f in [0.5, 1); inf / denormal ranges clamp below
-  e = e - 1 < -126 ? -126 : (e - 1 > 126 ? 126 : e - 1);
-  return ldexpf(1.0f, e);
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_constant__ Fp8Args a) {
   extern __shared__ __align__(1024) char smem_raw[];
@@ -107,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
   // The gate/up GEMM follows the routing launch that writes the tile table; the down GEMM
   // follows the gate/up GEMM, whose own pdl_wait() came after routing had finished.
   if (MODE == 0) pdl_wait();
-  const int ntiles = a.tiles[0].expert;
+  const int ntiles = load_tile(a.tiles).expert;
   const int ncb = MODE == 0 ? a.I / 128 : (a.H + 255) / 256;
   const int nwork = ntiles * ncb;
   if ((int)blockIdx.x >= nwork) return;
@@ -149,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
   pdl_trigger();
 
   auto item = [&](int wk, TileEntry& te, int& nb0, int& nb1, int& nsub) {
-    te = a.tiles[1 + wk / ncb];
+    te = load_tile(a.tiles + 1 + wk / ncb);
     const int cb = wk % ncb;
     if (MODE == 0) {
       nb0 = cb * 128;
@@ -175,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
   auto row_norm = [&](const TileEntry& te, int j, float smax) {
     if (j >= te.rows) return 1.f;
     const int src = MODE == 0 ? a.perm[te.row0 + j] / a.k : te.row0 + j;
-    return pow2_norm(a.rowmax[src], smax);
+    return pow2_norm(__ldcg(a.rowmax + src), smax);
   };
 
   if (warp == kProdWarp) {
@@ -262,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
       if (real) xrow = a.act + (size_t)(MODE == 0 ? a.perm[te.row0 + j] / a.k : te.row0 + j) * a.K + q * 16;
       auto load = [&](int kc, uint4& v0, uint4& v1) {
         if (xrow != nullptr && kc < nK) {
-          v0 = __ldg((const uint4*)(xrow + kc * kKC));
-          v1 = __ldg((const uint4*)(xrow + kc * kKC + 8));
+          v0 = __ldcg((const uint4*)(xrow + kc * kKC));
+          v1 = __ldcg((const uint4*)(xrow + kc * kKC + 8));
         } else {
           v0 = v1 = make_uint4(0u, 0u, 0u, 0u);
         }

@@ -66,14 +66,22 @@ struct WFmt<MOE_FMT_NVFP4_W4A16> {
 
 // Shared-memory rings: weight chunks (kStagesW) and activation chunks (SB, each BN rows x 128 K
 // bf16 as two 128-byte swizzle atoms); the gather threads keep LAG chunks in flight.
+// Weight stages fill what the activation ring leaves of ~220 KB, up to 12: a weight stream from
+// HBM needs ~150 KB in flight per SM (about 3.4 us of latency under load at its bandwidth share).
 template <int FMT, int BN>
 struct TcCfg {
   static constexpr int kWSub = WFmt<FMT>::kSubBytes;
-  static constexpr int kStagesW = (FMT == MOE_FMT_FP8_B128_W8A16 && BN == 128) ? 3 : 4;
   static constexpr int kBStage = BN * 256;
-  static constexpr int SB = BN <= 32 ? 4 : (1024 + kStagesW * 2 * kWSub + 4 * kBStage <= 200 * 1024 ? 4 : 3);
+  static constexpr int SB = BN <= 32 ? 4 : (BN == 64 ? 4 : 3);
+  static constexpr int kWFree = 220 * 1024 - 1024 - SB * kBStage;
+  static constexpr int kStagesWFit = kWFree / (2 * kWSub + 2048);
+  static constexpr int kStagesW = kStagesWFit > 12 ? 12 : (kStagesWFit < 2 ? 2 : kStagesWFit);
   static constexpr int LAG = SB - 2;
-  static constexpr size_t kSmem = 1024 + (size_t)kStagesW * 2 * kWSub + (size_t)SB * kBStage;
+  // per weight stage, the chunk's scales (copied by the producer warp next to the TMA tile):
+  // FP8 one fp32 per sub-tile, INT4 128 fp16 per sub-tile, NVFP4 8 E4M3 bytes per row
+  static constexpr int kScaleSlot = 2048;
+  static constexpr size_t kSmem = 1024 + (size_t)kStagesW * 2 * kWSub + (size_t)SB * kBStage +
+                                  (size_t)kStagesW * kScaleSlot;
 };
 
 struct TcArgs {
@@ -240,6 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   char* smem = (char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   char* sW = smem;
   char* sB = smem + kStagesW * WSTAGE;
+  char* sS = sB + SB * BSTAGE;  // scale slots, one per weight stage
+  constexpr int kScaleSlot = Cfg::kScaleSlot;
   __shared__ uint64_t w_full[kStagesW], w_empty[kStagesW], a_full[kStagesA], a_empty[kStagesA], b_full[SB],
       b_empty[SB], acc_full, drain;
   __shared__ uint32_t s_tmem;
@@ -251,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   // gate/up: the tile table may come from the launch right before this one; down: it was final
   // before the gate/up GEMM passed its own pdl_wait(), so only the activations need the wait
   if (MODE == 0) pdl_wait();
-  const int ntiles = a.tiles[0].expert;  // header entry holds the tile count
+  const int ntiles = load_tile(a.tiles).expert;  // header entry holds the tile count
   const int ncb = MODE == 0 ? a.I / 128 : (a.H + 255) / 256;
   const int nwork = ntiles * ncb;
   if ((int)blockIdx.x >= nwork) return;
@@ -260,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStagesW; ++i) {
-      mbar_init(&w_full[i], 1);
+      mbar_init(&w_full[i], 1 + 32);  // the TMA issue plus one cp.async arrival per producer lane
       mbar_init(&w_empty[i], kConvWarps);
     }
     for (int i = 0; i < kStagesA; ++i) {
@@ -294,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   // per-item geometry
   auto item = [&](int wk, TileEntry& te, int& nb0, int& nb1, int& nsub) {
     const int tile = wk / ncb, cb = wk % ncb;
-    te = a.tiles[1 + tile];
+    te = load_tile(a.tiles + 1 + tile);
     if (MODE == 0) {
       nb0 = cb * 128;
       nb1 = a.I + nb0;
@@ -347,6 +357,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
+        {  // this chunk's weight scales into the stage's slot, completing on the same barrier
+          char* ss = sS + sw * kScaleSlot;
+          const int e = te.expert;
+          if (FMT == MOE_FMT_FP8_B128_W8A16) {
+            if (lane < nsub)
+              cp_async_4(smem_u32(ss + lane * 4),
+                         (const float*)a.wscale + ((size_t)e * (a.N / 128) + (lane == 0 ? nb0 : nb1) / 128) * (a.K / 128) + kc);
+          } else if (FMT == MOE_FMT_INT4_G128_W4A16) {
+            const int g = lane >> 4, piece = lane & 15;
+            if (g < nsub)
+              cp_async_16(smem_u32(ss + g * 256 + piece * 16),
+                          (const char*)a.wscale + (((size_t)e * (a.K / 128) + kc) * a.N + (g == 0 ? nb0 : nb1)) * 2 +
+                              piece * 16);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int row = lane + 32 * i, g = row >> 7;
+              if (g < nsub)
+                cp_async_8(smem_u32(ss + row * 8), (const uint8_t*)a.wscale +
+                                                       ((size_t)e * a.N + (g == 0 ? nb0 : nb1) + (row & 127)) * (a.K / 16) +
+                                                       kc * 8);
+            }
+          }
+          cp_async_mbar_arrive_noinc(&w_full[sw]);
+        }
       }
       if (!ok) break;
     }
@@ -472,24 +507,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         s_ct[buf][col] = ct;
         s_cw[buf][col] = cw;
       }
-      // per-chunk scales, fetched one chunk ahead so their latency hides behind a conversion
-      auto scale_of = [&](int kc) -> uint32_t {
-        if (!active) return 0u;
-        if (FMT == MOE_FMT_FP8_B128_W8A16)
-          return __float_as_uint(((const float*)a.wscale)[((size_t)e * (a.N / 128) + nb / 128) * (a.K / 128) + kc]);
-        if (FMT == MOE_FMT_INT4_G128_W4A16)
-          return __float_as_uint(__half2float(((const __half*)a.wscale)[((size_t)e * (a.K / 128) + kc) * a.N + nb + r]));
-        return *(const uint32_t*)((const uint8_t*)a.wscale + ((size_t)e * a.N + nb + r) * (a.K / 16) + kc * 8 + kh * 4);
-      };
-      uint32_t sc_next = scale_of(0);
       for (int kc = 0; kc < nK; ++kc, ++it) {
         const int sw = it % kStagesW, sa = it % kStagesA;
-        const uint32_t sc_raw = sc_next;
-        if (kc + 1 < nK) sc_next = scale_of(kc + 1);
-        const float sc = __uint_as_float(sc_raw);
-        const uint32_t bs4 = sc_raw;
         ok = __all_sync(0xffffffffu, mbar_wait(&w_full[sw], (it / kStagesW) & 1, &s_abort));
         if (!ok) break;
+        // the chunk's scale for this thread's row (or sub-tile), from the stage's scale slot
+        const char* ss = sS + sw * kScaleSlot;
+        uint32_t sc_raw = 0u;
+        if (active) {
+          if (FMT == MOE_FMT_FP8_B128_W8A16) sc_raw = *(const uint32_t*)(ss + g * 4);
+          else if (FMT == MOE_FMT_INT4_G128_W4A16) sc_raw = __float_as_uint(__half2float(*(const __half*)(ss + g * 256 + r * 2)));
+          else sc_raw = *(const uint32_t*)(ss + (g * 128 + r) * 8 + kh * 4);
+        }
+        const float sc = __uint_as_float(sc_raw);
+        const uint32_t bs4 = sc_raw;
         uint32_t v[32];
         if (active) {
           const char* sub = sW + sw * WSTAGE + g * WSUB;

@@ -61,6 +61,18 @@ __device__ __forceinline__ uint32_t f32_to_e2m1(float v) {
 struct TileEntry {
   int32_t expert, row0, rows, pad;
 };
+// Tile-table entries are read through L2 only (ld.global.cg): a GEMM that starts before its
+// predecessor has finished reads them before griddepcontrol.wait, and the table of an earlier
+// forward pass may still sit in this SM's L1.
+__device__ __forceinline__ TileEntry load_tile(const TileEntry* p) {
+  const int4 v = __ldcg((const int4*)p);
+  TileEntry t;
+  t.expert = v.x;
+  t.row0 = v.y;
+  t.rows = v.z;
+  t.pad = v.w;
+  return t;
+}
 
 // ---- workspace layout ----------------------------------------------------------------------
 struct WsLayout {
