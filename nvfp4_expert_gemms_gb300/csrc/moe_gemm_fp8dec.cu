@@ -223,27 +223,55 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
     const int t = threadIdx.x, j = t >> 3, q = t & 7;  // row j, 16-element group q of the chunk
     int it = 0, nitem = 0;
     bool ok = true;
-    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x, ++nitem) {
+    // Per-item setup (tile entry, then the row map / row maxima and tile scales that depend on it,
+    // then the reductions) for the next item is spread over the current item's chunks -- the
+    // tile entry after chunk 0, its dependent loads after chunk 1, the reductions after the last
+    // chunk -- so item boundaries cost the builders no load latency.
+    struct Setup {
       TileEntry te;
       int nb0, nb1, nsub;
-      item(wk, te, nb0, nb1, nsub);
+      float u, sc0, sc1;
+      const uint16_t* xrow;
+    };
+    auto setup = [&](int wk, Setup& st) {
+      item(wk, st.te, st.nb0, st.nb1, st.nsub);
+      st.u = row_norm(st.te, j, item_smax(st.te, st.nb0, st.nb1, st.nsub));
+      st.sc0 = scale_at(st.te, st.nb0, 0);
+      st.sc1 = st.nsub == 2 ? scale_at(st.te, st.nb1, 0) : 0.f;
+      st.xrow = nullptr;
+      if (j < st.te.rows)
+        st.xrow = a.act + (size_t)(MODE == 0 ? a.perm[st.te.row0 + j] / a.k : st.te.row0 + j) * a.K + q * 16;
+    };
+    Setup cur;
+    if ((int)blockIdx.x < nwork) setup(blockIdx.x, cur);
+    bool pref = false;  // n0*, n1* already hold chunks 0 and 1 of the item (loaded during the previous one)
+    uint4 n0a, n0b, n1a, n1b;
+    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x, ++nitem) {
+      const TileEntry te = cur.te;
+      const int nb0 = cur.nb0, nb1 = cur.nb1, nsub = cur.nsub;
       const bool real = j < te.rows;
-      // 16 bf16 of row j at K = 128 kc + 16q .. +15, loaded two chunks ahead of their use
-      const uint16_t* xrow = nullptr;
-      if (real) xrow = a.act + (size_t)(MODE == 0 ? a.perm[te.row0 + j] / a.k : te.row0 + j) * a.K + q * 16;
-      auto load = [&](int kc, uint4& v0, uint4& v1) {
-        if (xrow != nullptr && kc < nK) {
-          v0 = __ldcg((const uint4*)(xrow + kc * kKC));
-          v1 = __ldcg((const uint4*)(xrow + kc * kKC + 8));
+      const float u = cur.u;
+      const uint16_t* xrow = cur.xrow;
+      const int wk_next = wk + gridDim.x;
+      Setup nxt;
+      float nx_smax = 0.f, nx_rmax = 0.f;
+      int nx_src = 0;
+      // 16 bf16 of row j at K = 128 kc + 16q .. +15, loaded two chunks ahead of their use; the
+      // last two chunks of an item load the next item's first two once its row is known
+      auto load_from = [&](const uint16_t* row, int kc, uint4& v0, uint4& v1) {
+        if (row != nullptr && kc < nK) {
+          v0 = __ldcg((const uint4*)(row + kc * kKC));
+          v1 = __ldcg((const uint4*)(row + kc * kKC + 8));
         } else {
           v0 = v1 = make_uint4(0u, 0u, 0u, 0u);
         }
       };
-      uint4 n0a, n0b, n1a, n1b;
-      load(0, n0a, n0b);
-      load(1, n1a, n1b);
-      const float u = row_norm(te, j, item_smax(te, nb0, nb1, nsub));
-      float sc_next0 = scale_at(te, nb0, 0), sc_next1 = nsub == 2 ? scale_at(te, nb1, 0) : 0.f;
+      if (!pref) {
+        load_from(xrow, 0, n0a, n0b);
+        load_from(xrow, 1, n1a, n1b);
+      }
+      bool next_x = false, next0 = false;
+      float sc_next0 = cur.sc0, sc_next1 = cur.sc1;
       for (int kc = 0; kc < nK; ++kc, ++it) {
         const int sa = it % kStagesA;
         const float f0 = sc_next0 * u, f1 = sc_next1 * u;
@@ -254,7 +282,14 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
         const uint4 x0 = n0a, x1 = n0b;
         n0a = n1a;
         n0b = n1b;
-        load(kc + 2, n1a, n1b);
+        if (kc + 2 < nK) {
+          load_from(xrow, kc + 2, n1a, n1b);
+        } else if (next_x) {
+          load_from(nxt.xrow, kc + 2 - nK, n1a, n1b);
+          next0 |= kc + 2 == nK;
+        } else {
+          n1a = n1b = make_uint4(0u, 0u, 0u, 0u);
+        }
         ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[sa], ((it / kStagesA) & 1) ^ 1, &s_abort));
         if (!ok) break;
         const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
@@ -284,7 +319,29 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[sa]);
+        if (wk_next < nwork) {
+          const int kB = nK > 2 ? 1 : 0, kB2 = kB + 1 < nK ? kB + 1 : nK - 1;
+          if (kc == 0) item(wk_next, nxt.te, nxt.nb0, nxt.nb1, nxt.nsub);
+          if (kc == kB) {
+            for (int i = lane; i < nxt.nsub * nK; i += 32)
+              nx_smax = fmaxf(nx_smax, scale_at(nxt.te, i < nK ? nxt.nb0 : nxt.nb1, i % nK));
+            nxt.sc0 = scale_at(nxt.te, nxt.nb0, 0);
+            nxt.sc1 = nxt.nsub == 2 ? scale_at(nxt.te, nxt.nb1, 0) : 0.f;
+            if (j < nxt.te.rows) nx_src = MODE == 0 ? a.perm[nxt.te.row0 + j] / a.k : nxt.te.row0 + j;
+          }
+          if (kc == kB2) {
+            if (j < nxt.te.rows) nx_rmax = __ldcg(a.rowmax + nx_src);
+            nxt.xrow = j < nxt.te.rows ? a.act + (size_t)nx_src * a.K + q * 16 : nullptr;
+            next_x = true;
+          }
+          if (kc == nK - 1) {
+            for (int off = 16; off > 0; off >>= 1) nx_smax = fmaxf(nx_smax, __shfl_xor_sync(0xffffffffu, nx_smax, off));
+            nxt.u = j < nxt.te.rows ? pow2_norm(nx_rmax, nx_smax) : 1.f;
+          }
+        }
       }
+      cur = nxt;
+      pref = next0;
     }
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
     // ---------------- epilogue: thread = weight row, columns = activation rows ----------------
@@ -296,12 +353,19 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
       int nb0, nb1, nsub;
       item(wk, te, nb0, nb1, nsub);
       const int ab = nitem & 1;
+      // normalizers of the tile's rows (lane j < 16 computes row j's, then broadcast), loaded
+      // before the accumulator is ready
+      const float smax = item_smax(te, nb0, nb1, nsub);
+      const float u_l = row_norm(te, lane & 15, smax);
+      int p_l = 0;
+      float w_l = 0.f;
+      if (MODE == 1 && lane < te.rows && lane < kRows) {
+        p_l = a.perm[te.row0 + lane];
+        w_l = a.topk_w[p_l];
+      }
       ok = mbar_wait(&acc_full[ab], (nitem >> 1) & 1, &s_abort);
       if (!ok) break;
       fence_after_sync();
-      // normalizers of the tile's rows: lane j < 16 computes row j's, then broadcast
-      const float smax = item_smax(te, nb0, nb1, nsub);
-      const float u_l = row_norm(te, lane & 15, smax);
       if (MODE == 0) {
         if (g == 0) {  // sub-tile 0 threads own gate row r and up row r of the column block
           uint32_t G[32], U[32];
@@ -331,12 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
         tmem_ld_32x16(taddr(tmem, q * 32, ab * 64 + g * 32 + 16), Y + 16);
         tmem_ld_wait();
         const int c = (g == 0 ? nb0 : nb1) + r;
-        int p_l = 0;
-        float w_l = 0.f;
-        if (lane < te.rows && lane < kRows) {
-          p_l = a.perm[te.row0 + lane];
-          w_l = a.topk_w[p_l];
-        }
 #pragma unroll
         for (int j = 0; j < kRows; ++j) {
           const float inv_u = 1.0f / __shfl_sync(0xffffffffu, u_l, j);
