@@ -47,7 +47,7 @@ WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
     L.hs = take(R * I / 16);
     L.hg = take(4 * R);
   }
-  if (fmt != MOE_FMT_NVFP4_W4A4 && tc_row_block(T, k, E) >= kTcPermuteFromRows) L.xp = take(2 * R * H);
+  if (fmt != MOE_FMT_NVFP4_W4A4 && tc_row_block(fmt, T, k, E) >= kTcPermuteFromRows) L.xp = take(2 * R * H);
   if (host_io) {
     L.x_stage = take(2 * (size_t)T * H);
     L.lg_stage = take(4 * (size_t)T * E);
@@ -97,7 +97,7 @@ static moe_status_t forward_checked(const void* x, const float* logits, int T, c
   if (dv != MOE_OK) return dv;
   char* w = (char*)ws;
   const int rb =
-      d->fmt == MOE_FMT_NVFP4_W4A4 && !fp4_supported(*d) ? simt_row_block() : tc_row_block(T, k, d->E);
+      d->fmt == MOE_FMT_NVFP4_W4A4 && !fp4_supported(*d) ? simt_row_block() : tc_row_block(d->fmt, T, k, d->E);
   RoutePrelude pre;
   pre.zero_f32 = (float*)(w + L.out_acc);
   pre.n_f32 = (size_t)T * d->H;

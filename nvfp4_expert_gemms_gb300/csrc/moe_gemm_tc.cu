@@ -683,10 +683,14 @@ bool tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
 int tc_num_sms() { return num_sms(); }
 
 // Token rows per GEMM tile: the next power of two >= the mean rows per active expert, 16..128.
-int tc_row_block(int T, int k, int E) {
+// The weight-converting formats (INT4, NVFP4 W4A16) take twice that: their MMA and conversion
+// cost per tile does not depend on the rows it holds (an M = 128 MMA costs the same up to
+// N = 128), so fewer, fuller tiles convert and stream each expert's weights fewer times.
+int tc_row_block(int fmt, int T, int k, int E) {
   const long R = (long)T * k;
   const long active = R < E ? (R > 0 ? R : 1) : E;
-  const long avg = (R + active - 1) / active;
+  long avg = (R + active - 1) / active;
+  if (fmt == MOE_FMT_INT4_G128_W4A16 || fmt == MOE_FMT_NVFP4_W4A16) avg *= 2;
   int bn = 16;
   while (bn < 128 && bn < avg) bn *= 2;
   return bn;

@@ -156,7 +156,7 @@ inline void record_event(cudaEvent_t ev, cudaStream_t s) {
 void note_launches(int n);
 int simt_row_block();
 // Tensor-core path (FP8 W8A16, INT4 W4A16, NVFP4 W4A16): row block per tile, and the two GEMMs.
-int tc_row_block(int T, int k, int E);
+int tc_row_block(int fmt, int T, int k, int E);
 bool tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1, uint64_t pitch,
                  uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw);
 int tc_num_sms();
