@@ -36,7 +36,7 @@ WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
   L.inv = take(4 * R);
   L.tiles = take(sizeof(TileEntry) * (size_t)(L.max_tiles + 1));
   L.h = take(2 * R * I);
-  L.out_acc = take(4 * (size_t)T * H);
+  L.y = take(4 * R * (size_t)H);
   L.xmax = take(4 * (size_t)T);
   L.hmax = take(4 * R);
   if (fmt == MOE_FMT_NVFP4_W4A4) {  // activation codes per permuted row (first T rows: per token)
@@ -99,8 +99,6 @@ static moe_status_t forward_checked(const void* x, const float* logits, int T, c
   const int rb =
       d->fmt == MOE_FMT_NVFP4_W4A4 && !fp4_supported(*d) ? simt_row_block() : tc_row_block(d->fmt, T, k, d->E);
   RoutePrelude pre;
-  pre.zero_f32 = (float*)(w + L.out_acc);
-  pre.n_f32 = (size_t)T * d->H;
   if (d->fmt == MOE_FMT_FP8_B128_W8A16 && rb == fp8dec_row_block()) {  // FP8 decode path needs row maxima
     pre.zero_u32 = (unsigned*)(w + L.hmax);
     pre.n_u32 = (size_t)T * k;

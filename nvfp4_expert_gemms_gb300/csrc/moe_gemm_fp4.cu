@@ -62,7 +62,7 @@ struct Fp4Args {
   const float* topk_w;
   const TileEntry* tiles;
   uint16_t* h_out;          // MODE 0 output [R, I] bf16
-  float* out_acc;           // MODE 1 output [T, H] fp32
+  float* y_out;             // MODE 1 output: routing-weighted rows [R, H] fp32, permuted order
   int* err;
   int k, N, K, I, H;
 };
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (c0 + j < te.rows) atomicAdd(&a.out_acc[(size_t)tok[j] * a.H + c], sc[j] * __uint_as_float(Y[j]));
+            if (c0 + j < te.rows) a.y_out[(size_t)(te.row0 + c0 + j) * a.H + c] = sc[j] * __uint_as_float(Y[j]);
         }
       }
       fence_before_sync();
@@ -464,7 +464,7 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   a.topk_w = (const float*)(ws + L.topk_w);
   a.tiles = (const TileEntry*)(ws + L.tiles);
   a.h_out = (uint16_t*)(ws + L.h);
-  a.out_acc = (float*)(ws + L.out_acc);
+  a.y_out = (float*)(ws + L.y);
   a.err = (int*)(ws + L.err);
   a.k = k;
   a.I = I;

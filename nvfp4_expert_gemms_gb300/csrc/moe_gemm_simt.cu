@@ -1,7 +1,7 @@
 // Grouped expert GEMMs on CUDA cores (fp32 FMA), one CTA per (row block of one expert,
 // column block).  Dequantization uses each format's rule on the fly; SiLU(gate)*up is fused
-// into the gate/up GEMM, and the routing-weighted combine into the down GEMM (fp32 atomics
-// into an fp32 accumulator, then one rounding to bf16).
+// into the gate/up GEMM; the down GEMM writes each permuted row times its routing weight (fp32),
+// and finalize_kernel sums a token's k rows in slot order and rounds once to bf16.
 //
 // The pages dequantize the selected experts to bf16 and call a grouped matmul
 // (clef-omni-NVFP4, "How it was made"; clef-omni-fp8, "How this checkpoint runs"); here the
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(128) down_simt_kernel(MatView dn, const uint16
                                                         const int32_t* __restrict__ perm,
                                                         const float* __restrict__ topk_w, int k,
                                                         const TileEntry* __restrict__ tiles,
-                                                        float* __restrict__ out_acc) {
+                                                        float* __restrict__ y_out) {
   extern __shared__ float hs[];
   __shared__ int src_row[kSimtRB];
   if ((int)blockIdx.x >= tiles[0].expert) return;
@@ -129,26 +129,31 @@ __global__ void __launch_bounds__(128) down_simt_kernel(MatView dn, const uint16
     if (lane == 0)
       for (int r = 0; r < te.rows; ++r) {
         const int p = perm[te.row0 + r];
-        atomicAdd(&out_acc[(size_t)(p / k) * H + c], topk_w[p] * acc[r]);
+        y_out[(size_t)(te.row0 + r) * H + c] = topk_w[p] * acc[r];
       }
   }
 }
 
-__global__ void finalize_kernel(const float* __restrict__ acc, uint16_t* __restrict__ out, size_t n) {
+// The combine (deterministic): out[t, :] = bf16( sum over slots j = 0..k-1, in order, of the
+// routing-weighted down row y[inv[t*k + j], :] ), one thread per 4 output columns.
+__global__ void finalize_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, int k, int T, int H,
+                                uint16_t* __restrict__ out) {
   pdl_wait();
   const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
-  if (i >= n) return;
-  if (i + 3 < n) {
-    const float4 v = *(const float4*)(acc + i);
-    uint2 o;
-    o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x)) |
-          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y)) << 16);
-    o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.z)) |
-          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.w)) << 16);
-    *(uint2*)(out + i) = o;
-  } else {
-    for (size_t j = i; j < n; ++j) out[j] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+  if (i >= (size_t)T * H) return;
+  const int t = (int)(i / H), c = (int)(i % H);
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < k; ++j) {
+    const float4 v = __ldcg((const float4*)(y + (size_t)inv[(size_t)t * k + j] * H + c));
+    s.x += v.x;
+    s.y += v.y;
+    s.z += v.z;
+    s.w += v.w;
   }
+  uint2 o;
+  o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s.x)) | ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s.y)) << 16);
+  o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s.z)) | ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s.w)) << 16);
+  *(uint2*)(out + i) = o;
 }
 
 template <int FMT, bool A4>
@@ -172,7 +177,7 @@ cudaError_t run_simt(const moe_packed_desc_t& d, const char* packed, const __nv_
   record_event(ev.start[1], s);
   down_simt_kernel<FMT, A4><<<dim3(L.max_tiles, H / kSimtNB), 128, smem_d, s>>>(
       dn, (const uint16_t*)(ws + L.h), (const uint8_t*)(ws + L.hq), (const uint8_t*)(ws + L.hs),
-      (const float*)(ws + L.hg), perm, (const float*)(ws + L.topk_w), k, tiles, (float*)(ws + L.out_acc));
+      (const float*)(ws + L.hg), perm, (const float*)(ws + L.topk_w), k, tiles, (float*)(ws + L.y));
   record_event(ev.stop[1], s);
   note_launches(2);
   return cudaGetLastError();
@@ -184,7 +189,7 @@ cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const
                            int row_block, const WsLayout& L, char* ws, __nv_bfloat16* out, const StepEvents& ev,
                            cudaStream_t s) {
   const size_t n_out = (size_t)T * d.H;
-  if (T == 0) return cudaGetLastError();  // the routing launch has zeroed the fp32 accumulator
+  if (T == 0) return cudaGetLastError();
   cudaError_t e;
   if (d.fmt == MOE_FMT_NVFP4_W4A4 && fp4_supported(d)) {
     e = launch_experts_fp4(d, packed, x, T, k, row_block, L, ws, ev, s);
@@ -199,8 +204,8 @@ cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const
   if (e != cudaSuccess) return e;
   const unsigned blocks = (unsigned)((n_out / 4 + 255) / 256 + 1);
   note_launches(1);
-  return launch_pdl(finalize_kernel, dim3(blocks), dim3(256), 0, s, (const float*)(ws + L.out_acc), (uint16_t*)out,
-                    n_out);
+  return launch_pdl(finalize_kernel, dim3(blocks), dim3(256), 0, s, (const float*)(ws + L.y),
+                    (const int32_t*)(ws + L.inv), k, T, d.H, (uint16_t*)out);
 }
 
 int simt_row_block() { return kSimtRB; }

@@ -14,8 +14,8 @@
 // kernel streams weights.  Each CTA covers one row block of one expert (from the routing tile
 // table) and two 128-row weight sub-tiles: gate rows n0.. and up rows I+n0.. for the gate/up
 // GEMM (so SiLU(gate)*up is computed in the epilogue from two TMEM accumulators), or 256
-// consecutive output features for the down GEMM (whose epilogue scales by the routing weight
-// and adds into the fp32 token-order accumulator).
+// consecutive output features for the down GEMM (whose epilogue writes the row times its
+// routing weight, fp32, for the slot-ordered combine).
 //
 // Warp roles (640 threads): warps 0-15 convert (warp w: sub-tile (w/4)%2, K half w/8, TMEM lanes
 // 32*(w%4)..) and later run the epilogue; warp 16 issues TMA; warp 17 owns TMEM and issues the
@@ -94,7 +94,7 @@ struct TcArgs {
   const float* topk_w;
   const TileEntry* tiles;
   uint16_t* h_out;
-  float* out_acc;
+  float* y_out;  // down: routing-weighted rows [R, H] fp32, permuted order
   int* err;
   int k, N, K, I, H;
 };
@@ -232,7 +232,7 @@ __device__ __forceinline__ void conv_nvfp4(const char* sub, int r, int kh, uint3
 // with a stride of gridDim.x; the pipeline rings keep their phases across items, so the TMA for
 // the next item runs while the current item's epilogue executes.
 // MODE 0: gate/up GEMM + SiLU(gate)*up -> h (bf16, permuted row order).
-// MODE 1: down GEMM + routing weight -> fp32 red.add into the token-order accumulator.
+// MODE 1: down GEMM x routing weight -> fp32 rows [R, H] in permuted order (combined later).
 template <int FMT, int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __grid_constant__ TcArgs a) {
   using Cfg = TcCfg<FMT, BN>;
@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c0 + j;
-            if (col < te.rows) atomicAdd(&a.out_acc[(size_t)ct[col] * a.H + c], cw[col] * __uint_as_float(Y[j]));
+            if (col < te.rows) a.y_out[(size_t)(te.row0 + col) * a.H + c] = cw[col] * __uint_as_float(Y[j]);
           }
         }
       }
@@ -707,7 +707,7 @@ cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, co
   a.topk_w = (const float*)(ws + L.topk_w);
   a.tiles = (const TileEntry*)(ws + L.tiles);
   a.h_out = (uint16_t*)(ws + L.h);
-  a.out_acc = (float*)(ws + L.out_acc);
+  a.y_out = (float*)(ws + L.y);
   a.err = (int*)(ws + L.err);
   a.k = k;
   a.I = I;

@@ -77,7 +77,7 @@ __device__ __forceinline__ TileEntry load_tile(const TileEntry* p) {
 // ---- workspace layout ----------------------------------------------------------------------
 struct WsLayout {
   size_t err, topk_idx, topk_w, blkcnt, blkbase, offsets, perm, inv, tiles;
-  size_t h, out_acc, xq, xs, xg, hq, hs, hg;
+  size_t h, y, xq, xs, xg, hq, hs, hg;  // y: routing-weighted down rows [R, H] fp32 (permuted order)
   size_t xp;          // expert-permuted bf16 copy of x (tensor-core path, row blocks >= 64)
   size_t xmax, hmax;  // per-row max |activation| (FP8 decode path)
   size_t x_stage, lg_stage, out_stage;

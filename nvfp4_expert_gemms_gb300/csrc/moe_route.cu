@@ -16,7 +16,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kRouteSmallZeroMax = 1 << 18;  // fp32 accumulators one block zeroes quickly (1 MB)
+constexpr int kRouteSmallZeroMax = 1 << 18;  // fp32 words one block zeroes quickly (1 MB)
 
 struct Cand {
   float v;
