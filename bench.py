@@ -18,6 +18,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -204,6 +205,22 @@ class OracleSample:
         return self.oracle.max_threads()
 
 
+def cpu_model():
+    """The host CPU's model name (x86 'model name', Arm implementer/part), or the machine type."""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model name", "Hardware"):
+        for ln in info:
+            if ln.split(":")[0].strip() == key:
+                return ln.split(":", 1)[1].strip()
+    parts = {ln.split(":")[0].strip(): ln.split(":", 1)[1].strip() for ln in info if ":" in ln}
+    if "CPU implementer" in parts:
+        return f"{platform.machine()} implementer {parts['CPU implementer']} part {parts.get('CPU part', '?')}"
+    return platform.machine()
+
+
 # ------------------------------------------------------------------------------------------
 # Our arm
 # ------------------------------------------------------------------------------------------
@@ -247,7 +264,8 @@ def run_ours(args, c, rank, world, local_rank):
     def step(timed_events=None):
         for l in range(L):
             if timed_events is not None and l in timed_events:
-                M.moe_time_next_step(0, *timed_events[l])
+                M.moe_time_next_step(0, *timed_events[l][:2])
+                M.moe_time_next_step(1, *timed_events[l][2:])
             M.moe_layer_forward(x, lg[l], layers[l].desc, layers[l].packed, k, outs[l], ws)
 
     def as_runner(fn):
@@ -265,10 +283,10 @@ def run_ours(args, c, rank, world, local_rank):
             fn()
         return g.replay, M.moe_kernel_launch_count() - n0
 
-    ev = {l: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for l in sampled}
-    for a_, b_ in ev.values():  # torch creates the CUDA event on first record; the library re-records it
-        a_.record()
-        b_.record()
+    ev = {l: tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for l in sampled}
+    for evs in ev.values():  # torch creates the CUDA event on first record; the library re-records it
+        for e_ in evs:
+            e_.record()
     run, launches_per_step = as_runner(lambda: step(ev))
     for _ in range(args.warmup):
         run()
@@ -282,9 +300,12 @@ def run_ours(args, c, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     t_start.record()
+    step_ev[0].record()
     for s in range(args.steps):
         run()
+        step_ev[s + 1].record()
     t_stop.record()
     torch.cuda.synchronize()
     n_launch = launches_per_step * args.steps
@@ -294,6 +315,11 @@ def run_ours(args, c, rank, world, local_rank):
         torch.distributed.barrier()
     ms_total = t_start.elapsed_time(t_stop)
     gu_ms = [ev[l][0].elapsed_time(ev[l][1]) for l in sampled]  # the last timed step's sampled launches
+    dn_ms = [ev[l][2].elapsed_time(ev[l][3]) for l in sampled]
+    per_step = sorted(step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps))
+
+    def pct(q):
+        return per_step[min(len(per_step) - 1, int(round(q * (len(per_step) - 1))))]
     mt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
     if world > 1:
         torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
@@ -318,7 +344,8 @@ def run_ours(args, c, rank, world, local_rank):
         traffic = round(traffic * statistics.mean(gu_bytes[l] for l in sampled) / statistics.mean(gu_bytes))
     roof.update({"traffic": traffic, "kernel": "grouped gate/up GEMM",
                  "launch_ms": round(gu_avg_s * 1e3, 4), "peak_source": peak_src,
-                 "step_fraction": round(gu_avg_s * 1e3 * L / ms_step, 3), "sampled_layers": len(sampled)})
+                 "step_fraction": round(gu_avg_s * 1e3 * L / ms_step, 3), "sampled_layers": len(sampled),
+                 "down_launch_ms": round(statistics.mean(dn_ms), 4)})
     layer_s = ms_step / 1e3 / L
     whole = {"hbm_gbs": round(statistics.mean(layer_bytes) / layer_s / 1e9, 1),
              "tflops": round(flops_layer / layer_s / 1e12, 2),
@@ -377,8 +404,10 @@ def run_ours(args, c, rank, world, local_rank):
             torch.cuda.synchronize()
             sweep[str(Ts)] = round(Ts * L / (a.elapsed_time(b) / 3 / 1e3), 1)
 
+    step_stats = {"median": round(statistics.median(per_step), 4), "p10": round(pct(0.1), 4),
+                  "p90": round(pct(0.9), 4)}
     return {"value": value, "ms_per_step": ms_step, "roofline": roof, "layer": whole, "e2e": e2e,
-            "gpu_launches": int(n_launch), "clocks": clk, "sweep": sweep}
+            "gpu_launches": int(n_launch), "clocks": clk, "sweep": sweep, "step_ms": step_stats}
 
 
 def main():
@@ -411,7 +440,7 @@ def main():
         line = dict(base, impl="reference", value=round(v, 3), ms_per_step=round(1e3 * c["T"] * c["L"] / v, 3),
                     dtype="f64", n_gpus=1,
                     cpu_baseline={"value": round(v, 3), "unit": "tokens/s", "cores": smp.cores(), "kind": "oracle",
-                                  "sample": smp.desc},
+                                  "sample": smp.desc, "cpu_model": cpu_model(), "nproc": os.cpu_count()},
                     e2e={"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                          "d2h_bytes_per_step": 0},
                     note=(f"CPU oracle timed on the host cores; each step is the bounded sample above "
@@ -429,13 +458,13 @@ def main():
         smp = OracleSample(c, args.seed)
         v, spent = smp.run(min_seconds=10.0)
         cpu = {"value": round(v, 3), "unit": "tokens/s", "cores": smp.cores(), "kind": "oracle", "sample": smp.desc,
-               "seconds": round(spent, 1)}
+               "seconds": round(spent, 1), "cpu_model": cpu_model(), "nproc": os.cpu_count()}
     if rank == 0:
         dtype = {"fp8": "f32 (e4m3 x bf16 products)", "int4": "f32", "nvfp4_w4a16": "f32",
                  "nvfp4_w4a4": "f32"}[c["fmt"]]
         line = dict(base, value=round(r["value"], 1), ms_per_step=round(r["ms_per_step"], 4), dtype=dtype,
                     roofline=r["roofline"], cpu_baseline=cpu, e2e=r["e2e"], gpu_launches=r["gpu_launches"],
-                    clocks=r["clocks"], layer=r["layer"])
+                    clocks=r["clocks"], layer=r["layer"], step_ms=r["step_ms"])
         if r["sweep"]:
             line["sweep_tokens_per_s"] = r["sweep"]
         print(json.dumps(line))
