@@ -256,22 +256,48 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
     }
   }
   __syncthreads();
-  if (tid == 0) {  // E <= 256: a serial scan is a few hundred cycles
-    int a = 0, b = 0;
-    for (int i = 0; i < E; ++i) {
-      off_s[i] = a;
-      toff_s[i] = b;
-      a += cnt[i];
-      b += (cnt[i] + row_block - 1) / row_block;
+  if (warp == 0) {  // exclusive scans of rows and tiles per expert: lane l owns experts 8l .. 8l+7
+    constexpr int kPer = kMaxE / 32;
+    int rows[kPer], ntl[kPer], ra = 0, ta = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane * kPer + i;
+      rows[i] = e < E ? cnt[e] : 0;
+      ntl[i] = (rows[i] + row_block - 1) / row_block;
+      ra += rows[i];
+      ta += ntl[i];
     }
-    off_s[E] = a;
-    toff_s[E] = b;
-    TileEntry h;
-    h.expert = min(b, max_tiles);
-    h.row0 = a;
-    h.rows = row_block;
-    h.pad = 0;
-    tiles[0] = h;
+    int ri = ra, ti = ta;  // inclusive warp scans of the per-lane sums
+    for (int off = 1; off < 32; off <<= 1) {
+      const int rv = __shfl_up_sync(0xffffffffu, ri, off), tv = __shfl_up_sync(0xffffffffu, ti, off);
+      if (lane >= off) {
+        ri += rv;
+        ti += tv;
+      }
+    }
+    int a = ri - ra, b = ti - ta;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane * kPer + i;
+      if (e <= E) {
+        off_s[e] = a;
+        toff_s[e] = b;
+      }
+      a += rows[i];
+      b += ntl[i];
+    }
+    if (lane == 31) {
+      TileEntry h;
+      h.expert = min(ti, max_tiles);
+      h.row0 = ri;
+      h.rows = row_block;
+      h.pad = 0;
+      tiles[0] = h;
+      if (E == kMaxE) {  // off_s[E] and toff_s[E] lie past the last lane's experts
+        off_s[E] = ri;
+        toff_s[E] = ti;
+      }
+    }
   }
   __syncthreads();
   if (tid <= E) offsets[tid] = off_s[tid];

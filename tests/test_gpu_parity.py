@@ -112,7 +112,7 @@ def test_quant_act_bit_exact(orc):
 
 # ------------------------------------------------------------------ routing
 @pytest.mark.parametrize("T,E,k,zipf", [(64, 8, 2, None), (1, 128, 8, None), (300, 128, 8, 1.1), (257, 256, 8, None),
-                                        (5, 6, 6, None), (1000, 37, 3, None)])
+                                        (5, 6, 6, None), (1000, 37, 3, None), (100, 256, 8, 1.1), (50, 37, 3, None)])
 def test_route_bit_exact(orc, T, E, k, zipf):
     lg = synth.gen_logits(T, E, seed=T + E, zipf_alpha=zipf)
     d = M.moe_packed_size("fp8", E, 128, 128)
