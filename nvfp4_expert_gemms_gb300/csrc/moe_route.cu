@@ -111,7 +111,55 @@ __device__ __forceinline__ int route_token(const float* __restrict__ logits, int
   return mi;
 }
 
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+// Exclusive scans of rows and tiles per expert by one warp (lane l owns experts 8l .. 8l+7):
+// off_s[e] = first permuted row of expert e, toff_s[e] = its first tile (both for e = 0..E), and
+// the tile table's header entry.
+__device__ __forceinline__ void expert_scan(const int* cnt, int E, int row_block, int max_tiles, int* off_s,
+                                            int* toff_s, TileEntry* tiles, int lane) {
+  constexpr int kPer = kMaxE / 32;
+  int rows[kPer], ntl[kPer], ra = 0, ta = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane * kPer + i;
+    rows[i] = e < E ? cnt[e] : 0;
+    ntl[i] = (rows[i] + row_block - 1) / row_block;
+    ra += rows[i];
+    ta += ntl[i];
+  }
+  int ri = ra, ti = ta;  // inclusive warp scans of the per-lane sums
+  for (int off = 1; off < 32; off <<= 1) {
+    const int rv = __shfl_up_sync(0xffffffffu, ri, off), tv = __shfl_up_sync(0xffffffffu, ti, off);
+    if (lane >= off) {
+      ri += rv;
+      ti += tv;
+    }
+  }
+  int a = ri - ra, b = ti - ta;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane * kPer + i;
+    if (e <= E) {
+      off_s[e] = a;
+      toff_s[e] = b;
+    }
+    a += rows[i];
+    b += ntl[i];
+  }
+  if (lane == 31) {
+    TileEntry h;
+    h.expert = min(ti, max_tiles);
+    h.row0 = ri;
+    h.rows = row_block;
+    h.pad = 0;
+    tiles[0] = h;
+    if (E == kMaxE) {  // off_s[E] and toff_s[E] lie past the last lane's experts
+      off_s[E] = ri;
+      toff_s[E] = ti;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int32_t* __restrict__ topk_idx,
                                                          float* __restrict__ topk_w,
                                                          int32_t* __restrict__ blkcnt, int* err, RoutePrelude pre) {
@@ -124,7 +172,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   if (blockIdx.x == 0 && tid == 0) *err = kDevOk;  // each forward pass reports its own errors
   __syncthreads();
   const int t_end = min(T, (int)(blockIdx.x + 1) * kRouteTB);
-  for (int t = blockIdx.x * kRouteTB + warp; t < t_end; t += 8) {  // tokens round-robin over the warps
+  for (int t = blockIdx.x * kRouteTB + warp; t < t_end; t += 32) {  // 4 tokens per warp
     if (pre.x) row_absmax(pre, t, lane);
     const int mi = route_token(logits, t, E, k, lane, topk_idx, topk_w);
     if (lane < k) atomicAdd(&cnt[mi], 1);
@@ -145,26 +193,18 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
   pdl_trigger();
   if (e < E) {
     int s = 0;
+#pragma unroll 8
     for (int b = 0; b < nb; ++b) s += blkcnt[(size_t)b * E + e];
     tot[e] = s;
     ntl[e] = (s + row_block - 1) / row_block;
   }
   __syncthreads();
-  if (e == 0) {  // E <= 256: a serial scan is a few hundred cycles
-    int a = 0, b = 0;
-    for (int i = 0; i < E; ++i) {
-      off_s[i] = a;
-      toff_s[i] = b;
-      a += tot[i];
-      b += ntl[i];
-    }
-    off_s[E] = a;
-    toff_s[E] = b;
-  }
+  if (e < 32) expert_scan(tot, E, row_block, max_tiles, off_s, toff_s, tiles, e);
   __syncthreads();
   if (e <= E) offsets[e] = off_s[e];
   if (e < E) {
     int run = off_s[e];
+#pragma unroll 8
     for (int b = 0; b < nb; ++b) {
       blkbase[(size_t)b * E + e] = run;
       run += blkcnt[(size_t)b * E + e];
@@ -182,14 +222,6 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
       te.pad = 0;
       tiles[1 + t0 + i] = te;
     }
-  }
-  if (e == 0) {
-    TileEntry h;
-    h.expert = min(toff_s[E], max_tiles);
-    h.row0 = off_s[E];
-    h.rows = row_block;
-    h.pad = 0;
-    tiles[0] = h;
   }
 }
 
@@ -256,49 +288,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
     }
   }
   __syncthreads();
-  if (warp == 0) {  // exclusive scans of rows and tiles per expert: lane l owns experts 8l .. 8l+7
-    constexpr int kPer = kMaxE / 32;
-    int rows[kPer], ntl[kPer], ra = 0, ta = 0;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = lane * kPer + i;
-      rows[i] = e < E ? cnt[e] : 0;
-      ntl[i] = (rows[i] + row_block - 1) / row_block;
-      ra += rows[i];
-      ta += ntl[i];
-    }
-    int ri = ra, ti = ta;  // inclusive warp scans of the per-lane sums
-    for (int off = 1; off < 32; off <<= 1) {
-      const int rv = __shfl_up_sync(0xffffffffu, ri, off), tv = __shfl_up_sync(0xffffffffu, ti, off);
-      if (lane >= off) {
-        ri += rv;
-        ti += tv;
-      }
-    }
-    int a = ri - ra, b = ti - ta;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = lane * kPer + i;
-      if (e <= E) {
-        off_s[e] = a;
-        toff_s[e] = b;
-      }
-      a += rows[i];
-      b += ntl[i];
-    }
-    if (lane == 31) {
-      TileEntry h;
-      h.expert = min(ti, max_tiles);
-      h.row0 = ri;
-      h.rows = row_block;
-      h.pad = 0;
-      tiles[0] = h;
-      if (E == kMaxE) {  // off_s[E] and toff_s[E] lie past the last lane's experts
-        off_s[E] = ri;
-        toff_s[E] = ti;
-      }
-    }
-  }
+  if (warp == 0) expert_scan(cnt, E, row_block, max_tiles, off_s, toff_s, tiles, lane);
   __syncthreads();
   if (tid <= E) offsets[tid] = off_s[tid];
   if (tid < E) {
@@ -350,7 +340,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int row_block
                       w, off, perm, inv, tiles, err, pre);
   }
   cudaError_t e = cudaSuccess;
-  if (T > 0) e = launch_pdl(route_topk_kernel, dim3(nb), dim3(256), 0, s, logits, T, E, k, idx, w, blkcnt, err, pre);
+  if (T > 0) e = launch_pdl(route_topk_kernel, dim3(nb), dim3(1024), 0, s, logits, T, E, k, idx, w, blkcnt, err, pre);
   else e = cudaMemsetAsync(err, 0, sizeof(int), s);
   if (e == cudaSuccess)
     e = launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)blkcnt, T > 0 ? nb : 0, E, row_block,
