@@ -36,7 +36,7 @@ WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
   L.inv = take(4 * R);
   L.tiles = take(sizeof(TileEntry) * (size_t)(L.max_tiles + 1));
   L.h = take(2 * R * I);
-  L.y = take(4 * R * (size_t)H);
+  L.y = take(2 * R * (size_t)H);
   L.xmax = take(4 * (size_t)T);
   L.hmax = take(4 * R);
   if (fmt == MOE_FMT_NVFP4_W4A4) {  // activation codes per permuted row (first T rows: per token)

@@ -62,7 +62,7 @@ struct Fp4Args {
   const float* topk_w;
   const TileEntry* tiles;
   uint16_t* h_out;          // MODE 0 output [R, I] bf16
-  float* y_out;             // MODE 1 output: routing-weighted rows [R, H] fp32, permuted order
+  uint16_t* y_out;          // MODE 1 output: routing-weighted rows [R, H] bf16, permuted order
   int* err;
   int k, N, K, I, H;
 };
@@ -399,7 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (c0 + j < te.rows) a.y_out[(size_t)(te.row0 + c0 + j) * a.H + c] = sc[j] * __uint_as_float(Y[j]);
+            if (c0 + j < te.rows)
+              a.y_out[(size_t)(te.row0 + c0 + j) * a.H + c] = bf16_bits(sc[j] * __uint_as_float(Y[j]));
         }
       }
       fence_before_sync();
@@ -456,7 +457,7 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   uint8_t* xsf = (uint8_t*)(ws + L.xs);
   uint8_t* hq = (uint8_t*)(ws + L.hq);
   uint8_t* hsf = (uint8_t*)(ws + L.hs);
-  launch_quant_rows(x, (const int32_t*)(ws + L.inv), k, T, H, xq, xsf, (float*)(ws + L.xg), s);
+  launch_quant_rows(x, (const int32_t*)(ws + L.inv), k, T, H, xq, xsf, (float*)(ws + L.xg), s, true);
 
   Fp4Args a;
   memset(&a, 0, sizeof(a));
@@ -464,7 +465,7 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   a.topk_w = (const float*)(ws + L.topk_w);
   a.tiles = (const TileEntry*)(ws + L.tiles);
   a.h_out = (uint16_t*)(ws + L.h);
-  a.y_out = (float*)(ws + L.y);
+  a.y_out = (uint16_t*)(ws + L.y);
   a.err = (int*)(ws + L.err);
   a.k = k;
   a.I = I;

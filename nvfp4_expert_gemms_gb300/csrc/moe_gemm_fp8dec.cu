@@ -59,7 +59,7 @@ struct Fp8Args {
   const TileEntry* tiles;
   uint16_t* h_out;         // MODE 0 output [R, I] bf16
   unsigned* h_rowmax;      // MODE 0: running max |h| per permuted row (fp32 bits)
-  float* y_out;            // MODE 1 output: routing-weighted rows [R, H] fp32, permuted order
+  uint16_t* y_out;         // MODE 1 output: routing-weighted rows [R, H] bf16, permuted order
   int* err;
   int k, N, K, I, H;
 };
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
           const float w = __shfl_sync(0xffffffffu, w_l, j);
           if (j < te.rows) {
             const float y = (__uint_as_float(Y[j]) + __uint_as_float(Y[16 + j])) * inv_u * w;
-            a.y_out[(size_t)(te.row0 + j) * a.H + c] = y;
+            a.y_out[(size_t)(te.row0 + j) * a.H + c] = bf16_bits(y);
           }
         }
       }
@@ -446,7 +446,7 @@ cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed
   a.tiles = (const TileEntry*)(ws + L.tiles);
   a.h_out = (uint16_t*)(ws + L.h);
   a.h_rowmax = (unsigned*)(ws + L.hmax);
-  a.y_out = (float*)(ws + L.y);
+  a.y_out = (uint16_t*)(ws + L.y);
   a.err = (int*)(ws + L.err);
   a.k = k;
   a.I = I;

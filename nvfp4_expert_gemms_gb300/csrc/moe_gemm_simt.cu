@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(128) down_simt_kernel(MatView dn, const uint16
                                                         const int32_t* __restrict__ perm,
                                                         const float* __restrict__ topk_w, int k,
                                                         const TileEntry* __restrict__ tiles,
-                                                        float* __restrict__ y_out) {
+                                                        uint16_t* __restrict__ y_out) {
   extern __shared__ float hs[];
   __shared__ int src_row[kSimtRB];
   if ((int)blockIdx.x >= tiles[0].expert) return;
@@ -129,31 +129,45 @@ __global__ void __launch_bounds__(128) down_simt_kernel(MatView dn, const uint16
     if (lane == 0)
       for (int r = 0; r < te.rows; ++r) {
         const int p = perm[te.row0 + r];
-        y_out[(size_t)(te.row0 + r) * H + c] = topk_w[p] * acc[r];
+        y_out[(size_t)(te.row0 + r) * H + c] = bf16_bits(topk_w[p] * acc[r]);
       }
   }
 }
 
 // The combine (deterministic): out[t, :] = bf16( sum over slots j = 0..k-1, in order, of the
-// routing-weighted down row y[inv[t*k + j], :] ), one thread per 4 output columns.
-__global__ void finalize_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, int k, int T, int H,
-                                uint16_t* __restrict__ out) {
+// routing-weighted down row y[inv[t*k + j], :] ) with y in bf16, one thread per 8 output columns.
+__global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ inv,
+                                                       int k, int T, int H, uint16_t* __restrict__ out) {
+  const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;  // 8 columns of one token
+  const bool live = i < (size_t)T * H;
+  const int t = live ? (int)(i / H) : 0, c = (int)(i % H);
   pdl_wait();
-  const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
-  if (i >= (size_t)T * H) return;
-  const int t = (int)(i / H), c = (int)(i % H);
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < k; ++j) {
-    const float4 v = __ldcg((const float4*)(y + (size_t)inv[(size_t)t * k + j] * H + c));
-    s.x += v.x;
-    s.y += v.y;
-    s.z += v.z;
-    s.w += v.w;
+  if (!live) return;
+  int src[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) src[j] = j < k ? __ldg(inv + (size_t)t * k + j) : 0;
+  uint4 v[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j < k) v[j] = __ldcs((const uint4*)(y + (size_t)src[j] * H + c));
+  float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j < k) {
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s[2 * e] += __uint_as_float(w[e] << 16);
+        s[2 * e + 1] += __uint_as_float(w[e] & 0xFFFF0000u);
+      }
+    }
   }
-  uint2 o;
-  o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s.x)) | ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s.y)) << 16);
-  o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s.z)) | ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s.w)) << 16);
-  *(uint2*)(out + i) = o;
+  uint4 o;
+  o.x = (uint32_t)bf16_bits(s[0]) | ((uint32_t)bf16_bits(s[1]) << 16);
+  o.y = (uint32_t)bf16_bits(s[2]) | ((uint32_t)bf16_bits(s[3]) << 16);
+  o.z = (uint32_t)bf16_bits(s[4]) | ((uint32_t)bf16_bits(s[5]) << 16);
+  o.w = (uint32_t)bf16_bits(s[6]) | ((uint32_t)bf16_bits(s[7]) << 16);
+  *(uint4*)(out + i) = o;
 }
 
 template <int FMT, bool A4>
@@ -177,7 +191,7 @@ cudaError_t run_simt(const moe_packed_desc_t& d, const char* packed, const __nv_
   record_event(ev.start[1], s);
   down_simt_kernel<FMT, A4><<<dim3(L.max_tiles, H / kSimtNB), 128, smem_d, s>>>(
       dn, (const uint16_t*)(ws + L.h), (const uint8_t*)(ws + L.hq), (const uint8_t*)(ws + L.hs),
-      (const float*)(ws + L.hg), perm, (const float*)(ws + L.topk_w), k, tiles, (float*)(ws + L.y));
+      (const float*)(ws + L.hg), perm, (const float*)(ws + L.topk_w), k, tiles, (uint16_t*)(ws + L.y));
   record_event(ev.stop[1], s);
   note_launches(2);
   return cudaGetLastError();
@@ -202,9 +216,9 @@ cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const
     e = launch_experts_tc(d, packed, x, T, k, row_block, L, ws, ev, s);
   }
   if (e != cudaSuccess) return e;
-  const unsigned blocks = (unsigned)((n_out / 4 + 255) / 256 + 1);
+  const unsigned blocks = (unsigned)((n_out / 8 + 255) / 256);
   note_launches(1);
-  return launch_pdl(finalize_kernel, dim3(blocks), dim3(256), 0, s, (const float*)(ws + L.y),
+  return launch_pdl(finalize_kernel, dim3(blocks), dim3(256), 0, s, (const uint16_t*)(ws + L.y),
                     (const int32_t*)(ws + L.inv), k, T, d.H, (uint16_t*)out);
 }
 

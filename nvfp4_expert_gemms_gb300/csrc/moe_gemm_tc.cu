@@ -94,7 +94,7 @@ struct TcArgs {
   const float* topk_w;
   const TileEntry* tiles;
   uint16_t* h_out;
-  float* y_out;  // down: routing-weighted rows [R, H] fp32, permuted order
+  uint16_t* y_out;  // down: routing-weighted rows [R, H] bf16, permuted order
   int* err;
   int k, N, K, I, H;
 };
@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c0 + j;
-            if (col < te.rows) a.y_out[(size_t)(te.row0 + col) * a.H + c] = cw[col] * __uint_as_float(Y[j]);
+            if (col < te.rows) a.y_out[(size_t)(te.row0 + col) * a.H + c] = bf16_bits(cw[col] * __uint_as_float(Y[j]));
           }
         }
       }
@@ -707,7 +707,7 @@ cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, co
   a.topk_w = (const float*)(ws + L.topk_w);
   a.tiles = (const TileEntry*)(ws + L.tiles);
   a.h_out = (uint16_t*)(ws + L.h);
-  a.y_out = (float*)(ws + L.y);
+  a.y_out = (uint16_t*)(ws + L.y);
   a.err = (int*)(ws + L.err);
   a.k = k;
   a.I = I;

@@ -23,6 +23,7 @@ __device__ __forceinline__ void set_dev_error(int* err, int code) { atomicCAS(er
 
 // ---- scalar codecs (device) --------------------------------------------------------------
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+__device__ __forceinline__ uint16_t bf16_bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
 // E4M3 ("e4m3fn") code -> float; exact.
 __device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
@@ -38,21 +39,6 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
   const float m[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
   float v = m[c & 7];
   return (c & 8) ? -v : v;
-}
-// float -> E2M1: nearest grid point, a tie goes to the even code, saturating at 6; the sign
-// bit is kept even when the magnitude rounds to zero.
-__device__ __forceinline__ uint32_t f32_to_e2m1(float v) {
-  float a = fabsf(v);
-  uint32_t m;
-  if (a <= 0.25f) m = 0;
-  else if (a < 0.75f) m = 1;
-  else if (a <= 1.25f) m = 2;
-  else if (a < 1.75f) m = 3;
-  else if (a <= 2.5f) m = 4;
-  else if (a < 3.5f) m = 5;
-  else if (a <= 5.0f) m = 6;
-  else m = 7;
-  return m | (signbit(v) ? 8u : 0u);
 }
 
 // ---- routing tile table ------------------------------------------------------------------
@@ -107,9 +93,10 @@ cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, co
 cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e, int which, float* out,
                            cudaStream_t s);
 // NVFP4 quantization of bf16 rows; row r's codes go to output row r, or (scatter != null) to
-// rows scatter[r*k .. r*k+k-1].
+// rows scatter[r*k .. r*k+k-1].  early: x was final before the preceding kernel of the stream
+// passed its pdl_wait() (true only right after routing), so x is read before this launch's wait.
 cudaError_t launch_quant_rows(const __nv_bfloat16* x, const int32_t* scatter, int k, int rows, int K, uint8_t* q,
-                              uint8_t* sf, float* gs, cudaStream_t s);
+                              uint8_t* sf, float* gs, cudaStream_t s, bool early = false);
 // out[r] = x[map[r] / k] for r < rows (rows of K bf16).
 cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* map, int k, int rows, int K, __nv_bfloat16* out,
                                cudaStream_t s);

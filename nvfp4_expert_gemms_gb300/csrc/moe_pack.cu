@@ -86,23 +86,64 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const uint16_t* __restr
   if (threadIdx.x == 0) atomicMax(&slot[e], __float_as_uint(amax));
 }
 
-// One NVFP4 16-block of a row with global scale gs: 8 code bytes and 1 scale byte.
-__device__ __forceinline__ void nvfp4_block(const float v[16], float gs, uint2* codes8, uint8_t* scale) {
-  float amax = 0.f;
+// Eight floats to eight E2M1 codes (element i in bits 4i..4i+3) with the hardware conversion:
+// round to nearest, ties to the even code, saturating at 6, sign kept.
+__device__ __forceinline__ uint32_t e2m1x8(const float f[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]));
+  return r;
+}
+
+// Codes of eight elements: E2M1(fl(v / eff)), fl = fp32 division rounded to nearest.
+// Bracketing: with r = fl(1/eff), a = fl(v * fl(r * (1 - 2^-20))) and b = fl(v * fl(r * (1 + 2^-20)))
+// carry at most three roundings of 2^-24 each, so |a| < |v/eff| < |b| (outside the subnormal
+// range, where every candidate is far below the first rounding boundary 0.25 and codes 0).
+// fl is monotone, so |a| <= |fl(v/eff)| <= |b|, and because the conversion is monotone too,
+// equal codes for a and b are the code of fl(v/eff).  Only a pair that straddles a rounding
+// boundary pays the exact division.
+__device__ __forceinline__ uint32_t e2m1x8_div(const float* v, float eff, float rd, float ru) {
+  float a[8], b[8];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  for (int i = 0; i < 8; ++i) {
+    a[i] = __fmul_rn(v[i], rd);
+    b[i] = __fmul_rn(v[i], ru);
+  }
+  const uint32_t ca = e2m1x8(a);
+  if (ca == e2m1x8(b)) return ca;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = __fdiv_rn(v[i], eff);
+  return e2m1x8(a);
+}
+
+// One NVFP4 16-block of a row with global scale gs and block maximum amax = max |v|:
+// 8 code bytes and 1 scale byte.
+__device__ __forceinline__ void nvfp4_encode(const float v[16], float amax, float gs, uint2* codes8, uint8_t* scale) {
   const uint8_t bsc = f32_to_e4m3(__fmul_rn(__fdiv_rn(amax, 6.0f), gs));
   const float bs = e4m3_to_f32(bsc);
   uint32_t lo = 0, hi = 0;
   if (bs != 0.0f) {
     const float eff = __fdiv_rn(bs, gs);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) lo |= f32_to_e2m1(__fdiv_rn(v[i], eff)) << (4 * i);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) hi |= f32_to_e2m1(__fdiv_rn(v[8 + i], eff)) << (4 * i);
+    const float r = __frcp_rn(eff);
+    const float rd = __fmul_rn(r, 1.0f - 0x1p-20f), ru = __fmul_rn(r, 1.0f + 0x1p-20f);
+    lo = e2m1x8_div(v, eff, rd, ru);
+    hi = e2m1x8_div(v + 8, eff, rd, ru);
   }
   *codes8 = make_uint2(lo, hi);
   *scale = bsc;
+}
+
+__device__ __forceinline__ void nvfp4_block(const float v[16], float gs, uint2* codes8, uint8_t* scale) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  nvfp4_encode(v, amax, gs, codes8, scale);
 }
 
 // thread = one (row, 16-block) of one expert matrix.
@@ -182,6 +223,98 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
   }
 }
 
+// The same quantization with RPW whole rows of K = 16*NBLK elements held in registers.  The
+// rows are contiguous, so their 16-blocks form one flat run of RPW*NBLK blocks: lane l owns
+// blocks l, l+32, ..., loads all of them before any arithmetic and reads each row once.  Block
+// and row maxima are taken on the bf16 magnitude bits (for finite values the integer order of
+// |v| is the float order).  EARLY: the rows were final before the preceding kernel of the stream
+// passed its own pdl_wait(), so they are loaded before this kernel's wait and only the stores
+// follow it.
+template <int NBLK, int RPW, bool EARLY>
+__global__ void __launch_bounds__(256) quant_rows_flat_kernel(const uint16_t* __restrict__ x,
+                                                              const int32_t* __restrict__ scatter, int k, int rows,
+                                                              uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                                              float* __restrict__ gs_out) {
+  constexpr int K = 16 * NBLK, kFlat = NBLK * RPW, NB = (kFlat + 31) / 32;
+  static_assert(NB <= 8 && RPW * kMaxTopK <= 32, "flat quantizer shape");
+  const int lane = threadIdx.x & 31;
+  const int r0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RPW;
+  const uint4* base = (const uint4*)(x + (size_t)r0 * K);
+  if (!EARLY) pdl_wait();
+  uint4 u[NB][2];
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+    const int f = lane + 32 * j;
+    if (f < kFlat && r0 + f / NBLK < rows) {
+      u[j][0] = __ldcs(base + 2 * f);
+      u[j][1] = __ldcs(base + 2 * f + 1);
+    } else {
+      u[j][0] = u[j][1] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  if (EARLY) pdl_wait();
+  pdl_trigger();
+
+  uint32_t bmax[NB], rmax[RPW];
+#pragma unroll
+  for (int rr = 0; rr < RPW; ++rr) rmax[rr] = 0u;
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+    const uint32_t m = 0x7FFF7FFFu;
+    uint32_t t = __vmaxu2(__vmaxu2(u[j][0].x & m, u[j][0].y & m), __vmaxu2(u[j][0].z & m, u[j][0].w & m));
+    t = __vmaxu2(t, __vmaxu2(__vmaxu2(u[j][1].x & m, u[j][1].y & m), __vmaxu2(u[j][1].z & m, u[j][1].w & m)));
+    bmax[j] = max(t & 0xFFFFu, t >> 16);
+    const int row = (lane + 32 * j) / NBLK;
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr)
+      if (row == rr) rmax[rr] = max(rmax[rr], bmax[j]);
+  }
+  float gs[RPW];
+#pragma unroll
+  for (int rr = 0; rr < RPW; ++rr) {
+    float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, rmax[rr]) << 16);
+    if (amax < 1e-12f) amax = 1e-12f;
+    gs[rr] = __fdiv_rn(2688.0f, amax);
+  }
+  // destinations: lane rr*k + c holds row rr's copy c (scatter), else row r0 + rr
+  const int ncopy = scatter ? k : 1;
+  int my_dst = 0;
+  if (scatter) {
+    if (lane < RPW * k && r0 + lane / k < rows) my_dst = scatter[(size_t)(r0 + lane / k) * k + lane % k];
+  } else {
+    my_dst = r0 + lane;
+  }
+#pragma unroll
+  for (int rr = 0; rr < RPW; ++rr)
+    if (lane / ncopy == rr && lane < RPW * ncopy && r0 + rr < rows) gs_out[my_dst] = gs[rr];
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+    const int f = lane + 32 * j, row = f / NBLK, b = f % NBLK;
+    const bool live = f < kFlat && r0 + row < rows;
+    float g = gs[0];
+#pragma unroll
+    for (int rr = 1; rr < RPW; ++rr)
+      if (row == rr) g = gs[rr];
+    const uint32_t ww[8] = {u[j][0].x, u[j][0].y, u[j][0].z, u[j][0].w, u[j][1].x, u[j][1].y, u[j][1].z, u[j][1].w};
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = __uint_as_float(ww[i] << 16);
+      v[2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
+    }
+    uint2 code;
+    uint8_t scale;
+    nvfp4_encode(v, __uint_as_float(bmax[j] << 16), g, &code, &scale);
+    for (int c = 0; c < ncopy; ++c) {  // warp-uniform trip count: the shuffle sees every lane
+      const int d = __shfl_sync(0xffffffffu, my_dst, (row < RPW ? row : 0) * ncopy + c);
+      if (live) {
+        *(uint2*)(q + (size_t)d * (K / 2) + b * 8) = code;
+        sf[(size_t)d * (K / 16) + b] = scale;
+      }
+    }
+  }
+}
+
 // out[r] = x[map[r] / k]: the expert-permuted copy of the activation rows (one warp per row).
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ map,
                                                           int k, int rows, int row_vec, uint4* __restrict__ out) {
@@ -246,12 +379,36 @@ cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e
   return cudaGetLastError();
 }
 
+template <int NBLK, int RPW>
+static cudaError_t launch_quant_flat(bool early, const __nv_bfloat16* x, const int32_t* scatter, int k, int rows,
+                                     uint8_t* q, uint8_t* sf, float* gs, cudaStream_t s) {
+  const dim3 grid((rows + 8 * RPW - 1) / (8 * RPW));
+  if (early)
+    return launch_pdl(quant_rows_flat_kernel<NBLK, RPW, true>, grid, dim3(256), 0, s, (const uint16_t*)x, scatter, k,
+                      rows, q, sf, gs);
+  return launch_pdl(quant_rows_flat_kernel<NBLK, RPW, false>, grid, dim3(256), 0, s, (const uint16_t*)x, scatter, k,
+                    rows, q, sf, gs);
+}
+
 cudaError_t launch_quant_rows(const __nv_bfloat16* x, const int32_t* scatter, int k, int rows, int K, uint8_t* q,
-                              uint8_t* sf, float* gs, cudaStream_t s) {
+                              uint8_t* sf, float* gs, cudaStream_t s, bool early) {
   if (rows <= 0) return cudaGetLastError();
   note_launches(1);
-  return launch_pdl(quant_rows_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, (const uint16_t*)x, scatter, k, rows, K,
-                    q, sf, gs);
+  switch (K) {  // register-resident shapes: RPW rows fill whole 32-lane passes of 16-blocks
+    case 128: return launch_quant_flat<8, 4>(early, x, scatter, k, rows, q, sf, gs, s);
+    case 256: return launch_quant_flat<16, 2>(early, x, scatter, k, rows, q, sf, gs, s);
+    case 512: return launch_quant_flat<32, 1>(early, x, scatter, k, rows, q, sf, gs, s);
+    case 768: return launch_quant_flat<48, 2>(early, x, scatter, k, rows, q, sf, gs, s);
+    case 1024: return launch_quant_flat<64, 1>(early, x, scatter, k, rows, q, sf, gs, s);
+    case 1280: return launch_quant_flat<80, 2>(early, x, scatter, k, rows, q, sf, gs, s);
+    case 1536: return launch_quant_flat<96, 1>(early, x, scatter, k, rows, q, sf, gs, s);
+    case 2048: return launch_quant_flat<128, 1>(early, x, scatter, k, rows, q, sf, gs, s);
+    case 3072: return launch_quant_flat<192, 1>(early, x, scatter, k, rows, q, sf, gs, s);
+    case 4096: return launch_quant_flat<256, 1>(early, x, scatter, k, rows, q, sf, gs, s);
+    default:
+      return launch_pdl(quant_rows_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, (const uint16_t*)x, scatter, k, rows,
+                        K, q, sf, gs);
+  }
 }
 
 cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* map, int k, int rows, int K, __nv_bfloat16* out,

@@ -111,6 +111,52 @@ def test_quant_act_bit_exact(orc):
 
 
 # ------------------------------------------------------------------ routing
+def _tie_rows(T, K, seed):
+    """Rows whose block quotients v/eff land exactly on the E2M1 rounding boundaries.
+
+    Element 0 is 2688 * 2^m, so gs = 2^-m and eff = bs / gs keeps v/eff independent of m.
+    Block 0 (eff = 448): the boundaries 0.25 .. 5 times 448, their negatives, and -1 (rounds
+    to -0).  Block 1 (eff = 2, exact reciprocal): boundaries, one bf16 step either side, the
+    saturating maximum 12.  Block 2: zeros and -0.0 (block scale 0).  Block 3 (eff = 3,
+    inexact reciprocal): boundaries times 3.  The remaining blocks are ~N(0,1) * 2^m.
+    """
+    rng = np.random.default_rng(seed)
+    bnd = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    b0 = [2688.0] + [t * 448 for t in bnd] + [-t * 448 for t in bnd] + [-1.0]
+    def step(v, d):  # the bf16 value d units in the last place away from v (same sign)
+        b = synth.f32_to_bf16_bits(np.array([v], np.float32)).astype(np.int32) + d
+        return float(synth.bf16_bits_to_f32(b.astype(np.uint16))[0])
+
+    b1 = [12.0] + [2 * t for t in bnd] + [step(2 * t, 1) for t in bnd[:4]] + [-step(2 * t, -1) for t in bnd[:4]]
+    b2 = [0.0] * 15 + [-0.0]
+    b3 = [18.0] + [3 * t for t in bnd] + [-3 * t for t in bnd] + [-(2.0 ** -7)]
+    blocks = [b0, b1, b2, b3]
+    nb = K // 16
+    x = (rng.standard_normal((T, K))).astype(np.float32)
+    for r in range(T):
+        m = float(2.0 ** ((r % 9) - 4))
+        row = x[r] * m
+        for i, b in enumerate(blocks[:nb]):
+            row[16 * i:16 * (i + 1)] = np.array(b, np.float32) * m
+        x[r] = row
+    bits = synth.f32_to_bf16_bits(x)
+    n = 16 * min(nb, len(blocks))
+    assert np.array_equal(synth.bf16_bits_to_f32(bits)[:, :n], x[:, :n])  # the planted values are exact in bf16
+    return bits
+
+
+@pytest.mark.parametrize("K", [48, 128, 256, 400, 768, 2048])
+def test_quant_act_rounding_boundaries_bit_exact(orc, K):
+    """Every register-resident row shape and the generic one, on exact E2M1 ties, signed
+    zeros and values one step off a boundary: codes, block scales and gs equal the oracle's."""
+    x = _tie_rows(37, K, seed=K)
+    q, s, g = M.moe_debug_quant_act(dev_bf16(x))
+    rq, rs, rg = orc.quant_act_nvfp4(x)
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert g.cpu().numpy().tobytes() == rg.tobytes()
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
 @pytest.mark.parametrize("T,E,k,zipf", [(64, 8, 2, None), (1, 128, 8, None), (300, 128, 8, 1.1), (257, 256, 8, None),
                                         (5, 6, 6, None), (1000, 37, 3, None), (100, 256, 8, 1.1), (50, 37, 3, None)])
 def test_route_bit_exact(orc, T, E, k, zipf):
