@@ -97,7 +97,7 @@ static moe_status_t forward_checked(const void* x, const float* logits, int T, c
   if (dv != MOE_OK) return dv;
   char* w = (char*)ws;
   const int rb =
-      d->fmt == MOE_FMT_NVFP4_W4A4 && !fp4_supported(*d) ? simt_row_block() : tc_row_block(d->fmt, T, k, d->E);
+      d->fmt != MOE_FMT_NVFP4_W4A4 ? tc_row_block(d->fmt, T, k, d->E) : fp4_supported(*d) ? fp4_row_block() : simt_row_block();
   RoutePrelude pre;
   if (d->fmt == MOE_FMT_FP8_B128_W8A16 && rb == fp8dec_row_block()) {  // FP8 decode path needs row maxima
     pre.zero_u32 = (unsigned*)(w + L.hmax);

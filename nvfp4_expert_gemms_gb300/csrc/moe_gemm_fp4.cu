@@ -6,20 +6,24 @@
 // "How it was made"):
 //   weights      E2M1 codes [N, K/2] + E4M3 block scales [N, K/16] + global scale gs_w (per matrix)
 //   activations  E2M1 codes [rows, K/2] + E4M3 block scales [rows, K/16] + global scale gs_a (per row)
-// The MMA forms sum_k (q_w * bs_w)(q_a * bs_a) exactly in fp32, and the epilogue divides by
-// gs_w * gs_a.  Codes arrive by TMA tiles in the 128-byte swizzle: weights in 128-row tiles,
-// activations in BN-row tiles of their expert-permuted rows (x is quantized straight into that
-// order, one copy per routed token slot, so the gate/up GEMM needs no row gather).  The weight block
-// scales arrive by TMA next to their codes; the activation block scales are read from global
-// memory by the four scale warps (16 bytes per row and chunk, fetched one chunk ahead), which
-// place both in tensor memory in the layout the MMA reads (per K = 64 step and 128 rows:
-// 4 columns; lane l, column j = the four scales of row l + 32 j, repeated in every lane quarter).
+// The MMA forms sum_k (q_a * bs_a)(q_w * bs_w) exactly in fp32, and the epilogue divides by
+// gs_a * gs_w.
 //
-//   D[weight row, act row] += A[weight row, k] * B[act row, k]     M = 128, N = BN <= 128, K = 64
+// One work item = 128 expert-permuted activation rows (one routing tile) x 256 weight rows:
+//   D[act row, weight row] += A[act row, k] * B[weight row, k]     M = 128, N = 256, K = 64
+// gate/up: the 256 weight rows are 128 gate rows over the 128 matching up rows, so a thread
+// of the epilogue holds gate and up of the same features of its token; down: 256 consecutive
+// output features.  An N = 256 block-scaled MMA costs the tensor pipe the same issue time as
+// N = 64 or 128, so one instruction per K step covers what two N = 128 ones did.  Codes arrive
+// by TMA tiles in the 128-byte swizzle (x is quantized straight into permuted row order, one copy
+// per routed token slot, so the gate/up GEMM needs no row gather).  The weight block scales
+// and the activation block scales arrive by TMA next to their codes; the four scale warps place
+// both in tensor memory in the layout the MMA reads (per K = 64 step: row r of the operand in lane
+// r % 32 of column r / 32, four scales per word, repeated in every lane quarter).
 //
-// Warps (448 threads): 0-3 stage scale factors, 4-11 run the epilogue (thread = weight row),
-// 12 issues TMA, 13 owns TMEM and issues the MMAs.  Persistent CTAs walk (row tile, column
-// block) work items.
+// Warps (448 threads): 0-3 stage scale factors, 4-11 run the epilogue (thread = token row, 64
+// or 128 contiguous output features), 12 issues TMA, 13 owns TMEM and issues the MMAs.
+// Persistent CTAs walk (routing tile, column block) work items.
 #include <cudaTypedefs.h>
 
 #include "moe_formats.cuh"
@@ -32,30 +36,22 @@ namespace {
 using namespace tc;
 
 constexpr int kKC = 256;                  // K per chunk: 128 bytes of codes per row
-constexpr int kStagesX = 4, kStagesS = 4;
+constexpr int kRows = 128;                // activation rows per item (MMA M): the routing row block
+constexpr int kStagesW = 4, kStagesX = 4, kStagesS = 4;
 constexpr int kSfWarps = 4, kEpiWarp0 = 4, kEpiWarps = 8, kProdWarp = 12, kMmaWarp = 13;
 constexpr int kThreads = 14 * 32;
-constexpr int kWCodes = 128 * 128;        // 128 rows x 128 B (256 codes), 128-byte swizzle
-constexpr int kWSf = 128 * 16;            // 128 rows x 16 scales
-constexpr int kWStage = 2 * kWCodes + 2 * kWSf;
-constexpr uint32_t kSfCol = 256;          // TMEM: [0, 2*BN) accumulators, then 4 x 48 scale-factor columns
-constexpr uint32_t kSfStageCols = 48;     // sub-tile 0 A scales (16), sub-tile 1 (16), B scales (16)
-
-// Shared memory: weight stages, activation stages, and (gate/up) the h tile staged for
-// coalesced stores: BN token rows x 128 intermediate columns of bf16.
-template <int MODE, int BN>
-struct Fp4Cfg {
-  static constexpr int kStagesW = MODE == 0 ? 3 : 4;
-  static constexpr int kXBytes = BN * 128;                        // codes, 128-byte swizzle
-  static constexpr int kXStage = (kXBytes + 1023) / 1024 * 1024;  // stages start 1024-aligned
-  static constexpr int kHBytes = MODE == 0 ? BN * 256 : 0;
-  static constexpr size_t kSmem = 1024 + (size_t)kStagesW * kWStage + (size_t)kStagesX * kXStage + kHBytes;
-};
+constexpr int kWCodes = 128 * 128;        // one 128-row weight tile, 128-byte swizzle
+constexpr int kWSf = 128 * 16;            // its 128 rows x 16 scales
+constexpr int kWStage = 2 * kWCodes + 2 * kWSf;  // two tiles = the 256 B rows of one item
+constexpr int kXCodes = kRows * 128;      // activation codes, 128-byte swizzle
+constexpr int kXStage = kXCodes + kRows * 16;  // then their 128 rows x 16 scales
+constexpr size_t kSmem = 1024 + (size_t)kStagesW * kWStage + (size_t)kStagesX * kXStage;
+constexpr uint32_t kSfCol = 256;          // TMEM: [0, 256) accumulator, then 4 x 48 scale-factor columns
+constexpr uint32_t kSfStageCols = 48;     // A (activation) scales 4 x 4 columns, B (weight) scales 4 x 8
 
 struct Fp4Args {
   CUtensorMap wcode, wsf;   // weight codes [E*N, K/2], scales [E*N, K/16]
-  CUtensorMap xcode;        // activation codes [R, K/2] in permuted row order
-  const uint8_t* asf;       // activation block scales [R, K/16]
+  CUtensorMap xcode, xsf;   // activation codes [R, K/2] and block scales [R, K/16], permuted row order
   const float* wgs;         // weight global scales [E]
   const float* ags;         // activation global scales [R]
   const int32_t* perm;
@@ -90,43 +86,26 @@ __device__ __forceinline__ void tmem_st_32x16(uint32_t taddr, const uint32_t* v)
       : "memory");
 }
 
-// Scale tile [rows][16 bytes] -> 16 TMEM words for lane l: word (4*ks + j) = bytes 4ks..4ks+3 of
-// row l + 32j (zero for rows >= nrows).
-__device__ __forceinline__ void sf_words(const char* tile, int l, int nrows, uint32_t* v) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int row = l + 32 * j;
-    const uint4 s = row < nrows ? *(const uint4*)(tile + row * 16) : make_uint4(0, 0, 0, 0);
-    v[0 + j] = s.x;
-    v[4 + j] = s.y;
-    v[8 + j] = s.z;
-    v[12 + j] = s.w;
-  }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (uint32_t)bf16_bits(lo) | ((uint32_t)bf16_bits(hi) << 16);
 }
 
-template <int MODE, int BN>
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant__ Fp4Args a) {
-  constexpr int kStagesW = Fp4Cfg<MODE, BN>::kStagesW;
-  constexpr int kXStage = Fp4Cfg<MODE, BN>::kXStage;
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = (char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   char* sW = smem;
   char* sX = sW + kStagesW * kWStage;
-  char* sH = sX + kStagesX * kXStage;
   __shared__ uint64_t w_full[kStagesW], w_empty[kStagesW], x_full[kStagesX], x_empty[kStagesX], s_full[kStagesS],
       s_empty[kStagesS], acc_full, acc_empty, drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  // per output column of the current item (double-buffered by item parity): the scale that
-  // undoes both global scales (times the routing weight for the down GEMM) and the token row
-  __shared__ __align__(16) float s_cs[2][BN];
-  __shared__ __align__(16) int s_ct[2][BN];
 
   // gate/up: wait for the activation quantization (and, before it, routing); down: the tile table
   // was final before the gate/up GEMM passed its own pdl_wait(), so only the h codes need the wait
   if (MODE == 0) pdl_wait();
   const int ntiles = load_tile(a.tiles).expert;
-  const int ncb = MODE == 0 ? a.I / 128 : (a.H + 255) / 256;
+  const int ncb = MODE == 0 ? a.I / 128 : a.H / 256;
   const int nwork = ntiles * ncb;
   if ((int)blockIdx.x >= nwork) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -159,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
     prefetch_tmap(&a.wcode);
     prefetch_tmap(&a.wsf);
     prefetch_tmap(&a.xcode);
+    prefetch_tmap(&a.xsf);
   }
   fence_before_sync();
   __syncthreads();
@@ -167,18 +147,12 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   if (MODE == 1 && warp != kProdWarp) pdl_wait();  // the producer waits before its first h tile
   pdl_trigger();
 
-  auto item = [&](int wk, TileEntry& te, int& nb0, int& nb1, int& nsub) {
+  // item wk: routing tile wk / ncb; weight rows w0 .. w0+127 and w1 .. w1+127 of its expert
+  auto item = [&](int wk, TileEntry& te, int& w0, int& w1) {
     te = load_tile(a.tiles + 1 + wk / ncb);
     const int cb = wk % ncb;
-    if (MODE == 0) {
-      nb0 = cb * 128;
-      nb1 = a.I + nb0;
-      nsub = 2;
-    } else {
-      nb0 = cb * 256;
-      nb1 = nb0 + 128;
-      nsub = (a.H - nb0) >= 256 ? 2 : 1;
-    }
+    w0 = MODE == 0 ? cb * 128 : cb * 256;
+    w1 = MODE == 0 ? a.I + w0 : w0 + 128;
   };
 
   if (warp == kProdWarp) {
@@ -188,18 +162,18 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
     int armed_w[kStagesW] = {0}, armed_x[kStagesX] = {0};
     for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x) {
       TileEntry te;
-      int nb0, nb1, nsub;
-      item(wk, te, nb0, nb1, nsub);
+      int w0, w1;
+      item(wk, te, w0, w1);
       for (int kc = 0; kc < nK; ++kc, ++it) {
         const int sw = it % kStagesW, sx = it % kStagesX;
         if (lane == 0) {
           ok = mbar_wait(&w_empty[sw], ((it / kStagesW) & 1) ^ 1, &s_abort);
           if (ok) {
             char* ws = sW + sw * kWStage;
-            mbar_arrive_expect_tx(&w_full[sw], nsub * (kWCodes + kWSf));
+            mbar_arrive_expect_tx(&w_full[sw], 2 * (kWCodes + kWSf));
             ++armed_w[sw];
-            for (int g = 0; g < nsub; ++g) {
-              const int row = te.expert * a.N + (g == 0 ? nb0 : nb1);
+            for (int g = 0; g < 2; ++g) {
+              const int row = te.expert * a.N + (g == 0 ? w0 : w1);
               tma_load_2d(ws + g * kWCodes, &a.wcode, &w_full[sw], kc * (kKC / 2), row);
               tma_load_2d(ws + 2 * kWCodes + g * kWSf, &a.wsf, &w_full[sw], kc * (kKC / 16), row);
             }
@@ -208,9 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
             ok = mbar_wait(&x_empty[sx], ((it / kStagesX) & 1) ^ 1, &s_abort);
             if (MODE == 1 && it == 0) pdl_wait();
             if (ok) {
-              mbar_arrive_expect_tx(&x_full[sx], Fp4Cfg<MODE, BN>::kXBytes);
+              mbar_arrive_expect_tx(&x_full[sx], kXStage);
               ++armed_x[sx];
               tma_load_2d(sX + sx * kXStage, &a.xcode, &x_full[sx], kc * (kKC / 2), te.row0);
+              tma_load_2d(sX + sx * kXStage + kXCodes, &a.xsf, &x_full[sx], kc * (kKC / 16), te.row0);
             }
           }
         }
@@ -228,13 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer (whole warp waits, lane 0 issues) ----------------
-    const uint32_t idesc = idesc_nvf4(128, BN);
+    const uint32_t idesc = idesc_nvf4(kRows, 256);
     int it = 0, nitem = 0;
     bool ok = true;
     for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x, ++nitem) {
-      TileEntry te;
-      int nb0, nb1, nsub;
-      item(wk, te, nb0, nb1, nsub);
       ok = mbar_wait(&acc_empty, (nitem & 1) ^ 1, &s_abort);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
@@ -248,15 +220,12 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
         if (!ok) break;
         fence_after_sync();
         if (lane == 0) {
-          const uint32_t xa = smem_u32(sX + sx * kXStage);
-          for (int g = 0; g < nsub; ++g) {
-            const uint32_t wa = smem_u32(sW + sw * kWStage + g * kWCodes);
-            const uint32_t sfa = tmem + kSfCol + ss * kSfStageCols + g * 16, sfb = tmem + kSfCol + ss * kSfStageCols + 32;
+          const uint32_t xa = smem_u32(sX + sx * kXStage), wa = smem_u32(sW + sw * kWStage);
+          const uint32_t sfa = tmem + kSfCol + ss * kSfStageCols, sfb = sfa + 16;
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_nvf4(tmem + g * BN, sdesc_k_sw128(wa + ks * 32), sdesc_k_sw128(xa + ks * 32), idesc, sfa + 4 * ks,
-                       sfb + 4 * ks, (kc | ks) != 0);
-          }
+          for (int ks = 0; ks < 4; ++ks)
+            mma_nvf4(tmem, sdesc_k_sw128(xa + ks * 32), sdesc_k_sw128(wa + ks * 32), idesc, sfa + 4 * ks,
+                     sfb + 8 * ks, (kc | ks) != 0);
           mma_commit(&w_empty[sw]);
           mma_commit(&x_empty[sx]);
           mma_commit(&s_empty[ss]);
@@ -275,43 +244,48 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
     bool ok = true;
     for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x) {
       TileEntry te;
-      int nb0, nb1, nsub;
-      item(wk, te, nb0, nb1, nsub);
-      // source rows of the activation scales this lane places: tile rows l + 32 j
-      const uint8_t* src[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int row = l + 32 * j;
-        src[j] = nullptr;
-        if (row < te.rows && row < BN) src[j] = a.asf + (size_t)(te.row0 + row) * (a.K / 16);
-      }
-      uint4 nxt[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) nxt[j] = src[j] ? *(const uint4*)(src[j]) : make_uint4(0, 0, 0, 0);
+      int w0, w1;
+      item(wk, te, w0, w1);
       for (int kc = 0; kc < nK; ++kc, ++it) {
-        const int sw = it % kStagesW, ss = it % kStagesS;
-        uint4 cur[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          cur[j] = nxt[j];
-          if (kc + 1 < nK) nxt[j] = src[j] ? *(const uint4*)(src[j] + (kc + 1) * 16) : make_uint4(0, 0, 0, 0);
-        }
+        const int sw = it % kStagesW, sx = it % kStagesX, ss = it % kStagesS;
         ok = __all_sync(0xffffffffu, mbar_wait(&w_full[sw], (it / kStagesW) & 1, &s_abort) &&
+                                         mbar_wait(&x_full[sx], (it / kStagesX) & 1, &s_abort) &&
                                          mbar_wait(&s_empty[ss], ((it / kStagesS) & 1) ^ 1, &s_abort));
         if (!ok) break;
         fence_after_sync();
         const uint32_t col = kSfCol + ss * kSfStageCols;
+        // A: column 4 ks + j holds the K-step-ks word of activation row l + 32 j (rows past the
+        // tile scale by 0)
+        const char* xsf = sX + sx * kXStage + kXCodes;
+        uint4 x4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          x4[j] = l + 32 * j < te.rows ? *(const uint4*)(xsf + (l + 32 * j) * 16) : make_uint4(0u, 0u, 0u, 0u);
         uint32_t v[16];
-        for (int g = 0; g < nsub; ++g) {
-          sf_words(sW + sw * kWStage + 2 * kWCodes + g * kWSf, l, 128, v);
-          tmem_st_32x16(taddr(tmem, q * 32, col + g * 16), v);
-        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          v[0 + j] = cur[j].x;
-          v[4 + j] = cur[j].y;
-          v[8 + j] = cur[j].z;
-          v[12 + j] = cur[j].w;
+          v[0 + j] = x4[j].x;
+          v[4 + j] = x4[j].y;
+          v[8 + j] = x4[j].z;
+          v[12 + j] = x4[j].w;
+        }
+        tmem_st_32x16(taddr(tmem, q * 32, col), v);
+        // B: column 16 + 8 ks + j holds the K-step-ks word of weight row l + 32 j (j < 4: first
+        // 128-row tile, j >= 4: second)
+        uint4 w[8];
+        const char* wsf = sW + sw * kWStage + 2 * kWCodes;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = *(const uint4*)(wsf + (j >> 2) * kWSf + (l + 32 * (j & 3)) * 16);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[0 + j] = w[j].x;
+          v[8 + j] = w[j].y;
+        }
+        tmem_st_32x16(taddr(tmem, q * 32, col + 16), v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[0 + j] = w[j].z;
+          v[8 + j] = w[j].w;
         }
         tmem_st_32x16(taddr(tmem, q * 32, col + 32), v);
         tmem_st_wait();
@@ -321,91 +295,84 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
       }
     }
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
-    // ---------------- epilogue: thread = weight row, columns = activation rows ----------------
-    const int ge = (warp - kEpiWarp0) >> 2, q = warp & 3, r = q * 32 + lane;
-    const int et = threadIdx.x - kEpiWarp0 * 32;
+    // ---------------- epilogue: thread = token row of the tile ----------------
+    const int q = warp & 3, half = (warp - kEpiWarp0) >> 2, r = q * 32 + lane;
     int nitem = 0;
     bool ok = true;
     for (int wk = blockIdx.x; wk < nwork; wk += gridDim.x, ++nitem) {
       TileEntry te;
-      int nb0, nb1, nsub;
-      item(wk, te, nb0, nb1, nsub);
-      const int buf = nitem & 1;
-      // column table of this item, filled while its MMAs run
-      if (et < BN) {
-        float cs = 0.f;
-        int ct = 0;
-        if (et < te.rows) {
-          const float gw = a.wgs[te.expert];
-          if (MODE == 0) {
-            cs = 1.0f / (gw * a.ags[te.row0 + et]);
-          } else {
-            const int p = a.perm[te.row0 + et];
-            cs = a.topk_w[p] / (gw * a.ags[te.row0 + et]);
-            ct = p / a.k;
-          }
-        }
-        s_cs[buf][et] = cs;
-        s_ct[buf][et] = ct;
+      int w0, w1;
+      item(wk, te, w0, w1);
+      // the row's scale (1 / (gs_w gs_a), times the routing weight for the down GEMM), read
+      // while the MMAs run
+      const bool live = r < te.rows;
+      float cs = 0.f;
+      if (live) {
+        const float g = a.wgs[te.expert] * a.ags[te.row0 + r];
+        cs = MODE == 0 ? 1.0f / g : a.topk_w[a.perm[te.row0 + r]] / g;
       }
       ok = mbar_wait(&acc_full, nitem & 1, &s_abort);
-      // every epilogue thread takes the same branch: the table is complete and no one has aborted
+      // every epilogue thread takes the same branch
       ok = named_bar_and(1, kEpiWarps * 32, ok);
       if (!ok) break;
       fence_after_sync();
-      const float* cs = s_cs[buf];
       if (MODE == 0) {
-        // both warp groups own the same weight rows (gate in sub-tile 0, up in sub-tile 1) and
-        // split the token columns; h goes to the staged tile [token][weight row] first
-        const int c_beg = BN <= 16 ? (ge == 0 ? 0 : BN) : ge * (BN / 2);
-        const int c_end = BN <= 16 ? (ge == 0 ? BN : BN) : c_beg + BN / 2;
-        uint16_t* sh = (uint16_t*)sH;
-        for (int c0 = c_beg; c0 < c_end; c0 += 16) {
-          uint32_t G[16], U[16];
-          tmem_ld_32x16(taddr(tmem, q * 32, c0), G);
-          tmem_ld_32x16(taddr(tmem, q * 32, BN + c0), U);
-          float sc[16];
+        // features w0 + 64 half .. + 63: gate in accumulator columns c, up in 128 + c
+        uint16_t* dst = a.h_out + (size_t)(te.row0 + r) * a.I + w0 + 64 * half;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) *(float4*)(sc + 4 * i) = *(const float4*)(cs + c0 + 4 * i);
+        for (int b = 0; b < 2; ++b) {
+          const int c = 64 * half + 32 * b;
+          uint32_t G[32], U[32];
+          tmem_ld_32x16(taddr(tmem, q * 32, c), G);
+          tmem_ld_32x16(taddr(tmem, q * 32, c + 16), G + 16);
+          tmem_ld_32x16(taddr(tmem, q * 32, 128 + c), U);
+          tmem_ld_32x16(taddr(tmem, q * 32, 128 + c + 16), U + 16);
           tmem_ld_wait();
+          if (b == 1) {  // the accumulator is free once every warp has read it
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty);
+          }
+          uint32_t hw[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float gv = __uint_as_float(G[j]) * sc[j], uv = __uint_as_float(U[j]) * sc[j];
-            const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
-            sh[(c0 + j) * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
-          }
-        }
-        // the tile's valid token rows leave as 256-byte row segments in 16-byte stores
-        named_bar_sync(2, kEpiWarps * 32);
-        const int nrows = te.rows < BN ? te.rows : BN;
-        for (int idx = et; idx < nrows * 16; idx += kEpiWarps * 32) {
-          const int row = idx >> 4, piece = idx & 15;
-          *(uint4*)(a.h_out + (size_t)(te.row0 + row) * a.I + nb0 + piece * 8) =
-              *(const uint4*)(sH + row * 256 + piece * 16);
-        }
-      } else if (ge < nsub) {
-        const int c = (ge == 0 ? nb0 : nb1) + r;
-        const int* ct = s_ct[buf];
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          uint32_t Y[16];
-          tmem_ld_32x16(taddr(tmem, q * 32, ge * BN + c0), Y);
-          float sc[16];
-          int tok[16];
+            float hv[2];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            *(float4*)(sc + 4 * i) = *(const float4*)(cs + c0 + 4 * i);
-            *(int4*)(tok + 4 * i) = *(const int4*)(ct + c0 + 4 * i);
+            for (int e = 0; e < 2; ++e) {
+              const float gv = __uint_as_float(G[2 * j + e]) * cs, uv = __uint_as_float(U[2 * j + e]) * cs;
+              hv[e] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+            }
+            hw[j] = pack_bf16x2(hv[0], hv[1]);
           }
+          if (live)
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              *(uint4*)(dst + 32 * b + 8 * v4) = make_uint4(hw[4 * v4], hw[4 * v4 + 1], hw[4 * v4 + 2], hw[4 * v4 + 3]);
+        }
+      } else {
+        // output features w0 + 128 half .. + 127 of the routing-weighted row
+        uint16_t* dst = a.y_out + (size_t)(te.row0 + r) * a.H + w0 + 128 * half;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int c = 128 * half + 64 * b;
+          uint32_t Y[64];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) tmem_ld_32x16(taddr(tmem, q * 32, c + 16 * i), Y + 16 * i);
           tmem_ld_wait();
+          if (b == 1) {
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty);
+          }
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < te.rows)
-              a.y_out[(size_t)(te.row0 + c0 + j) * a.H + c] = bf16_bits(sc[j] * __uint_as_float(Y[j]));
+          for (int j = 0; j < 32; ++j)  // in place: word j reads words 2j, 2j+1 >= j
+            Y[j] = pack_bf16x2(__uint_as_float(Y[2 * j]) * cs, __uint_as_float(Y[2 * j + 1]) * cs);
+          if (live)
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              *(uint4*)(dst + 64 * b + 8 * v4) = make_uint4(Y[4 * v4], Y[4 * v4 + 1], Y[4 * v4 + 2], Y[4 * v4 + 3]);
         }
       }
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty);
     }
   }
 
@@ -424,32 +391,21 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
 
 // The FP4 path needs whole 256-element K chunks in both GEMMs.
 bool fp4_supported(const moe_packed_desc_t& d) { return d.H % 256 == 0 && d.I % 256 == 0; }
+int fp4_row_block() { return kRows; }
 
-template <int MODE, int BN>
-static cudaError_t launch_fp4_one(const Fp4Args& a, int work, cudaStream_t s) {
+template <int MODE>
+static cudaError_t launch_fp4(const Fp4Args& a, int work, cudaStream_t s) {
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(fp4_kernel<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)Fp4Cfg<MODE, BN>::kSmem);
+    cudaFuncSetAttribute(fp4_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     attr = true;
   }
   const int sms = tc_num_sms();
-  return launch_pdl(fp4_kernel<MODE, BN>, dim3(work < sms ? work : sms), dim3(kThreads), Fp4Cfg<MODE, BN>::kSmem, s,
-                    a);
-}
-
-template <int MODE>
-static cudaError_t launch_fp4_bn(int bn, const Fp4Args& a, int work, cudaStream_t s) {
-  switch (bn) {
-    case 16: return launch_fp4_one<MODE, 16>(a, work, s);
-    case 32: return launch_fp4_one<MODE, 32>(a, work, s);
-    case 64: return launch_fp4_one<MODE, 64>(a, work, s);
-    default: return launch_fp4_one<MODE, 128>(a, work, s);
-  }
+  return launch_pdl(fp4_kernel<MODE>, dim3(work < sms ? work : sms), dim3(kThreads), kSmem, s, a);
 }
 
 cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
-                               int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s) {
+                               const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s) {
   const int E = d.E, H = d.H, I = d.I;
   const size_t R = (size_t)T * k;
   const MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
@@ -470,37 +426,37 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   a.k = k;
   a.I = I;
   a.H = H;
-  const int max_tiles = (int)(R / bn + (R < (size_t)E ? R : (size_t)E) + 1);
+  const int max_tiles = (int)(R / kRows + (R < (size_t)E ? R : (size_t)E) + 1);
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 
-  // gate/up: A = fused [2I, H] NVFP4 weights, B = quantized x in permuted row order
+  // gate/up: A = quantized x in permuted row order, B = fused [2I, H] NVFP4 weights
   if (!tc_make_map(&a.wcode, u8, gu.a, H / 2, (uint64_t)E * 2 * I, H / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tc_make_map(&a.wsf, u8, gu.b, H / 16, (uint64_t)E * 2 * I, H / 16, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !tc_make_map(&a.xcode, u8, xq, H / 2, (uint64_t)R, H / 2, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B))
+      !tc_make_map(&a.xcode, u8, xq, H / 2, (uint64_t)R, H / 2, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc_make_map(&a.xsf, u8, xsf, H / 16, (uint64_t)R, H / 16, 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  a.asf = xsf;
   a.wgs = gu.gs;
   a.ags = (const float*)(ws + L.xg);
   a.N = 2 * I;
   a.K = H;
   record_event(ev.start[0], s);
-  cudaError_t err = launch_fp4_bn<0>(bn, a, max_tiles * (I / 128), s);
+  cudaError_t err = launch_fp4<0>(a, max_tiles * (I / 128), s);
   record_event(ev.stop[0], s);
   if (err != cudaSuccess) return err;
 
-  // h -> NVFP4 per permuted row (its own global scale), then down: A = [H, I] weights, B = h rows
+  // h -> NVFP4 per permuted row (its own global scale), then down: A = h rows, B = [H, I] weights
   launch_quant_rows((const __nv_bfloat16*)(ws + L.h), nullptr, 1, (int)R, I, hq, hsf, (float*)(ws + L.hg), s);
   if (!tc_make_map(&a.wcode, u8, dn.a, I / 2, (uint64_t)E * H, I / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tc_make_map(&a.wsf, u8, dn.b, I / 16, (uint64_t)E * H, I / 16, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !tc_make_map(&a.xcode, u8, hq, I / 2, (uint64_t)R, I / 2, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B))
+      !tc_make_map(&a.xcode, u8, hq, I / 2, (uint64_t)R, I / 2, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc_make_map(&a.xsf, u8, hsf, I / 16, (uint64_t)R, I / 16, 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  a.asf = hsf;
   a.wgs = dn.gs;
   a.ags = (const float*)(ws + L.hg);
   a.N = H;
   a.K = I;
   record_event(ev.start[1], s);
-  err = launch_fp4_bn<1>(bn, a, max_tiles * ((H + 255) / 256), s);
+  err = launch_fp4<1>(a, max_tiles * (H / 256), s);
   record_event(ev.stop[1], s);
   note_launches(2);
   return err;

@@ -206,7 +206,7 @@ cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const
   if (T == 0) return cudaGetLastError();
   cudaError_t e;
   if (d.fmt == MOE_FMT_NVFP4_W4A4 && fp4_supported(d)) {
-    e = launch_experts_fp4(d, packed, x, T, k, row_block, L, ws, ev, s);
+    e = launch_experts_fp4(d, packed, x, T, k, L, ws, ev, s);
   } else if (d.fmt == MOE_FMT_NVFP4_W4A4) {
     launch_quant_rows(x, nullptr, 1, T, d.H, (uint8_t*)(ws + L.xq), (uint8_t*)(ws + L.xs), (float*)(ws + L.xg), s);
     e = run_simt<MOE_FMT_NVFP4_W4A16, true>(d, packed, x, T, k, L, ws, ev, s);

@@ -151,10 +151,11 @@ int tc_num_sms();
 int fp8dec_row_block();
 cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,
                                   int k, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);
-// NVFP4 W4A4 path on block-scaled FP4 MMAs (H and I multiples of 256).
+// NVFP4 W4A4 path on block-scaled FP4 MMAs (H and I multiples of 256; 128-row routing tiles).
 bool fp4_supported(const moe_packed_desc_t& d);
+int fp4_row_block();
 cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
-                               int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);
+                               const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);
 cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
                               int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);
 

@@ -245,7 +245,7 @@ def test_layer_full_size_sampled(orc, fmt, T, zipf, sample):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-@pytest.mark.parametrize("T,E,k", [(64, 8, 2), (45, 16, 4), (300, 32, 8)])
+@pytest.mark.parametrize("T,E,k", [(64, 8, 2), (45, 16, 4), (300, 32, 8), (700, 4, 2)])
 def test_layer_k256_shapes(orc, fmt, T, E, k):
     """Hidden and intermediate sizes that are multiples of 256 (the block-scaled FP4 path's
     K chunk): several tiles per expert, ragged tails, and row blocks from 16 to 128."""
