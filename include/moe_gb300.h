@@ -71,6 +71,12 @@ typedef enum {
  *          GU_B = weight_scale E4M3 [E, 2I, H/16]
  *          D_A  = weight_packed u8 [E, H, I/2]  D_B = weight_scale E4M3 [E, H, I/16]
  *          GU_GS / D_GS = weight_global_scale f32 [E] (the quantize multiplier 2688/amax)
+ *   NVFP4 W4A4 with H and I multiples of 256 also carries a copy of each weight_scale tensor
+ *   re-tiled for the block-scaled tensor-core path, every (128-row tile, 256-column chunk) one
+ *   contiguous 2 KB block:
+ *          GU_BT = E4M3 [E, 2I/128, H/256, 128, 16]   D_BT = E4M3 [E, H/128, I/256, 128, 16]
+ *          (element [e, t, c, r, j] = weight_scale[e, 128 t + r, 16 c + j]); written by
+ *          moe_pack_experts next to the canonical tensors, not part of the checkpoint format.
  * Every tensor starts on a 256-byte boundary of the packed buffer. */
 enum {
   MOE_T_GU_A = 0,
@@ -79,6 +85,8 @@ enum {
   MOE_T_D_B = 3,
   MOE_T_GU_GS = 4,
   MOE_T_D_GS = 5,
+  MOE_T_GU_BT = 6,
+  MOE_T_D_BT = 7,
   MOE_T_COUNT = 8
 };
 

@@ -22,7 +22,7 @@ FMT_NVFP4_W4A16 = 3
 FMT_NVFP4_W4A4 = 4
 FORMATS = {"fp8": FMT_FP8, "int4": FMT_INT4, "nvfp4_w4a16": FMT_NVFP4_W4A16, "nvfp4_w4a4": FMT_NVFP4_W4A4}
 
-MOE_T_GU_A, MOE_T_GU_B, MOE_T_D_A, MOE_T_D_B, MOE_T_GU_GS, MOE_T_D_GS = range(6)
+MOE_T_GU_A, MOE_T_GU_B, MOE_T_D_A, MOE_T_D_B, MOE_T_GU_GS, MOE_T_D_GS, MOE_T_GU_BT, MOE_T_D_BT = range(8)
 
 EXPORTS = ("moe_packed_size", "moe_pack_experts", "moe_workspace_size", "moe_layer_forward",
            "moe_workspace_size_host_io", "moe_layer_forward_host", "moe_get_device_error", "moe_status_string",
@@ -205,10 +205,12 @@ def packed_view(desc: PackedDesc, packed, which: int):
     o, n = int(desc.offset[which]), int(desc.size[which])
     raw = packed[o:o + n]
     fmt = desc.fmt
-    gu = which in (MOE_T_GU_A, MOE_T_GU_B)
+    gu = which in (MOE_T_GU_A, MOE_T_GU_B, MOE_T_GU_BT)
     N, K = (2 * I, H) if gu else (H, I)
     if which in (MOE_T_GU_GS, MOE_T_D_GS):
         return raw.view(torch.float32)
+    if which in (MOE_T_GU_BT, MOE_T_D_BT):
+        return raw.view(E, N // 128, K // 256, 128, 16)
     if fmt == FMT_FP8:
         return raw.view(E, N, K) if which in (MOE_T_GU_A, MOE_T_D_A) else raw.view(torch.float32).view(
             E, N // 128, K // 128)

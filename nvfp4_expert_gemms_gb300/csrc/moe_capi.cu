@@ -41,10 +41,10 @@ WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
   L.hmax = take(4 * R);
   if (fmt == MOE_FMT_NVFP4_W4A4) {  // activation codes per permuted row (first T rows: per token)
     L.xq = take(R * H / 2);
-    L.xs = take(R * H / 16);
+    L.xs = take((size_t)sf_plane_rows(R) * H / 16);
     L.xg = take(4 * R);
     L.hq = take(R * I / 2);
-    L.hs = take(R * I / 16);
+    L.hs = take((size_t)sf_plane_rows(R) * I / 16);
     L.hg = take(4 * R);
   }
   if (fmt != MOE_FMT_NVFP4_W4A4 && tc_row_block(fmt, T, k, E) >= kTcPermuteFromRows) L.xp = take(2 * R * H);
@@ -149,6 +149,10 @@ moe_status_t moe_packed_size(int fmt, int E, int H, int I, moe_packed_desc_t* d)
       sz[MOE_T_D_B] = e * dn / 16;
       sz[MOE_T_GU_GS] = e * 4;
       sz[MOE_T_D_GS] = e * 4;
+      if (fmt == MOE_FMT_NVFP4_W4A4 && fp4_supported(*d)) {  // re-tiled scales for the FP4 MMA path
+        sz[MOE_T_GU_BT] = sz[MOE_T_GU_B];
+        sz[MOE_T_D_BT] = sz[MOE_T_D_B];
+      }
       break;
   }
   size_t cur = 0;

@@ -16,8 +16,10 @@
 // output features.  An N = 256 block-scaled MMA costs the tensor pipe the same issue time as
 // N = 64 or 128, so one instruction per K step covers what two N = 128 ones did.  Codes arrive
 // by TMA tiles in the 128-byte swizzle (x is quantized straight into permuted row order, one copy
-// per routed token slot, so the gate/up GEMM needs no row gather).  The weight block scales
-// and the activation block scales arrive by TMA next to their codes; the four scale warps place
+// per routed token slot, so the gate/up GEMM needs no row gather).  The block scales come in
+// layouts where the 128 rows of one 256-column chunk are one contiguous 2 KB block (the packed
+// re-tiled weight-scale copy; the quantizer writes activation scales chunk-major), each one bulk
+// copy next to its codes rather than 128 strided 16-byte pieces; the four scale warps place
 // both in tensor memory in the layout the MMA reads (per K = 64 step: row r of the operand in lane
 // r % 32 of column r / 32, four scales per word, repeated in every lane quarter).
 //
@@ -38,6 +40,7 @@ using namespace tc;
 constexpr int kKC = 256;                  // K per chunk: 128 bytes of codes per row
 constexpr int kRows = 128;                // activation rows per item (MMA M): the routing row block
 constexpr int kStagesW = 4, kStagesX = 4, kStagesS = 4;
+constexpr int kRing = 8;                  // work items handed from the producer to the other warps
 constexpr int kSfWarps = 4, kEpiWarp0 = 4, kEpiWarps = 8, kProdWarp = 12, kMmaWarp = 13;
 constexpr int kThreads = 14 * 32;
 constexpr int kWCodes = 128 * 128;        // one 128-row weight tile, 128-byte swizzle
@@ -50,8 +53,11 @@ constexpr uint32_t kSfCol = 256;          // TMEM: [0, 256) accumulator, then 4 
 constexpr uint32_t kSfStageCols = 48;     // A (activation) scales 4 x 4 columns, B (weight) scales 4 x 8
 
 struct Fp4Args {
-  CUtensorMap wcode, wsf;   // weight codes [E*N, K/2], scales [E*N, K/16]
-  CUtensorMap xcode, xsf;   // activation codes [R, K/2] and block scales [R, K/16], permuted row order
+  CUtensorMap wcode;        // weight codes [E*N, K/2]
+  CUtensorMap xcode;        // activation codes [R, K/2], permuted row order
+  const uint8_t* wsft;      // weight block scales re-tiled [E, N/128, K/256, 128, 16]
+  const uint8_t* asft;      // activation block scales chunk-major [K/256][sf_rows][16]
+  int sf_rows;
   const float* wgs;         // weight global scales [E]
   const float* ags;         // activation global scales [R]
   const int32_t* perm;
@@ -60,6 +66,7 @@ struct Fp4Args {
   uint16_t* h_out;          // MODE 0 output [R, I] bf16
   uint16_t* y_out;          // MODE 1 output: routing-weighted rows [R, H] bf16, permuted order
   int* err;
+  int* work_ctr;            // items handed out past each CTA's first (zeroed by routing)
   int k, N, K, I, H;
 };
 
@@ -98,6 +105,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   char* sX = sW + kStagesW * kWStage;
   __shared__ uint64_t w_full[kStagesW], w_empty[kStagesW], x_full[kStagesX], x_empty[kStagesX], s_full[kStagesS],
       s_empty[kStagesS], acc_full, acc_empty, drain;
+  __shared__ uint64_t work_full[kRing], work_empty[kRing];
+  __shared__ int s_work[kRing];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -124,6 +133,10 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
       mbar_init(&s_full[i], kSfWarps);
       mbar_init(&s_empty[i], 1);
     }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&work_full[i], 1);
+      mbar_init(&work_empty[i], kSfWarps + 1 + kEpiWarps);  // every consuming warp
+    }
     mbar_init(&acc_full, 1);
     mbar_init(&acc_empty, kEpiWarps);
     mbar_init(&drain, 1);
@@ -136,9 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   }
   if (warp == kProdWarp && lane == 0) {
     prefetch_tmap(&a.wcode);
-    prefetch_tmap(&a.wsf);
     prefetch_tmap(&a.xcode);
-    prefetch_tmap(&a.xsf);
   }
   fence_before_sync();
   __syncthreads();
@@ -147,6 +158,18 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   if (MODE == 1 && warp != kProdWarp) pdl_wait();  // the producer waits before its first h tile
   pdl_trigger();
 
+  // Work items are handed out dynamically (SMs do not all stream at the same rate): the
+  // producer takes each CTA's first item statically and the rest from a global counter, and
+  // passes every item id (then -1) through a shared-memory ring to the other warps.
+  auto next_item = [&](int n, bool& ok) -> int {  // consumer side, whole warp
+    const int slot = n % kRing;
+    ok = __all_sync(0xffffffffu, mbar_wait(&work_full[slot], (n / kRing) & 1, &s_abort));
+    if (!ok) return -1;
+    const int wk = *(volatile int*)&s_work[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&work_empty[slot]);
+    return wk;
+  };
   // item wk: routing tile wk / ncb; weight rows w0 .. w0+127 and w1 .. w1+127 of its expert
   auto item = [&](int wk, TileEntry& te, int& w0, int& w1) {
     te = load_tile(a.tiles + 1 + wk / ncb);
@@ -160,7 +183,21 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
     int it = 0;
     bool ok = true;
     int armed_w[kStagesW] = {0}, armed_x[kStagesX] = {0};
-    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x) {
+    for (int n = 0; ok; ++n) {
+      int wk = -1;
+      if (lane == 0) {
+        wk = n == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.work_ctr, 1);
+        if (wk >= nwork) wk = -1;
+        const int slot = n % kRing;
+        ok = mbar_wait(&work_empty[slot], ((n / kRing) & 1) ^ 1, &s_abort);
+        if (ok) {
+          s_work[slot] = wk;
+          mbar_arrive(&work_full[slot]);
+        }
+      }
+      wk = __shfl_sync(0xffffffffu, wk, 0);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok || wk < 0) break;
       TileEntry te;
       int w0, w1;
       item(wk, te, w0, w1);
@@ -173,9 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
             mbar_arrive_expect_tx(&w_full[sw], 2 * (kWCodes + kWSf));
             ++armed_w[sw];
             for (int g = 0; g < 2; ++g) {
-              const int row = te.expert * a.N + (g == 0 ? w0 : w1);
-              tma_load_2d(ws + g * kWCodes, &a.wcode, &w_full[sw], kc * (kKC / 2), row);
-              tma_load_2d(ws + 2 * kWCodes + g * kWSf, &a.wsf, &w_full[sw], kc * (kKC / 16), row);
+              const int wr = g == 0 ? w0 : w1;
+              tma_load_2d(ws + g * kWCodes, &a.wcode, &w_full[sw], kc * (kKC / 2), te.expert * a.N + wr);
+              // the 128 rows' scales of this chunk: one contiguous 2 KB block of the re-tiled copy
+              const size_t blk = ((size_t)te.expert * (a.N / 128) + wr / 128) * nK + kc;
+              bulk_load(ws + 2 * kWCodes + g * kWSf, a.wsft + blk * kWSf, kWSf, &w_full[sw]);
             }
           }
           if (ok) {
@@ -185,7 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
               mbar_arrive_expect_tx(&x_full[sx], kXStage);
               ++armed_x[sx];
               tma_load_2d(sX + sx * kXStage, &a.xcode, &x_full[sx], kc * (kKC / 2), te.row0);
-              tma_load_2d(sX + sx * kXStage + kXCodes, &a.xsf, &x_full[sx], kc * (kKC / 16), te.row0);
+              bulk_load(sX + sx * kXStage + kXCodes, a.asft + ((size_t)kc * a.sf_rows + te.row0) * 16, kRows * 16,
+                        &x_full[sx]);
             }
           }
         }
@@ -204,9 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer (whole warp waits, lane 0 issues) ----------------
     const uint32_t idesc = idesc_nvf4(kRows, 256);
-    int it = 0, nitem = 0;
+    int it = 0;
     bool ok = true;
-    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x, ++nitem) {
+    for (int nitem = 0; ok; ++nitem) {
+      if (next_item(nitem, ok) < 0) break;
       ok = mbar_wait(&acc_empty, (nitem & 1) ^ 1, &s_abort);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
@@ -242,7 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
     const int q = warp, l = lane;
     int it = 0;
     bool ok = true;
-    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x) {
+    for (int n = 0; ok; ++n) {
+      const int wk = next_item(n, ok);
+      if (wk < 0) break;
       TileEntry te;
       int w0, w1;
       item(wk, te, w0, w1);
@@ -297,9 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
     // ---------------- epilogue: thread = token row of the tile ----------------
     const int q = warp & 3, half = (warp - kEpiWarp0) >> 2, r = q * 32 + lane;
-    int nitem = 0;
     bool ok = true;
-    for (int wk = blockIdx.x; wk < nwork; wk += gridDim.x, ++nitem) {
+    for (int nitem = 0; ok; ++nitem) {
+      const int wk = next_item(nitem, ok);
+      if (wk < 0) break;
       TileEntry te;
       int w0, w1;
       item(wk, te, w0, w1);
@@ -344,10 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
             }
             hw[j] = pack_bf16x2(hv[0], hv[1]);
           }
-          if (live)
+          if (live)  // 32-byte stores: each lane writes whole sectors of its own row
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              *(uint4*)(dst + 32 * b + 8 * v4) = make_uint4(hw[4 * v4], hw[4 * v4 + 1], hw[4 * v4 + 2], hw[4 * v4 + 3]);
+            for (int v = 0; v < 2; ++v) st_global_v8(dst + 32 * b + 16 * v, hw + 8 * v);
         }
       } else {
         // output features w0 + 128 half .. + 127 of the routing-weighted row
@@ -369,8 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
             Y[j] = pack_bf16x2(__uint_as_float(Y[2 * j]) * cs, __uint_as_float(Y[2 * j + 1]) * cs);
           if (live)
 #pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              *(uint4*)(dst + 64 * b + 8 * v4) = make_uint4(Y[4 * v4], Y[4 * v4 + 1], Y[4 * v4 + 2], Y[4 * v4 + 3]);
+            for (int v = 0; v < 4; ++v) st_global_v8(dst + 64 * b + 16 * v, Y + 8 * v);
         }
       }
     }
@@ -413,7 +455,8 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   uint8_t* xsf = (uint8_t*)(ws + L.xs);
   uint8_t* hq = (uint8_t*)(ws + L.hq);
   uint8_t* hsf = (uint8_t*)(ws + L.hs);
-  launch_quant_rows(x, (const int32_t*)(ws + L.inv), k, T, H, xq, xsf, (float*)(ws + L.xg), s, true);
+  const int sf_rows = sf_plane_rows(R);
+  launch_quant_rows(x, (const int32_t*)(ws + L.inv), k, T, H, xq, xsf, (float*)(ws + L.xg), s, true, sf_rows);
 
   Fp4Args a;
   memset(&a, 0, sizeof(a));
@@ -426,15 +469,17 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   a.k = k;
   a.I = I;
   a.H = H;
+  a.sf_rows = sf_rows;
+  a.work_ctr = (int*)(ws + L.err) + 1;
   const int max_tiles = (int)(R / kRows + (R < (size_t)E ? R : (size_t)E) + 1);
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 
   // gate/up: A = quantized x in permuted row order, B = fused [2I, H] NVFP4 weights
   if (!tc_make_map(&a.wcode, u8, gu.a, H / 2, (uint64_t)E * 2 * I, H / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc_make_map(&a.wsf, u8, gu.b, H / 16, (uint64_t)E * 2 * I, H / 16, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !tc_make_map(&a.xcode, u8, xq, H / 2, (uint64_t)R, H / 2, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc_make_map(&a.xsf, u8, xsf, H / 16, (uint64_t)R, H / 16, 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+      !tc_make_map(&a.xcode, u8, xq, H / 2, (uint64_t)R, H / 2, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  a.wsft = (const uint8_t*)packed + d.offset[MOE_T_GU_BT];
+  a.asft = xsf;
   a.wgs = gu.gs;
   a.ags = (const float*)(ws + L.xg);
   a.N = 2 * I;
@@ -445,16 +490,18 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   if (err != cudaSuccess) return err;
 
   // h -> NVFP4 per permuted row (its own global scale), then down: A = h rows, B = [H, I] weights
-  launch_quant_rows((const __nv_bfloat16*)(ws + L.h), nullptr, 1, (int)R, I, hq, hsf, (float*)(ws + L.hg), s);
+  launch_quant_rows((const __nv_bfloat16*)(ws + L.h), nullptr, 1, (int)R, I, hq, hsf, (float*)(ws + L.hg), s, false,
+                    sf_rows);
   if (!tc_make_map(&a.wcode, u8, dn.a, I / 2, (uint64_t)E * H, I / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc_make_map(&a.wsf, u8, dn.b, I / 16, (uint64_t)E * H, I / 16, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !tc_make_map(&a.xcode, u8, hq, I / 2, (uint64_t)R, I / 2, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc_make_map(&a.xsf, u8, hsf, I / 16, (uint64_t)R, I / 16, 16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+      !tc_make_map(&a.xcode, u8, hq, I / 2, (uint64_t)R, I / 2, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  a.wsft = (const uint8_t*)packed + d.offset[MOE_T_D_BT];
+  a.asft = hsf;
   a.wgs = dn.gs;
   a.ags = (const float*)(ws + L.hg);
   a.N = H;
   a.K = I;
+  a.work_ctr = (int*)(ws + L.err) + 2;
   record_event(ev.start[1], s);
   err = launch_fp4<1>(a, max_tiles * (H / 256), s);
   record_event(ev.stop[1], s);

@@ -22,6 +22,15 @@ enum : int { kDevOk = 0, kDevTimeout = MOE_ERR_DEVICE_TIMEOUT, kDevFault = MOE_E
 __device__ __forceinline__ void set_dev_error(int* err, int code) { atomicCAS(err, 0, code); }
 
 // ---- scalar codecs (device) --------------------------------------------------------------
+// The workspace status block (256 bytes): int 0 is the device error word; ints 1 .. kSchedCounters
+// are the work counters of the persistent GEMM kernels that hand out items dynamically.  The
+// routing kernel of every forward pass resets them all.
+constexpr int kSchedCounters = 2;
+__device__ __forceinline__ void reset_status(int* status) {
+  status[0] = kDevOk;
+  for (int i = 1; i <= kSchedCounters; ++i) status[i] = 0;
+}
+
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 __device__ __forceinline__ uint16_t bf16_bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
@@ -95,8 +104,12 @@ cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e
 // NVFP4 quantization of bf16 rows; row r's codes go to output row r, or (scatter != null) to
 // rows scatter[r*k .. r*k+k-1].  early: x was final before the preceding kernel of the stream
 // passed its pdl_wait() (true only right after routing), so x is read before this launch's wait.
+// sf_rows = 0: scales row-major [rows, K/16]; else chunk-major [K/256][sf_rows][16].
 cudaError_t launch_quant_rows(const __nv_bfloat16* x, const int32_t* scatter, int k, int rows, int K, uint8_t* q,
-                              uint8_t* sf, float* gs, cudaStream_t s, bool early = false);
+                              uint8_t* sf, float* gs, cudaStream_t s, bool early = false, int sf_rows = 0);
+// Rows of one chunk plane of chunk-major activation scales for R routed rows: a 128-row tile
+// starting at any row below R stays inside its plane.
+inline int sf_plane_rows(size_t R) { return (int)R + 128; }
 // out[r] = x[map[r] / k] for r < rows (rows of K bf16).
 cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* map, int k, int rows, int K, __nv_bfloat16* out,
                                cudaStream_t s);

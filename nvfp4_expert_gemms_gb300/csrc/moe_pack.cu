@@ -165,6 +165,19 @@ __global__ void __launch_bounds__(256) nvfp4_pack_kernel(const uint16_t* __restr
   nvfp4_block(v, gs, (uint2*)(packed + (size_t)e * N * K / 2 + i * 8), scales + (size_t)e * nblk + i);
 }
 
+// Re-tile NVFP4 block scales [E, N, K/16] into [E, N/128, K/256, 128, 16]: thread = one
+// 16-byte (row, 256-column chunk) piece.
+__global__ void __launch_bounds__(256) nvfp4_retile_kernel(const uint4* __restrict__ src, int E, int N, int K,
+                                                           uint4* __restrict__ dst) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int nc = K / 256;
+  if (i >= (size_t)E * N * nc) return;
+  const size_t row = i / nc;  // e * N + n
+  const int c = (int)(i % nc), n = (int)(row % N);
+  const size_t e = row / N;
+  dst[((e * (N / 128) + n / 128) * nc + c) * 128 + n % 128] = src[i];
+}
+
 __global__ void nvfp4_finish_kernel(unsigned* slot, int E) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e < E) {
@@ -174,6 +187,13 @@ __global__ void nvfp4_finish_kernel(unsigned* slot, int E) {
   }
 }
 
+// Byte offset of the block scale of 16-block b of row d: row-major [rows, K/16], or with
+// sf_rows > 0 chunk-major [K/256][sf_rows][16] (every 256-column chunk of a run of rows is
+// one contiguous block, as the block-scaled MMA path loads it).
+__device__ __forceinline__ size_t sf_index(size_t d, int b, int K, int sf_rows) {
+  return sf_rows ? ((size_t)(b >> 4) * sf_rows + d) * 16 + (b & 15) : d * (K / 16) + b;
+}
+
 // Dynamic NVFP4 quantization of bf16 rows (W4A4 activations): one warp per input row r;
 // gs_row = 2688 / max(amax_row, 1e-12), then blocks exactly as for weights.  The codes, scales
 // and gs_row go to output row r, or, with a scatter map, to each of rows scatter[r*k .. r*k+k-1]
@@ -181,7 +201,7 @@ __global__ void nvfp4_finish_kernel(unsigned* slot, int E) {
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restrict__ x,
                                                          const int32_t* __restrict__ scatter, int k, int rows, int K,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                                         float* __restrict__ gs_out) {
+                                                         float* __restrict__ gs_out, int sf_rows) {
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   pdl_wait();
@@ -218,7 +238,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
     for (int c = 0; c < ncopy; ++c) {
       const size_t d = scatter ? (size_t)scatter[(size_t)r * k + c] : (size_t)r;
       *(uint2*)(q + d * (K / 2) + b * 8) = code;
-      sf[d * (K / 16) + b] = scale;
+      sf[sf_index(d, b, K, sf_rows)] = scale;
     }
   }
 }
@@ -234,7 +254,7 @@ template <int NBLK, int RPW, bool EARLY>
 __global__ void __launch_bounds__(256) quant_rows_flat_kernel(const uint16_t* __restrict__ x,
                                                               const int32_t* __restrict__ scatter, int k, int rows,
                                                               uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                                              float* __restrict__ gs_out) {
+                                                              float* __restrict__ gs_out, int sf_rows) {
   constexpr int K = 16 * NBLK, kFlat = NBLK * RPW, NB = (kFlat + 31) / 32;
   static_assert(NB <= 8 && RPW * kMaxTopK <= 32, "flat quantizer shape");
   const int lane = threadIdx.x & 31;
@@ -309,7 +329,7 @@ __global__ void __launch_bounds__(256) quant_rows_flat_kernel(const uint16_t* __
       const int d = __shfl_sync(0xffffffffu, my_dst, (row < RPW ? row : 0) * ncopy + c);
       if (live) {
         *(uint2*)(q + (size_t)d * (K / 2) + b * 8) = code;
-        sf[(size_t)d * (K / 16) + b] = scale;
+        sf[sf_index((size_t)d, b, K, sf_rows)] = scale;
       }
     }
   }
@@ -362,6 +382,13 @@ cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, co
       nvfp4_pack_kernel<<<dim3((unsigned)((nblk + 255) / 256), E), 256, 0, s>>>(w, N, K, slot, a, b);
       nvfp4_finish_kernel<<<(E + 127) / 128, 128, 0, s>>>(slot, E);
       note_launches(2);
+      const int bt = which == 0 ? MOE_T_GU_BT : MOE_T_D_BT;
+      if (d.size[bt]) {
+        const size_t pieces = (size_t)E * N * (K / 256);
+        nvfp4_retile_kernel<<<(unsigned)((pieces + 255) / 256), 256, 0, s>>>((const uint4*)b, E, N, K,
+                                                                             (uint4*)(packed + d.offset[bt]));
+        note_launches(1);
+      }
     }
     note_launches(1);
   }
@@ -381,33 +408,33 @@ cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e
 
 template <int NBLK, int RPW>
 static cudaError_t launch_quant_flat(bool early, const __nv_bfloat16* x, const int32_t* scatter, int k, int rows,
-                                     uint8_t* q, uint8_t* sf, float* gs, cudaStream_t s) {
+                                     uint8_t* q, uint8_t* sf, float* gs, int sf_rows, cudaStream_t s) {
   const dim3 grid((rows + 8 * RPW - 1) / (8 * RPW));
   if (early)
     return launch_pdl(quant_rows_flat_kernel<NBLK, RPW, true>, grid, dim3(256), 0, s, (const uint16_t*)x, scatter, k,
-                      rows, q, sf, gs);
+                      rows, q, sf, gs, sf_rows);
   return launch_pdl(quant_rows_flat_kernel<NBLK, RPW, false>, grid, dim3(256), 0, s, (const uint16_t*)x, scatter, k,
-                    rows, q, sf, gs);
+                    rows, q, sf, gs, sf_rows);
 }
 
 cudaError_t launch_quant_rows(const __nv_bfloat16* x, const int32_t* scatter, int k, int rows, int K, uint8_t* q,
-                              uint8_t* sf, float* gs, cudaStream_t s, bool early) {
+                              uint8_t* sf, float* gs, cudaStream_t s, bool early, int sf_rows) {
   if (rows <= 0) return cudaGetLastError();
   note_launches(1);
   switch (K) {  // register-resident shapes: RPW rows fill whole 32-lane passes of 16-blocks
-    case 128: return launch_quant_flat<8, 4>(early, x, scatter, k, rows, q, sf, gs, s);
-    case 256: return launch_quant_flat<16, 2>(early, x, scatter, k, rows, q, sf, gs, s);
-    case 512: return launch_quant_flat<32, 1>(early, x, scatter, k, rows, q, sf, gs, s);
-    case 768: return launch_quant_flat<48, 2>(early, x, scatter, k, rows, q, sf, gs, s);
-    case 1024: return launch_quant_flat<64, 1>(early, x, scatter, k, rows, q, sf, gs, s);
-    case 1280: return launch_quant_flat<80, 2>(early, x, scatter, k, rows, q, sf, gs, s);
-    case 1536: return launch_quant_flat<96, 1>(early, x, scatter, k, rows, q, sf, gs, s);
-    case 2048: return launch_quant_flat<128, 1>(early, x, scatter, k, rows, q, sf, gs, s);
-    case 3072: return launch_quant_flat<192, 1>(early, x, scatter, k, rows, q, sf, gs, s);
-    case 4096: return launch_quant_flat<256, 1>(early, x, scatter, k, rows, q, sf, gs, s);
+    case 128: return launch_quant_flat<8, 4>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
+    case 256: return launch_quant_flat<16, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
+    case 512: return launch_quant_flat<32, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
+    case 768: return launch_quant_flat<48, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
+    case 1024: return launch_quant_flat<64, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
+    case 1280: return launch_quant_flat<80, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
+    case 1536: return launch_quant_flat<96, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
+    case 2048: return launch_quant_flat<128, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
+    case 3072: return launch_quant_flat<192, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
+    case 4096: return launch_quant_flat<256, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
     default:
       return launch_pdl(quant_rows_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, (const uint16_t*)x, scatter, k, rows,
-                        K, q, sf, gs);
+                        K, q, sf, gs, sf_rows);
   }
 }
 

@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(1024) route_topk_kernel(const float* __restric
   pdl_wait();
   pdl_trigger();
   zero_prelude(pre);
-  if (blockIdx.x == 0 && tid == 0) *err = kDevOk;  // each forward pass reports its own errors
+  if (blockIdx.x == 0 && tid == 0) reset_status(err);  // each forward pass reports its own errors
   __syncthreads();
   const int t_end = min(T, (int)(blockIdx.x + 1) * kRouteTB);
   for (int t = blockIdx.x * kRouteTB + warp; t < t_end; t += 32) {  // 4 tokens per warp
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
   pdl_wait();  // the previous kernel of the stream may still read the accumulators zeroed here
   pdl_trigger();
   zero_prelude(pre);
-  if (tid == 0) *err = kDevOk;
+  if (tid == 0) reset_status(err);
   __syncthreads();
   for (int t = warp; t < T; t += 32) {
     if (pre.x) row_absmax(pre, t, lane);

@@ -41,9 +41,13 @@ def test_packed_sizes_match_canonical_shapes(orc):
         assert got == E * want, (fmt, got)
         assert all(int(d.offset[i]) % 256 == 0 for i in range(8))
         assert d.bytes >= got
-    # the NVFP4 layer is the 0.32 GiB the page quotes
+    # the NVFP4 layer is the 0.32 GiB the page quotes (canonical tensors; the W4A4 buffer adds
+    # its re-tiled copy of the two scale tensors)
     d = M.moe_packed_size("nvfp4_w4a4", E, H, I)
-    assert round(sum(int(d.size[i]) for i in range(8)) / 2 ** 30, 2) == 0.32
+    assert round(sum(int(d.size[i]) for i in range(6)) / 2 ** 30, 2) == 0.32
+    assert int(d.size[M.MOE_T_GU_BT]) == int(d.size[M.MOE_T_GU_B]) and int(d.size[M.MOE_T_D_BT]) == int(
+        d.size[M.MOE_T_D_B])
+    assert int(M.moe_packed_size("nvfp4_w4a16", E, H, I).size[M.MOE_T_GU_BT]) == 0
 
 
 def test_packed_tensor_sizes_equal_oracle_outputs(orc):

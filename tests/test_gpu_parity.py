@@ -81,6 +81,24 @@ def test_pack_bit_exact(orc, fmt):
             assert got.tobytes() == ref[name][2].tobytes()
 
 
+def test_w4a4_retiled_scales(orc):
+    """The W4A4 buffer's re-tiled scale copies are the canonical weight_scale tensors (bit-exact
+    with the oracle's packing) rearranged to [E, N/128, K/256, 128, 16]."""
+    E, H, I = 3, 512, 256
+    wgu, wd = synth.gen_expert_weights(E, H, I, seed=6)
+    layer = M.MoELayer("nvfp4_w4a4", dev_bf16(wgu), dev_bf16(wd))
+    torch.cuda.synchronize()
+    ref = orc.pack_experts(FID["nvfp4_w4a4"], wgu, wd)
+    d = layer.desc
+    for canon, tiled, name, (N, K) in ((M.MOE_T_GU_B, M.MOE_T_GU_BT, "gu", (2 * I, H)),
+                                       (M.MOE_T_D_B, M.MOE_T_D_BT, "d", (H, I))):
+        sc = M.packed_view(d, layer.packed, canon).cpu().numpy()
+        assert sc.tobytes() == np.ascontiguousarray(ref[name][1]).tobytes()
+        want = sc.reshape(E, N // 128, 128, K // 256, 16).transpose(0, 1, 3, 2, 4)
+        got = M.packed_view(d, layer.packed, tiled).cpu().numpy()
+        assert np.array_equal(got, want), name
+
+
 @pytest.mark.parametrize("fmt", ["fp8", "int4", "nvfp4_w4a16"])
 def test_dequant_view_bit_exact(orc, fmt):
     E, H, I = 2, 256, 128
