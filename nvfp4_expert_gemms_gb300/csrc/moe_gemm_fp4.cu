@@ -343,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
     bool ok = true;
     for (int nitem = 0; ok; ++nitem) {
       const int wk = next_item(nitem, ok);
-      if (wk < 0) break;
+      // the epilogue warps leave together (they meet in a named barrier every item)
+      if (!named_bar_and(1, kEpiWarps * 32, ok && wk >= 0)) break;
       TileEntry te;
       int w0, w1;
       item(wk, te, w0, w1);

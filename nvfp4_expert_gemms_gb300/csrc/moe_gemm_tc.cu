@@ -43,6 +43,7 @@ constexpr int kConvWarps = 16;    // warps 0-15: converters + epilogue
 constexpr int kProdWarp = 16;     // TMA producer
 constexpr int kMmaWarp = 17;      // TMEM owner and MMA issuer
 constexpr int kGathWarp0 = 18, kGathWarps = 2;  // activation row gather (gate/up)
+constexpr int kRing = 8;           // work items handed from the producer to the other warps
 constexpr int kThreads = 20 * 32;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: [0, 2*BN) accumulators (two sub-tiles), then a ring of converted A chunks of 128
@@ -96,6 +97,7 @@ struct TcArgs {
   uint16_t* h_out;
   uint16_t* y_out;  // down: routing-weighted rows [R, H] bf16, permuted order
   int* err;
+  int* work_ctr;  // items handed out past each CTA's first (zeroed by routing)
   int k, N, K, I, H;
 };
 
@@ -252,6 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   constexpr int kScaleSlot = Cfg::kScaleSlot;
   __shared__ uint64_t w_full[kStagesW], w_empty[kStagesW], a_full[kStagesA], a_empty[kStagesA], b_full[SB],
       b_empty[SB], acc_full, drain;
+  __shared__ uint64_t work_full[kRing], work_empty[kRing];
+  __shared__ int s_work[kRing];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_tok[2][BN];     // gather: token of each row of the item (double-buffered)
@@ -281,6 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       mbar_init(&b_full[i], kGather ? kGathWarps : 1);
       mbar_init(&b_empty[i], 1);
     }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&work_full[i], 1);
+      mbar_init(&work_empty[i], (kGather ? kGathWarps : 0) + 1 + kConvWarps);  // every consuming warp
+    }
     mbar_init(&acc_full, 1);
     mbar_init(&drain, 1);
     s_abort = 0;
@@ -301,6 +309,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   if (MODE == 1 && warp != kProdWarp) pdl_wait();  // the producer waits before its first h tile
   pdl_trigger();
 
+  // Work items are handed out dynamically (SMs do not all stream at the same rate): the
+  // producer takes each CTA's first item statically and the rest from a global counter, and
+  // passes every item id (then -1) through a shared-memory ring to the other warps.
+  auto next_item = [&](int n, bool& ok) -> int {  // consumer side, whole warp
+    const int slot = n % kRing;
+    ok = __all_sync(0xffffffffu, mbar_wait(&work_full[slot], (n / kRing) & 1, &s_abort));
+    if (!ok) return -1;
+    const int wk = *(volatile int*)&s_work[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&work_empty[slot]);
+    return wk;
+  };
   // per-item geometry
   auto item = [&](int wk, TileEntry& te, int& nb0, int& nb1, int& nsub) {
     const int tile = wk / ncb, cb = wk % ncb;
@@ -320,11 +340,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     // ---------------- TMA producer (the whole warp walks the loop, lane 0 issues) ----------------
     int it = 0;
     int armed_w[kStagesW] = {0}, armed_b[SB] = {0};
-    for (int wk = blockIdx.x; wk < nwork; wk += gridDim.x) {
+    for (int n = 0;; ++n) {
+      int wk = -1;
+      bool ok = true;
+      if (lane == 0) {
+        wk = n == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.work_ctr, 1);
+        if (wk >= nwork) wk = -1;
+        const int slot = n % kRing;
+        ok = mbar_wait(&work_empty[slot], ((n / kRing) & 1) ^ 1, &s_abort);
+        if (ok) {
+          s_work[slot] = wk;
+          mbar_arrive(&work_full[slot]);
+        }
+      }
+      wk = __shfl_sync(0xffffffffu, wk, 0);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok || wk < 0) break;
       TileEntry te;
       int nb0, nb1, nsub;
       item(wk, te, nb0, nb1, nsub);
-      bool ok = true;
       for (int kc = 0; kc < nK; ++kc, ++it) {
         const int sw = it % kStagesW, sb = it % SB;
         if (lane == 0) {
@@ -402,9 +436,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     const int gt = (warp - kGathWarp0) * 32 + lane;
     const int piece = gt & 15, rsub = gt >> 4;
     const uint32_t dpiece = (uint32_t)(piece >> 3) * BN * 128;
-    int it = 0, pend = 0, nitem = 0;
+    int it = 0, pend = 0;
     bool ok = true;
-    for (int wk = blockIdx.x; wk < nwork; wk += gridDim.x, ++nitem) {
+    for (int nitem = 0;; ++nitem) {
+      const int wk = next_item(nitem, ok);
+      // the gather warps leave together (they meet in a named barrier every item)
+      if (!named_bar_and(2, kGathWarps * 32, ok && wk >= 0)) break;
       TileEntry te;
       int nb0, nb1, nsub;
       item(wk, te, nb0, nb1, nsub);
@@ -452,7 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     const uint32_t idesc = idesc_bf16_f32(128, BN);
     int it = 0;
     bool ok = true;
-    for (int wk = blockIdx.x; wk < nwork && ok; wk += gridDim.x) {
+    for (int nitem = 0; ok; ++nitem) {
+      const int wk = next_item(nitem, ok);
+      if (wk < 0) break;
       TileEntry te;
       int nb0, nb1, nsub;
       item(wk, te, nb0, nb1, nsub);
@@ -484,9 +523,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   } else if (warp < kConvWarps) {
     // ---------------- converters (16 warps) and epilogue ----------------
     const int g = (warp >> 2) & 1, kh = warp >> 3, q = warp & 3, r = q * 32 + lane;
-    int it = 0, nitem = 0;
+    int it = 0;
     bool ok = true;
-    for (int wk = blockIdx.x; wk < nwork; wk += gridDim.x, ++nitem) {
+    for (int nitem = 0;; ++nitem) {
+      const int wk = next_item(nitem, ok);
+      // the converter warps leave together (they meet in a named barrier every item)
+      if (!named_bar_and(1, kConvWarps * 32, ok && wk >= 0)) break;
       TileEntry te;
       int nb0, nb1, nsub;
       item(wk, te, nb0, nb1, nsub);
@@ -727,6 +769,7 @@ cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, co
   a.wscale = gu.b;
   a.wgs = gu.gs;
   a.N = 2 * I;
+  a.work_ctr = (int*)(ws + L.err) + 1;
   a.K = H;
   record_event(ev.start[0], s);
   cudaError_t err = launch_fmt<0>(d.fmt, bn, a, gx, I / 128, s);
@@ -741,6 +784,7 @@ cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, co
   a.wscale = dn.b;
   a.wgs = dn.gs;
   a.N = H;
+  a.work_ctr = (int*)(ws + L.err) + 2;
   a.K = I;
   record_event(ev.start[1], s);
   err = launch_fmt<1>(d.fmt, bn, a, gx, (H + 255) / 256, s);
