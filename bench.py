@@ -46,7 +46,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
+    p.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4, 5])
     p.add_argument("--tokens", type=int, default=None, help="tokens per step (default: the config's largest)")
     p.add_argument("--layers", type=int, default=None, help="layers per step (default 48)")
     p.add_argument("--seed", type=int, default=0)
@@ -63,8 +63,13 @@ def workload(args):
     return c
 
 
+def format_mix(c):
+    fm = synth.layer_formats(c, c["L"])
+    return " + ".join(f"{f} x{fm.count(f)}" for f in dict.fromkeys(fm))
+
+
 def describe(c):
-    return (f"{c['name']}: {c['fmt']} experts, T={c['T']} tokens x {c['L']} layers, hidden {c['H']}, "
+    return (f"{c['name']}: {format_mix(c)} experts, T={c['T']} tokens x {c['L']} layers, hidden {c['H']}, "
             f"intermediate {c['I']}, {c['E']} experts, top-{c['k']}"
             + (f", Zipf({c['zipf']}) routing skew" if c["zipf"] else ", N(0,1) logits"))
 
@@ -173,19 +178,22 @@ class OracleSample:
         oracle.build()
         self.oracle = oracle
         self.c = c
-        self.fid = FMT_ID[c["fmt"]]
         T, H, I, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
         self.x = synth.gen_x(T, H, seed)
         self.n_tok = T if T <= 64 else 64
         self.items = []
-        for layer in range(min(layers, c["L"])):
+        fmts = synth.layer_formats(c, c["L"])
+        first = [fmts.index(f) for f in dict.fromkeys(fmts)]  # one layer of each format, then the next ones
+        order = first + [l for l in range(c["L"]) if l not in first]
+        for layer in order[:min(layers, c["L"])]:
+            fid = FMT_ID[fmts[layer]]
             lg = synth.gen_logits(T, E, seed, layer, zipf_alpha=c["zipf"])
             toks = None if self.n_tok == T else np.sort(
                 np.random.default_rng([seed, layer]).choice(T, size=self.n_tok, replace=False)).astype(np.int32)
             idx, _ = oracle.route(lg if toks is None else lg[toks], k)
             experts = np.unique(idx)
             wgu, wd = synth.gen_expert_weights(E, H, I, seed, layer, experts=experts)
-            self.items.append((lg, toks, oracle.pack_experts(self.fid, wgu, wd, experts=experts)))
+            self.items.append((fid, lg, toks, oracle.pack_experts(fid, wgu, wd, experts=experts)))
         self.desc = (f"{len(self.items)} layer(s) x {self.n_tok} of {T} tokens of the same workload "
                      f"(only routed experts drawn; packing untimed)")
 
@@ -193,9 +201,9 @@ class OracleSample:
         """Oracle forward over the sample (repeated until min_seconds); returns (tokens/s, seconds)."""
         spent, tokens = 0.0, 0
         while True:
-            for lg, toks, packed in self.items:
+            for fid, lg, toks, packed in self.items:
                 t0 = time.perf_counter()
-                self.oracle.moe_layer(self.fid, self.x, lg, packed, self.c["k"], tokens=toks)
+                self.oracle.moe_layer(fid, self.x, lg, packed, self.c["k"], tokens=toks)
                 spent += time.perf_counter() - t0
                 tokens += self.n_tok
             if spent >= min_seconds:
@@ -232,11 +240,12 @@ def run_ours(args, c, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     fmt, T, H, I, E, k, L = c["fmt"], c["T"], c["H"], c["I"], c["E"], c["k"], c["L"]
+    fmts = synth.layer_formats(c, L)  # fmt throughout, or a mixed stack
     seed = args.seed + 7919 * rank
     layers = []
     for l in range(L):
         wgu, wd = synth.gen_expert_weights_device(E, H, I, seed, l, dev)
-        layers.append(M.MoELayer(fmt, wgu, wd))
+        layers.append(M.MoELayer(fmts[l], wgu, wd))
         del wgu, wd
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -244,22 +253,29 @@ def run_ours(args, c, rank, world, local_rank):
     lg_host = np.stack([synth.gen_logits(T, E, seed, l, zipf_alpha=c["zipf"]) for l in range(L)])
     lg = torch.from_numpy(lg_host).to(dev)
     outs = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(M.moe_workspace_size(layers[0].desc, T, k), dtype=torch.uint8, device=dev)
+    first_of = {f: layers[fmts.index(f)].desc for f in dict.fromkeys(fmts)}
+
+    def ws_bytes(Ts, host_io=False):  # one workspace serves every layer: the largest format's size
+        size = M.moe_workspace_size_host_io if host_io else M.moe_workspace_size
+        return max(size(d, Ts, k) for d in first_of.values())
+
+    ws = torch.empty(ws_bytes(T), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     # distinct routed experts per layer: the unit of algorithmic weight bytes
     D = [int(torch.unique(torch.topk(lg[l], k, dim=-1).indices).numel()) for l in range(L)]
-    gu_b, dn_b = per_expert_bytes(fmt, H, I)
+    peb = {f: per_expert_bytes(f, H, I) for f in first_of}  # (gate/up, down) packed bytes per expert
     x_b, lg_b, out_b = T * H * 2, T * E * 4, T * H * 2
-    layer_bytes = [d * (gu_b + dn_b) + x_b + lg_b + out_b for d in D]
-    gu_bytes = [d * gu_b + x_b for d in D]
+    layer_bytes = [D[l] * sum(peb[fmts[l]]) + x_b + lg_b + out_b for l in range(L)]
+    gu_bytes = [D[l] * peb[fmts[l]][0] + x_b for l in range(L)]
+    main_layers = [l for l in range(L) if fmts[l] == fmt]  # the roofline's kernel: the config's format
     flops_layer = 2.0 * T * k * (H * 2 * I + I * H)
     gu_flops = 2.0 * T * k * H * 2 * I
 
     # gate/up launch times are sampled on every 8th layer: an event between two kernels is a
     # graph node that also cuts the programmatic (overlapped) launch edge, so the other layers
     # run without events
-    sampled = [l for l in range(L) if l % 8 == min(7, L - 1)] or [L - 1]
+    sampled = [l for l in main_layers if l % 8 == min(7, L - 1)] or [main_layers[-1]]
 
     def step(timed_events=None):
         for l in range(L):
@@ -341,21 +357,22 @@ def run_ours(args, c, rank, world, local_rank):
                 "frac": round(achieved / peak, 4)}
     traffic = recorded_traffic(fmt, T)  # recorded per launch at the 48-layer mean; rescaled to the sampled layers
     if traffic is not None:
-        traffic = round(traffic * statistics.mean(gu_bytes[l] for l in sampled) / statistics.mean(gu_bytes))
+        traffic = round(traffic * statistics.mean(gu_bytes[l] for l in sampled) /
+                        statistics.mean(gu_bytes[l] for l in main_layers))
     roof.update({"traffic": traffic, "kernel": "grouped gate/up GEMM",
                  "launch_ms": round(gu_avg_s * 1e3, 4), "peak_source": peak_src,
                  "step_fraction": round(gu_avg_s * 1e3 * L / ms_step, 3), "sampled_layers": len(sampled),
                  "down_launch_ms": round(statistics.mean(dn_ms), 4)})
     layer_s = ms_step / 1e3 / L
+    bound_s = sum(max(layer_bytes[l] / (peaks["hbm_gbs"] * 1e9),
+                      flops_layer / (peaks["bf16_tflops_sustained"] * TENSOR_RATIO[fmts[l]] * 1e12)) for l in range(L))
     whole = {"hbm_gbs": round(statistics.mean(layer_bytes) / layer_s / 1e9, 1),
              "tflops": round(flops_layer / layer_s / 1e12, 2),
-             "roofline_frac": round(max(statistics.mean(layer_bytes) / (peaks["hbm_gbs"] * 1e9),
-                                        flops_layer / (peaks["bf16_tflops_sustained"] * TENSOR_RATIO[fmt] * 1e12))
-                                    / layer_s, 4),
+             "roofline_frac": round(bound_s / (ms_step / 1e3), 4),
              "distinct_experts_per_layer": round(statistics.mean(D), 1)}
 
     # end to end through the host-buffer entry point: inputs copied in, results copied out
-    ws_io = torch.empty(M.moe_workspace_size_host_io(layers[0].desc, T, k), dtype=torch.uint8, device=dev)
+    ws_io = torch.empty(ws_bytes(T, host_io=True), dtype=torch.uint8, device=dev)
     x_h = torch.from_numpy(synth.gen_x(T, H, seed).view(np.int16)).view(torch.bfloat16).pin_memory()
     lg_h = torch.from_numpy(lg_host).pin_memory()
     out_h = torch.empty((L, T, H), dtype=torch.bfloat16).pin_memory()
@@ -391,7 +408,7 @@ def run_ours(args, c, rank, world, local_rank):
                 continue
             xs = x[:Ts].contiguous()
             lgs = [lg[l, :Ts].contiguous() for l in range(L)]
-            wss = torch.empty(M.moe_workspace_size(layers[0].desc, Ts, k), dtype=torch.uint8, device=dev)
+            wss = torch.empty(ws_bytes(Ts), dtype=torch.uint8, device=dev)
             run_s, _ = as_runner(lambda: [M.moe_layer_forward(xs, lgs[l], layers[l].desc, layers[l].packed, k,
                                                               outs[l, :Ts], wss) for l in range(L)])
             for _ in range(2):
@@ -419,7 +436,7 @@ def main():
     base = {"metric": METRIC, "unit": "tokens/s", "n_gpus": max(world, args.gpus if world == 1 else world),
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "data": "synthetic (seeded; see DESIGN.md input recipe)",
-            "config": {"workload": describe(c), "format": c["fmt"], "tokens": c["T"], "layers": c["L"],
+            "config": {"workload": describe(c), "format": format_mix(c), "tokens": c["T"], "layers": c["L"],
                        "hidden": c["H"], "intermediate": c["I"], "experts": c["E"], "top_k": c["k"],
                        "l2": "inputs larger than L2: each step streams the distinct weights of all layers",
                        "parallelism": f"replicas x{world}",

@@ -117,4 +117,15 @@ CONFIGS = {
             zipf=None, layers=48),
     3: dict(name="nvfp4-w4a16", fmt="nvfp4_w4a16", T=[4096], H=2048, I=768, E=128, k=8, zipf=1.1, layers=48),
     4: dict(name="nvfp4-w4a4", fmt="nvfp4_w4a4", T=[16384], H=2048, I=768, E=128, k=8, zipf=1.1, layers=48),
+    # mixed per-layer formats: the first 17/32 of the stack FP8, the rest NVFP4 W4A4 (the hybrid
+    # page's split of a 32-layer model, layers 0-16 FP8 and 17-31 NVFP4, scaled to the stack)
+    5: dict(name="mixed-fp8-nvfp4-w4a4", fmt="nvfp4_w4a4", T=[16, 16384], H=2048, I=768, E=128, k=8, zipf=1.1,
+            layers=48, fp8_fraction=17 / 32),
 }
+
+
+def layer_formats(c: dict, L: int) -> list:
+    """Format of each of L layers: c["fmt"] throughout, or with c["fp8_fraction"] the first
+    round(L * fraction) layers FP8 and the rest c["fmt"]."""
+    n = int(L * c["fp8_fraction"] + 0.5) if c.get("fp8_fraction") else 0
+    return ["fp8"] * n + [c["fmt"]] * (L - n)

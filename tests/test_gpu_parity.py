@@ -271,6 +271,24 @@ def test_layer_k256_shapes(orc, fmt, T, E, k):
     check_close(synth.bf16_bits_to_f32(c.run()), c.oracle(orc), f"{fmt} T={T}")
 
 
+def test_mixed_format_stack_shared_workspace(orc):
+    """A stack whose layers use different formats (FP8, then NVFP4 W4A4, as in the hybrid page's
+    split) runs back to back on one workspace sized for the largest format; every layer matches
+    its oracle."""
+    T, H, I, E, k = 200, 512, 256, 16, 4
+    cases = [Case("fp8", T, H, I, E, k, seed=31), Case("nvfp4_w4a4", T, H, I, E, k, seed=32, zipf=1.1)]
+    ws = torch.empty(max(M.moe_workspace_size(c.layer.desc, T, k) for c in cases), dtype=torch.uint8, device="cuda")
+    outs = []
+    for c in cases:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        M.moe_layer_forward(dev_bf16(c.x), torch.from_numpy(c.lg).cuda(), c.layer.desc, c.layer.packed, k, out, ws)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert M.moe_get_device_error(ws) == 0
+    for c, out in zip(cases, outs):
+        check_close(synth.bf16_bits_to_f32(host_bits(out)), c.oracle(orc), c.fmt)
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_layer_deterministic(fmt):
     """Two forward passes on the same inputs give bit-identical outputs (the combine sums each
