@@ -18,6 +18,10 @@
  *   MOE_FMT_NVFP4_W4A4      the same weights with activations quantized to NVFP4 at run time
  *                           (clef-flash-NVFP4-Hybrid, layer table: 16-element groups, FP8 group
  *                           scales, one fp32 global scale), here one global scale per row.
+ *   MOE_FMT_BF16            unquantized bf16 weights and activations through the same routing,
+ *                           GEMM and combine kernels: the comparison point every quantized
+ *                           checkpoint is measured against (clef-omni-fp8, "Which Clef-Omni quant
+ *                           should I use?": the BF16 original is the reference row).
  *
  * Conventions for every call:
  *   - Pointers marked (dev) are device pointers; (host) are host pointers.  All memory is owned
@@ -46,7 +50,8 @@ typedef enum {
   MOE_FMT_FP8_B128_W8A16 = 1,
   MOE_FMT_INT4_G128_W4A16 = 2,
   MOE_FMT_NVFP4_W4A16 = 3,
-  MOE_FMT_NVFP4_W4A4 = 4
+  MOE_FMT_NVFP4_W4A4 = 4,
+  MOE_FMT_BF16 = 5
 } moe_format_t;
 
 typedef enum {
@@ -71,6 +76,7 @@ typedef enum {
  *          GU_B = weight_scale E4M3 [E, 2I, H/16]
  *          D_A  = weight_packed u8 [E, H, I/2]  D_B = weight_scale E4M3 [E, H, I/16]
  *          GU_GS / D_GS = weight_global_scale f32 [E] (the quantize multiplier 2688/amax)
+ *   BF16:  GU_A = bf16 [E, 2I, H]               D_A = bf16 [E, H, I]  (the weights as given)
  *   NVFP4 W4A4 with H and I multiples of 256 also carries a copy of each weight_scale tensor
  *   re-tiled for the block-scaled tensor-core path, every (128-row tile, 256-column chunk) one
  *   contiguous 2 KB block:

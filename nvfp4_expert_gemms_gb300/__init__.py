@@ -20,7 +20,9 @@ FMT_FP8 = 1
 FMT_INT4 = 2
 FMT_NVFP4_W4A16 = 3
 FMT_NVFP4_W4A4 = 4
-FORMATS = {"fp8": FMT_FP8, "int4": FMT_INT4, "nvfp4_w4a16": FMT_NVFP4_W4A16, "nvfp4_w4a4": FMT_NVFP4_W4A4}
+FMT_BF16 = 5
+FORMATS = {"fp8": FMT_FP8, "int4": FMT_INT4, "nvfp4_w4a16": FMT_NVFP4_W4A16, "nvfp4_w4a4": FMT_NVFP4_W4A4,
+           "bf16": FMT_BF16}
 
 MOE_T_GU_A, MOE_T_GU_B, MOE_T_D_A, MOE_T_D_B, MOE_T_GU_GS, MOE_T_D_GS, MOE_T_GU_BT, MOE_T_D_BT = range(8)
 
@@ -211,6 +213,8 @@ def packed_view(desc: PackedDesc, packed, which: int):
         return raw.view(torch.float32)
     if which in (MOE_T_GU_BT, MOE_T_D_BT):
         return raw.view(E, N // 128, K // 256, 128, 16)
+    if fmt == FMT_BF16:
+        return raw.view(torch.bfloat16).view(E, N, K)
     if fmt == FMT_FP8:
         return raw.view(E, N, K) if which in (MOE_T_GU_A, MOE_T_D_A) else raw.view(torch.float32).view(
             E, N // 128, K // 128)

@@ -57,7 +57,7 @@ WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
   return L;
 }
 
-static bool fmt_ok(int f) { return f >= MOE_FMT_FP8_B128_W8A16 && f <= MOE_FMT_NVFP4_W4A4; }
+static bool fmt_ok(int f) { return f >= MOE_FMT_FP8_B128_W8A16 && f <= MOE_FMT_BF16; }
 
 static bool desc_ok(const moe_packed_desc_t* d) {
   return d && fmt_ok(d->fmt) && d->E >= 1 && d->E <= kMaxE && d->H >= 128 && d->I >= 128 && d->H % 128 == 0 &&
@@ -141,6 +141,10 @@ moe_status_t moe_packed_size(int fmt, int E, int H, int I, moe_packed_desc_t* d)
       sz[MOE_T_GU_B] = e * gu / 128 * 2;
       sz[MOE_T_D_A] = e * dn / 2;
       sz[MOE_T_D_B] = e * dn / 128 * 2;
+      break;
+    case MOE_FMT_BF16:
+      sz[MOE_T_GU_A] = e * gu * 2;
+      sz[MOE_T_D_A] = e * dn * 2;
       break;
     default:
       sz[MOE_T_GU_A] = e * gu / 2;

@@ -3,6 +3,7 @@
 //   FP8   (clef-omni-fp8, "Recipe"):            e4m3(code) * scale_inv[n/128][k/128]
 //   INT4  (clef-omni-int4, "What was quantized"): (code - 8) * fp16 scale[k/128][n]
 //   NVFP4 (clef-omni-NVFP4, "How it was made"):  (e2m1(q) * e4m3(bs[n][k/16])) / gs
+//   BF16  (unquantized):                         the bf16 weight
 #pragma once
 #include "moe_internal.cuh"
 
@@ -38,6 +39,14 @@ __device__ __forceinline__ void load_w8(const MatView& m, int e, int n, int k0, 
     for (int i = 0; i < 4; ++i) w[i] = e4m3_to_f32((c.x >> (8 * i)) & 0xFF) * s;
 #pragma unroll
     for (int i = 0; i < 4; ++i) w[4 + i] = e4m3_to_f32((c.y >> (8 * i)) & 0xFF) * s;
+  } else if constexpr (FMT == MOE_FMT_BF16) {
+    const uint4 c = *(const uint4*)(m.a + (((size_t)e * m.N + n) * m.K + k0) * 2);
+    const uint32_t ww[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[2 * i] = __uint_as_float(ww[i] << 16);
+      w[2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
+    }
   } else if constexpr (FMT == MOE_FMT_INT4_G128_W4A16) {
     const uint32_t q = ((const uint32_t*)m.a)[((size_t)e * (m.K / 8) + k0 / 8) * m.N + n];
     const float s = __half2float(((const __half*)m.b)[((size_t)e * (m.K / 128) + k0 / 128) * m.N + n]);

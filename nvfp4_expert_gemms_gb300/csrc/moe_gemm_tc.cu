@@ -64,6 +64,10 @@ template <>
 struct WFmt<MOE_FMT_NVFP4_W4A16> {
   static constexpr int kSubBytes = 128 * 64;  // 128 rows x 64 bytes (128 codes), 64-byte swizzle
 };
+template <>
+struct WFmt<MOE_FMT_BF16> {
+  static constexpr int kSubBytes = 2 * 128 * 128;  // two 128-byte swizzle atoms (64 K each) x 128 rows
+};
 
 // Shared-memory rings: weight chunks (kStagesW) and activation chunks (SB, each BN rows x 128 K
 // bf16 as two 128-byte swizzle atoms); the gather threads keep LAG chunks in flight.
@@ -73,14 +77,14 @@ template <int FMT, int BN>
 struct TcCfg {
   static constexpr int kWSub = WFmt<FMT>::kSubBytes;
   static constexpr int kBStage = BN * 256;
-  static constexpr int SB = BN <= 32 ? 4 : (BN == 64 ? 4 : 3);
+  static constexpr int SB = BN <= 32 ? 4 : (BN == 64 ? 4 : (FMT == MOE_FMT_BF16 ? 2 : 3));  // BF16: 32 KB weight sub-tiles
   static constexpr int kWFree = 220 * 1024 - 1024 - SB * kBStage;
-  static constexpr int kStagesWFit = kWFree / (2 * kWSub + 2048);
+  static constexpr int kStagesWFit = kWFree / (2 * kWSub + (FMT == MOE_FMT_BF16 ? 0 : 2048));
   static constexpr int kStagesW = kStagesWFit > 12 ? 12 : (kStagesWFit < 2 ? 2 : kStagesWFit);
   static constexpr int LAG = SB - 2;
   // per weight stage, the chunk's scales (copied by the producer warp next to the TMA tile):
-  // FP8 one fp32 per sub-tile, INT4 128 fp16 per sub-tile, NVFP4 8 E4M3 bytes per row
-  static constexpr int kScaleSlot = 2048;
+  // FP8 one fp32 per sub-tile, INT4 128 fp16 per sub-tile, NVFP4 8 E4M3 bytes per row, BF16 none
+  static constexpr int kScaleSlot = FMT == MOE_FMT_BF16 ? 0 : 2048;
   static constexpr size_t kSmem = 1024 + (size_t)kStagesW * 2 * kWSub + (size_t)SB * kBStage +
                                   (size_t)kStagesW * kScaleSlot;
 };
@@ -230,6 +234,21 @@ __device__ __forceinline__ void conv_nvfp4(const char* sub, int r, int kh, uint3
   }
 }
 
+// BF16: the weights are the operand already; half a chunk of row r is unswizzled out of its
+// 128-byte atom (chunk c of row r sits at chunk position c ^ (r % 8)).
+__device__ __forceinline__ void conv_bf16(const char* sub, int r, int kh, uint32_t* out) {
+  uint4 q[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) q[c] = *(const uint4*)(sub + kh * 128 * 128 + r * 128 + ((c ^ (r & 7)) * 16));
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    out[c * 4 + 0] = q[c].x;
+    out[c * 4 + 1] = q[c].y;
+    out[c * 4 + 2] = q[c].z;
+    out[c * 4 + 3] = q[c].w;
+  }
+}
+
 // Persistent kernel: one CTA per SM walks the work items (row tile of one expert x column block)
 // with a stride of gridDim.x; the pipeline rings keep their phases across items, so the TMA for
 // the next item runs while the current item's epilogue executes.
@@ -369,7 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
             for (int g = 0; g < nsub; ++g) {
               char* dst = sW + sw * WSTAGE + g * WSUB;
               const int nb = g == 0 ? nb0 : nb1;
-              if (FMT == MOE_FMT_FP8_B128_W8A16)
+              if (FMT == MOE_FMT_BF16) {  // two 64-K boxes of the bf16 rows
+                tma_load_2d(dst, &a.wmap, &w_full[sw], kc * kKC, te.expert * a.N + nb);
+                tma_load_2d(dst + 128 * 128, &a.wmap, &w_full[sw], kc * kKC + 64, te.expert * a.N + nb);
+              } else if (FMT == MOE_FMT_FP8_B128_W8A16)
                 tma_load_2d(dst, &a.wmap, &w_full[sw], kc * kKC, te.expert * a.N + nb);
               else if (FMT == MOE_FMT_INT4_G128_W4A16)
                 tma_load_2d(dst, &a.wmap, &w_full[sw], nb, te.expert * (a.K / 8) + kc * 16);
@@ -394,7 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         {  // this chunk's weight scales into the stage's slot, completing on the same barrier
           char* ss = sS + sw * kScaleSlot;
           const int e = te.expert;
-          if (FMT == MOE_FMT_FP8_B128_W8A16) {
+          if (FMT == MOE_FMT_BF16) {
+            // no scales: the arrival below still completes this lane's share of the barrier
+          } else if (FMT == MOE_FMT_FP8_B128_W8A16) {
             if (lane < nsub)
               cp_async_4(smem_u32(ss + lane * 4),
                          (const float*)a.wscale + ((size_t)e * (a.N / 128) + (lane == 0 ? nb0 : nb1) / 128) * (a.K / 128) + kc);
@@ -556,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         // the chunk's scale for this thread's row (or sub-tile), from the stage's scale slot
         const char* ss = sS + sw * kScaleSlot;
         uint32_t sc_raw = 0u;
-        if (active) {
+        if (active && FMT != MOE_FMT_BF16) {
           if (FMT == MOE_FMT_FP8_B128_W8A16) sc_raw = *(const uint32_t*)(ss + g * 4);
           else if (FMT == MOE_FMT_INT4_G128_W4A16) sc_raw = __float_as_uint(__half2float(*(const __half*)(ss + g * 256 + r * 2)));
           else sc_raw = *(const uint32_t*)(ss + (g * 128 + r) * 8 + kh * 4);
@@ -566,7 +590,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         uint32_t v[32];
         if (active) {
           const char* sub = sW + sw * WSTAGE + g * WSUB;
-          if (FMT == MOE_FMT_FP8_B128_W8A16) conv_fp8(sub, r, kh, sc, v);
+          if (FMT == MOE_FMT_BF16) conv_bf16(sub, r, kh, v);
+          else if (FMT == MOE_FMT_FP8_B128_W8A16) conv_fp8(sub, r, kh, sc, v);
           else if (FMT == MOE_FMT_INT4_G128_W4A16) conv_int4(sub, r, kh, sc, v);
           else conv_nvfp4(sub, r, kh, bs4, v);
         }
@@ -675,6 +700,9 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
 }
 
 bool weight_map(CUtensorMap* m, int fmt, const MatView& v, int E) {
+  if (fmt == MOE_FMT_BF16)
+    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v.a, v.K, (uint64_t)E * v.N, (uint64_t)v.K * 2, 64, 128,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
   if (fmt == MOE_FMT_FP8_B128_W8A16)
     return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, v.a, v.K, (uint64_t)E * v.N, v.K, 128, 128,
                     CU_TENSOR_MAP_SWIZZLE_128B);
@@ -713,6 +741,7 @@ template <int MODE>
 cudaError_t launch_fmt(int fmt, int bn, const TcArgs& args, int gx, int gy, cudaStream_t s) {
   if (fmt == MOE_FMT_FP8_B128_W8A16) return launch_bn<MOE_FMT_FP8_B128_W8A16, MODE>(bn, args, gx, gy, s);
   if (fmt == MOE_FMT_INT4_G128_W4A16) return launch_bn<MOE_FMT_INT4_G128_W4A16, MODE>(bn, args, gx, gy, s);
+  if (fmt == MOE_FMT_BF16) return launch_bn<MOE_FMT_BF16, MODE>(bn, args, gx, gy, s);
   return launch_bn<MOE_FMT_NVFP4_W4A16, MODE>(bn, args, gx, gy, s);
 }
 

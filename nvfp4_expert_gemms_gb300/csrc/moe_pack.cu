@@ -369,6 +369,11 @@ cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, co
     const int N = which == 0 ? 2 * I : H, K = which == 0 ? H : I;
     uint8_t* a = (uint8_t*)(packed + d.offset[which == 0 ? MOE_T_GU_A : MOE_T_D_A]);
     uint8_t* b = (uint8_t*)(packed + d.offset[which == 0 ? MOE_T_GU_B : MOE_T_D_B]);
+    if (d.fmt == MOE_FMT_BF16) {  // unquantized: the canonical tensors are the weights themselves
+      const cudaError_t e = cudaMemcpyAsync(a, w, (size_t)E * N * K * 2, cudaMemcpyDeviceToDevice, s);
+      if (e != cudaSuccess) return e;
+      continue;
+    }
     if (d.fmt == MOE_FMT_FP8_B128_W8A16) {
       pack_fp8_kernel<<<dim3(K / 128, N / 128, E), 256, 0, s>>>(w, N, K, a, (float*)b);
     } else if (d.fmt == MOE_FMT_INT4_G128_W4A16) {
@@ -400,6 +405,7 @@ cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e
   const MatView m = mat_view(d, packed, which);
   const unsigned blocks = (unsigned)(((size_t)m.N * m.K / 8 + 255) / 256);
   if (d.fmt == MOE_FMT_FP8_B128_W8A16) dequant_kernel<MOE_FMT_FP8_B128_W8A16><<<blocks, 256, 0, s>>>(m, e, out);
+  else if (d.fmt == MOE_FMT_BF16) dequant_kernel<MOE_FMT_BF16><<<blocks, 256, 0, s>>>(m, e, out);
   else if (d.fmt == MOE_FMT_INT4_G128_W4A16) dequant_kernel<MOE_FMT_INT4_G128_W4A16><<<blocks, 256, 0, s>>>(m, e, out);
   else dequant_kernel<MOE_FMT_NVFP4_W4A16><<<blocks, 256, 0, s>>>(m, e, out);
   note_launches(1);

@@ -19,8 +19,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-FMT_FP8, FMT_INT4, FMT_NVFP4_W4A16, FMT_NVFP4_W4A4 = 1, 2, 3, 4
-FMT_IDS = {"fp8": 1, "int4": 2, "nvfp4_w4a16": 3, "nvfp4_w4a4": 4}
+FMT_FP8, FMT_INT4, FMT_NVFP4_W4A16, FMT_NVFP4_W4A4, FMT_BF16 = 1, 2, 3, 4, 5
+FMT_IDS = {"fp8": 1, "int4": 2, "nvfp4_w4a16": 3, "nvfp4_w4a4": 4, "bf16": 5}
 
 
 def build(force: bool = False) -> str:
@@ -214,7 +214,11 @@ def pack_experts(fmt: int, wgu: np.ndarray, wd: np.ndarray, experts=None) -> dic
     pool = ThreadPoolExecutor(max_workers=os.cpu_count() or 1)  # ctypes calls release the GIL
     out = {}
     for name, W, N, K in (("gu", wgu, 2 * I, H), ("d", wd, H, I)):
-        if fmt == FMT_FP8:
+        if fmt == FMT_BF16:  # unquantized: the weights as given
+            a = np.zeros((E, N, K), np.uint16)
+            a[list(sel)] = np.asarray(W, dtype=np.uint16)[list(sel)]
+            b = g = None
+        elif fmt == FMT_FP8:
             a = np.zeros((E, N, K), np.uint8)
             b = np.zeros((E, N // 128, K // 128), np.float32)
             g = None
@@ -254,8 +258,8 @@ def moe_layer(fmt: int, x: np.ndarray, logits: np.ndarray, packed: dict, k: int,
         tok_p, n_tok = _p(tk), len(tk)
     out = np.empty((n_tok, H), np.float64)
     none = C.c_void_p(0)
-    rc = lib().orc_moe_layer(fmt, T, H, I, E, k, _p(xx), _p(lg), _p(gu_a), _p(gu_b),
-                             _p(gu_g) if gu_g is not None else none, _p(d_a), _p(d_b),
+    rc = lib().orc_moe_layer(fmt, T, H, I, E, k, _p(xx), _p(lg), _p(gu_a), _p(gu_b) if gu_b is not None else none,
+                             _p(gu_g) if gu_g is not None else none, _p(d_a), _p(d_b) if d_b is not None else none,
                              _p(d_g) if d_g is not None else none, tok_p, n_tok, int(dense), int(nthreads),
                              _p(out))
     if rc != 0:

@@ -21,6 +21,8 @@
  *           one matrix), round-to-nearest-even on the FP4 grid, plain min-max scaling.
  *   [w4a4]  clef-flash-NVFP4-Hybrid, layer table: NVFP4 W4A4 = 16-element groups, FP8 group
  *           scales, one FP32 global scale; here computed at run time per activation row.
+ *   [bf16]  clef-omni-fp8, "Which Clef-Omni quant should I use?": the BF16 original is the
+ *           reference every quant is compared with; its weights are used as stored.
  *
  * Readings where the pages are silent (each also listed in the design doc):
  *   - E4M3 is the OCP "e4m3fn" variant (max 448, no infinities); encode saturates at 448.
@@ -42,7 +44,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_FP8 = 1, ORC_INT4 = 2, ORC_NVFP4_W4A16 = 3, ORC_NVFP4_W4A4 = 4 };
+enum { ORC_FP8 = 1, ORC_INT4 = 2, ORC_NVFP4_W4A16 = 3, ORC_NVFP4_W4A4 = 4, ORC_BF16 = 5 };
 
 /* ------------------------------------------------------------------------------------ */
 /* Scalar formats: a sign-magnitude minifloat with `mbits` mantissa bits and exponent   */
@@ -317,6 +319,9 @@ static void dequant_expert(int fmt, int which, int e, int H, int I, const void* 
     orc_dequant_fp8((const uint8_t*)a + NK * e, (const float*)b + (size_t)(N / 128) * (K / 128) * e, N, K, out);
   } else if (fmt == ORC_INT4) {
     orc_dequant_int4((const int32_t*)a + NK / 8 * e, (const uint16_t*)b + (size_t)(K / 128) * N * e, N, K, out);
+  } else if (fmt == ORC_BF16) {  /* the stored bf16 value itself */
+    const uint16_t* w = (const uint16_t*)a + NK * e;
+    for (size_t i = 0; i < NK; ++i) out[i] = bf16f(w[i]);
   } else {
     orc_dequant_nvfp4((const uint8_t*)a + NK / 2 * e, (const uint8_t*)b + NK / 16 * e, gs[e], N, K, out);
   }
@@ -376,7 +381,7 @@ static void act_row(int fmt, const uint16_t* xrow, int H, double* a) {
    dense != 0 runs the dense masked definition instead: every token through all E experts,
    weighted by the routing weights scattered over experts (zero for unselected ones).
    Weights are passed per format: fp8 (codes, scale_inv, -), int4 (qweight, scales, -),
-   nvfp4 (packed, block scales, global scales).  Returns 0 on success. */
+   nvfp4 (packed, block scales, global scales), bf16 (weights, -, -).  Returns 0 on success. */
 int orc_moe_layer(int fmt, int T, int H, int I, int E, int k, const uint16_t* x, const float* logits,
                   const void* gu_a, const void* gu_b, const float* gu_gs, const void* d_a, const void* d_b,
                   const float* d_gs, const int32_t* tok, int n_tok, int dense, int nthreads, double* out) {

@@ -14,8 +14,8 @@ import synth
 
 pytestmark = pytest.mark.gpu
 
-FMTS = ["fp8", "int4", "nvfp4_w4a16", "nvfp4_w4a4"]
-FID = {"fp8": 1, "int4": 2, "nvfp4_w4a16": 3, "nvfp4_w4a4": 4}
+FMTS = ["fp8", "int4", "nvfp4_w4a16", "nvfp4_w4a4", "bf16"]
+FID = {"fp8": 1, "int4": 2, "nvfp4_w4a16": 3, "nvfp4_w4a4": 4, "bf16": 5}
 REL_FRO, REL_MAX = 1e-2, 2e-2
 
 
@@ -79,6 +79,21 @@ def test_pack_bit_exact(orc, fmt):
         for which, name in ((M.MOE_T_GU_GS, "gu"), (M.MOE_T_D_GS, "d")):
             got = M.packed_view(d, layer.packed, which).cpu().numpy()
             assert got.tobytes() == ref[name][2].tobytes()
+
+
+def test_bf16_pack_and_dequant_are_the_weights():
+    """BF16 'packing' stores the weights as given, and the dequant view widens them exactly."""
+    E, H, I = 3, 256, 128
+    wgu, wd = synth.gen_expert_weights(E, H, I, seed=8)
+    layer = M.MoELayer("bf16", dev_bf16(wgu), dev_bf16(wd))
+    torch.cuda.synchronize()
+    for which, w in ((M.MOE_T_GU_A, wgu), (M.MOE_T_D_A, wd)):
+        got = M.packed_view(layer.desc, layer.packed, which).cpu().view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, w)
+    for which, w in ((0, wgu), (1, wd)):
+        for e in range(E):
+            got = M.moe_debug_dequant(layer.desc, layer.packed, e, which).cpu().numpy()
+            assert got.tobytes() == synth.bf16_bits_to_f32(w[e]).tobytes()
 
 
 def test_w4a4_retiled_scales(orc):
@@ -250,7 +265,8 @@ FULL = dict(H=2048, I=768, E=128, k=8)
 
 
 @pytest.mark.parametrize("fmt,T,zipf,sample", [("fp8", 16, None, None), ("int4", 256, None, 24),
-                                               ("nvfp4_w4a16", 4096, 1.1, 24), ("nvfp4_w4a4", 16384, 1.1, 16)])
+                                               ("nvfp4_w4a16", 4096, 1.1, 24), ("nvfp4_w4a4", 16384, 1.1, 16),
+                                               ("bf16", 16, None, None), ("bf16", 4096, 1.1, 24)])
 def test_layer_full_size_sampled(orc, fmt, T, zipf, sample):
     c = Case(fmt, T, FULL["H"], FULL["I"], FULL["E"], FULL["k"], seed=0, zipf=zipf)
     got = synth.bf16_bits_to_f32(c.run())

@@ -14,7 +14,7 @@ import torch.nn.functional as F
 
 import synth
 
-FP8, INT4, W4A16, W4A4 = 1, 2, 3, 4
+FP8, INT4, W4A16, W4A4, BF16 = 1, 2, 3, 4, 5
 
 
 def test_topk_brute_force_small(orc):
@@ -76,6 +76,9 @@ def _torch_reference(fmt, x_bits, logits, packed, k, orc):
         elif fmt == INT4:
             wgu.append(orc.dequant_int4(gu_a[e], gu_b[e]))
             wd.append(orc.dequant_int4(d_a[e], d_b[e]))
+        elif fmt == BF16:  # the stored bf16 bits, widened by numpy
+            wgu.append(synth.bf16_bits_to_f32(gu_a[e]))
+            wd.append(synth.bf16_bits_to_f32(d_a[e]))
         else:
             wgu.append(orc.dequant_nvfp4(gu_a[e], gu_b[e], gu_g[e]))
             wd.append(orc.dequant_nvfp4(d_a[e], d_b[e], d_g[e]))
@@ -104,7 +107,7 @@ def _torch_reference(fmt, x_bits, logits, packed, k, orc):
     return torch.einsum("te,teh->th", mask, Y).numpy()
 
 
-@pytest.mark.parametrize("fmt", [FP8, INT4, W4A16, W4A4])
+@pytest.mark.parametrize("fmt", [FP8, INT4, W4A16, W4A4, BF16])
 def test_layer_matches_torch_dense_composition(orc, fmt):
     E, H, I, T, k = 8, 256, 128, 24, 2
     wgu, wd = synth.gen_expert_weights(E, H, I, seed=0)
@@ -122,7 +125,7 @@ def test_layer_matches_torch_dense_composition(orc, fmt):
         np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12 * np.abs(ref).max())
 
 
-@pytest.mark.parametrize("fmt", [FP8, W4A4])
+@pytest.mark.parametrize("fmt", [FP8, W4A4, BF16])
 def test_sparse_equals_dense_masked_definition(orc, fmt):
     E, H, I, T, k = 8, 256, 128, 16, 3
     wgu, wd = synth.gen_expert_weights(E, H, I, seed=1)
