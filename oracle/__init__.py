@@ -57,7 +57,7 @@ def lib():
         L.orc_bf16_encode.restype = C.c_uint16
         L.orc_bf16_encode.argtypes = [C.c_double]
         for f in ("orc_pack_fp8", "orc_pack_int4", "orc_pack_nvfp4", "orc_dequant_fp8", "orc_dequant_int4",
-                  "orc_quant_act_nvfp4", "orc_route", "orc_permute"):
+                  "orc_quant_act_nvfp4", "orc_quant_act_nvfp4_static", "orc_route", "orc_permute"):
             getattr(L, f).restype = None
         L.orc_pack_fp8.argtypes = [P, C.c_int, C.c_int, P, P]
         L.orc_dequant_fp8.argtypes = [P, P, C.c_int, C.c_int, P]
@@ -67,10 +67,11 @@ def lib():
         L.orc_dequant_nvfp4.restype = None
         L.orc_dequant_nvfp4.argtypes = [P, P, C.c_float, C.c_int, C.c_int, P]
         L.orc_quant_act_nvfp4.argtypes = [P, C.c_int, C.c_int, P, P, P]
+        L.orc_quant_act_nvfp4_static.argtypes = [P, C.c_int, C.c_int, C.c_float, P, P]
         L.orc_route.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
         L.orc_permute.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P, P]
         L.orc_moe_layer.restype = C.c_int
-        L.orc_moe_layer.argtypes = [C.c_int] * 6 + [P] * 8 + [P, C.c_int, C.c_int, C.c_int, P]
+        L.orc_moe_layer.argtypes = [C.c_int] * 6 + [P] * 8 + [P, C.c_int, C.c_int, C.c_int, P, P]
         L.orc_max_threads.restype = C.c_int
         _lib = L
     return _lib
@@ -166,14 +167,21 @@ def dequant_nvfp4(packed, scales, gs):
     return out
 
 
-def quant_act_nvfp4(x_bf16: np.ndarray):
-    """x [T, H] bf16 bits -> (codes u8 [T, H/2], scales u8 [T, H/16], gs f32 [T])."""
+def quant_act_nvfp4(x_bf16: np.ndarray, static_gs=None):
+    """x [T, H] bf16 bits -> (codes u8 [T, H/2], scales u8 [T, H/16], gs f32 [T]).
+
+    static_gs None: each row's own dynamic global scale; else that one fp32 scale for every row.
+    """
     T, H = x_bf16.shape
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     q = np.empty((T, H // 2), np.uint8)
     s = np.empty((T, H // 16), np.uint8)
-    g = np.empty(T, np.float32)
-    lib().orc_quant_act_nvfp4(_p(x), T, H, _p(q), _p(s), _p(g))
+    if static_gs is None:
+        g = np.empty(T, np.float32)
+        lib().orc_quant_act_nvfp4(_p(x), T, H, _p(q), _p(s), _p(g))
+    else:
+        g = np.full(T, np.float32(static_gs), np.float32)
+        lib().orc_quant_act_nvfp4_static(_p(x), T, H, C.c_float(float(np.float32(static_gs))), _p(q), _p(s))
     return q, s, g
 
 
@@ -242,8 +250,10 @@ def pack_experts(fmt: int, wgu: np.ndarray, wd: np.ndarray, experts=None) -> dic
 
 
 def moe_layer(fmt: int, x: np.ndarray, logits: np.ndarray, packed: dict, k: int, tokens=None,
-              dense: bool = False, nthreads: int = 0) -> np.ndarray:
-    """Forward pass in fp64 for the given tokens (all when None). Returns [n_tok, H] float64."""
+              dense: bool = False, nthreads: int = 0, act_gs=None) -> np.ndarray:
+    """Forward pass in fp64 for the given tokens (all when None). Returns [n_tok, H] float64.
+
+    act_gs (W4A4): None for dynamic per-row activation scales, else the static (x, h) pair."""
     T, H = x.shape
     E = logits.shape[1]
     gu_a, gu_b, gu_g = packed["gu"]
@@ -258,10 +268,11 @@ def moe_layer(fmt: int, x: np.ndarray, logits: np.ndarray, packed: dict, k: int,
         tok_p, n_tok = _p(tk), len(tk)
     out = np.empty((n_tok, H), np.float64)
     none = C.c_void_p(0)
+    ags = None if act_gs is None else np.ascontiguousarray(np.asarray(act_gs, dtype=np.float32))
     rc = lib().orc_moe_layer(fmt, T, H, I, E, k, _p(xx), _p(lg), _p(gu_a), _p(gu_b) if gu_b is not None else none,
                              _p(gu_g) if gu_g is not None else none, _p(d_a), _p(d_b) if d_b is not None else none,
                              _p(d_g) if d_g is not None else none, tok_p, n_tok, int(dense), int(nthreads),
-                             _p(out))
+                             _p(ags) if ags is not None else none, _p(out))
     if rc != 0:
         raise ValueError(f"orc_moe_layer rejected its arguments (rc={rc})")
     return out

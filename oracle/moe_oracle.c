@@ -246,6 +246,18 @@ void orc_dequant_nvfp4(const uint8_t* packed, const uint8_t* scales, float gs, i
 
 /* [w4a4], dynamic: each row of a [T, H] bf16 activation gets gs_t = 2688/max(amax_t, 1e-12)
    and is block-quantized like a weight row.  codes [T, H/2], scales [T, H/16], gs [T]. */
+/* The same with one static global scale gs for every row (calibrated ahead of time; the
+   clef-flash-NVFP4-Hybrid layer table's "activation global scales calibrated"): block scales
+   saturate at 448 and codes at 6 where a block exceeds the calibrated range. */
+void orc_quant_act_nvfp4_static(const uint16_t* x, int T, int H, float gs, uint8_t* codes, uint8_t* scales) {
+  float* row = (float*)malloc(sizeof(float) * H);
+  for (int t = 0; t < T; ++t) {
+    for (int k = 0; k < H; ++k) row[k] = bf16f(x[(size_t)t * H + k]);
+    nvfp4_row(row, H, gs, codes + (size_t)t * (H / 2), scales + (size_t)t * (H / 16));
+  }
+  free(row);
+}
+
 void orc_quant_act_nvfp4(const uint16_t* x, int T, int H, uint8_t* codes, uint8_t* scales, float* gs) {
   float* row = (float*)malloc(sizeof(float) * H);
   for (int t = 0; t < T; ++t) {
@@ -331,7 +343,8 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 /* y = Wd * act(Wgu * a) for one (token, expert) pair; h per the format's rules. */
 static void expert_mlp(int fmt, int H, int I, const float* wgu, const float* wd, const double* a,
-                       double* h, uint16_t* hb, uint8_t* hq, uint8_t* hs, float* hdq, double* y) {
+                       const float* act_gs, double* h, uint16_t* hb, uint8_t* hq, uint8_t* hs, float* hdq,
+                       double* y) {
   for (int n = 0; n < I; ++n) {
     double g = 0.0, u = 0.0;
     const float* wg = wgu + (size_t)n * H;
@@ -345,7 +358,12 @@ static void expert_mlp(int fmt, int H, int I, const float* wgu, const float* wd,
   if (fmt == ORC_NVFP4_W4A4) {
     float gsr;
     for (int n = 0; n < I; ++n) hb[n] = orc_bf16_encode(h[n]);
-    orc_quant_act_nvfp4(hb, 1, I, hq, hs, &gsr);
+    if (act_gs) {
+      gsr = act_gs[1];
+      orc_quant_act_nvfp4_static(hb, 1, I, gsr, hq, hs);
+    } else {
+      orc_quant_act_nvfp4(hb, 1, I, hq, hs, &gsr);
+    }
     orc_dequant_nvfp4(hq, hs, gsr, 1, I, hdq);
     for (int n = 0; n < I; ++n) h[n] = (double)hdq[n];
   }
@@ -358,13 +376,18 @@ static void expert_mlp(int fmt, int H, int I, const float* wgu, const float* wd,
 }
 
 /* Activation row a_t: bf16 x (W8A16, W4A16) or the dequantized NVFP4 row (W4A4). */
-static void act_row(int fmt, const uint16_t* xrow, int H, double* a) {
+static void act_row(int fmt, const uint16_t* xrow, int H, const float* act_gs, double* a) {
   if (fmt == ORC_NVFP4_W4A4) {
     uint8_t* q = (uint8_t*)malloc((size_t)H / 2);
     uint8_t* s = (uint8_t*)malloc((size_t)H / 16);
     float* d = (float*)malloc(sizeof(float) * H);
     float gs;
-    orc_quant_act_nvfp4(xrow, 1, H, q, s, &gs);
+    if (act_gs) {
+      gs = act_gs[0];
+      orc_quant_act_nvfp4_static(xrow, 1, H, gs, q, s);
+    } else {
+      orc_quant_act_nvfp4(xrow, 1, H, q, s, &gs);
+    }
     orc_dequant_nvfp4(q, s, gs, 1, H, d);
     for (int k = 0; k < H; ++k) a[k] = (double)d[k];
     free(q);
@@ -381,10 +404,13 @@ static void act_row(int fmt, const uint16_t* xrow, int H, double* a) {
    dense != 0 runs the dense masked definition instead: every token through all E experts,
    weighted by the routing weights scattered over experts (zero for unselected ones).
    Weights are passed per format: fp8 (codes, scale_inv, -), int4 (qweight, scales, -),
-   nvfp4 (packed, block scales, global scales), bf16 (weights, -, -).  Returns 0 on success. */
+   nvfp4 (packed, block scales, global scales), bf16 (weights, -, -).  act_gs (W4A4 only): NULL
+   quantizes x and h rows with their own dynamic global scales, else with the static scales
+   act_gs[0] (x) and act_gs[1] (h).  Returns 0 on success. */
 int orc_moe_layer(int fmt, int T, int H, int I, int E, int k, const uint16_t* x, const float* logits,
                   const void* gu_a, const void* gu_b, const float* gu_gs, const void* d_a, const void* d_b,
-                  const float* d_gs, const int32_t* tok, int n_tok, int dense, int nthreads, double* out) {
+                  const float* d_gs, const int32_t* tok, int n_tok, int dense, int nthreads, const float* act_gs,
+                  double* out) {
   if (H % 128 || I % 128 || k < 1 || k > E) return 1;
   if (tok == NULL) n_tok = T;
 #ifdef _OPENMP
@@ -398,7 +424,7 @@ int orc_moe_layer(int fmt, int T, int H, int I, int E, int k, const uint16_t* x,
   for (int i = 0; i < n_tok; ++i) {
     int t = tok ? tok[i] : i;
     orc_route(logits + (size_t)t * E, 1, E, k, idx + (size_t)i * k, w + (size_t)i * k);
-    act_row(fmt, x + (size_t)t * H, H, acts + (size_t)i * H);
+    act_row(fmt, x + (size_t)t * H, H, act_gs, acts + (size_t)i * H);
   }
   int slots = dense ? E : k;
   double* ybuf = (double*)calloc((size_t)n_tok * slots * H, sizeof(double));
@@ -427,7 +453,7 @@ int orc_moe_layer(int fmt, int T, int H, int I, int E, int k, const uint16_t* x,
           for (int j = 0; j < k; ++j)
             if (idx[(size_t)i * k + j] == e) slot = j;
         if (slot < 0) continue;
-        expert_mlp(fmt, H, I, wgu, wd, acts + (size_t)i * H, h, hb, hq, hs, hdq,
+        expert_mlp(fmt, H, I, wgu, wd, acts + (size_t)i * H, act_gs, h, hb, hq, hs, hdq,
                    ybuf + ((size_t)i * slots + slot) * H);
         used[(size_t)i * slots + slot] = 1;
       }

@@ -317,3 +317,28 @@ def test_act_quant_hand_worked_row(orc):
     assert gs[0] == np.float32(448.0)
     assert [int(b) for b in q[0]] == [int(x, 16) for x in d["bytes"]]
     assert [int(b) for b in s[0]] == [int(x, 16) for x in d["scales"]]
+
+
+def test_static_activation_scale_reduces_to_dynamic_rows(orc):
+    """With each row's own dynamic scale passed as the static one, the static quantizer returns
+    the dynamic codes and block scales (the static path differs only in where gs comes from)."""
+    import synth
+    x = synth.gen_x(9, 512, seed=12)
+    q, s, g = orc.quant_act_nvfp4(x)
+    for t in range(len(x)):
+        qs, ss, gs = orc.quant_act_nvfp4(x[t:t + 1], static_gs=g[t])
+        assert np.array_equal(qs[0], q[t]) and np.array_equal(ss[0], s[t]) and gs[0] == g[t]
+
+
+def test_static_activation_scale_saturates_outside_calibration(orc):
+    """Calibrated amax 1 (gs = 2688): a block whose amax is 4 needs a block scale of 4 * 448,
+    which saturates at 448 (E4M3 0x7E); its largest elements then need 24 on the E2M1 grid and
+    saturate at 6 (code 7, sign kept); a block inside the range is unaffected."""
+    import synth
+    row = np.zeros((1, 32), np.float32)
+    row[0, :16] = np.linspace(-4.0, 4.0, 16, dtype=np.float32)  # |max| 4: over range
+    row[0, 16] = 1.0                                             # second block: amax 1
+    q, s, g = orc.quant_act_nvfp4(synth.f32_to_bf16_bits(row), static_gs=2688.0)
+    assert s[0, 0] == 0x7E and g[0] == np.float32(2688.0)
+    assert q[0, 0] & 0x0F == 0xF and (q[0, 7] >> 4) == 0x7  # -4 -> -6 (0xF), +4 -> +6 (0x7)
+    assert s[0, 1] == orc.e4m3_encode(np.float32(448.0)) and (q[0, 8] & 0x0F) == 0x7  # 1 -> 6 in its own block

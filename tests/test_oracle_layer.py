@@ -63,7 +63,7 @@ def test_permutation_is_stable_sort_by_expert(orc):
     assert np.array_equal(inv[perm], np.arange(T * k))
 
 
-def _torch_reference(fmt, x_bits, logits, packed, k, orc):
+def _torch_reference(fmt, x_bits, logits, packed, k, orc, act_gs=None):
     """Independent composition in torch fp64: dense einsum over all experts with the mask."""
     E = logits.shape[1]
     gu_a, gu_b, gu_g = packed["gu"]
@@ -86,7 +86,7 @@ def _torch_reference(fmt, x_bits, logits, packed, k, orc):
     Wd = torch.from_numpy(np.stack(wd)).double()
     I = Wgu.shape[1] // 2
     if fmt == W4A4:
-        q, s, gsa = orc.quant_act_nvfp4(x_bits)
+        q, s, gsa = orc.quant_act_nvfp4(x_bits, static_gs=None if act_gs is None else act_gs[0])
         a = torch.from_numpy(np.stack([orc.dequant_nvfp4(q[t:t + 1], s[t:t + 1], gsa[t])[0]
                                        for t in range(len(q))])).double()
     else:
@@ -100,7 +100,7 @@ def _torch_reference(fmt, x_bits, logits, packed, k, orc):
     if fmt == W4A4:
         T_ = Hh.shape[0]
         hb = synth.f32_to_bf16_bits(Hh.reshape(-1, I).float().numpy())  # fp32 then bf16: see below
-        hq, hs, hg = orc.quant_act_nvfp4(hb)
+        hq, hs, hg = orc.quant_act_nvfp4(hb, static_gs=None if act_gs is None else act_gs[1])
         hd = np.stack([orc.dequant_nvfp4(hq[r:r + 1], hs[r:r + 1], hg[r])[0] for r in range(len(hq))])
         Hh = torch.from_numpy(hd).double().reshape(T_, E, I)
     Y = torch.einsum("ehi,tei->teh", Wd, Hh)
@@ -161,3 +161,20 @@ def test_token_subset_equals_full_rows(orc):
     full = orc.moe_layer(W4A4, x, lg, packed, k)
     sub = orc.moe_layer(W4A4, x, lg, packed, k, tokens=[17, 3, 3, 0])
     assert np.array_equal(sub, full[[17, 3, 3, 0]])
+
+
+def test_static_activation_scales_layer_matches_torch_composition(orc):
+    """W4A4 with static (calibrated) activation scales, one too small for part of x so that
+    some blocks saturate: the oracle layer equals the torch fp64 composition."""
+    E, H, I, T, k = 8, 256, 128, 24, 2
+    wgu, wd = synth.gen_expert_weights(E, H, I, seed=4)
+    x = synth.gen_x(T, H, seed=4)
+    lg = synth.gen_logits(T, E, seed=4)
+    packed = orc.pack_experts(W4A4, wgu, wd)
+    act_gs = np.array([2688.0 / 2.5, 2688.0 / 0.05], np.float32)  # x beyond 2.5 saturates
+    got = orc.moe_layer(W4A4, x, lg, packed, k, act_gs=act_gs)
+    ref = _torch_reference(W4A4, x, lg, packed, k, orc, act_gs=act_gs)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel < 2e-3, rel  # h rounding to bf16 may differ by an ulp between the two (see above)
+    dyn = orc.moe_layer(W4A4, x, lg, packed, k)
+    assert not np.allclose(got, dyn)  # the static scales change the result
