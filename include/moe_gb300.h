@@ -128,6 +128,29 @@ moe_status_t moe_layer_forward(const void* x, const float* router_logits, int T,
                                const void* packed, int top_k, void* out, void* workspace, size_t ws_bytes,
                                moe_stream_t stream);
 
+/* NVFP4 W4A4 with static activation scales (clef-flash-NVFP4-Hybrid, "Quantization details":
+ * one FP32 global scale per tensor, the activation scales calibrated ahead of time): the same
+ * pass as moe_layer_forward, but every row of x is quantized with the one global scale
+ * act_gs[0] and every row of h with act_gs[1] (the quantize multiplier, as for the weights:
+ * codes = E2M1(value / (E4M3 block scale / gs))); blocks beyond the calibrated range saturate.
+ * h is quantized inside the gate/up GEMM and never written in bf16.
+ *   act_gs (dev) f32 [2], 4-byte aligned, read by the kernels of this call (stream-ordered).
+ * MOE_ERR_INVALID_ARG for any other format or a null act_gs; otherwise as moe_layer_forward. */
+moe_status_t moe_layer_forward_static_act(const void* x, const float* router_logits, int T,
+                                          const moe_packed_desc_t* desc, const void* packed, int top_k,
+                                          const float* act_gs, void* out, void* workspace, size_t ws_bytes,
+                                          moe_stream_t stream);
+
+/* Calibration of those static scales on one batch (W4A4 with H and I multiples of 256, T >= 1):
+ * act_gs[0] = 2688 / max |x| over the batch; then x is quantized with it, the gate/up GEMM runs,
+ * and act_gs[1] = 2688 / max |h| over every routed row (h in bf16); each amax is clamped to
+ * >= 1e-12 as in the dynamic rule.  No output is written; the workspace is that of
+ * moe_layer_forward.  act_gs (dev) f32 [2], 4-byte aligned, written stream-ordered.
+ * MOE_ERR_UNSUPPORTED for W4A4 shapes outside the block-scaled FP4 path. */
+moe_status_t moe_calibrate_act_scales(const void* x, const float* router_logits, int T, const moe_packed_desc_t* desc,
+                                      const void* packed, int top_k, float* act_gs, void* workspace,
+                                      size_t ws_bytes, moe_stream_t stream);
+
 /* Bytes of workspace moe_layer_forward_host needs: moe_workspace_size plus device staging for
  * x, the logits and out (host only). */
 moe_status_t moe_workspace_size_host_io(const moe_packed_desc_t* desc, int T, int top_k, size_t* bytes);
@@ -167,6 +190,11 @@ moe_status_t moe_debug_dequant(const moe_packed_desc_t* desc, const void* packed
  * [T, H/16], gs f32 [T] = 2688 / max(amax(row), 1e-12).  Bit-identical to the W4A4 rule. */
 moe_status_t moe_debug_quant_act(const void* x, int T, int H, uint8_t* codes, uint8_t* scales, float* gs,
                                  moe_stream_t stream);
+
+/* The same with one static global scale for every row: gs_static (dev) f32 [1] (the quantize
+ * multiplier); codes and scales as above (what moe_layer_forward_static_act feeds the GEMMs). */
+moe_status_t moe_debug_quant_act_static(const void* x, int T, int H, const float* gs_static, uint8_t* codes,
+                                        uint8_t* scales, moe_stream_t stream);
 
 /* ---- routing without any caller workspace ----------------------------------------------- */
 

@@ -29,7 +29,8 @@ MOE_T_GU_A, MOE_T_GU_B, MOE_T_D_A, MOE_T_D_B, MOE_T_GU_GS, MOE_T_D_GS, MOE_T_GU_
 EXPORTS = ("moe_packed_size", "moe_pack_experts", "moe_workspace_size", "moe_layer_forward",
            "moe_workspace_size_host_io", "moe_layer_forward_host", "moe_get_device_error", "moe_status_string",
            "moe_debug_route", "moe_debug_dequant", "moe_debug_quant_act", "moe_kernel_launch_count",
-           "moe_time_next_step")
+           "moe_time_next_step", "moe_layer_forward_static_act", "moe_calibrate_act_scales",
+           "moe_debug_quant_act_static")
 
 
 class PackedDesc(C.Structure):
@@ -72,6 +73,9 @@ def lib() -> C.CDLL:
         L.moe_debug_route.argtypes = [P, I32, I32, I32, P, P, P, P, P, P, SZ, P]
         L.moe_debug_dequant.argtypes = [PD, P, I32, I32, P, P]
         L.moe_debug_quant_act.argtypes = [P, I32, I32, P, P, P, P]
+        L.moe_debug_quant_act_static.argtypes = [P, I32, I32, P, P, P, P]
+        L.moe_layer_forward_static_act.argtypes = [P, P, I32, PD, P, I32, P, P, P, SZ, P]
+        L.moe_calibrate_act_scales.argtypes = [P, P, I32, PD, P, I32, P, P, SZ, P]
         L.moe_kernel_launch_count.restype = C.c_uint64
         L.moe_kernel_launch_count.argtypes = []
         L.moe_time_next_step.argtypes = [I32, P, P]
@@ -133,6 +137,28 @@ def moe_layer_forward(x, router_logits, desc: PackedDesc, packed, top_k: int, ou
            "moe_layer_forward")
 
 
+def moe_layer_forward_static_act(x, router_logits, desc: PackedDesc, packed, top_k: int, act_gs, out, workspace,
+                                 stream=None):
+    """W4A4 with static activation scales act_gs (device f32 [2]: x's, then h's)."""
+    T = int(x.shape[0])
+    _check(lib().moe_layer_forward_static_act(_ptr(x), _ptr(router_logits), T, C.byref(desc), _ptr(packed), top_k,
+                                              _ptr(act_gs), _ptr(out), _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_layer_forward_static_act")
+
+
+def moe_calibrate_act_scales(x, router_logits, desc: PackedDesc, packed, top_k: int, workspace, stream=None):
+    """The static W4A4 activation scales of this batch: device f32 [2] (x's, then h's)."""
+    import torch
+
+    T = int(x.shape[0])
+    act_gs = torch.empty(2, dtype=torch.float32, device=x.device)
+    _check(lib().moe_calibrate_act_scales(_ptr(x), _ptr(router_logits), T, C.byref(desc), _ptr(packed), top_k,
+                                          _ptr(act_gs), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _stream(stream)), "moe_calibrate_act_scales")
+    return act_gs
+
+
 def moe_layer_forward_host(x_host, logits_host, desc: PackedDesc, packed, top_k: int, out_host, workspace,
                            stream=None):
     T = int(x_host.shape[0])
@@ -185,6 +211,18 @@ def moe_debug_dequant(desc: PackedDesc, packed, expert: int, which: int, stream=
     _check(lib().moe_debug_dequant(C.byref(desc), _ptr(packed), expert, which, _ptr(out), _stream(stream)),
            "moe_debug_dequant")
     return out
+
+
+def moe_debug_quant_act_static(x, gs_static, stream=None):
+    """NVFP4 codes and block scales of x's rows with one static global scale (device f32 [1])."""
+    import torch
+
+    T, H = (int(s) for s in x.shape)
+    q = torch.empty((T, H // 2), dtype=torch.uint8, device=x.device)
+    s = torch.empty((T, H // 16), dtype=torch.uint8, device=x.device)
+    _check(lib().moe_debug_quant_act_static(_ptr(x), T, H, _ptr(gs_static), _ptr(q), _ptr(s), _stream(stream)),
+           "moe_debug_quant_act_static")
+    return q, s
 
 
 def moe_debug_quant_act(x, stream=None):

@@ -83,12 +83,21 @@ static moe_status_t device_ok() {
 
 static moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// act_gs: null, or the static activation scales (dev, [2], W4A4 only).  calibrate: act_gs is
+// the output of the calibration instead (out unused, fp4 shapes only).
 static moe_status_t forward_checked(const void* x, const float* logits, int T, const moe_packed_desc_t* d,
                                     const void* packed, int k, void* out, void* ws, size_t ws_bytes,
-                                    cudaStream_t s, bool host_io_layout) {
+                                    cudaStream_t s, bool host_io_layout, const float* act_gs = nullptr,
+                                    bool calibrate = false) {
   if (!desc_ok(d) || T < 0 || k < 1 || k > kMaxTopK || k > d->E) return MOE_ERR_INVALID_ARG;
+  if (act_gs && (d->fmt != MOE_FMT_NVFP4_W4A4 || !aligned(act_gs, 4))) return MOE_ERR_INVALID_ARG;
+  if (calibrate) {
+    if (!act_gs || T < 1) return MOE_ERR_INVALID_ARG;
+    if (!fp4_supported(*d)) return MOE_ERR_UNSUPPORTED;
+    out = (void*)act_gs;  // checked below like an output; never written as one
+  }
   if (T > 0 && (!x || !logits || !packed || !out || !ws)) return MOE_ERR_INVALID_ARG;
-  if (!aligned(ws, 256) || !aligned(x, 16) || !aligned(out, 16) || !aligned(packed, 256))
+  if (!aligned(ws, 256) || !aligned(x, 16) || !aligned(out, calibrate ? 4 : 16) || !aligned(packed, 256))
     return MOE_ERR_INVALID_ARG;
   if (T > 0 && x == out) return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(d->fmt, d->E, d->H, d->I, T, k, host_io_layout);
@@ -109,8 +118,11 @@ static moe_status_t forward_checked(const void* x, const float* logits, int T, c
   if (launch_route(logits, T, d->E, k, rb, L, w, pre, s) != cudaSuccess) return MOE_ERR_CUDA;
   const StepEvents ev = g_pending_events;
   g_pending_events = StepEvents();
+  if (calibrate)
+    return cuda_status(launch_experts_fp4(*d, (const char*)packed, (const __nv_bfloat16*)x, T, k, L, w, ev, s, act_gs,
+                                          true));
   return cuda_status(launch_experts(*d, (const char*)packed, (const __nv_bfloat16*)x, T, k, rb, L, w,
-                                    (__nv_bfloat16*)out, ev, s));
+                                    (__nv_bfloat16*)out, ev, s, act_gs));
 }
 
 }  // namespace moe
@@ -198,6 +210,22 @@ moe_status_t moe_layer_forward(const void* x, const float* router_logits, int T,
                                moe_stream_t stream) {
   return forward_checked(x, router_logits, T, d, packed, top_k, out, workspace, ws_bytes, (cudaStream_t)stream,
                          false);
+}
+
+moe_status_t moe_layer_forward_static_act(const void* x, const float* router_logits, int T,
+                                          const moe_packed_desc_t* d, const void* packed, int top_k,
+                                          const float* act_gs, void* out, void* workspace, size_t ws_bytes,
+                                          moe_stream_t stream) {
+  if (!act_gs) return MOE_ERR_INVALID_ARG;
+  return forward_checked(x, router_logits, T, d, packed, top_k, out, workspace, ws_bytes, (cudaStream_t)stream,
+                         false, act_gs);
+}
+
+moe_status_t moe_calibrate_act_scales(const void* x, const float* router_logits, int T, const moe_packed_desc_t* d,
+                                      const void* packed, int top_k, float* act_gs, void* workspace,
+                                      size_t ws_bytes, moe_stream_t stream) {
+  return forward_checked(x, router_logits, T, d, packed, top_k, nullptr, workspace, ws_bytes, (cudaStream_t)stream,
+                         false, act_gs, true);
 }
 
 moe_status_t moe_layer_forward_host(const void* x_host, const float* logits_host, int T, const moe_packed_desc_t* d,
@@ -291,6 +319,17 @@ moe_status_t moe_debug_dequant(const moe_packed_desc_t* d, const void* packed, i
   const moe_status_t dv = device_ok();
   if (dv != MOE_OK) return dv;
   return cuda_status(launch_dequant(*d, (const char*)packed, expert, which, out, (cudaStream_t)stream));
+}
+
+moe_status_t moe_debug_quant_act_static(const void* x, int T, int H, const float* gs_static, uint8_t* codes,
+                                        uint8_t* scales, moe_stream_t stream) {
+  if (T < 0 || H < 16 || H % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !codes || !scales || !gs_static || !aligned(x, 16) || !aligned(gs_static, 4)))
+    return MOE_ERR_INVALID_ARG;
+  const moe_status_t dv = device_ok();
+  if (dv != MOE_OK) return dv;
+  return cuda_status(launch_quant_rows((const __nv_bfloat16*)x, nullptr, 1, T, H, codes, scales, nullptr,
+                                       (cudaStream_t)stream, false, 0, gs_static));
 }
 
 moe_status_t moe_debug_quant_act(const void* x, int T, int H, uint8_t* codes, uint8_t* scales, float* gs,

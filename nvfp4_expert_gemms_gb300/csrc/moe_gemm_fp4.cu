@@ -29,6 +29,7 @@
 #include <cudaTypedefs.h>
 
 #include "moe_formats.cuh"
+#include "moe_nvfp4.cuh"
 #include "moe_tc.cuh"
 
 namespace moe {
@@ -63,7 +64,11 @@ struct Fp4Args {
   const int32_t* perm;
   const float* topk_w;
   const TileEntry* tiles;
-  uint16_t* h_out;          // MODE 0 output [R, I] bf16
+  uint16_t* h_out;          // MODE 0 output [R, I] bf16 (dynamic activation scales)
+  const float* hgs_static;  // MODE 0 with static activation scales: h's global scale (dev); then h
+  uint8_t* hq_out;          //   leaves NVFP4-quantized instead: codes [R, I/2], chunk-major block
+  uint8_t* hsf_out;         //   scales [I/256][sf_rows][16] and the global scale per row [R]
+  float* hg_out;
   uint16_t* y_out;          // MODE 1 output: routing-weighted rows [R, H] bf16, permuted order
   int* err;
   int* work_ctr;            // items handed out past each CTA's first (zeroed by routing)
@@ -364,6 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
       if (MODE == 0) {
         // features w0 + 64 half .. + 63: gate in accumulator columns c, up in 128 + c
         uint16_t* dst = a.h_out + (size_t)(te.row0 + r) * a.I + w0 + 64 * half;
+        const bool fuse = a.hgs_static != nullptr;  // static scales: quantize h here
+        const float ghs = fuse ? *a.hgs_static : 0.f;
+        uint32_t hc[8];  // codes of the thread's four 16-blocks (fused), then their scales
+        uint32_t hs4 = 0u;
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           const int c = 64 * half + 32 * b;
@@ -389,9 +398,37 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
             }
             hw[j] = pack_bf16x2(hv[0], hv[1]);
           }
-          if (live)  // 32-byte stores: each lane writes whole sectors of its own row
+          if (!fuse) {
+            if (live)  // 32-byte stores: each lane writes whole sectors of its own row
 #pragma unroll
-            for (int v = 0; v < 2; ++v) st_global_v8(dst + 32 * b + 16 * v, hw + 8 * v);
+              for (int v = 0; v < 2; ++v) st_global_v8(dst + 32 * b + 16 * v, hw + 8 * v);
+          } else {
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {  // the bf16 h block -> NVFP4 with the static scale
+              float v[16];
+              uint32_t m = 0u;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const uint32_t w = hw[8 * blk + i];
+                v[2 * i] = __uint_as_float(w << 16);
+                v[2 * i + 1] = __uint_as_float(w & 0xFFFF0000u);
+                m = max(m, max(w & 0x7FFFu, (w >> 16) & 0x7FFFu));
+              }
+              uint2 code;
+              uint8_t sc;
+              nvfp4_encode(v, __uint_as_float(m << 16), ghs, &code, &sc);
+              hc[2 * (2 * b + blk)] = code.x;
+              hc[2 * (2 * b + blk) + 1] = code.y;
+              hs4 |= (uint32_t)sc << (8 * (2 * b + blk));
+            }
+          }
+        }
+        if (fuse && live) {
+          const size_t row = (size_t)te.row0 + r;
+          const int f0 = w0 + 64 * half;  // four whole blocks of one 256-column chunk
+          st_global_v8(a.hq_out + row * (a.I / 2) + f0 / 2, hc);
+          *(uint32_t*)(a.hsf_out + ((size_t)(f0 >> 8) * a.sf_rows + row) * 16 + ((f0 & 255) >> 4)) = hs4;
+          if (f0 == 0) a.hg_out[row] = ghs;
         }
       } else {
         // output features w0 + 128 half .. + 127 of the routing-weighted row
@@ -448,7 +485,8 @@ static cudaError_t launch_fp4(const Fp4Args& a, int work, cudaStream_t s) {
 }
 
 cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
-                               const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s) {
+                               const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, const float* act_gs,
+                               bool calibrate) {
   const int E = d.E, H = d.H, I = d.I;
   const size_t R = (size_t)T * k;
   const MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
@@ -457,7 +495,9 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   uint8_t* hq = (uint8_t*)(ws + L.hq);
   uint8_t* hsf = (uint8_t*)(ws + L.hs);
   const int sf_rows = sf_plane_rows(R);
-  launch_quant_rows(x, (const int32_t*)(ws + L.inv), k, T, H, xq, xsf, (float*)(ws + L.xg), s, true, sf_rows);
+  float* cal = calibrate ? const_cast<float*>(act_gs) : nullptr;  // calibration writes the two scales
+  if (cal && launch_act_scale((const uint16_t*)x, (size_t)T * H, cal, s) != cudaSuccess) return cudaGetLastError();
+  launch_quant_rows(x, (const int32_t*)(ws + L.inv), k, T, H, xq, xsf, (float*)(ws + L.xg), s, !cal, sf_rows, act_gs);
 
   Fp4Args a;
   memset(&a, 0, sizeof(a));
@@ -465,6 +505,10 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   a.topk_w = (const float*)(ws + L.topk_w);
   a.tiles = (const TileEntry*)(ws + L.tiles);
   a.h_out = (uint16_t*)(ws + L.h);
+  a.hgs_static = act_gs && !calibrate ? act_gs + 1 : nullptr;
+  a.hq_out = hq;
+  a.hsf_out = hsf;
+  a.hg_out = (float*)(ws + L.hg);
   a.y_out = (uint16_t*)(ws + L.y);
   a.err = (int*)(ws + L.err);
   a.k = k;
@@ -490,9 +534,12 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   record_event(ev.stop[0], s);
   if (err != cudaSuccess) return err;
 
-  // h -> NVFP4 per permuted row (its own global scale), then down: A = h rows, B = [H, I] weights
-  launch_quant_rows((const __nv_bfloat16*)(ws + L.h), nullptr, 1, (int)R, I, hq, hsf, (float*)(ws + L.hg), s, false,
-                    sf_rows);
+  if (cal) return launch_act_scale((const uint16_t*)(ws + L.h), R * I, cal + 1, s);  // h's scale; no down GEMM
+  // h -> NVFP4 per permuted row (its own global scale; with static scales the gate/up epilogue
+  // has already quantized it), then down: A = h rows, B = [H, I] weights
+  if (!act_gs)
+    launch_quant_rows((const __nv_bfloat16*)(ws + L.h), nullptr, 1, (int)R, I, hq, hsf, (float*)(ws + L.hg), s, false,
+                      sf_rows);
   if (!tc_make_map(&a.wcode, u8, dn.a, I / 2, (uint64_t)E * H, I / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tc_make_map(&a.xcode, u8, hq, I / 2, (uint64_t)R, I / 2, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;

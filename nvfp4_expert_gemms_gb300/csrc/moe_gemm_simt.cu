@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restric
 
 template <int FMT, bool A4>
 cudaError_t run_simt(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
-                     const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s) {
+                     const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, const float* h_gs = nullptr) {
   const int H = d.H, I = d.I;
   const MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
   const TileEntry* tiles = (const TileEntry*)(ws + L.tiles);
@@ -187,7 +187,7 @@ cudaError_t run_simt(const moe_packed_desc_t& d, const char* packed, const __nv_
   record_event(ev.stop[0], s);
   if (A4)
     launch_quant_rows((const __nv_bfloat16*)(ws + L.h), nullptr, 1, T * k, I, (uint8_t*)(ws + L.hq), (uint8_t*)(ws + L.hs),
-                      (float*)(ws + L.hg), s);
+                      (float*)(ws + L.hg), s, false, 0, h_gs);
   record_event(ev.start[1], s);
   down_simt_kernel<FMT, A4><<<dim3(L.max_tiles, H / kSimtNB), 128, smem_d, s>>>(
       dn, (const uint16_t*)(ws + L.h), (const uint8_t*)(ws + L.hq), (const uint8_t*)(ws + L.hs),
@@ -201,15 +201,16 @@ cudaError_t run_simt(const moe_packed_desc_t& d, const char* packed, const __nv_
 
 cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
                            int row_block, const WsLayout& L, char* ws, __nv_bfloat16* out, const StepEvents& ev,
-                           cudaStream_t s) {
+                           cudaStream_t s, const float* act_gs) {
   const size_t n_out = (size_t)T * d.H;
   if (T == 0) return cudaGetLastError();
   cudaError_t e;
   if (d.fmt == MOE_FMT_NVFP4_W4A4 && fp4_supported(d)) {
-    e = launch_experts_fp4(d, packed, x, T, k, L, ws, ev, s);
+    e = launch_experts_fp4(d, packed, x, T, k, L, ws, ev, s, act_gs);
   } else if (d.fmt == MOE_FMT_NVFP4_W4A4) {
-    launch_quant_rows(x, nullptr, 1, T, d.H, (uint8_t*)(ws + L.xq), (uint8_t*)(ws + L.xs), (float*)(ws + L.xg), s);
-    e = run_simt<MOE_FMT_NVFP4_W4A16, true>(d, packed, x, T, k, L, ws, ev, s);
+    launch_quant_rows(x, nullptr, 1, T, d.H, (uint8_t*)(ws + L.xq), (uint8_t*)(ws + L.xs), (float*)(ws + L.xg), s,
+                      false, 0, act_gs);
+    e = run_simt<MOE_FMT_NVFP4_W4A16, true>(d, packed, x, T, k, L, ws, ev, s, act_gs ? act_gs + 1 : nullptr);
   } else if (d.fmt == MOE_FMT_FP8_B128_W8A16 && row_block == fp8dec_row_block()) {
     e = launch_experts_fp8dec(d, packed, x, T, k, L, ws, ev, s);
   } else {

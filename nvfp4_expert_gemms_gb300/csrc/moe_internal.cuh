@@ -105,8 +105,11 @@ cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e
 // rows scatter[r*k .. r*k+k-1].  early: x was final before the preceding kernel of the stream
 // passed its pdl_wait() (true only right after routing), so x is read before this launch's wait.
 // sf_rows = 0: scales row-major [rows, K/16]; else chunk-major [K/256][sf_rows][16].
+// static_gs (dev, one float) != null: that global scale for every row instead of each row's own.
+// gs may be null (the per-row scales are then not stored).
 cudaError_t launch_quant_rows(const __nv_bfloat16* x, const int32_t* scatter, int k, int rows, int K, uint8_t* q,
-                              uint8_t* sf, float* gs, cudaStream_t s, bool early = false, int sf_rows = 0);
+                              uint8_t* sf, float* gs, cudaStream_t s, bool early = false, int sf_rows = 0,
+                              const float* static_gs = nullptr);
 // Rows of one chunk plane of chunk-major activation scales for R routed rows: a 128-row tile
 // starting at any row below R stays inside its plane.
 inline int sf_plane_rows(size_t R) { return (int)R + 128; }
@@ -119,9 +122,13 @@ constexpr int kTcPermuteFromRows = 64;
 struct StepEvents {
   cudaEvent_t start[2] = {nullptr, nullptr}, stop[2] = {nullptr, nullptr};
 };
+// act_gs (dev, [2]; W4A4 only): null = dynamic per-row activation scales, else the static global
+// scales of x and h.
 cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,
                            int k, int row_block, const WsLayout& L, char* ws, __nv_bfloat16* out,
-                           const StepEvents& ev, cudaStream_t s);
+                           const StepEvents& ev, cudaStream_t s, const float* act_gs = nullptr);
+// gs = 2688 / max(amax over n bf16 values, 1e-12) into *gs (dev): a static activation scale.
+cudaError_t launch_act_scale(const uint16_t* v, size_t n, float* gs, cudaStream_t s);
 // Programmatic dependent launch.  A kernel started with launch_pdl may begin while the previous
 // kernel of the stream is still running (in a CUDA graph the edge becomes programmatic): it sets
 // up shared and tensor memory, then calls pdl_wait() before it touches memory that earlier
@@ -167,8 +174,11 @@ cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed
 // NVFP4 W4A4 path on block-scaled FP4 MMAs (H and I multiples of 256; 128-row routing tiles).
 bool fp4_supported(const moe_packed_desc_t& d);
 int fp4_row_block();
+// act_gs: static activation scales (dev, [2]) or null; calibrate: instead of the layer, write the
+// static scales of this batch into act_gs (x's from x, then h's from the gate/up output).
 cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
-                               const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);
+                               const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s,
+                               const float* act_gs = nullptr, bool calibrate = false);
 cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
                               int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);
 

@@ -10,6 +10,7 @@
 // A zero amax is clamped to 1e-12 (FP8 tiles, NVFP4 matrices); an INT4 group with a zero
 // scale stores the zero code 8.
 #include "moe_formats.cuh"
+#include "moe_nvfp4.cuh"
 
 namespace moe {
 
@@ -86,59 +87,6 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const uint16_t* __restr
   if (threadIdx.x == 0) atomicMax(&slot[e], __float_as_uint(amax));
 }
 
-// Eight floats to eight E2M1 codes (element i in bits 4i..4i+3) with the hardware conversion:
-// round to nearest, ties to the even code, saturating at 6, sign kept.
-__device__ __forceinline__ uint32_t e2m1x8(const float f[8]) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
-      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
-      : "=r"(r)
-      : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]));
-  return r;
-}
-
-// Codes of eight elements: E2M1(fl(v / eff)), fl = fp32 division rounded to nearest.
-// Bracketing: with r = fl(1/eff), a = fl(v * fl(r * (1 - 2^-20))) and b = fl(v * fl(r * (1 + 2^-20)))
-// carry at most three roundings of 2^-24 each, so |a| < |v/eff| < |b| (outside the subnormal
-// range, where every candidate is far below the first rounding boundary 0.25 and codes 0).
-// fl is monotone, so |a| <= |fl(v/eff)| <= |b|, and because the conversion is monotone too,
-// equal codes for a and b are the code of fl(v/eff).  Only a pair that straddles a rounding
-// boundary pays the exact division.
-__device__ __forceinline__ uint32_t e2m1x8_div(const float* v, float eff, float rd, float ru) {
-  float a[8], b[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    a[i] = __fmul_rn(v[i], rd);
-    b[i] = __fmul_rn(v[i], ru);
-  }
-  const uint32_t ca = e2m1x8(a);
-  if (ca == e2m1x8(b)) return ca;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) a[i] = __fdiv_rn(v[i], eff);
-  return e2m1x8(a);
-}
-
-// One NVFP4 16-block of a row with global scale gs and block maximum amax = max |v|:
-// 8 code bytes and 1 scale byte.
-__device__ __forceinline__ void nvfp4_encode(const float v[16], float amax, float gs, uint2* codes8, uint8_t* scale) {
-  const uint8_t bsc = f32_to_e4m3(__fmul_rn(__fdiv_rn(amax, 6.0f), gs));
-  const float bs = e4m3_to_f32(bsc);
-  uint32_t lo = 0, hi = 0;
-  if (bs != 0.0f) {
-    const float eff = __fdiv_rn(bs, gs);
-    const float r = __frcp_rn(eff);
-    const float rd = __fmul_rn(r, 1.0f - 0x1p-20f), ru = __fmul_rn(r, 1.0f + 0x1p-20f);
-    lo = e2m1x8_div(v, eff, rd, ru);
-    hi = e2m1x8_div(v + 8, eff, rd, ru);
-  }
-  *codes8 = make_uint2(lo, hi);
-  *scale = bsc;
-}
-
 __device__ __forceinline__ void nvfp4_block(const float v[16], float gs, uint2* codes8, uint8_t* scale) {
   float amax = 0.f;
 #pragma unroll
@@ -201,7 +149,8 @@ __device__ __forceinline__ size_t sf_index(size_t d, int b, int K, int sf_rows) 
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restrict__ x,
                                                          const int32_t* __restrict__ scatter, int k, int rows, int K,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                                         float* __restrict__ gs_out, int sf_rows) {
+                                                         float* __restrict__ gs_out, int sf_rows,
+                                                         const float* __restrict__ static_gs) {
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   pdl_wait();
@@ -220,9 +169,9 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
   }
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   if (amax < 1e-12f) amax = 1e-12f;
-  const float gs = __fdiv_rn(2688.0f, amax);
+  const float gs = static_gs ? *static_gs : __fdiv_rn(2688.0f, amax);
   const int ncopy = scatter ? k : 1;
-  if (lane < ncopy) gs_out[scatter ? scatter[(size_t)r * k + lane] : r] = gs;
+  if (gs_out && lane < ncopy) gs_out[scatter ? scatter[(size_t)r * k + lane] : r] = gs;
   for (int b = lane; b < K / 16; b += 32) {
     const uint4 u0 = *(const uint4*)(row + b * 16), u1 = *(const uint4*)(row + b * 16 + 8);
     const uint32_t ww[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
@@ -254,7 +203,8 @@ template <int NBLK, int RPW, bool EARLY>
 __global__ void __launch_bounds__(256) quant_rows_flat_kernel(const uint16_t* __restrict__ x,
                                                               const int32_t* __restrict__ scatter, int k, int rows,
                                                               uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                                              float* __restrict__ gs_out, int sf_rows) {
+                                                              float* __restrict__ gs_out, int sf_rows,
+                                                              const float* __restrict__ static_gs) {
   constexpr int K = 16 * NBLK, kFlat = NBLK * RPW, NB = (kFlat + 31) / 32;
   static_assert(NB <= 8 && RPW * kMaxTopK <= 32, "flat quantizer shape");
   const int lane = threadIdx.x & 31;
@@ -294,7 +244,7 @@ __global__ void __launch_bounds__(256) quant_rows_flat_kernel(const uint16_t* __
   for (int rr = 0; rr < RPW; ++rr) {
     float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, rmax[rr]) << 16);
     if (amax < 1e-12f) amax = 1e-12f;
-    gs[rr] = __fdiv_rn(2688.0f, amax);
+    gs[rr] = static_gs ? *static_gs : __fdiv_rn(2688.0f, amax);
   }
   // destinations: lane rr*k + c holds row rr's copy c (scatter), else row r0 + rr
   const int ncopy = scatter ? k : 1;
@@ -306,7 +256,7 @@ __global__ void __launch_bounds__(256) quant_rows_flat_kernel(const uint16_t* __
   }
 #pragma unroll
   for (int rr = 0; rr < RPW; ++rr)
-    if (lane / ncopy == rr && lane < RPW * ncopy && r0 + rr < rows) gs_out[my_dst] = gs[rr];
+    if (gs_out && lane / ncopy == rr && lane < RPW * ncopy && r0 + rr < rows) gs_out[my_dst] = gs[rr];
 #pragma unroll
   for (int j = 0; j < NB; ++j) {
     const int f = lane + 32 * j, row = f / NBLK, b = f % NBLK;
@@ -400,6 +350,16 @@ cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, co
   return cudaGetLastError();
 }
 
+cudaError_t launch_act_scale(const uint16_t* v, size_t n, float* gs, cudaStream_t s) {
+  // the dynamic rule over a whole tensor: gs = 2688 / max(amax, 1e-12), amax over n bf16 values
+  const cudaError_t e = cudaMemsetAsync(gs, 0, sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  nvfp4_amax_kernel<<<dim3(64, 1), 256, 0, s>>>(v, n, (unsigned*)gs);
+  nvfp4_finish_kernel<<<1, 128, 0, s>>>((unsigned*)gs, 1);
+  note_launches(2);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e, int which, float* out,
                            cudaStream_t s) {
   const MatView m = mat_view(d, packed, which);
@@ -414,33 +374,35 @@ cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e
 
 template <int NBLK, int RPW>
 static cudaError_t launch_quant_flat(bool early, const __nv_bfloat16* x, const int32_t* scatter, int k, int rows,
-                                     uint8_t* q, uint8_t* sf, float* gs, int sf_rows, cudaStream_t s) {
+                                     uint8_t* q, uint8_t* sf, float* gs, int sf_rows, const float* static_gs,
+                                     cudaStream_t s) {
   const dim3 grid((rows + 8 * RPW - 1) / (8 * RPW));
   if (early)
     return launch_pdl(quant_rows_flat_kernel<NBLK, RPW, true>, grid, dim3(256), 0, s, (const uint16_t*)x, scatter, k,
-                      rows, q, sf, gs, sf_rows);
+                      rows, q, sf, gs, sf_rows, static_gs);
   return launch_pdl(quant_rows_flat_kernel<NBLK, RPW, false>, grid, dim3(256), 0, s, (const uint16_t*)x, scatter, k,
-                    rows, q, sf, gs, sf_rows);
+                    rows, q, sf, gs, sf_rows, static_gs);
 }
 
 cudaError_t launch_quant_rows(const __nv_bfloat16* x, const int32_t* scatter, int k, int rows, int K, uint8_t* q,
-                              uint8_t* sf, float* gs, cudaStream_t s, bool early, int sf_rows) {
+                              uint8_t* sf, float* gs, cudaStream_t s, bool early, int sf_rows,
+                              const float* static_gs) {
   if (rows <= 0) return cudaGetLastError();
   note_launches(1);
   switch (K) {  // register-resident shapes: RPW rows fill whole 32-lane passes of 16-blocks
-    case 128: return launch_quant_flat<8, 4>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
-    case 256: return launch_quant_flat<16, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
-    case 512: return launch_quant_flat<32, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
-    case 768: return launch_quant_flat<48, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
-    case 1024: return launch_quant_flat<64, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
-    case 1280: return launch_quant_flat<80, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
-    case 1536: return launch_quant_flat<96, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
-    case 2048: return launch_quant_flat<128, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
-    case 3072: return launch_quant_flat<192, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
-    case 4096: return launch_quant_flat<256, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, s);
+    case 128: return launch_quant_flat<8, 4>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
+    case 256: return launch_quant_flat<16, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
+    case 512: return launch_quant_flat<32, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
+    case 768: return launch_quant_flat<48, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
+    case 1024: return launch_quant_flat<64, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
+    case 1280: return launch_quant_flat<80, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
+    case 1536: return launch_quant_flat<96, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
+    case 2048: return launch_quant_flat<128, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
+    case 3072: return launch_quant_flat<192, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
+    case 4096: return launch_quant_flat<256, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
     default:
       return launch_pdl(quant_rows_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, (const uint16_t*)x, scatter, k, rows,
-                        K, q, sf, gs, sf_rows);
+                        K, q, sf, gs, sf_rows, static_gs);
   }
 }
 

@@ -190,6 +190,84 @@ def test_quant_act_rounding_boundaries_bit_exact(orc, K):
     assert np.array_equal(q.cpu().numpy(), rq)
 
 
+def _gs_of(amax):
+    """The quantize multiplier 2688 / amax in fp32, as the scale rule defines it."""
+    return np.float32(2688.0) / np.float32(max(float(amax), 1e-12))
+
+
+@pytest.mark.parametrize("K", [48, 256, 768, 2048])
+def test_quant_act_static_bit_exact(orc, K):
+    """Static activation scale: every row quantized with one given global scale (part of the
+    rows exceed its range and saturate); codes and block scales equal the oracle's."""
+    x = np.concatenate([_tie_rows(9, K, seed=K), synth.gen_x(23, K, seed=K + 1)])
+    gs = _gs_of(3.0)
+    q, s = M.moe_debug_quant_act_static(dev_bf16(x), torch.tensor([gs], device="cuda"))
+    rq, rs, _ = orc.quant_act_nvfp4(x, static_gs=gs)
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
+class StaticCase(Case):
+    def __init__(self, T, H, I, E, k, seed, zipf=None, h_amax=1.0):
+        super().__init__("nvfp4_w4a4", T, H, I, E, k, seed=seed, zipf=zipf)
+        self.act_gs = np.array([_gs_of(np.abs(synth.bf16_bits_to_f32(self.x)).max()), _gs_of(h_amax)], np.float32)
+
+    def run(self):
+        out = torch.empty((self.T, self.H), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(M.moe_workspace_size(self.layer.desc, self.T, self.k), dtype=torch.uint8, device="cuda")
+        M.moe_layer_forward_static_act(dev_bf16(self.x), torch.from_numpy(self.lg).cuda(), self.layer.desc,
+                                       self.layer.packed, self.k, torch.from_numpy(self.act_gs).cuda(), out, ws)
+        torch.cuda.synchronize()
+        assert M.moe_get_device_error(ws) == 0
+        return host_bits(out)
+
+    def oracle(self, orc, tokens=None):
+        idx, _ = orc.route(self.lg if tokens is None else self.lg[tokens], self.k)
+        p = orc.pack_experts(FID[self.fmt], self.wgu, self.wd, experts=np.unique(idx))
+        return orc.moe_layer(FID[self.fmt], self.x, self.lg, p, self.k, tokens=tokens, act_gs=self.act_gs)
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(200, 512, 256, 16, 4), (64, 256, 128, 8, 2), (700, 512, 256, 4, 2)])
+def test_layer_static_act_scales(orc, T, H, I, E, k):
+    """W4A4 with static activation scales on the block-scaled FP4 path (h quantized inside the
+    gate/up GEMM; several tiles per expert) and on the generic path (H, I not multiples of 256)."""
+    c = StaticCase(T, H, I, E, k, seed=T + H, h_amax=0.5)
+    check_close(synth.bf16_bits_to_f32(c.run()), c.oracle(orc), f"static T={T}")
+
+
+def test_layer_static_act_scales_full_size_sampled(orc):
+    c = StaticCase(16384, FULL["H"], FULL["I"], FULL["E"], FULL["k"], seed=0, zipf=1.1, h_amax=1.0)
+    got = synth.bf16_bits_to_f32(c.run())
+    toks = np.sort(np.random.default_rng(99).choice(16384, size=16, replace=False)).astype(np.int32)
+    check_close(got[toks], c.oracle(orc, tokens=toks), "static full size")
+
+
+def test_calibrate_act_scales(orc):
+    """Calibration: x's scale is exactly 2688 / max|x|; h's is 2688 / max|h| over the routed rows,
+    with h recomputed here from oracle primitives (x quantized with that scale, fp64 GEMVs,
+    bf16 rounding), equal up to one bf16 step of the maximum."""
+    T, H, I, E, k = 96, 512, 256, 8, 2
+    c = Case("nvfp4_w4a4", T, H, I, E, k, seed=41)
+    ws = torch.empty(M.moe_workspace_size(c.layer.desc, T, k), dtype=torch.uint8, device="cuda")
+    gs = M.moe_calibrate_act_scales(dev_bf16(c.x), torch.from_numpy(c.lg).cuda(), c.layer.desc, c.layer.packed, k,
+                                    ws).cpu().numpy()
+    torch.cuda.synchronize()
+    gx = _gs_of(np.abs(synth.bf16_bits_to_f32(c.x)).max())
+    assert gs[0] == gx
+    q, s, g = orc.quant_act_nvfp4(c.x, static_gs=gx)
+    a = np.stack([orc.dequant_nvfp4(q[t:t + 1], s[t:t + 1], g[t])[0] for t in range(T)]).astype(np.float64)
+    idx, _ = orc.route(c.lg, k)
+    p = orc.pack_experts(FID["nvfp4_w4a4"], c.wgu, c.wd, experts=np.unique(idx))
+    hmax = 0.0
+    for e in np.unique(idx):
+        w = orc.dequant_nvfp4(p["gu"][0][e], p["gu"][1][e], p["gu"][2][e]).astype(np.float64)
+        toks = np.nonzero((idx == e).any(axis=1))[0]
+        gu = a[toks] @ w.T
+        h = gu[:, :I] / (1.0 + np.exp(-gu[:, :I])) * gu[:, I:]
+        hmax = max(hmax, float(np.abs(synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(h.astype(np.float32)))).max()))
+    assert abs(gs[1] / _gs_of(hmax) - 1.0) <= 2.0 ** -7, (gs[1], _gs_of(hmax))
+
+
 @pytest.mark.parametrize("T,E,k,zipf", [(64, 8, 2, None), (1, 128, 8, None), (300, 128, 8, 1.1), (257, 256, 8, None),
                                         (5, 6, 6, None), (1000, 37, 3, None), (100, 256, 8, 1.1), (50, 37, 3, None)])
 def test_route_bit_exact(orc, T, E, k, zipf):
