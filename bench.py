@@ -46,7 +46,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4, 5, 6])
+    p.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4, 5, 6, 7])
     p.add_argument("--tokens", type=int, default=None, help="tokens per step (default: the config's largest)")
     p.add_argument("--layers", type=int, default=None, help="layers per step (default 48)")
     p.add_argument("--seed", type=int, default=0)
@@ -71,7 +71,8 @@ def format_mix(c):
 def describe(c):
     return (f"{c['name']}: {format_mix(c)} experts, T={c['T']} tokens x {c['L']} layers, hidden {c['H']}, "
             f"intermediate {c['I']}, {c['E']} experts, top-{c['k']}"
-            + (f", Zipf({c['zipf']}) routing skew" if c["zipf"] else ", N(0,1) logits"))
+            + (f", Zipf({c['zipf']}) routing skew" if c["zipf"] else ", N(0,1) logits")
+            + (", static activation scales calibrated on the batch" if c.get("static_act") else ""))
 
 
 def load_peaks():
@@ -200,10 +201,14 @@ class OracleSample:
     def run(self, min_seconds=0.0):
         """Oracle forward over the sample (repeated until min_seconds); returns (tokens/s, seconds)."""
         spent, tokens = 0.0, 0
+        act_gs = None
+        if self.c.get("static_act"):  # x's scale from the batch, h's a fixed calibrated-range stand-in
+            amax = float(np.abs(synth.bf16_bits_to_f32(self.x)).max())
+            act_gs = np.array([np.float32(2688.0) / np.float32(amax), np.float32(2688.0)], np.float32)
         while True:
             for fid, lg, toks, packed in self.items:
                 t0 = time.perf_counter()
-                self.oracle.moe_layer(fid, self.x, lg, packed, self.c["k"], tokens=toks)
+                self.oracle.moe_layer(fid, self.x, lg, packed, self.c["k"], tokens=toks, act_gs=act_gs)
                 spent += time.perf_counter() - t0
                 tokens += self.n_tok
             if spent >= min_seconds:
@@ -277,12 +282,24 @@ def run_ours(args, c, rank, world, local_rank):
     # run without events
     sampled = [l for l in main_layers if l % 8 == min(7, L - 1)] or [main_layers[-1]]
 
+    act = None
+    if c.get("static_act"):  # static activation scales, calibrated per layer on this batch (untimed)
+        act = torch.stack([M.moe_calibrate_act_scales(x, lg[l], layers[l].desc, layers[l].packed, k, ws)
+                           for l in range(L)])
+        torch.cuda.synchronize()
+
+    def forward(l, xx, lgl, out_l, wsp):
+        if act is None:
+            M.moe_layer_forward(xx, lgl, layers[l].desc, layers[l].packed, k, out_l, wsp)
+        else:
+            M.moe_layer_forward_static_act(xx, lgl, layers[l].desc, layers[l].packed, k, act[l], out_l, wsp)
+
     def step(timed_events=None):
         for l in range(L):
             if timed_events is not None and l in timed_events:
                 M.moe_time_next_step(0, *timed_events[l][:2])
                 M.moe_time_next_step(1, *timed_events[l][2:])
-            M.moe_layer_forward(x, lg[l], layers[l].desc, layers[l].packed, k, outs[l], ws)
+            forward(l, x, lg[l], outs[l], ws)
 
     def as_runner(fn):
         """The step as a CUDA graph (captured after an eager warm-up call) or as eager launches.
@@ -355,7 +372,8 @@ def run_ours(args, c, rank, world, local_rank):
         achieved = gu_flops / gu_avg_s / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4)}
-    traffic = recorded_traffic(fmt, T)  # recorded per launch at the 48-layer mean; rescaled to the sampled layers
+    traffic = recorded_traffic(fmt + ("_static" if c.get("static_act") else ""), T)  # recorded per launch at the
+    # 48-layer mean; rescaled to the sampled layers
     if traffic is not None:
         traffic = round(traffic * statistics.mean(gu_bytes[l] for l in sampled) /
                         statistics.mean(gu_bytes[l] for l in main_layers))
@@ -377,9 +395,18 @@ def run_ours(args, c, rank, world, local_rank):
     lg_h = torch.from_numpy(lg_host).pin_memory()
     out_h = torch.empty((L, T, H), dtype=torch.bfloat16).pin_memory()
 
+    x_d = torch.empty_like(x)
+    lg_d = torch.empty_like(lg[0])
+
     def step_host():
         for l in range(L):
-            M.moe_layer_forward_host(x_h, lg_h[l], layers[l].desc, layers[l].packed, k, out_h[l], ws_io)
+            if act is None:
+                M.moe_layer_forward_host(x_h, lg_h[l], layers[l].desc, layers[l].packed, k, out_h[l], ws_io)
+            else:  # the static entry has device I/O: the same copies, issued around it
+                x_d.copy_(x_h, non_blocking=True)
+                lg_d.copy_(lg_h[l], non_blocking=True)
+                forward(l, x_d, lg_d, outs[l], ws_io)
+                out_h[l].copy_(outs[l], non_blocking=True)
 
     run_host, _ = as_runner(step_host)
     for _ in range(args.warmup):
@@ -397,7 +424,9 @@ def run_ours(args, c, rank, world, local_rank):
         torch.distributed.all_reduce(me, op=torch.distributed.ReduceOp.MAX)
     e2e = {"value": round(world * T * L / float(me.item()), 1), "unit": "tokens/s",
            "h2d_bytes_per_step": L * (x_b + lg_b), "d2h_bytes_per_step": L * out_b,
-           "api": "moe_layer_forward_host (pinned host buffers)" + ("" if args.no_graph else ", CUDA graph")}
+           "api": ("moe_layer_forward_host (pinned host buffers)" if act is None else
+                   "moe_layer_forward_static_act between copies from / to pinned host buffers")
+                  + ("" if args.no_graph else ", CUDA graph")}
 
     sweep = None
     if not args.no_sweep and rank == 0 and len(synth.CONFIGS[args.config]["T"]) > 1:
@@ -409,8 +438,7 @@ def run_ours(args, c, rank, world, local_rank):
             xs = x[:Ts].contiguous()
             lgs = [lg[l, :Ts].contiguous() for l in range(L)]
             wss = torch.empty(ws_bytes(Ts), dtype=torch.uint8, device=dev)
-            run_s, _ = as_runner(lambda: [M.moe_layer_forward(xs, lgs[l], layers[l].desc, layers[l].packed, k,
-                                                              outs[l, :Ts], wss) for l in range(L)])
+            run_s, _ = as_runner(lambda: [forward(l, xs, lgs[l], outs[l, :Ts], wss) for l in range(L)])
             for _ in range(2):
                 run_s()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -65,7 +65,7 @@ struct Fp4Args {
   const float* topk_w;
   const TileEntry* tiles;
   uint16_t* h_out;          // MODE 0 output [R, I] bf16 (dynamic activation scales)
-  const float* hgs_static;  // MODE 0 with static activation scales: h's global scale (dev); then h
+  const float* hgs_static;  // MODE 2 (gate/up, static activation scales): h's global scale (dev); h
   uint8_t* hq_out;          //   leaves NVFP4-quantized instead: codes [R, I/2], chunk-major block
   uint8_t* hsf_out;         //   scales [I/256][sf_rows][16] and the global scale per row [R]
   float* hg_out;
@@ -102,8 +102,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)bf16_bits(lo) | ((uint32_t)bf16_bits(hi) << 16);
 }
 
+// MODE 0: gate/up (h in bf16), 1: down, 2: gate/up with static activation scales (h leaves as
+// NVFP4 codes, block scales and global scales).
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant__ Fp4Args a) {
+  constexpr bool kGateUp = MODE != 1, kFuseH = MODE == 2;
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = (char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   char* sW = smem;
@@ -117,9 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
 
   // gate/up: wait for the activation quantization (and, before it, routing); down: the tile table
   // was final before the gate/up GEMM passed its own pdl_wait(), so only the h codes need the wait
-  if (MODE == 0) pdl_wait();
+  if (kGateUp) pdl_wait();
   const int ntiles = load_tile(a.tiles).expert;
-  const int ncb = MODE == 0 ? a.I / 128 : a.H / 256;
+  const int ncb = kGateUp ? a.I / 128 : a.H / 256;
   const int nwork = ntiles * ncb;
   if ((int)blockIdx.x >= nwork) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -179,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   auto item = [&](int wk, TileEntry& te, int& w0, int& w1) {
     te = load_tile(a.tiles + 1 + wk / ncb);
     const int cb = wk % ncb;
-    w0 = MODE == 0 ? cb * 128 : cb * 256;
-    w1 = MODE == 0 ? a.I + w0 : w0 + 128;
+    w0 = kGateUp ? cb * 128 : cb * 256;
+    w1 = kGateUp ? a.I + w0 : w0 + 128;
   };
 
   if (warp == kProdWarp) {
@@ -359,20 +362,18 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
       float cs = 0.f;
       if (live) {
         const float g = a.wgs[te.expert] * a.ags[te.row0 + r];
-        cs = MODE == 0 ? 1.0f / g : a.topk_w[a.perm[te.row0 + r]] / g;
+        cs = kGateUp ? 1.0f / g : a.topk_w[a.perm[te.row0 + r]] / g;
       }
       ok = mbar_wait(&acc_full, nitem & 1, &s_abort);
       // every epilogue thread takes the same branch
       ok = named_bar_and(1, kEpiWarps * 32, ok);
       if (!ok) break;
       fence_after_sync();
-      if (MODE == 0) {
+      if (kGateUp) {
         // features w0 + 64 half .. + 63: gate in accumulator columns c, up in 128 + c
         uint16_t* dst = a.h_out + (size_t)(te.row0 + r) * a.I + w0 + 64 * half;
-        const bool fuse = a.hgs_static != nullptr;  // static scales: quantize h here
-        const float ghs = fuse ? *a.hgs_static : 0.f;
-        uint32_t hc[8];  // codes of the thread's four 16-blocks (fused), then their scales
-        uint32_t hs4 = 0u;
+        const float ghs = kFuseH ? *a.hgs_static : 0.f;  // static scales: quantize h here
+        uint32_t hall[32];  // fused: the row's 64 bf16 h values, encoded once the accumulator is free
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           const int c = 64 * half + 32 * b;
@@ -398,32 +399,38 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
             }
             hw[j] = pack_bf16x2(hv[0], hv[1]);
           }
-          if (!fuse) {
+          if (!kFuseH) {
             if (live)  // 32-byte stores: each lane writes whole sectors of its own row
 #pragma unroll
               for (int v = 0; v < 2; ++v) st_global_v8(dst + 32 * b + 16 * v, hw + 8 * v);
           } else {
 #pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {  // the bf16 h block -> NVFP4 with the static scale
-              float v[16];
-              uint32_t m = 0u;
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const uint32_t w = hw[8 * blk + i];
-                v[2 * i] = __uint_as_float(w << 16);
-                v[2 * i + 1] = __uint_as_float(w & 0xFFFF0000u);
-                m = max(m, max(w & 0x7FFFu, (w >> 16) & 0x7FFFu));
-              }
-              uint2 code;
-              uint8_t sc;
-              nvfp4_encode(v, __uint_as_float(m << 16), ghs, &code, &sc);
-              hc[2 * (2 * b + blk)] = code.x;
-              hc[2 * (2 * b + blk) + 1] = code.y;
-              hs4 |= (uint32_t)sc << (8 * (2 * b + blk));
-            }
+            for (int j = 0; j < 16; ++j) hall[16 * b + j] = hw[j];
           }
         }
-        if (fuse && live) {
+        uint32_t hc[8];  // fused: codes of the thread's four 16-blocks and their scales
+        uint32_t hs4 = 0u;
+        if (kFuseH) {
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {  // the bf16 h block -> NVFP4 with the static scale
+            float v[16];
+            uint32_t m = 0u;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t w = hall[8 * blk + i];
+              v[2 * i] = __uint_as_float(w << 16);
+              v[2 * i + 1] = __uint_as_float(w & 0xFFFF0000u);
+              m = max(m, max(w & 0x7FFFu, (w >> 16) & 0x7FFFu));
+            }
+            uint2 code;
+            uint8_t sc;
+            nvfp4_encode(v, __uint_as_float(m << 16), ghs, &code, &sc);
+            hc[2 * blk] = code.x;
+            hc[2 * blk + 1] = code.y;
+            hs4 |= (uint32_t)sc << (8 * blk);
+          }
+        }
+        if (kFuseH && live) {
           const size_t row = (size_t)te.row0 + r;
           const int f0 = w0 + 64 * half;  // four whole blocks of one 256-column chunk
           st_global_v8(a.hq_out + row * (a.I / 2) + f0 / 2, hc);
@@ -530,7 +537,7 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   a.N = 2 * I;
   a.K = H;
   record_event(ev.start[0], s);
-  cudaError_t err = launch_fp4<0>(a, max_tiles * (I / 128), s);
+  cudaError_t err = a.hgs_static ? launch_fp4<2>(a, max_tiles * (I / 128), s) : launch_fp4<0>(a, max_tiles * (I / 128), s);
   record_event(ev.stop[0], s);
   if (err != cudaSuccess) return err;
 

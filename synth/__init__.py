@@ -119,6 +119,10 @@ CONFIGS = {
     4: dict(name="nvfp4-w4a4", fmt="nvfp4_w4a4", T=[16384], H=2048, I=768, E=128, k=8, zipf=1.1, layers=48),
     # mixed per-layer formats: the first 17/32 of the stack FP8, the rest NVFP4 W4A4 (the hybrid
     # page's split of a 32-layer model, layers 0-16 FP8 and 17-31 NVFP4, scaled to the stack)
+    # W4A4 with static activation global scales, calibrated on the batch before timing (the hybrid
+    # page's calibrated activation scales; here from synthetic data)
+    7: dict(name="nvfp4-w4a4-static", fmt="nvfp4_w4a4", T=[16384], H=2048, I=768, E=128, k=8, zipf=1.1, layers=48,
+            static_act=True),
     # unquantized bf16 experts through the same kernels: the comparison point of the quantized formats
     6: dict(name="bf16", fmt="bf16", T=[16, 4096], H=2048, I=768, E=128, k=8, zipf=1.1, layers=48),
     5: dict(name="mixed-fp8-nvfp4-w4a4", fmt="nvfp4_w4a4", T=[16, 16384], H=2048, I=768, E=128, k=8, zipf=1.1,
