@@ -22,12 +22,6 @@ struct Cand {
   float v;
   int i;
 };
-// a beats b: larger logit, or equal logit and lower expert index; i == INT_MAX is "none".
-__device__ __forceinline__ bool beats(float av, int ai, float bv, int bi) {
-  if (bi == INT_MAX) return ai != INT_MAX;
-  if (ai == INT_MAX) return false;
-  return av > bv || (av == bv && ai < bi);
-}
 
 // Zero the accumulators of this forward pass (grid-stride over all launched threads).
 __device__ __forceinline__ void zero_prelude(const RoutePrelude& pre) {
@@ -67,31 +61,30 @@ __device__ __forceinline__ int route_token(const float* __restrict__ logits, int
     float x = e < E ? logits[(size_t)t * E + e] : -INFINITY;
     v[m] = isnan(x) ? -INFINITY : x;
   }
-  uint32_t taken = 0;  // bit m: candidate lane + 32m already selected
+  // Order-preserving 32-bit keys (larger key = larger logit; -0 counts as +0, as a float compare
+  // does).  Each round takes the largest key over the warp, then the lowest expert index among
+  // the candidates holding it: two warp reductions instead of a five-step shuffle tournament.
+  uint32_t key[kMaxE / 32];
+#pragma unroll
+  for (int m = 0; m < kMaxE / 32; ++m) {
+    const uint32_t u = __float_as_uint(v[m] == 0.f ? 0.f : v[m]);
+    key[m] = lane + 32 * m < E ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;  // 0: no candidate
+  }
   float selv[kMaxTopK];
   int seli[kMaxTopK];
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = INT_MAX;
+    uint32_t bk = 0u;
+    int be = INT_MAX;
 #pragma unroll
-    for (int m = 0; m < kMaxE / 32; ++m) {
-      const int e = lane + 32 * m;
-      if (e < E && !((taken >> m) & 1u) && beats(v[m], e, bv, bi)) {
-        bv = v[m];
-        bi = e;
+    for (int m = 0; m < kMaxE / 32; ++m)  // ascending m: the lane's lowest index wins its ties
+      if (key[m] > bk) {
+        bk = key[m];
+        be = lane + 32 * m;
       }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (beats(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    selv[j] = bv;
+    const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+    const int bi = (int)__reduce_min_sync(0xffffffffu, bk == wk ? (uint32_t)be : 0xFFFFFFFFu);
+    if ((bi & 31) == lane) key[bi >> 5] = 0u;  // taken
+    selv[j] = __uint_as_float((wk & 0x80000000u) ? (wk & 0x7FFFFFFFu) : ~wk);
     seli[j] = bi;
   }
   // renormalised softmax over the selected logits (descending: selv[0] is the max)
