@@ -181,13 +181,22 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
                                                           int32_t* __restrict__ blkbase,
                                                           TileEntry* __restrict__ tiles, int* err) {
   __shared__ int tot[kMaxE], ntl[kMaxE], off_s[kMaxE + 1], toff_s[kMaxE + 1];
-  const int e = threadIdx.x;
+  __shared__ int psum[1024];  // [part][expert]: the blocks of each expert split into 1024 / E parts
+  const int tid = threadIdx.x, e = tid;
+  const int parts = 1024 / E, pe = tid % E, pp = tid / E;  // thread (part pp, expert pe)
+  const int chunk = (nb + parts - 1) / parts, b0 = pp * chunk, b1 = min(nb, b0 + chunk);
   pdl_wait();
   pdl_trigger();
-  if (e < E) {
+  if (pp < parts) {
     int s = 0;
 #pragma unroll 8
-    for (int b = 0; b < nb; ++b) s += blkcnt[(size_t)b * E + e];
+    for (int b = b0; b < b1; ++b) s += blkcnt[(size_t)b * E + pe];
+    psum[pp * E + pe] = s;
+  }
+  __syncthreads();
+  if (e < E) {
+    int s = 0;
+    for (int p = 0; p < parts; ++p) s += psum[p * E + e];
     tot[e] = s;
     ntl[e] = (s + row_block - 1) / row_block;
   }
@@ -195,13 +204,16 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
   if (e < 32) expert_scan(tot, E, row_block, max_tiles, off_s, toff_s, tiles, e);
   __syncthreads();
   if (e <= E) offsets[e] = off_s[e];
-  if (e < E) {
-    int run = off_s[e];
+  if (pp < parts) {  // each part's blocks start after the earlier parts' rows of the expert
+    int run = off_s[pe];
+    for (int p = 0; p < pp; ++p) run += psum[p * E + pe];
 #pragma unroll 8
-    for (int b = 0; b < nb; ++b) {
-      blkbase[(size_t)b * E + e] = run;
-      run += blkcnt[(size_t)b * E + e];
+    for (int b = b0; b < b1; ++b) {
+      blkbase[(size_t)b * E + pe] = run;
+      run += blkcnt[(size_t)b * E + pe];
     }
+  }
+  if (e < E) {
     const int t0 = toff_s[e];
     for (int i = 0; i < ntl[e]; ++i) {
       if (t0 + i >= max_tiles) {
