@@ -84,6 +84,29 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# ------------------------------------------------------------------------------------------
+# Replicas across ranks (weak scaling: every rank runs the whole layer stack on its own tokens)
+# ------------------------------------------------------------------------------------------
+def rank_seed(seed, rank):
+    """Seed of a rank's synthetic tokens and weights: every replica draws its own batch."""
+    return seed + 7919 * rank
+
+
+def max_over_ranks(value, device, world):
+    """The largest value over all ranks (the job is as slow as its slowest replica)."""
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, T, L, seconds_per_step):
+    """Whole-job throughput: every rank's T tokens through L layers per step."""
+    return world * T * L / seconds_per_step
+
+
 def per_expert_bytes(fmt, H, I):
     import nvfp4_expert_gemms_gb300 as M
 
@@ -246,7 +269,7 @@ def run_ours(args, c, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     fmt, T, H, I, E, k, L = c["fmt"], c["T"], c["H"], c["I"], c["E"], c["k"], c["L"]
     fmts = synth.layer_formats(c, L)  # fmt throughout, or a mixed stack
-    seed = args.seed + 7919 * rank
+    seed = rank_seed(args.seed, rank)
     layers = []
     for l in range(L):
         wgu, wd = synth.gen_expert_weights_device(E, H, I, seed, l, dev)
@@ -353,12 +376,9 @@ def run_ours(args, c, rank, world, local_rank):
 
     def pct(q):
         return per_step[min(len(per_step) - 1, int(round(q * (len(per_step) - 1))))]
-    mt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
-    ms_total = float(mt.item())
+    ms_total = max_over_ranks(ms_total, dev, world)
     ms_step = ms_total / args.steps
-    value = world * T * L / (ms_step / 1e3)
+    value = job_tokens_per_s(world, T, L, ms_step / 1e3)
 
     peaks, peak_src = load_peaks()
     gu_avg_s = statistics.mean(gu_ms) / 1e3
@@ -419,10 +439,7 @@ def run_ours(args, c, rank, world, local_rank):
         run_host()
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / args.steps
-    me = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(me, op=torch.distributed.ReduceOp.MAX)
-    e2e = {"value": round(world * T * L / float(me.item()), 1), "unit": "tokens/s",
+    e2e = {"value": round(job_tokens_per_s(world, T, L, max_over_ranks(e2e_s, dev, world)), 1), "unit": "tokens/s",
            "h2d_bytes_per_step": L * (x_b + lg_b), "d2h_bytes_per_step": L * out_b,
            "api": ("moe_layer_forward_host (pinned host buffers)" if act is None else
                    "moe_layer_forward_static_act between copies from / to pinned host buffers")
