@@ -21,7 +21,6 @@ enum : int { kDevOk = 0, kDevTimeout = MOE_ERR_DEVICE_TIMEOUT, kDevFault = MOE_E
 
 __device__ __forceinline__ void set_dev_error(int* err, int code) { atomicCAS(err, 0, code); }
 
-// ---- scalar codecs (device) --------------------------------------------------------------
 // The workspace status block (256 bytes): int 0 is the device error word; ints 1 .. kSchedCounters
 // are the work counters of the persistent GEMM kernels that hand out items dynamically.  The
 // routing kernel of every forward pass resets them all.
@@ -31,6 +30,7 @@ __device__ __forceinline__ void reset_status(int* status) {
   for (int i = 1; i <= kSchedCounters; ++i) status[i] = 0;
 }
 
+// ---- scalar codecs (device) --------------------------------------------------------------
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 __device__ __forceinline__ uint16_t bf16_bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
@@ -72,7 +72,7 @@ __device__ __forceinline__ TileEntry load_tile(const TileEntry* p) {
 // ---- workspace layout ----------------------------------------------------------------------
 struct WsLayout {
   size_t err, topk_idx, topk_w, blkcnt, blkbase, offsets, perm, inv, tiles;
-  size_t h, y, xq, xs, xg, hq, hs, hg;  // y: routing-weighted down rows [R, H] fp32 (permuted order)
+  size_t h, y, xq, xs, xg, hq, hs, hg;  // y: routing-weighted down rows [R, H] bf16 (permuted order)
   size_t xp;          // expert-permuted bf16 copy of x (tensor-core path, row blocks >= 64)
   size_t xmax, hmax;  // per-row max |activation| (FP8 decode path)
   size_t x_stage, lg_stage, out_stage;
@@ -84,11 +84,9 @@ struct WsLayout {
 WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io);
 
 // ---- launches (each returns cudaGetLastError() after enqueueing) -------------------------
-// Work folded into the first routing launch: zero two accumulators and (optionally) record the
-// max |x| of every activation row.
+// Work folded into the first routing launch: zero the h row maxima and (optionally) record the
+// max |x| of every activation row (FP8 decode path).
 struct RoutePrelude {
-  float* zero_f32 = nullptr;
-  size_t n_f32 = 0;  // multiple of 4
   unsigned* zero_u32 = nullptr;
   size_t n_u32 = 0;
   const uint16_t* x = nullptr;  // bf16 [T, H] or null
@@ -133,8 +131,10 @@ cudaError_t launch_act_scale(const uint16_t* v, size_t n, float* gs, cudaStream_
 // kernel of the stream is still running (in a CUDA graph the edge becomes programmatic): it sets
 // up shared and tensor memory, then calls pdl_wait() before it touches memory that earlier
 // kernels write or read, and pdl_trigger() to let its own dependent start setting up.  Only
-// read-only data (packed weights) and the routing tile table, which is final before the
-// previous GEMM passed its own pdl_wait(), may be read before pdl_wait().
+// read-only data (packed weights), the routing tile table (final before the previous GEMM
+// passed its own pdl_wait()) and, in the activation quantizer that follows routing, the layer
+// input x (final before the routing kernels, which wait before they trigger, started) may be
+// read before pdl_wait().
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 template <typename... KArgs, typename... Args>
@@ -162,7 +162,7 @@ inline void record_event(cudaEvent_t ev, cudaStream_t s) {
 // Running count of kernels enqueued by the library (moe_kernel_launch_count).
 void note_launches(int n);
 int simt_row_block();
-// Tensor-core path (FP8 W8A16, INT4 W4A16, NVFP4 W4A16): row block per tile, and the two GEMMs.
+// Tensor-core path (FP8 W8A16, INT4 W4A16, NVFP4 W4A16, BF16): row block per tile, and the two GEMMs.
 int tc_row_block(int fmt, int T, int k, int E);
 bool tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1, uint64_t pitch,
                  uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw);

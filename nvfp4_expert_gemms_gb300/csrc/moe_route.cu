@@ -16,17 +16,15 @@ namespace moe {
 
 namespace {
 
-constexpr int kRouteSmallZeroMax = 1 << 18;  // fp32 words one block zeroes quickly (1 MB)
 
 struct Cand {
   float v;
   int i;
 };
 
-// Zero the accumulators of this forward pass (grid-stride over all launched threads).
+// Zero this forward pass's running maxima (grid-stride over all launched threads).
 __device__ __forceinline__ void zero_prelude(const RoutePrelude& pre) {
   const size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t i = g; i < pre.n_f32 / 4; i += stride) ((float4*)pre.zero_f32)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (size_t i = g; i < pre.n_u32; i += stride) pre.zero_u32[i] = 0u;
 }
 
@@ -339,7 +337,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int row_block
   int32_t* inv = (int32_t*)(ws + L.inv);
   TileEntry* tiles = (TileEntry*)(ws + L.tiles);
   const int nb = L.nb;
-  if (T > 0 && T <= kRouteTB && pre.n_f32 <= (size_t)kRouteSmallZeroMax) {
+  if (T > 0 && T <= kRouteTB) {
     note_launches(1);
     return launch_pdl(route_small_kernel, dim3(1), dim3(1024), 0, s, logits, T, E, k, row_block, L.max_tiles, idx,
                       w, off, perm, inv, tiles, err, pre);
