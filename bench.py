@@ -64,8 +64,10 @@ def workload(args):
 
 
 def format_mix(c):
+    """The format, or for a mixed stack each format with its layer count."""
     fm = synth.layer_formats(c, c["L"])
-    return " + ".join(f"{f} x{fm.count(f)}" for f in dict.fromkeys(fm))
+    kinds = list(dict.fromkeys(fm))
+    return kinds[0] if len(kinds) == 1 else " + ".join(f"{f} x{fm.count(f)}" for f in kinds)
 
 
 def describe(c):
