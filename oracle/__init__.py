@@ -5,7 +5,8 @@ baseline leg of bench.py -- never by the product package.  Every function here t
 and returns numpy arrays and calls the C oracle; no arithmetic of the method lives
 in this file beyond reshaping.
 
-Format ids: 1 = FP8 block-128 W8A16, 2 = INT4 g128 W4A16, 3 = NVFP4 W4A16, 4 = NVFP4 W4A4.
+Format ids: 1 = FP8 block-128 W8A16, 2 = INT4 g128 W4A16, 3 = NVFP4 W4A16, 4 = NVFP4 W4A4,
+5 = BF16, 6 = FP8 block-128 weights with FP8 1x128-group activations (W8A8).
 """
 from __future__ import annotations
 
@@ -19,8 +20,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-FMT_FP8, FMT_INT4, FMT_NVFP4_W4A16, FMT_NVFP4_W4A4, FMT_BF16 = 1, 2, 3, 4, 5
-FMT_IDS = {"fp8": 1, "int4": 2, "nvfp4_w4a16": 3, "nvfp4_w4a4": 4, "bf16": 5}
+FMT_FP8, FMT_INT4, FMT_NVFP4_W4A16, FMT_NVFP4_W4A4, FMT_BF16, FMT_FP8_W8A8 = 1, 2, 3, 4, 5, 6
+FMT_IDS = {"fp8": 1, "int4": 2, "nvfp4_w4a16": 3, "nvfp4_w4a4": 4, "bf16": 5, "fp8_w8a8": 6}
 
 
 def build(force: bool = False) -> str:
@@ -57,7 +58,8 @@ def lib():
         L.orc_bf16_encode.restype = C.c_uint16
         L.orc_bf16_encode.argtypes = [C.c_double]
         for f in ("orc_pack_fp8", "orc_pack_int4", "orc_pack_nvfp4", "orc_dequant_fp8", "orc_dequant_int4",
-                  "orc_quant_act_nvfp4", "orc_quant_act_nvfp4_static", "orc_route", "orc_permute"):
+                  "orc_quant_act_nvfp4", "orc_quant_act_nvfp4_static", "orc_quant_act_fp8",
+                  "orc_dequant_act_fp8", "orc_route", "orc_permute"):
             getattr(L, f).restype = None
         L.orc_pack_fp8.argtypes = [P, C.c_int, C.c_int, P, P]
         L.orc_dequant_fp8.argtypes = [P, P, C.c_int, C.c_int, P]
@@ -68,6 +70,8 @@ def lib():
         L.orc_dequant_nvfp4.argtypes = [P, P, C.c_float, C.c_int, C.c_int, P]
         L.orc_quant_act_nvfp4.argtypes = [P, C.c_int, C.c_int, P, P, P]
         L.orc_quant_act_nvfp4_static.argtypes = [P, C.c_int, C.c_int, C.c_float, P, P]
+        L.orc_quant_act_fp8.argtypes = [P, C.c_int, C.c_int, P, P]
+        L.orc_dequant_act_fp8.argtypes = [P, P, C.c_int, C.c_int, P]
         L.orc_route.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
         L.orc_permute.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P, P]
         L.orc_moe_layer.restype = C.c_int
@@ -185,6 +189,25 @@ def quant_act_nvfp4(x_bf16: np.ndarray, static_gs=None):
     return q, s, g
 
 
+def quant_act_fp8(x_bf16: np.ndarray):
+    """x [T, H] bf16 bits -> (codes E4M3 u8 [T, H], scale_inv f32 [T, H/128]): one scale per
+    1x128 group of a row."""
+    T, H = x_bf16.shape
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    q = np.empty((T, H), np.uint8)
+    s = np.empty((T, H // 128), np.float32)
+    lib().orc_quant_act_fp8(_p(x), T, H, _p(q), _p(s))
+    return q, s
+
+
+def dequant_act_fp8(codes, scale_inv):
+    T, H = codes.shape
+    out = np.empty((T, H), np.float32)
+    lib().orc_dequant_act_fp8(_p(np.ascontiguousarray(codes)), _p(np.ascontiguousarray(scale_inv, np.float32)), T, H,
+                              _p(out))
+    return out
+
+
 # ---- routing ----------------------------------------------------------------------------
 def route(logits: np.ndarray, k: int):
     """logits [T, E] f32 -> (idx int32 [T, k], w float64 [T, k])."""
@@ -226,7 +249,7 @@ def pack_experts(fmt: int, wgu: np.ndarray, wd: np.ndarray, experts=None) -> dic
             a = np.zeros((E, N, K), np.uint16)
             a[list(sel)] = np.asarray(W, dtype=np.uint16)[list(sel)]
             b = g = None
-        elif fmt == FMT_FP8:
+        elif fmt in (FMT_FP8, FMT_FP8_W8A8):  # W8A8 stores the same FP8 block weights
             a = np.zeros((E, N, K), np.uint8)
             b = np.zeros((E, N // 128, K // 128), np.float32)
             g = None

@@ -23,6 +23,8 @@
  *           scales, one FP32 global scale; here computed at run time per activation row.
  *   [bf16]  clef-omni-fp8, "Which Clef-Omni quant should I use?": the BF16 original is the
  *           reference every quant is compared with; its weights are used as stored.
+ *   [w8a8]  clef-omni-fp8, "What was quantized": the same FP8 block weights with activations
+ *           quantized to FP8 at run time, one scale per 1x128 group of a row.
  *
  * Readings where the pages are silent (each also listed in the design doc):
  *   - E4M3 is the OCP "e4m3fn" variant (max 448, no infinities); encode saturates at 448.
@@ -35,6 +37,9 @@
  *     the softmax over them; permuted rows are ordered by (expert, token, slot).
  *   - W4A4 quantizes each activation row with its own global scale 2688/amax(row); the
  *     gated intermediate h is rounded to bf16 first and quantized the same way.
+ *   - W8A8 quantizes each 1x128 activation group with the [fp8] weight recipe applied to that
+ *     group (s = 448/amax, E4M3 round-to-nearest, 1/s stored); h is rounded to bf16 first and
+ *     quantized the same way.
  */
 #include <math.h>
 #include <stdint.h>
@@ -44,7 +49,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_FP8 = 1, ORC_INT4 = 2, ORC_NVFP4_W4A16 = 3, ORC_NVFP4_W4A4 = 4, ORC_BF16 = 5 };
+enum { ORC_FP8 = 1, ORC_INT4 = 2, ORC_NVFP4_W4A16 = 3, ORC_NVFP4_W4A4 = 4, ORC_BF16 = 5, ORC_FP8_W8A8 = 6 };
 
 /* ------------------------------------------------------------------------------------ */
 /* Scalar formats: a sign-magnitude minifloat with `mbits` mantissa bits and exponent   */
@@ -274,6 +279,34 @@ void orc_quant_act_nvfp4(const uint16_t* x, int T, int H, uint8_t* codes, uint8_
   free(row);
 }
 
+/* [w8a8]: each group of 128 consecutive elements of a [T, H] bf16 row is quantized like one
+   [fp8] weight tile: s = 448/max(amax, 1e-12), code = E4M3(v*s), 1/s stored.
+   codes [T, H] E4M3; scale_inv [T, H/128]. */
+void orc_quant_act_fp8(const uint16_t* x, int T, int H, uint8_t* codes, float* scale_inv) {
+  for (int t = 0; t < T; ++t)
+    for (int g = 0; g < H / 128; ++g) {
+      const uint16_t* v = x + (size_t)t * H + g * 128;
+      float amax = 0.0f;
+      for (int i = 0; i < 128; ++i) {
+        float a = fabsf(bf16f(v[i]));
+        if (a > amax) amax = a;
+      }
+      if (amax < 1e-12f) amax = 1e-12f;
+      float s = 448.0f / amax;
+      for (int i = 0; i < 128; ++i) codes[(size_t)t * H + g * 128 + i] = orc_e4m3_encode(bf16f(v[i]) * s);
+      scale_inv[(size_t)t * (H / 128) + g] = 1.0f / s;
+    }
+}
+
+/* value = E4M3(code) * scale_inv(group), one fp32 rounding (as the weights' dequantization). */
+void orc_dequant_act_fp8(const uint8_t* codes, const float* scale_inv, int T, int H, float* out) {
+  for (int t = 0; t < T; ++t)
+    for (int k = 0; k < H; ++k) {
+      size_t i = (size_t)t * H + k;
+      out[i] = (float)orc_e4m3_decode(codes[i]) * scale_inv[(size_t)t * (H / 128) + k / 128];
+    }
+}
+
 /* ------------------------------------------------------------------------------------ */
 /* Routing: top-k of the router logits, renormalised softmax, permutation by expert.    */
 /* ------------------------------------------------------------------------------------ */
@@ -327,7 +360,7 @@ static void dequant_expert(int fmt, int which, int e, int H, int I, const void* 
                            const float* gs, float* out) {
   int N = which == 0 ? 2 * I : H, K = which == 0 ? H : I;
   size_t NK = (size_t)N * K;
-  if (fmt == ORC_FP8) {
+  if (fmt == ORC_FP8 || fmt == ORC_FP8_W8A8) {
     orc_dequant_fp8((const uint8_t*)a + NK * e, (const float*)b + (size_t)(N / 128) * (K / 128) * e, N, K, out);
   } else if (fmt == ORC_INT4) {
     orc_dequant_int4((const int32_t*)a + NK / 8 * e, (const uint16_t*)b + (size_t)(K / 128) * N * e, N, K, out);
@@ -343,8 +376,8 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 /* y = Wd * act(Wgu * a) for one (token, expert) pair; h per the format's rules. */
 static void expert_mlp(int fmt, int H, int I, const float* wgu, const float* wd, const double* a,
-                       const float* act_gs, double* h, uint16_t* hb, uint8_t* hq, uint8_t* hs, float* hdq,
-                       double* y) {
+                       const float* act_gs, double* h, uint16_t* hb, uint8_t* hq, uint8_t* hs, uint8_t* hq8,
+                       float* hdq, double* y) {
   for (int n = 0; n < I; ++n) {
     double g = 0.0, u = 0.0;
     const float* wg = wgu + (size_t)n * H;
@@ -366,6 +399,13 @@ static void expert_mlp(int fmt, int H, int I, const float* wgu, const float* wd,
     }
     orc_dequant_nvfp4(hq, hs, gsr, 1, I, hdq);
     for (int n = 0; n < I; ++n) h[n] = (double)hdq[n];
+  } else if (fmt == ORC_FP8_W8A8) {
+    float* hsi = (float*)malloc(sizeof(float) * (I / 128));
+    for (int n = 0; n < I; ++n) hb[n] = orc_bf16_encode(h[n]);
+    orc_quant_act_fp8(hb, 1, I, hq8, hsi);
+    orc_dequant_act_fp8(hq8, hsi, 1, I, hdq);
+    for (int n = 0; n < I; ++n) h[n] = (double)hdq[n];
+    free(hsi);
   }
   for (int c = 0; c < H; ++c) {
     double acc = 0.0;
@@ -375,9 +415,19 @@ static void expert_mlp(int fmt, int H, int I, const float* wgu, const float* wd,
   }
 }
 
-/* Activation row a_t: bf16 x (W8A16, W4A16) or the dequantized NVFP4 row (W4A4). */
+/* Activation row a_t: bf16 x (W8A16, W4A16) or the dequantized NVFP4 (W4A4) or FP8 (W8A8) row. */
 static void act_row(int fmt, const uint16_t* xrow, int H, const float* act_gs, double* a) {
-  if (fmt == ORC_NVFP4_W4A4) {
+  if (fmt == ORC_FP8_W8A8) {
+    uint8_t* q = (uint8_t*)malloc((size_t)H);
+    float* si = (float*)malloc(sizeof(float) * (H / 128));
+    float* d = (float*)malloc(sizeof(float) * H);
+    orc_quant_act_fp8(xrow, 1, H, q, si);
+    orc_dequant_act_fp8(q, si, 1, H, d);
+    for (int k = 0; k < H; ++k) a[k] = (double)d[k];
+    free(q);
+    free(si);
+    free(d);
+  } else if (fmt == ORC_NVFP4_W4A4) {
     uint8_t* q = (uint8_t*)malloc((size_t)H / 2);
     uint8_t* s = (uint8_t*)malloc((size_t)H / 16);
     float* d = (float*)malloc(sizeof(float) * H);
@@ -403,7 +453,7 @@ static void act_row(int fmt, const uint16_t* xrow, int H, const float* act_gs, d
    out_t = sum_j w_j y_j summed in slot order; everything accumulated in fp64.
    dense != 0 runs the dense masked definition instead: every token through all E experts,
    weighted by the routing weights scattered over experts (zero for unselected ones).
-   Weights are passed per format: fp8 (codes, scale_inv, -), int4 (qweight, scales, -),
+   Weights are passed per format: fp8 and fp8 W8A8 (codes, scale_inv, -), int4 (qweight, scales, -),
    nvfp4 (packed, block scales, global scales), bf16 (weights, -, -).  act_gs (W4A4 only): NULL
    quantizes x and h rows with their own dynamic global scales, else with the static scales
    act_gs[0] (x) and act_gs[1] (h).  Returns 0 on success. */
@@ -438,6 +488,7 @@ int orc_moe_layer(int fmt, int T, int H, int I, int E, int k, const uint16_t* x,
     uint16_t* hb = (uint16_t*)malloc(sizeof(uint16_t) * I);
     uint8_t* hq = (uint8_t*)malloc((size_t)I / 2);
     uint8_t* hs = (uint8_t*)malloc((size_t)I / 16);
+    uint8_t* hq8 = (uint8_t*)malloc((size_t)I);
     float* hdq = (float*)malloc(sizeof(float) * I);
 #pragma omp for schedule(dynamic, 1)
     for (int e = 0; e < E; ++e) {
@@ -453,7 +504,7 @@ int orc_moe_layer(int fmt, int T, int H, int I, int E, int k, const uint16_t* x,
           for (int j = 0; j < k; ++j)
             if (idx[(size_t)i * k + j] == e) slot = j;
         if (slot < 0) continue;
-        expert_mlp(fmt, H, I, wgu, wd, acts + (size_t)i * H, act_gs, h, hb, hq, hs, hdq,
+        expert_mlp(fmt, H, I, wgu, wd, acts + (size_t)i * H, act_gs, h, hb, hq, hs, hq8, hdq,
                    ybuf + ((size_t)i * slots + slot) * H);
         used[(size_t)i * slots + slot] = 1;
       }
@@ -464,6 +515,7 @@ int orc_moe_layer(int fmt, int T, int H, int I, int E, int k, const uint16_t* x,
     free(hb);
     free(hq);
     free(hs);
+    free(hq8);
     free(hdq);
   }
 

@@ -342,3 +342,104 @@ def test_static_activation_scale_saturates_outside_calibration(orc):
     assert s[0, 0] == 0x7E and g[0] == np.float32(2688.0)
     assert q[0, 0] & 0x0F == 0xF and (q[0, 7] >> 4) == 0x7  # -4 -> -6 (0xF), +4 -> +6 (0x7)
     assert s[0, 1] == orc.e4m3_encode(np.float32(448.0)) and (q[0, 8] & 0x0F) == 0x7  # 1 -> 6 in its own block
+
+
+# ---------------------------------------------------------------- dynamic FP8 1x128 activation quant
+def test_fp8_act_quant_hand_worked_row(orc):
+    row = np.zeros((1, 256), np.float32)
+    expect, sinv = {}, {}
+    for r in _lines("fp8_act_group_example.txt"):
+        if r[0] == "scale_inv":
+            sinv[int(r[1])] = float(r[2])
+            continue
+        row[0, int(r[0])] = float(r[1])
+        expect[int(r[0])] = int(r[2], 16)
+    xb = bf16(row)
+    assert np.array_equal(synth.bf16_bits_to_f32(xb), row), "example values must be bf16-exact"
+    q, s = orc.quant_act_fp8(xb)
+    assert s.shape == (1, 2) and s[0, 0] == np.float32(sinv[0]) and s[0, 1] == np.float32(sinv[1])
+    for c in range(256):
+        assert q[0, c] == expect.get(c, 0), (c, hex(q[0, c]))
+
+
+def _e4m3_nearest_brute_force(v):
+    """Nearest finite E4M3 code to each fp32 value by exhaustive search over torch's decode of
+    the 127 finite magnitudes (ties to the even code), sign kept, saturating at 448."""
+    mags = torch.arange(0x7F, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    a = np.abs(v.astype(np.float64))[..., None]
+    d = np.abs(a - mags)
+    best = d.min(axis=-1, keepdims=True)
+    cand = d == best
+    even = cand & (np.arange(0x7F) % 2 == 0)
+    code = np.where(even.any(-1), np.argmax(even, -1), np.argmax(cand, -1))
+    return (code | (np.signbit(v) * 0x80)).astype(np.uint8)
+
+
+def test_fp8_act_quant_is_nearest_grid_point_brute_force(orc):
+    # groups of very different magnitude in one row: each must be scaled by its own amax
+    g = np.random.default_rng(21)
+    T, H = 6, 512
+    x = g.standard_normal((T, H)).astype(np.float32)
+    x *= np.repeat(np.array([1e-3, 1.0, 40.0, 3e-5], np.float32), 128)[None, :]
+    xb = bf16(x)
+    xf = synth.bf16_bits_to_f32(xb)
+    q, s = orc.quant_act_fp8(xb)
+    for t in range(T):
+        for gi in range(H // 128):
+            v = xf[t, gi * 128:(gi + 1) * 128]
+            sc = np.float32(448.0) / np.float32(np.abs(v).max())  # IEEE fp32 division
+            assert s[t, gi] == np.float32(1.0) / sc
+            assert np.array_equal(q[t, gi * 128:(gi + 1) * 128], _e4m3_nearest_brute_force(v * sc))
+
+
+def test_fp8_act_quant_groups_are_independent_and_bounded(orc):
+    g = np.random.default_rng(22)
+    x = g.standard_normal((4, 384)).astype(np.float32)
+    x *= np.repeat(np.array([2e-3, 5.0, 1e-1], np.float32), 128)[None, :]
+    xb = bf16(x)
+    xf = synth.bf16_bits_to_f32(xb)
+    q, s = orc.quant_act_fp8(xb)
+    d = orc.dequant_act_fp8(q, s)
+    for t in range(4):
+        for gi in range(3):
+            v = xf[t, gi * 128:(gi + 1) * 128]
+            amax = np.abs(v).max()
+            assert abs(s[t, gi] - amax / 448) <= 4e-7 * amax / 448
+            assert q[t, gi * 128 + np.argmax(np.abs(v))] & 0x7F == 0x7E  # the group max maps to 448
+            err = np.abs(d[t, gi * 128:(gi + 1) * 128] - v)
+            # 3 mantissa bits: relative error <= 2^-4 for normals, absolute <= 2^-10 / s below
+            assert np.all(err <= np.maximum(np.abs(v) * 2.0 ** -4, s[t, gi] * 2.0 ** -10) * (1 + 1e-6))
+    # rows are independent: quantizing a subset gives the same rows
+    q2, s2 = orc.quant_act_fp8(xb[2:3])
+    assert np.array_equal(q2[0], q[2]) and np.array_equal(s2[0], s[2])
+
+
+def test_fp8_act_quant_grid_exact_row_is_identity(orc):
+    """A group made of E4M3 grid values scaled by 2^j, with its largest magnitude exactly
+    448 * 2^j, has s = 2^-j: the codes are the ones the values were built from and the
+    dequantized row is the row itself."""
+    g = np.random.default_rng(23)
+    mags = torch.arange(0x7F, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    T, H = 3, 384
+    codes = g.integers(0, 0x7E, size=(T, H)).astype(np.uint8) | (g.integers(0, 2, size=(T, H)) * 0x80).astype(np.uint8)
+    codes[:, ::128] = 0x7E  # one element per group at the top of the range
+    j = g.integers(-12, 4, size=(T, H // 128))
+    vals = np.where(codes & 0x80, -1.0, 1.0) * mags[codes & 0x7F] * np.repeat(2.0 ** j, 128, axis=1)
+    vals = vals.astype(np.float32)
+    xb = bf16(vals)
+    assert np.array_equal(synth.bf16_bits_to_f32(xb), vals)
+    q, s = orc.quant_act_fp8(xb)
+    assert np.array_equal(q, codes)
+    assert np.array_equal(s, (2.0 ** j).astype(np.float32))
+    assert np.array_equal(orc.dequant_act_fp8(q, s), vals)
+
+
+def test_fp8_act_quant_zero_group(orc):
+    """An all-zero group (amax clamped to 1e-12) gives zero codes, the sign of -0 kept."""
+    row = np.zeros((1, 256), np.float32)
+    row[0, 5] = -0.0
+    row[0, 200] = 1.0
+    q, s = orc.quant_act_fp8(bf16(row))
+    assert q[0, 5] == 0x80 and np.all(np.delete(q[0, :128], 5) == 0)
+    assert s[0, 0] == np.float32(1.0) / (np.float32(448.0) / np.float32(1e-12))
+    assert q[0, 200] == 0x7E and s[0, 1] == np.float32(1.0) / np.float32(448.0)

@@ -14,7 +14,7 @@ import torch.nn.functional as F
 
 import synth
 
-FP8, INT4, W4A16, W4A4, BF16 = 1, 2, 3, 4, 5
+FP8, INT4, W4A16, W4A4, BF16, W8A8 = 1, 2, 3, 4, 5, 6
 
 
 def test_topk_brute_force_small(orc):
@@ -70,7 +70,7 @@ def _torch_reference(fmt, x_bits, logits, packed, k, orc, act_gs=None):
     d_a, d_b, d_g = packed["d"]
     wgu, wd = [], []
     for e in range(E):
-        if fmt == FP8:
+        if fmt in (FP8, W8A8):
             wgu.append(orc.dequant_fp8(gu_a[e], gu_b[e]))
             wd.append(orc.dequant_fp8(d_a[e], d_b[e]))
         elif fmt == INT4:
@@ -89,6 +89,8 @@ def _torch_reference(fmt, x_bits, logits, packed, k, orc, act_gs=None):
         q, s, gsa = orc.quant_act_nvfp4(x_bits, static_gs=None if act_gs is None else act_gs[0])
         a = torch.from_numpy(np.stack([orc.dequant_nvfp4(q[t:t + 1], s[t:t + 1], gsa[t])[0]
                                        for t in range(len(q))])).double()
+    elif fmt == W8A8:
+        a = torch.from_numpy(orc.dequant_act_fp8(*orc.quant_act_fp8(x_bits))).double()
     else:
         a = torch.from_numpy(synth.bf16_bits_to_f32(x_bits)).double()
     lg = torch.from_numpy(logits).double()
@@ -103,11 +105,16 @@ def _torch_reference(fmt, x_bits, logits, packed, k, orc, act_gs=None):
         hq, hs, hg = orc.quant_act_nvfp4(hb, static_gs=None if act_gs is None else act_gs[1])
         hd = np.stack([orc.dequant_nvfp4(hq[r:r + 1], hs[r:r + 1], hg[r])[0] for r in range(len(hq))])
         Hh = torch.from_numpy(hd).double().reshape(T_, E, I)
+    elif fmt == W8A8:
+        T_ = Hh.shape[0]
+        hb = synth.f32_to_bf16_bits(Hh.reshape(-1, I).float().numpy())
+        hd = orc.dequant_act_fp8(*orc.quant_act_fp8(hb))
+        Hh = torch.from_numpy(hd).double().reshape(T_, E, I)
     Y = torch.einsum("ehi,tei->teh", Wd, Hh)
     return torch.einsum("te,teh->th", mask, Y).numpy()
 
 
-@pytest.mark.parametrize("fmt", [FP8, INT4, W4A16, W4A4, BF16])
+@pytest.mark.parametrize("fmt", [FP8, INT4, W4A16, W4A4, BF16, W8A8])
 def test_layer_matches_torch_dense_composition(orc, fmt):
     E, H, I, T, k = 8, 256, 128, 24, 2
     wgu, wd = synth.gen_expert_weights(E, H, I, seed=0)
@@ -116,7 +123,7 @@ def test_layer_matches_torch_dense_composition(orc, fmt):
     packed = orc.pack_experts(fmt, wgu, wd)
     got = orc.moe_layer(fmt, x, lg, packed, k)
     ref = _torch_reference(fmt, x, lg, packed, k, orc)
-    if fmt == W4A4:
+    if fmt in (W4A4, W8A8):
         # the torch side rounds h through fp32 before bf16, the oracle rounds fp64 -> bf16
         # once; a few h elements may land one bf16 ulp apart and change their code
         rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
@@ -125,7 +132,7 @@ def test_layer_matches_torch_dense_composition(orc, fmt):
         np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12 * np.abs(ref).max())
 
 
-@pytest.mark.parametrize("fmt", [FP8, W4A4, BF16])
+@pytest.mark.parametrize("fmt", [FP8, W4A4, BF16, W8A8])
 def test_sparse_equals_dense_masked_definition(orc, fmt):
     E, H, I, T, k = 8, 256, 128, 16, 3
     wgu, wd = synth.gen_expert_weights(E, H, I, seed=1)
@@ -178,3 +185,18 @@ def test_static_activation_scales_layer_matches_torch_composition(orc):
     assert rel < 2e-3, rel  # h rounding to bf16 may differ by an ulp between the two (see above)
     dyn = orc.moe_layer(W4A4, x, lg, packed, k)
     assert not np.allclose(got, dyn)  # the static scales change the result
+
+
+def test_w8a8_differs_from_w8a16_by_the_activation_quantization_only(orc):
+    """W8A8 and W8A16 share the packed weights; W8A8 also quantizes x and h to E4M3 (3 mantissa
+    bits, ~2.6% relative RMS each), so the two layers differ by a few percent, not by a scale
+    factor, a sign or a permutation (each of which would give an O(1) difference)."""
+    E, H, I, T, k = 8, 256, 128, 24, 2
+    wgu, wd = synth.gen_expert_weights(E, H, I, seed=5)
+    x = synth.gen_x(T, H, seed=5)
+    lg = synth.gen_logits(T, E, seed=5)
+    packed = orc.pack_experts(W8A8, wgu, wd)
+    a8 = orc.moe_layer(W8A8, x, lg, packed, k)
+    a16 = orc.moe_layer(FP8, x, lg, packed, k)
+    rel = np.linalg.norm(a8 - a16) / np.linalg.norm(a16)
+    assert 0.01 < rel < 0.08, rel
