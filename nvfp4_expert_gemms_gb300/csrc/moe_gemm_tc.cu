@@ -1,9 +1,9 @@
 // Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05) for the weight-only
 // formats (FP8 W8A16, INT4 W4A16, NVFP4 W4A16).
 //
-// The pages run the experts as "dequantize, then a grouped matmul" (clef-omni-fp8, "How this
-// checkpoint runs"; clef-omni-int4, same section; clef-omni-NVFP4, "How it was made").  Here the
-// dequantization is fused into the GEMM and never reaches HBM:
+// The pages run the experts by dequantizing them, then calling a grouped matmul (clef-omni-fp8,
+// "How this checkpoint runs"; clef-omni-int4, same section; clef-omni-NVFP4, "How it was made").
+// Here the dequantization is fused into the GEMM and never reaches HBM:
 //
 //   weights (packed, HBM) --TMA--> shared memory --converter warps--> bf16 A operand in TMEM
 //   activations (bf16)    --TMA tile / cp.async gather--> shared memory (128-byte swizzle) = B operand

@@ -18,9 +18,11 @@
  *           symmetric, auto_gptq packing (8 codes per int32 along K).
  *   [nvfp4] clef-omni-NVFP4, "How it was made": E2M1 codes two per byte, one E4M3 scale per
  *           16 weights, one fp32 global scale 448*6/amax per expert matrix (gate+up fused as
- *           one matrix), round-to-nearest-even on the FP4 grid, plain min-max scaling.
- *   [w4a4]  clef-flash-NVFP4-Hybrid, layer table: NVFP4 W4A4 = 16-element groups, FP8 group
- *           scales, one FP32 global scale; here computed at run time per activation row.
+ *           one matrix), codes rounded to the nearest FP4 value with ties to even, scales from
+ *           the plain block maxima.
+ *   [w4a4]  clef-flash-NVFP4-Hybrid, layer table: NVFP4 for weights and activations, an E4M3
+ *           scale per 16 elements and one fp32 global scale; here computed at run time per
+ *           activation row.
  *   [bf16]  clef-omni-fp8, "Which Clef-Omni quant should I use?": the BF16 original is the
  *           reference every quant is compared with; its weights are used as stored.
  *   [w8a8]  clef-omni-fp8, "What was quantized": the same FP8 block weights with activations
@@ -252,7 +254,7 @@ void orc_dequant_nvfp4(const uint8_t* packed, const uint8_t* scales, float gs, i
 /* [w4a4], dynamic: each row of a [T, H] bf16 activation gets gs_t = 2688/max(amax_t, 1e-12)
    and is block-quantized like a weight row.  codes [T, H/2], scales [T, H/16], gs [T]. */
 /* The same with one static global scale gs for every row (calibrated ahead of time; the
-   clef-flash-NVFP4-Hybrid layer table's "activation global scales calibrated"): block scales
+   clef-flash-NVFP4-Hybrid layer table calibrates the activations' global scales): block scales
    saturate at 448 and codes at 6 where a block exceeds the calibrated range. */
 void orc_quant_act_nvfp4_static(const uint16_t* x, int T, int H, float gs, uint8_t* codes, uint8_t* scales) {
   float* row = (float*)malloc(sizeof(float) * H);
