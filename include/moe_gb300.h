@@ -22,6 +22,11 @@
  *                           GEMM and combine kernels: the comparison point every quantized
  *                           checkpoint is measured against (clef-omni-fp8, "Which Clef-Omni quant
  *                           should I use?": the BF16 original is the reference row).
+ *   MOE_FMT_FP8_B128_W8A8   the FP8 block weights of MOE_FMT_FP8_B128_W8A16 with activations
+ *                           quantized to E4M3 at run time, one fp32 scale per 1x128 group of a
+ *                           row (clef-omni-fp8, "What was quantized": dynamic FP8 per 1x128 group
+ *                           in engines); x and the gated intermediate h both.  Needs H a multiple
+ *                           of 256 (MOE_ERR_UNSUPPORTED otherwise).
  *
  * Conventions for every call:
  *   - Pointers marked (dev) are device pointers; (host) are host pointers.  All memory is owned
@@ -51,7 +56,8 @@ typedef enum {
   MOE_FMT_INT4_G128_W4A16 = 2,
   MOE_FMT_NVFP4_W4A16 = 3,
   MOE_FMT_NVFP4_W4A4 = 4,
-  MOE_FMT_BF16 = 5
+  MOE_FMT_BF16 = 5,
+  MOE_FMT_FP8_B128_W8A8 = 6
 } moe_format_t;
 
 typedef enum {
@@ -67,7 +73,8 @@ typedef enum {
 /* Canonical tensors inside a packed-expert buffer (index into moe_packed_desc_t arrays).
  * Per format, for all E experts back to back ("gu" = fused gate/up [2I, H] with gate rows
  * 0..I-1 then up rows I..2I-1, "d" = down [H, I]; torch Linear orientation [out, in]):
- *   FP8:   GU_A = codes u8 [E, 2I, H]      GU_B = scale_inv f32 [E, 2I/128, H/128]
+ *   FP8 (W8A16 and W8A8):
+ *          GU_A = codes u8 [E, 2I, H]      GU_B = scale_inv f32 [E, 2I/128, H/128]
  *          D_A  = codes u8 [E, H, I]       D_B  = scale_inv f32 [E, H/128, I/128]
  *   INT4:  GU_A = qweight i32 [E, H/8, 2I] GU_B = scales f16 [E, H/128, 2I]
  *          D_A  = qweight i32 [E, I/8, H]  D_B  = scales f16 [E, I/128, H]
@@ -195,6 +202,14 @@ moe_status_t moe_debug_quant_act(const void* x, int T, int H, uint8_t* codes, ui
  * multiplier); codes and scales as above (what moe_layer_forward_static_act feeds the GEMMs). */
 moe_status_t moe_debug_quant_act_static(const void* x, int T, int H, const float* gs_static, uint8_t* codes,
                                         uint8_t* scales, moe_stream_t stream);
+
+/* Dynamic FP8 quantization of bf16 rows x (dev) [T, H] as MOE_FMT_FP8_B128_W8A8 applies it
+ * (clef-omni-fp8, "What was quantized" and "Recipe", the tile rule on a 1x128 group): per group
+ * of 128 consecutive elements of a row, s = 448 / max(amax, 1e-12), codes E4M3(v * s) u8 [T, H]
+ * (round to nearest even, saturating at 448), scale_inv f32 [T, H/128] = 1 / s.  H a multiple
+ * of 128, x 16-byte aligned. */
+moe_status_t moe_debug_quant_act_fp8(const void* x, int T, int H, uint8_t* codes, float* scale_inv,
+                                     moe_stream_t stream);
 
 /* ---- routing without any caller workspace ----------------------------------------------- */
 

@@ -21,8 +21,9 @@ FMT_INT4 = 2
 FMT_NVFP4_W4A16 = 3
 FMT_NVFP4_W4A4 = 4
 FMT_BF16 = 5
+FMT_FP8_W8A8 = 6
 FORMATS = {"fp8": FMT_FP8, "int4": FMT_INT4, "nvfp4_w4a16": FMT_NVFP4_W4A16, "nvfp4_w4a4": FMT_NVFP4_W4A4,
-           "bf16": FMT_BF16}
+           "bf16": FMT_BF16, "fp8_w8a8": FMT_FP8_W8A8}
 
 MOE_T_GU_A, MOE_T_GU_B, MOE_T_D_A, MOE_T_D_B, MOE_T_GU_GS, MOE_T_D_GS, MOE_T_GU_BT, MOE_T_D_BT = range(8)
 
@@ -30,7 +31,7 @@ EXPORTS = ("moe_packed_size", "moe_pack_experts", "moe_workspace_size", "moe_lay
            "moe_workspace_size_host_io", "moe_layer_forward_host", "moe_get_device_error", "moe_status_string",
            "moe_debug_route", "moe_debug_dequant", "moe_debug_quant_act", "moe_kernel_launch_count",
            "moe_time_next_step", "moe_layer_forward_static_act", "moe_calibrate_act_scales",
-           "moe_debug_quant_act_static")
+           "moe_debug_quant_act_static", "moe_debug_quant_act_fp8")
 
 
 class PackedDesc(C.Structure):
@@ -74,6 +75,7 @@ def lib() -> C.CDLL:
         L.moe_debug_dequant.argtypes = [PD, P, I32, I32, P, P]
         L.moe_debug_quant_act.argtypes = [P, I32, I32, P, P, P, P]
         L.moe_debug_quant_act_static.argtypes = [P, I32, I32, P, P, P, P]
+        L.moe_debug_quant_act_fp8.argtypes = [P, I32, I32, P, P, P]
         L.moe_layer_forward_static_act.argtypes = [P, P, I32, PD, P, I32, P, P, P, SZ, P]
         L.moe_calibrate_act_scales.argtypes = [P, P, I32, PD, P, I32, P, P, SZ, P]
         L.moe_kernel_launch_count.restype = C.c_uint64
@@ -225,6 +227,17 @@ def moe_debug_quant_act_static(x, gs_static, stream=None):
     return q, s
 
 
+def moe_debug_quant_act_fp8(x, stream=None):
+    """E4M3 codes [T, H] and fp32 scale_inv [T, H/128] of x's rows, one scale per 1x128 group."""
+    import torch
+
+    T, H = (int(s) for s in x.shape)
+    q = torch.empty((T, H), dtype=torch.uint8, device=x.device)
+    s = torch.empty((T, H // 128), dtype=torch.float32, device=x.device)
+    _check(lib().moe_debug_quant_act_fp8(_ptr(x), T, H, _ptr(q), _ptr(s), _stream(stream)), "moe_debug_quant_act_fp8")
+    return q, s
+
+
 def moe_debug_quant_act(x, stream=None):
     import torch
 
@@ -253,7 +266,7 @@ def packed_view(desc: PackedDesc, packed, which: int):
         return raw.view(E, N // 128, K // 256, 128, 16)
     if fmt == FMT_BF16:
         return raw.view(torch.bfloat16).view(E, N, K)
-    if fmt == FMT_FP8:
+    if fmt in (FMT_FP8, FMT_FP8_W8A8):
         return raw.view(E, N, K) if which in (MOE_T_GU_A, MOE_T_D_A) else raw.view(torch.float32).view(
             E, N // 128, K // 128)
     if fmt == FMT_INT4:

@@ -5,6 +5,7 @@
 #include <atomic>
 
 #include "moe_internal.cuh"
+#include "moe_w8a8.cuh"
 
 namespace moe {
 
@@ -47,7 +48,14 @@ WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
     L.hs = take((size_t)sf_plane_rows(R) * I / 16);
     L.hg = take(4 * R);
   }
-  if (fmt != MOE_FMT_NVFP4_W4A4 && tc_row_block(fmt, T, k, E) >= kTcPermuteFromRows) L.xp = take(2 * R * H);
+  if (fmt == MOE_FMT_FP8_B128_W8A8) {  // E4M3 codes per permuted row + group-major 1x128 scales
+    L.xq = take(R * H);
+    L.xs = take(4 * (size_t)sf_plane_rows(R) * (H / 128));
+    L.hq = take(R * I);
+    L.hs = take(4 * (size_t)sf_plane_rows(R) * (I / 128));
+  }
+  if (fmt != MOE_FMT_NVFP4_W4A4 && fmt != MOE_FMT_FP8_B128_W8A8 && tc_row_block(fmt, T, k, E) >= kTcPermuteFromRows)
+    L.xp = take(2 * R * H);
   if (host_io) {
     L.x_stage = take(2 * (size_t)T * H);
     L.lg_stage = take(4 * (size_t)T * E);
@@ -57,7 +65,7 @@ WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
   return L;
 }
 
-static bool fmt_ok(int f) { return f >= MOE_FMT_FP8_B128_W8A16 && f <= MOE_FMT_BF16; }
+static bool fmt_ok(int f) { return f >= MOE_FMT_FP8_B128_W8A16 && f <= MOE_FMT_FP8_B128_W8A8; }
 
 static bool desc_ok(const moe_packed_desc_t* d) {
   return d && fmt_ok(d->fmt) && d->E >= 1 && d->E <= kMaxE && d->H >= 128 && d->I >= 128 && d->H % 128 == 0 &&
@@ -100,13 +108,16 @@ static moe_status_t forward_checked(const void* x, const float* logits, int T, c
   if (!aligned(ws, 256) || !aligned(x, 16) || !aligned(out, calibrate ? 4 : 16) || !aligned(packed, 256))
     return MOE_ERR_INVALID_ARG;
   if (T > 0 && x == out) return MOE_ERR_INVALID_ARG;
+  if (d->fmt == MOE_FMT_FP8_B128_W8A8 && !w8a8_supported(*d)) return MOE_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(d->fmt, d->E, d->H, d->I, T, k, host_io_layout);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   const moe_status_t dv = device_ok();
   if (dv != MOE_OK) return dv;
   char* w = (char*)ws;
-  const int rb =
-      d->fmt != MOE_FMT_NVFP4_W4A4 ? tc_row_block(d->fmt, T, k, d->E) : fp4_supported(*d) ? fp4_row_block() : simt_row_block();
+  const int rb = d->fmt == MOE_FMT_FP8_B128_W8A8 ? w8a8_row_block()
+                 : d->fmt != MOE_FMT_NVFP4_W4A4  ? tc_row_block(d->fmt, T, k, d->E)
+                 : fp4_supported(*d)             ? fp4_row_block()
+                                                 : simt_row_block();
   RoutePrelude pre;
   if (d->fmt == MOE_FMT_FP8_B128_W8A16 && rb == fp8dec_row_block()) {  // FP8 decode path needs row maxima
     pre.zero_u32 = (unsigned*)(w + L.hmax);
@@ -143,6 +154,7 @@ moe_status_t moe_packed_size(int fmt, int E, int H, int I, moe_packed_desc_t* d)
   size_t sz[MOE_T_COUNT] = {0};
   switch (fmt) {
     case MOE_FMT_FP8_B128_W8A16:
+    case MOE_FMT_FP8_B128_W8A8:  // the same stored weights
       sz[MOE_T_GU_A] = e * gu;
       sz[MOE_T_GU_B] = e * gu / (128 * 128) * 4;
       sz[MOE_T_D_A] = e * dn;
@@ -330,6 +342,17 @@ moe_status_t moe_debug_quant_act_static(const void* x, int T, int H, const float
   if (dv != MOE_OK) return dv;
   return cuda_status(launch_quant_rows((const __nv_bfloat16*)x, nullptr, 1, T, H, codes, scales, nullptr,
                                        (cudaStream_t)stream, false, 0, gs_static));
+}
+
+moe_status_t moe_debug_quant_act_fp8(const void* x, int T, int H, uint8_t* codes, float* scale_inv,
+                                     moe_stream_t stream) {
+  if (T < 0 || H < 128 || H % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !codes || !scale_inv || !aligned(x, 16) || !aligned(codes, 4) || !aligned(scale_inv, 4)))
+    return MOE_ERR_INVALID_ARG;
+  const moe_status_t dv = device_ok();
+  if (dv != MOE_OK) return dv;
+  return cuda_status(
+      launch_quant_fp8_rows((const __nv_bfloat16*)x, nullptr, 1, T, H, codes, scale_inv, 0, (cudaStream_t)stream));
 }
 
 moe_status_t moe_debug_quant_act(const void* x, int T, int H, uint8_t* codes, uint8_t* scales, float* gs,

@@ -7,6 +7,7 @@
 // (clef-omni-NVFP4, "How it was made"; clef-omni-fp8, "How this checkpoint runs"); here the
 // dequantization happens inside the GEMM and the bf16 copy of the weights never exists.
 #include "moe_formats.cuh"
+#include "moe_w8a8.cuh"
 
 namespace moe {
 
@@ -211,6 +212,8 @@ cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const
     launch_quant_rows(x, nullptr, 1, T, d.H, (uint8_t*)(ws + L.xq), (uint8_t*)(ws + L.xs), (float*)(ws + L.xg), s,
                       false, 0, act_gs);
     e = run_simt<MOE_FMT_NVFP4_W4A16, true>(d, packed, x, T, k, L, ws, ev, s, act_gs ? act_gs + 1 : nullptr);
+  } else if (d.fmt == MOE_FMT_FP8_B128_W8A8) {
+    e = launch_experts_w8a8(d, packed, x, T, k, L, ws, ev, s);
   } else if (d.fmt == MOE_FMT_FP8_B128_W8A16 && row_block == fp8dec_row_block()) {
     e = launch_experts_fp8dec(d, packed, x, T, k, L, ws, ev, s);
   } else {

@@ -324,7 +324,7 @@ cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, co
       if (e != cudaSuccess) return e;
       continue;
     }
-    if (d.fmt == MOE_FMT_FP8_B128_W8A16) {
+    if (d.fmt == MOE_FMT_FP8_B128_W8A16 || d.fmt == MOE_FMT_FP8_B128_W8A8) {
       pack_fp8_kernel<<<dim3(K / 128, N / 128, E), 256, 0, s>>>(w, N, K, a, (float*)b);
     } else if (d.fmt == MOE_FMT_INT4_G128_W4A16) {
       pack_int4_kernel<<<dim3(N / 128, K / 128, E), 128, 0, s>>>(w, N, K, (uint32_t*)a, (__half*)b);
@@ -364,7 +364,8 @@ cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e
                            cudaStream_t s) {
   const MatView m = mat_view(d, packed, which);
   const unsigned blocks = (unsigned)(((size_t)m.N * m.K / 8 + 255) / 256);
-  if (d.fmt == MOE_FMT_FP8_B128_W8A16) dequant_kernel<MOE_FMT_FP8_B128_W8A16><<<blocks, 256, 0, s>>>(m, e, out);
+  if (d.fmt == MOE_FMT_FP8_B128_W8A16 || d.fmt == MOE_FMT_FP8_B128_W8A8)
+    dequant_kernel<MOE_FMT_FP8_B128_W8A16><<<blocks, 256, 0, s>>>(m, e, out);
   else if (d.fmt == MOE_FMT_BF16) dequant_kernel<MOE_FMT_BF16><<<blocks, 256, 0, s>>>(m, e, out);
   else if (d.fmt == MOE_FMT_INT4_G128_W4A16) dequant_kernel<MOE_FMT_INT4_G128_W4A16><<<blocks, 256, 0, s>>>(m, e, out);
   else dequant_kernel<MOE_FMT_NVFP4_W4A16><<<blocks, 256, 0, s>>>(m, e, out);

@@ -54,7 +54,7 @@ def test_packed_tensor_sizes_equal_oracle_outputs(orc):
     import synth
 
     wgu, wd = synth.gen_expert_weights(2, 256, 128, seed=0)
-    for fmt_name, fid in (("fp8", 1), ("int4", 2), ("nvfp4_w4a16", 3)):
+    for fmt_name, fid in (("fp8", 1), ("int4", 2), ("nvfp4_w4a16", 3), ("fp8_w8a8", 6)):
         p = orc.pack_experts(fid, wgu, wd)
         d = M.moe_packed_size(fmt_name, 2, 256, 128)
         assert int(d.size[M.MOE_T_GU_A]) == p["gu"][0].nbytes
@@ -89,3 +89,27 @@ def test_workspace_grows_with_tokens():
     b = M.moe_workspace_size(d, 16384, 8)
     assert b > a > 0
     assert M.moe_workspace_size_host_io(d, 16, 8) > M.moe_workspace_size(d, 16, 8)
+
+
+def test_w8a8_layout_and_workspace():
+    """W8A8 stores the W8A16 FP8 tensors unchanged; its workspace adds the E4M3 codes and the
+    1x128-group scales of x and h for every permuted row; H not a multiple of 256 is refused
+    by the forward pass before anything is launched."""
+    E, H, I, T, k = 128, 2048, 768, 4096, 8
+    a, b = M.moe_packed_size("fp8", E, H, I), M.moe_packed_size("fp8_w8a8", E, H, I)
+    assert b.fmt == M.FMT_FP8_W8A8 and a.bytes == b.bytes
+    assert [int(a.offset[i]) for i in range(8)] == [int(b.offset[i]) for i in range(8)]
+    R = T * k
+    sf_rows = R + 128
+    act = R * H + 4 * sf_rows * (H // 128) + R * I + 4 * sf_rows * (I // 128)
+    assert M.moe_workspace_size(b, T, k) >= act
+    assert M.moe_workspace_size(b, T, k) > M.moe_workspace_size(b, T // 2, k)
+    lib = M.lib()
+    d = M.PackedDesc()
+    assert lib.moe_packed_size(6, 8, 384, 128, C.byref(d)) == 0  # packing and layout: any multiple of 128
+    n = C.c_size_t()
+    assert lib.moe_workspace_size(C.byref(d), 16, 2, C.byref(n)) == 0
+    st = lib.moe_layer_forward(C.c_void_p(256), C.c_void_p(256), 16, C.byref(d), C.c_void_p(256), 2,
+                               C.c_void_p(512), C.c_void_p(1024), n.value, None)
+    assert st == 2  # MOE_ERR_UNSUPPORTED: H = 384 is not a multiple of 256
+    assert lib.moe_debug_quant_act_fp8(C.c_void_p(256), 4, 200, C.c_void_p(512), C.c_void_p(1024), None) == 1
