@@ -33,10 +33,11 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s per format; HBM GB/s & tensor-pipe util vs GB300 peak"
-FMT_ID = {"fp8": 1, "int4": 2, "nvfp4_w4a16": 3, "nvfp4_w4a4": 4, "bf16": 5}
+FMT_ID = {"fp8": 1, "int4": 2, "nvfp4_w4a16": 3, "nvfp4_w4a4": 4, "bf16": 5, "fp8_w8a8": 6}
 # dense tensor rate of each format's MMA operands relative to bf16 (nominal GB300 figures:
-# bf16 2.25, fp4 13.5 PFLOP/s); W8A16 / W4A16 run bf16 operands after dequantization
-TENSOR_RATIO = {"fp8": 1.0, "int4": 1.0, "nvfp4_w4a16": 1.0, "nvfp4_w4a4": 13.5 / 2.25, "bf16": 1.0}
+# bf16 2.25, fp8 4.5, fp4 13.5 PFLOP/s); W8A16 / W4A16 run bf16 operands after dequantization
+TENSOR_RATIO = {"fp8": 1.0, "int4": 1.0, "nvfp4_w4a16": 1.0, "nvfp4_w4a4": 13.5 / 2.25, "bf16": 1.0,
+                "fp8_w8a8": 4.5 / 2.25}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -46,7 +47,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4, 5, 6, 7])
+    p.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4, 5, 6, 7, 8])
     p.add_argument("--tokens", type=int, default=None, help="tokens per step (default: the config's largest)")
     p.add_argument("--layers", type=int, default=None, help="layers per step (default 48)")
     p.add_argument("--seed", type=int, default=0)
@@ -525,7 +526,7 @@ def main():
                "seconds": round(spent, 1), "cpu_model": cpu_model(), "nproc": os.cpu_count()}
     if rank == 0:
         dtype = {"fp8": "f32 (e4m3 x bf16 products)", "int4": "f32", "nvfp4_w4a16": "f32",
-                 "nvfp4_w4a4": "f32", "bf16": "f32 (bf16 products)"}[c["fmt"]]
+                 "nvfp4_w4a4": "f32", "bf16": "f32 (bf16 products)", "fp8_w8a8": "f32 (e4m3 x e4m3 products)"}[c["fmt"]]
         line = dict(base, value=round(r["value"], 1), ms_per_step=round(r["ms_per_step"], 4), dtype=dtype,
                     roofline=r["roofline"], cpu_baseline=cpu, e2e=r["e2e"], gpu_launches=r["gpu_launches"],
                     clocks=r["clocks"], layer=r["layer"], step_ms=r["step_ms"])

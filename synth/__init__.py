@@ -127,6 +127,8 @@ CONFIGS = {
     6: dict(name="bf16", fmt="bf16", T=[16, 4096], H=2048, I=768, E=128, k=8, zipf=1.1, layers=48),
     5: dict(name="mixed-fp8-nvfp4-w4a4", fmt="nvfp4_w4a4", T=[16, 16384], H=2048, I=768, E=128, k=8, zipf=1.1,
             layers=48, fp8_fraction=17 / 32),
+    # FP8 block weights with FP8 activations (one scale per 1x128 group), the large-batch workload
+    8: dict(name="fp8-w8a8", fmt="fp8_w8a8", T=[16384], H=2048, I=768, E=128, k=8, zipf=1.1, layers=48),
 }
 
 
