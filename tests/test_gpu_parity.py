@@ -207,6 +207,43 @@ def test_quant_act_static_bit_exact(orc, K):
     assert np.array_equal(q.cpu().numpy(), rq)
 
 
+def test_quant_act_fp8_bit_exact(orc):
+    """W8A8 activation quantizer (one E4M3 scale per 1x128 group of a row): codes and fp32
+    scale_inv equal the oracle's, including an all-zero group and a tiny group whose codes are
+    negative zeros."""
+    x = synth.gen_x(37, 512, seed=31)
+    x[3, 128:256] = 0
+    x[5, :128] = synth.f32_to_bf16_bits(np.full(128, -1e-30, np.float32))
+    q, s = M.moe_debug_quant_act_fp8(dev_bf16(x))
+    torch.cuda.synchronize()
+    rq, rs = orc.quant_act_fp8(x)
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert s.cpu().numpy().tobytes() == rs.tobytes()
+
+
+def test_quant_act_fp8_hand_worked_row():
+    """The hand-worked two-group row of tests/golden/fp8_act_group_example.txt (an RNE tie, a
+    subnormal tie, the same value coded differently under the two group scales)."""
+    row = np.zeros((1, 256), np.float32)
+    row[0, [0, 1, 4, 7, 128, 129]] = [3.5, -0.75, 0.07421875, 2.288818359375e-05, 0.21875, -0.109375]
+    q, s = M.moe_debug_quant_act_fp8(dev_bf16(synth.f32_to_bf16_bits(row)))
+    q = q.cpu().numpy()[0]
+    assert [int(q[c]) for c in (0, 1, 4, 7, 128, 129)] == [0x7E, 0xEC, 0x52, 0x02, 0x7E, 0xF6]
+    assert s.cpu().numpy().tolist() == [[0.0078125, 0.00048828125]]
+
+
+def test_w8a8_pack_is_the_fp8_pack():
+    """W8A8 stores the W8A16 FP8 tensors: the canonical tensors of the two packed buffers are
+    identical (the alignment padding between them is never written)."""
+    E, H, I = 2, 512, 256
+    wgu, wd = synth.gen_expert_weights(E, H, I, seed=9)
+    a = M.MoELayer("fp8", dev_bf16(wgu), dev_bf16(wd))
+    b = M.MoELayer("fp8_w8a8", dev_bf16(wgu), dev_bf16(wd))
+    torch.cuda.synchronize()
+    for which in (M.MOE_T_GU_A, M.MOE_T_GU_B, M.MOE_T_D_A, M.MOE_T_D_B):
+        assert torch.equal(M.packed_view(a.desc, a.packed, which), M.packed_view(b.desc, b.packed, which))
+
+
 class StaticCase(Case):
     def __init__(self, T, H, I, E, k, seed, zipf=None, h_amax=1.0):
         super().__init__("nvfp4_w4a4", T, H, I, E, k, seed=seed, zipf=zipf)
