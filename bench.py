@@ -483,7 +483,7 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     base = {"metric": METRIC, "unit": "tokens/s", "n_gpus": max(world, args.gpus if world == 1 else world),
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "data": "synthetic (seeded; see DESIGN.md input recipe)",
+            "vs_baseline": None, "data": "synthetic (seeded draws of the synth module: bf16 N(0,1) activations, N(0,0.02) weights, N(0,1) logits)",
             "config": {"workload": describe(c), "format": format_mix(c), "tokens": c["T"], "layers": c["L"],
                        "hidden": c["H"], "intermediate": c["I"], "experts": c["E"], "top_k": c["k"],
                        "l2": "inputs larger than L2: each step streams the distinct weights of all layers",

@@ -28,7 +28,7 @@
  *   [w8a8]  clef-omni-fp8, "What was quantized": the same FP8 block weights with activations
  *           quantized to FP8 at run time, one scale per 1x128 group of a row.
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent:
  *   - E4M3 is the OCP "e4m3fn" variant (max 448, no infinities); encode saturates at 448.
  *   - E2M1 and E4M3 encodes keep the sign of a negative value that rounds to zero.
  *   - A zero tile / matrix / row amax is clamped to 1e-12 before dividing.
