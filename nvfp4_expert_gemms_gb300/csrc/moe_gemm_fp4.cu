@@ -2,8 +2,8 @@
 // (tcgen05.mma kind::mxf4nvf4, E2M1 operands, UE4M3 scale per 16 elements along K).
 //
 // Both operands stay in their packed NVFP4 form end to end (clef-flash-NVFP4-Hybrid, layer
-// table: "16-element groups, FP8 group scales, one FP32 global scale"; weights: clef-omni-NVFP4,
-// "How it was made"):
+// table: NVFP4 activations as well as weights, E4M3 scales per 16 and one fp32 global scale;
+// weights: clef-omni-NVFP4, "How it was made"):
 //   weights      E2M1 codes [N, K/2] + E4M3 block scales [N, K/16] + global scale gs_w (per matrix)
 //   activations  E2M1 codes [rows, K/2] + E4M3 block scales [rows, K/16] + global scale gs_a (per row)
 // The MMA forms sum_k (q_a * bs_a)(q_w * bs_w) exactly in fp32, and the epilogue divides by
