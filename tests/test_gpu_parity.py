@@ -15,7 +15,7 @@ import synth
 pytestmark = pytest.mark.gpu
 
 FMTS = ["fp8", "int4", "nvfp4_w4a16", "nvfp4_w4a4", "bf16"]
-FID = {"fp8": 1, "int4": 2, "nvfp4_w4a16": 3, "nvfp4_w4a4": 4, "bf16": 5}
+FID = {"fp8": 1, "int4": 2, "nvfp4_w4a16": 3, "nvfp4_w4a4": 4, "bf16": 5, "fp8_w8a8": 6}
 REL_FRO, REL_MAX = 1e-2, 2e-2
 
 
@@ -242,6 +242,20 @@ def test_w8a8_pack_is_the_fp8_pack():
     torch.cuda.synchronize()
     for which in (M.MOE_T_GU_A, M.MOE_T_GU_B, M.MOE_T_D_A, M.MOE_T_D_B):
         assert torch.equal(M.packed_view(a.desc, a.packed, which), M.packed_view(b.desc, b.packed, which))
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(24, 256, 128, 8, 2), (700, 512, 256, 16, 4), (1, 256, 128, 8, 2),
+                                       (300, 768, 384, 8, 8)])
+def test_w8a8_layer_small(orc, T, H, I, E, k):
+    """FP8 W8A8 layer (x and h quantized per 1x128 group, both GEMMs on E4M3 x E4M3 MMAs with
+    per-K-block promotion) against the oracle: the tiny config, a ragged multi-tile shape with
+    16 experts, one token, and H = 768 with top-8."""
+    c = Case("fp8_w8a8", T, H, I, E, k, seed=T)
+    got = synth.bf16_bits_to_f32(c.run())
+    idx, _ = orc.route(c.lg, k)
+    p = orc.pack_experts(FID["fp8_w8a8"], c.wgu, c.wd, experts=np.unique(idx))
+    ref = orc.moe_layer(FID["fp8_w8a8"], c.x, c.lg, p, k)
+    check_close(got, ref, f"w8a8 T={T}")
 
 
 class StaticCase(Case):
