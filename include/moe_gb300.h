@@ -24,9 +24,9 @@
  *                           should I use?": the BF16 original is the reference row).
  *   MOE_FMT_FP8_B128_W8A8   the FP8 block weights of MOE_FMT_FP8_B128_W8A16 with activations
  *                           quantized to E4M3 at run time, one fp32 scale per 1x128 group of a
- *                           row (clef-omni-fp8, "What was quantized": dynamic FP8 per 1x128 group
- *                           in engines); x and the gated intermediate h both.  Needs H a multiple
- *                           of 256 (MOE_ERR_UNSUPPORTED otherwise).
+ *                           row (clef-omni-fp8, "What was quantized": serving engines may run the
+ *                           FP8 experts this way); x and the gated intermediate h both.  Needs H
+ *                           a multiple of 256 (MOE_ERR_UNSUPPORTED otherwise).
  *
  * Conventions for every call:
  *   - Pointers marked (dev) are device pointers; (host) are host pointers.  All memory is owned
@@ -207,7 +207,8 @@ moe_status_t moe_debug_quant_act_static(const void* x, int T, int H, const float
  * (clef-omni-fp8, "What was quantized" and "Recipe", the tile rule on a 1x128 group): per group
  * of 128 consecutive elements of a row, s = 448 / max(amax, 1e-12), codes E4M3(v * s) u8 [T, H]
  * (round to nearest even, saturating at 448), scale_inv f32 [T, H/128] = 1 / s.  H a multiple
- * of 128, x 16-byte aligned. */
+ * of 128, x 16-byte aligned, codes and scale_inv 4-byte aligned, all caller-owned; otherwise
+ * MOE_ERR_INVALID_ARG and nothing is enqueued.  Asynchronous on stream. */
 moe_status_t moe_debug_quant_act_fp8(const void* x, int T, int H, uint8_t* codes, float* scale_inv,
                                      moe_stream_t stream);
 
