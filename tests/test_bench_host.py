@@ -89,3 +89,23 @@ def test_clock_record_without_samples(bench, monkeypatch):
     c = bench.Clocks(0)
     c.proc = None  # nvidia-smi could not be started
     assert c.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_reference_arm_runs_the_w8a8_workload():
+    """`bench.py --impl reference --config 8` times the oracle's W8A8 layer on a bounded sample and
+    prints one JSON line naming that workload."""
+    import json
+    import subprocess
+    import sys
+
+    env = dict(os.environ)
+    env.pop("CUDA_VISIBLE_DEVICES", None)
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        env.pop(k, None)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "8",
+                        "--layers", "1", "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
+                       timeout=300, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
+    assert line["config"]["format"] == "fp8_w8a8" and line["cpu_baseline"]["kind"] == "oracle"
