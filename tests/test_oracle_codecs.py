@@ -443,3 +443,28 @@ def test_fp8_act_quant_zero_group(orc):
     assert q[0, 5] == 0x80 and np.all(np.delete(q[0, :128], 5) == 0)
     assert s[0, 0] == np.float32(1.0) / (np.float32(448.0) / np.float32(1e-12))
     assert q[0, 200] == 0x7E and s[0, 1] == np.float32(1.0) / np.float32(448.0)
+
+
+def test_page_figures_whole_checkpoints(orc):
+    """The assumed expert shapes (hidden 2048, intermediate 768: the pages never print them) and
+    the oracle's FP8 and INT4 packings against three more page figures: the INT4 checkpoint's
+    ~19.4 GiB of weights and the FP8 checkpoint's 34.5 GB (each = 48 x 128 packed experts plus
+    the NVFP4 page's 3.1 + 2.4 GiB of non-expert bf16 weights), and experts = 97% of 30B
+    parameters.  A wrong code width, scale type or shape misses these by far more than 2%."""
+    figs = {row[0]: float(row[1]) for row in _lines("page_figures.txt")}
+    L, E, H, I = int(figs["layers"]), int(figs["experts"]), 2048, 768
+    nonexpert = (figs["nonexpert_text_gib"] + figs["nonexpert_towers_gib"]) * 2 ** 30
+    shapes = ((2 * I, H), (H, I))
+    fp8 = int4 = 0
+    for N, K in shapes:
+        w = np.zeros((N, K), np.uint16)
+        c, s = orc.pack_fp8(w)
+        fp8 += c.nbytes + s.nbytes
+        q, s16 = orc.pack_int4(w)
+        int4 += q.nbytes + s16.nbytes + (K // 128) * (N // 8) * 4  # + the checkpoint's qzeros [K/128, N/8] int32
+    fp8_gb = (L * E * fp8 + nonexpert) / 1e9
+    int4_gib = (L * E * int4 + nonexpert) / 2 ** 30
+    assert abs(fp8_gb / figs["fp8_checkpoint_gb"] - 1) < 0.02, fp8_gb
+    assert abs(int4_gib / figs["int4_weights_gib"] - 1) < 0.02, int4_gib
+    expert_params = L * E * 3 * H * I
+    assert abs(expert_params / (figs["total_params_b"] * 1e9) - figs["expert_param_fraction"]) < 0.01
