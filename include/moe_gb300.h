@@ -212,6 +212,14 @@ moe_status_t moe_debug_quant_act_static(const void* x, int T, int H, const float
 moe_status_t moe_debug_quant_act_fp8(const void* x, int T, int H, uint8_t* codes, float* scale_inv,
                                      moe_stream_t stream);
 
+/* Test-only check of device failure detection: enqueues one thread that waits on a barrier
+ * nothing completes, through the bounded wait every GEMM kernel uses (about 2*10^9 SM cycles,
+ * roughly one second).  When the wait gives up it records MOE_ERR_DEVICE_TIMEOUT in the error
+ * word of workspace (dev, 256-byte aligned, any workspace this library sized) and returns;
+ * moe_get_device_error() then reports it, and the CUDA context stays usable.  Returns
+ * MOE_ERR_INVALID_ARG for a null or misaligned workspace. */
+moe_status_t moe_debug_wait_timeout(void* workspace, moe_stream_t stream);
+
 /* ---- routing without any caller workspace ----------------------------------------------- */
 
 /* The pages have no counterpart to this entry point; it exists for callers that cannot obtain

@@ -31,7 +31,7 @@ EXPORTS = ("moe_packed_size", "moe_pack_experts", "moe_workspace_size", "moe_lay
            "moe_workspace_size_host_io", "moe_layer_forward_host", "moe_get_device_error", "moe_status_string",
            "moe_debug_route", "moe_debug_dequant", "moe_debug_quant_act", "moe_kernel_launch_count",
            "moe_time_next_step", "moe_layer_forward_static_act", "moe_calibrate_act_scales",
-           "moe_debug_quant_act_static", "moe_debug_quant_act_fp8")
+           "moe_debug_quant_act_static", "moe_debug_quant_act_fp8", "moe_debug_wait_timeout")
 
 
 class PackedDesc(C.Structure):
@@ -76,6 +76,7 @@ def lib() -> C.CDLL:
         L.moe_debug_quant_act.argtypes = [P, I32, I32, P, P, P, P]
         L.moe_debug_quant_act_static.argtypes = [P, I32, I32, P, P, P, P]
         L.moe_debug_quant_act_fp8.argtypes = [P, I32, I32, P, P, P]
+        L.moe_debug_wait_timeout.argtypes = [P, P]
         L.moe_layer_forward_static_act.argtypes = [P, P, I32, PD, P, I32, P, P, P, SZ, P]
         L.moe_calibrate_act_scales.argtypes = [P, P, I32, PD, P, I32, P, P, SZ, P]
         L.moe_kernel_launch_count.restype = C.c_uint64
@@ -236,6 +237,12 @@ def moe_debug_quant_act_fp8(x, stream=None):
     s = torch.empty((T, H // 128), dtype=torch.float32, device=x.device)
     _check(lib().moe_debug_quant_act_fp8(_ptr(x), T, H, _ptr(q), _ptr(s), _stream(stream)), "moe_debug_quant_act_fp8")
     return q, s
+
+
+def moe_debug_wait_timeout(workspace, stream=None):
+    """Enqueue a device wait that runs out (about a second) and records MOE_ERR_DEVICE_TIMEOUT in
+    the workspace's error word; read it with moe_get_device_error."""
+    _check(lib().moe_debug_wait_timeout(_ptr(workspace), _stream(stream)), "moe_debug_wait_timeout")
 
 
 def moe_debug_quant_act(x, stream=None):
