@@ -7,7 +7,9 @@ dequantization and SiLU*up, down GEMM with fused weighted combine) through every
 intermediate 768, top-8), on one batch of synthetic tokens.  Layers are independent: each
 consumes the same activations with its own router logits.
 
-Default workload: FP8 block-128x128 W8A16 decode at 16 tokens.  Prints one JSON line.
+Default workload: NVFP4 W4A4 (dynamic NVFP4 activations), 16,384 tokens x 48 layers with
+Zipf(1.1)-skewed routing -- the largest single-GPU configuration.  Prints one JSON line.
+--config 1 is FP8 block-128x128 W8A16 decode (T = 16, with the T = 1 and 4 sweep points).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--tokens T] [--impl ours|reference]
 Multi-GPU (torchrun): every rank runs its own replica on its own tokens (weak scaling, no
 collective on the data path; one all-reduce of the elapsed time only).
@@ -47,7 +49,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4, 5, 6, 7, 8])
+    p.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5, 6, 7, 8])
     p.add_argument("--tokens", type=int, default=None, help="tokens per step (default: the config's largest)")
     p.add_argument("--layers", type=int, default=None, help="layers per step (default 48)")
     p.add_argument("--seed", type=int, default=0)
@@ -224,8 +226,10 @@ class OracleSample:
         self.desc = (f"{len(self.items)} layer(s) x {self.n_tok} of {T} tokens of the same workload "
                      f"(only routed experts drawn; packing untimed)")
 
-    def run(self, min_seconds=0.0):
-        """Oracle forward over the sample (repeated until min_seconds); returns (tokens/s, seconds)."""
+    def run(self, min_seconds=0.0, nthreads=None):
+        """Oracle forward over the sample (repeated until min_seconds) on nthreads host threads
+        (default: all); returns (tokens/s, seconds)."""
+        nthreads = self.cores() if nthreads is None else nthreads
         spent, tokens = 0.0, 0
         act_gs = None
         if self.c.get("static_act"):  # x's scale from the batch, h's a fixed calibrated-range stand-in
@@ -234,14 +238,17 @@ class OracleSample:
         while True:
             for fid, lg, toks, packed in self.items:
                 t0 = time.perf_counter()
-                self.oracle.moe_layer(fid, self.x, lg, packed, self.c["k"], tokens=toks, act_gs=act_gs)
+                self.oracle.moe_layer(fid, self.x, lg, packed, self.c["k"], tokens=toks, act_gs=act_gs,
+                                      nthreads=nthreads)
                 spent += time.perf_counter() - t0
                 tokens += self.n_tok
             if spent >= min_seconds:
                 return tokens / spent, spent
 
     def cores(self):
-        return self.oracle.max_threads()
+        if not hasattr(self, "_cores"):  # read once: a single-threaded run lowers the OpenMP default
+            self._cores = self.oracle.max_threads()
+        return self._cores
 
 
 def cpu_model():
@@ -494,6 +501,7 @@ def main():
         if rank != 0:
             return
         smp = OracleSample(c, args.seed)
+        smp.cores()
         for _ in range(args.warmup):
             smp.run()
         vals = []
@@ -508,6 +516,7 @@ def main():
                                   "sample": smp.desc, "cpu_model": cpu_model(), "nproc": os.cpu_count()},
                     e2e={"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                          "d2h_bytes_per_step": 0},
+                    sampled_seconds=round(wall, 2), sampled_seconds_per_step=round(wall / max(args.steps, 1), 3),
                     note=(f"CPU oracle timed on the host cores; each step is the bounded sample above "
                           f"({wall:.1f} s wall for {args.steps} steps); ms_per_step extrapolates to the full step"))
         print(json.dumps(line))
@@ -521,11 +530,15 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         smp = OracleSample(c, args.seed)
-        v, spent = smp.run(min_seconds=10.0)
-        cpu = {"value": round(v, 3), "unit": "tokens/s", "cores": smp.cores(), "kind": "oracle", "sample": smp.desc,
-               "seconds": round(spent, 1), "cpu_model": cpu_model(), "nproc": os.cpu_count()}
+        cores = smp.cores()
+        v, spent = smp.run(min_seconds=10.0, nthreads=cores)  # OpenMP over tokens on every core
+        v1, spent1 = smp.run(min_seconds=5.0, nthreads=1)  # and on one core
+        cpu = {"value": round(v, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": smp.desc,
+               "seconds": round(spent, 1), "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+               "single_thread": {"value": round(v1, 3), "cores": 1, "seconds": round(spent1, 1)}}
     if rank == 0:
-        dtype = {"fp8": "f32 (e4m3 x bf16 products)", "int4": "f32", "nvfp4_w4a16": "f32",
+        dtype = {"fp8": ("f32 (e4m3 weight x two-term e4m3 split of the bf16 activations; exact except"
+                         " elements under ~1/1800 of their row maximum)"), "int4": "f32", "nvfp4_w4a16": "f32",
                  "nvfp4_w4a4": "f32", "bf16": "f32 (bf16 products)", "fp8_w8a8": "f32 (e4m3 x e4m3 products)"}[c["fmt"]]
         line = dict(base, value=round(r["value"], 1), ms_per_step=round(r["ms_per_step"], 4), dtype=dtype,
                     roofline=r["roofline"], cpu_baseline=cpu, e2e=r["e2e"], gpu_launches=r["gpu_launches"],

@@ -111,21 +111,42 @@ typedef struct {
   uint64_t size[MOE_T_COUNT];    /* byte size of each canonical tensor (0 if absent) */
 } moe_packed_desc_t;
 
-/* Fill *desc with the packed layout for (fmt, E, H, I).  Host only; no CUDA calls. */
+/* Fill *desc with the packed layout for (fmt, E, H, I).  Host only; no CUDA calls.
+ * The tensors and their sizes are the checkpoint tensors the pages name for each format:
+ * weight + weight_scale_inv (clef-omni-fp8, "What was quantized"), qweight + scales in
+ * auto_gptq packing (clef-omni-int4, "What was quantized"), weight_packed + weight_scale +
+ * weight_global_scale (clef-omni-NVFP4, "How it was made"), for the fused gate/up and the down
+ * matrix of each expert (clef-omni-int4, "How this checkpoint runs": the experts of a layer are
+ * stacked and run as one grouped matmul).
+ * Errors: MOE_ERR_INVALID_ARG for a null desc, an unknown format, E outside 1..256, or H, I not
+ * positive multiples of 128 (desc is then zeroed apart from the echoed arguments). */
 moe_status_t moe_packed_size(int fmt, int E, int H, int I, moe_packed_desc_t* desc);
 
 /* Quantize and pack bf16 expert weights on the GPU (stream-ordered, asynchronous).
- *   w_gate_up (dev) bf16 [E, 2I, H]; w_down (dev) bf16 [E, H, I]; packed (dev) desc->bytes.
- * Results are bit-identical to the quantizers defined above (per-tile / per-group / per-block
- * amax scaling, round-to-nearest-even).  Pages: see the format list at the top. */
+ *   w_gate_up (dev) bf16 [E, 2I, H]; w_down (dev) bf16 [E, H, I]; packed (dev) desc->bytes,
+ *   256-byte aligned; all three caller-owned and not modified apart from packed.
+ * Results are bit-identical to the quantizers the pages give (per-tile / per-group / per-block
+ * amax scaling, round-to-nearest-even): FP8 per 128x128 tile, s = 448/amax (clef-omni-fp8,
+ * "Recipe"); INT4 per 128-group along K, fp16 scale amax/7, codes + 8 (clef-omni-int4, "What was
+ * quantized"); NVFP4 16-element blocks, E4M3 block scales, one fp32 global scale per matrix with
+ * gate and up sharing it (clef-omni-NVFP4, "How it was made").
+ * Errors: MOE_ERR_INVALID_ARG for a bad desc (or one not produced by moe_packed_size for its
+ * own arguments), a null or misaligned pointer; MOE_ERR_UNSUPPORTED on a device other than
+ * sm_103; MOE_ERR_CUDA if a launch fails.  Nothing is enqueued on an argument error. */
 moe_status_t moe_pack_experts(const moe_packed_desc_t* desc, const void* w_gate_up, const void* w_down,
                               void* packed, moe_stream_t stream);
 
 /* Bytes of device workspace moe_layer_forward needs for T tokens and top_k (host only).
- * The same size also serves moe_debug_route and moe_get_device_error. */
+ * The same size also serves moe_debug_route and moe_get_device_error.  It holds the routing
+ * tables, the permutation and the intermediate h of the grouped matmuls (clef-omni-int4, "How
+ * this checkpoint runs": route, group the tokens by expert, one grouped matmul per projection).
+ * Errors: MOE_ERR_INVALID_ARG for a bad desc, a null bytes, T < 0 or top_k outside 1..min(E, 8). */
 moe_status_t moe_workspace_size(const moe_packed_desc_t* desc, int T, int top_k, size_t* bytes);
 
-/* The forward pass on `stream` (asynchronous; no host synchronisation, no allocation):
+/* The forward pass of one MoE layer (clef-omni-int4, "How this checkpoint runs": the routed
+ * experts of a layer run as one grouped matmul; clef-omni-fp8, "How this checkpoint runs": the
+ * same for the FP8 experts; the gated-MLP experts of the Qwen3-MoE backbone, clef-omni-NVFP4,
+ * "Credits"), on `stream` (asynchronous; no host synchronisation, no allocation):
  *   x (dev) bf16 [T, H]; router_logits (dev) f32 [T, E]; packed (dev) from moe_pack_experts;
  *   out (dev) bf16 [T, H], must not alias x; workspace (dev) >= moe_workspace_size bytes,
  *   256-byte aligned, contents need not be initialised and are overwritten.
@@ -159,47 +180,63 @@ moe_status_t moe_calibrate_act_scales(const void* x, const float* router_logits,
                                       size_t ws_bytes, moe_stream_t stream);
 
 /* Bytes of workspace moe_layer_forward_host needs: moe_workspace_size plus device staging for
- * x, the logits and out (host only). */
+ * x, the logits and out (host only).  Same errors as moe_workspace_size. */
 moe_status_t moe_workspace_size_host_io(const moe_packed_desc_t* desc, int T, int top_k, size_t* bytes);
 
-/* moe_layer_forward with HOST activations: copies x_host bf16 [T, H] and logits_host f32 [T, E]
- * into the workspace, runs the layer, copies the result to out_host bf16 [T, H], all on
- * `stream` and asynchronously (use pinned host memory for overlap; the caller synchronises
- * before reading out_host).  packed stays on the device. */
+/* moe_layer_forward (same passage) with HOST activations: copies x_host bf16 [T, H] and
+ * logits_host f32 [T, E] into the workspace, runs the layer, copies the result to out_host
+ * bf16 [T, H], all on `stream` and asynchronously (use pinned host memory for overlap; the
+ * caller synchronises before reading out_host).  packed stays on the device.  The workspace
+ * must have moe_workspace_size_host_io bytes.  Errors as moe_layer_forward. */
 moe_status_t moe_layer_forward_host(const void* x_host, const float* logits_host, int T,
                                     const moe_packed_desc_t* desc, const void* packed, int top_k,
                                     void* out_host, void* workspace, size_t ws_bytes, moe_stream_t stream);
 
 /* Synchronise `stream`, then read and clear the device error word kept in `workspace`.
- * *code receives MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_FAULT. */
+ * *code receives MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_FAULT.  The pages have no
+ * counterpart: it reports this library's own bounded device waits and bounds checks.
+ * Errors: MOE_ERR_INVALID_ARG for a null pointer; MOE_ERR_CUDA if the copy or sync fails. */
 moe_status_t moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* code);
 
-/* A static English description of a status code. */
+/* A static English description of a status code (library bookkeeping, no page counterpart). */
 const char* moe_status_string(int status);
 
 /* ---- inspection views of individual steps (same kernels as the forward pass) ---------- */
 
-/* Routing and permutation alone: topk_idx i32 [T, k] (descending logits, ties to the lower
- * expert), topk_w f32 [T, k] (renormalised softmax), offsets i32 [E+1], perm i32 [T*k]
+/* Routing and permutation alone, the first step of moe_layer_forward: the router's logits are
+ * left unquantized (clef-omni-fp8, page header and "What was quantized"), and grouping rows by
+ * expert feeds the grouped matmul (clef-omni-int4, "How this checkpoint runs").  Outputs:
+ * topk_idx i32 [T, k] (descending logits, ties to the lower expert), topk_w f32 [T, k]
+ * (renormalised softmax over the k selected logits), offsets i32 [E+1], perm i32 [T*k]
  * (row r holds t*k + j, rows sorted by expert, token, slot), inv i32 [T*k] (row of t*k + j).
- * All (dev).  workspace as for moe_layer_forward. */
+ * All (dev), caller-owned.  workspace as for moe_layer_forward (256-byte aligned).
+ * Errors: MOE_ERR_INVALID_ARG for bad sizes or null pointers; MOE_ERR_WORKSPACE if ws_bytes is
+ * too small; MOE_ERR_UNSUPPORTED off sm_103; MOE_ERR_CUDA if a launch or copy fails. */
 moe_status_t moe_debug_route(const float* router_logits, int T, int E, int top_k, int32_t* topk_idx,
                              float* topk_w, int32_t* offsets, int32_t* perm, int32_t* inv, void* workspace,
                              size_t ws_bytes, moe_stream_t stream);
 
-/* Dequantize one packed matrix to f32 (dev) [N, K]: which = 0 fused gate/up, 1 down.
+/* Dequantize one packed matrix to f32 (dev) [N, K]: which = 0 fused gate/up, 1 down: the
+ * pages' dequantize-then-matmul step (clef-omni-fp8, "How this checkpoint runs"; clef-omni-NVFP4,
+ * "How it was made"), here only an inspection view since the GEMMs dequantize in place.
  * Values are bit-identical to the format's dequantization rule:
- *   FP8 code * scale_inv; INT4 (code - 8) * scale; NVFP4 (e2m1 * e4m3) / global_scale. */
+ *   FP8 code * scale_inv; INT4 (code - 8) * scale; NVFP4 (e2m1 * e4m3) / global_scale.
+ * Errors: MOE_ERR_INVALID_ARG for a bad desc, expert or which, or a null pointer. */
 moe_status_t moe_debug_dequant(const moe_packed_desc_t* desc, const void* packed, int expert, int which,
                                float* out, moe_stream_t stream);
 
 /* Dynamic NVFP4 quantization of bf16 rows x (dev) [T, H]: codes u8 [T, H/2], scales E4M3
- * [T, H/16], gs f32 [T] = 2688 / max(amax(row), 1e-12).  Bit-identical to the W4A4 rule. */
+ * [T, H/16], gs f32 [T] = 2688 / max(amax(row), 1e-12).  Bit-identical to the W4A4 rule (the
+ * weight recipe of clef-omni-NVFP4, "How it was made", applied per activation row; NVFP4
+ * activations: clef-flash-NVFP4-Hybrid, "Quantization details").  x 16-byte aligned.
+ * Errors: MOE_ERR_INVALID_ARG for H not a multiple of 16 or a null pointer. */
 moe_status_t moe_debug_quant_act(const void* x, int T, int H, uint8_t* codes, uint8_t* scales, float* gs,
                                  moe_stream_t stream);
 
 /* The same with one static global scale for every row: gs_static (dev) f32 [1] (the quantize
- * multiplier); codes and scales as above (what moe_layer_forward_static_act feeds the GEMMs). */
+ * multiplier; the calibrated per-tensor activation scale of clef-flash-NVFP4-Hybrid,
+ * "Quantization details"); codes and scales as above (what moe_layer_forward_static_act feeds
+ * the GEMMs).  Errors as moe_debug_quant_act. */
 moe_status_t moe_debug_quant_act_static(const void* x, int T, int H, const float* gs_static, uint8_t* codes,
                                         uint8_t* scales, moe_stream_t stream);
 
@@ -212,8 +249,8 @@ moe_status_t moe_debug_quant_act_static(const void* x, int T, int H, const float
 moe_status_t moe_debug_quant_act_fp8(const void* x, int T, int H, uint8_t* codes, float* scale_inv,
                                      moe_stream_t stream);
 
-/* Test-only check of device failure detection: enqueues one thread that waits on a barrier
- * nothing completes, through the bounded wait every GEMM kernel uses (about 2*10^9 SM cycles,
+/* Test-only check of device failure detection (no page counterpart): enqueues one thread that
+ * waits on a barrier nothing completes, through the bounded wait every GEMM kernel uses (about 2*10^9 SM cycles,
  * roughly one second).  When the wait gives up it records MOE_ERR_DEVICE_TIMEOUT in the error
  * word of workspace (dev, 256-byte aligned, any workspace this library sized) and returns;
  * moe_get_device_error() then reports it, and the CUDA context stays usable.  Returns
@@ -246,10 +283,12 @@ moe_status_t moe_route_noalloc(const float* router_logits, int T, int E, int top
 /* ---- measurement hooks ------------------------------------------------------------------ */
 
 /* Total number of CUDA kernels this library has enqueued in the calling process (all threads,
- * all devices) since it was loaded.  Memsets and copies are not counted. */
+ * all devices) since it was loaded.  Memsets and copies are not counted.  Measurement only; no
+ * page counterpart. */
 uint64_t moe_kernel_launch_count(void);
 
-/* Ask the next moe_layer_forward / moe_layer_forward_host call made by this host thread to
+/* Measurement only (no page counterpart).
+ * Ask the next moe_layer_forward / moe_layer_forward_host call made by this host thread to
  * record `start` right before and `stop` right after the launches of one step, on the call's
  * stream (step 0 = grouped gate/up GEMM, 1 = grouped down GEMM).  The request is consumed by
  * that one call.  Events are cudaEvent_t passed as void*; pass NULL to cancel. */

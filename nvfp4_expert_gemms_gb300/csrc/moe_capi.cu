@@ -15,7 +15,7 @@ static thread_local StepEvents g_pending_events;
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
+WsLayout route_layout(int E, int T, int k) {
   WsLayout L;
   memset(&L, 0, sizeof(L));
   size_t cur = 0;
@@ -36,6 +36,19 @@ WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
   L.perm = take(4 * R);
   L.inv = take(4 * R);
   L.tiles = take(sizeof(TileEntry) * (size_t)(L.max_tiles + 1));
+  L.total = cur;
+  return L;
+}
+
+WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
+  WsLayout L = route_layout(E, T, k);
+  size_t cur = L.total;
+  auto take = [&](size_t bytes) {
+    const size_t o = cur;
+    cur += align256(bytes);
+    return o;
+  };
+  const size_t R = (size_t)T * k;
   L.h = take(2 * R * I);
   L.y = take(2 * R * (size_t)H);
   L.xmax = take(4 * (size_t)T);
@@ -75,7 +88,7 @@ static bool desc_ok(const moe_packed_desc_t* d) {
 static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 // The kernels are built for sm_103a only; refuse other devices before launching anything.
-static moe_status_t device_ok() {
+moe_status_t device_ok() {
   static int checked[64];  // 0 unknown, 1 ok, 2 unsupported
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;

@@ -82,6 +82,12 @@ struct WsLayout {
 };
 
 WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io);
+// The routing part alone (error word, top-k, histograms, offsets, permutation, tile table): the
+// prefix every ws_layout starts with, and all that routing by itself needs.
+WsLayout route_layout(int E, int T, int k);
+// MOE_OK on an sm_103 device (the only target the kernels are built for), else
+// MOE_ERR_UNSUPPORTED (or MOE_ERR_CUDA if the device cannot be queried).
+moe_status_t device_ok();
 
 // ---- launches (each returns cudaGetLastError() after enqueueing) -------------------------
 // Work folded into the first routing launch: zero the h row maxima and (optionally) record the

@@ -1,8 +1,8 @@
 // Routing: warp-level top-k with a renormalised softmax, per-expert histogram, exclusive
 // scan, and a deterministic permutation of (token, slot) rows by (expert, token, slot).
 //
-// The pages route with the model's BF16 router (clef-omni-fp8, page header: "router ... stay
-// BF16") and run the experts as one grouped matmul per layer (clef-omni-fp8, "How this
+// The pages leave the router unquantized (clef-omni-fp8, page header and "What was
+// quantized") and run the experts as one grouped matmul per layer (clef-omni-fp8, "How this
 // checkpoint runs"; clef-omni-int4, same section); grouping rows by expert is what a grouped
 // matmul consumes.  Three launches, no atomics whose order reaches the output:
 //   1. route_topk_kernel   one warp per token; per-block expert histogram in shared memory

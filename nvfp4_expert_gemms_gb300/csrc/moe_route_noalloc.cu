@@ -16,8 +16,6 @@
 // the one array and it keeps the previous call's contents; everything a call reads is written
 // earlier in the same call, and the error word is cleared by the call's first launch.  Calls
 // whose work overlaps on the GPU (on different streams) race on the array.
-#include <string.h>
-
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -26,34 +24,6 @@ namespace moe {
 namespace {
 
 static __device__ __align__(256) unsigned char g_route_scratch[MOE_ROUTE_NOALLOC_SCRATCH_BYTES];
-
-size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
-
-// The routing part of the forward-pass workspace layout, packed into the static array.
-WsLayout route_only_layout(int E, int T, int k) {
-  WsLayout L;
-  memset(&L, 0, sizeof(L));
-  size_t cur = 0;
-  auto take = [&](size_t bytes) {
-    const size_t o = cur;
-    cur += a256(bytes);
-    return o;
-  };
-  const size_t R = (size_t)T * k;
-  L.nb = T > 0 ? (T + kRouteTB - 1) / kRouteTB : 1;
-  L.max_tiles = (int)(R / kMinRowBlock + (R < (size_t)E ? R : (size_t)E) + 1);
-  L.err = take(256);
-  L.topk_idx = take(4 * R);
-  L.topk_w = take(4 * R);
-  L.blkcnt = take(4 * (size_t)L.nb * E);
-  L.blkbase = take(4 * (size_t)L.nb * E);
-  L.offsets = take(4 * (size_t)(E + 1));
-  L.perm = take(4 * R);
-  L.inv = take(4 * R);
-  L.tiles = take(sizeof(TileEntry) * (size_t)(L.max_tiles + 1));
-  L.total = cur;
-  return L;
-}
 
 std::mutex g_mu;
 char* g_scratch[64];  // device address of g_route_scratch, per device ordinal
@@ -84,8 +54,11 @@ extern "C" moe_status_t moe_route_noalloc(const float* logits, int T, int E, int
     return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!logits || !topk_idx || !topk_w || !perm || !inv)) return MOE_ERR_INVALID_ARG;
   if (T > MOE_ROUTE_NOALLOC_MAX_TOKENS) return MOE_ERR_WORKSPACE;
-  const WsLayout L = route_only_layout(E, T, top_k);
+  // the same routing layout the workspace-based entry points use, packed into the static array
+  const WsLayout L = route_layout(E, T, top_k);
   if (L.total > (size_t)MOE_ROUTE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+  const moe_status_t dv = device_ok();
+  if (dv != MOE_OK) return dv;
   char* w = nullptr;
   const moe_status_t st = scratch_address(&w);
   if (st != MOE_OK) return st;

@@ -407,6 +407,25 @@ def test_layer_full_size_sampled(orc, fmt, T, zipf, sample):
     check_close(got, c.oracle(orc, tokens=toks), f"{fmt} T={T}")
 
 
+@pytest.mark.parametrize("fmt,T", [("fp8", 1), ("fp8", 4), ("int4", 1), ("int4", 16), ("int4", 64)])
+def test_layer_full_size_decode_all_tokens(orc, fmt, T):
+    """The decode points of the FP8 and INT4 sweeps at the full 2048 / 768 / 128-expert / top-8
+    shape, every token checked: the small row blocks whose CTAs walk several weight tiles each."""
+    c = Case(fmt, T, FULL["H"], FULL["I"], FULL["E"], FULL["k"], seed=T + 1)
+    check_close(synth.bf16_bits_to_f32(c.run()), c.oracle(orc), f"{fmt} T={T}")
+
+
+def test_w8a8_layer_full_size_sampled(orc):
+    """FP8 W8A8 at 16,384 tokens with Zipf-skewed routing: every CTA of both GEMMs takes many work
+    items (the persistent item loop, the shared work counter, the promotion buffers reused across
+    items); 48 sampled tokens against the oracle."""
+    T = 16384
+    c = Case("fp8_w8a8", T, FULL["H"], FULL["I"], FULL["E"], FULL["k"], seed=77, zipf=1.1)
+    got = synth.bf16_bits_to_f32(c.run())
+    toks = np.sort(np.random.default_rng(5).choice(T, 48, replace=False)).astype(np.int32)
+    check_close(got[toks], c.oracle(orc, tokens=toks), "w8a8 full size")
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("T,E,k", [(64, 8, 2), (45, 16, 4), (300, 32, 8), (700, 4, 2)])
 def test_layer_k256_shapes(orc, fmt, T, E, k):

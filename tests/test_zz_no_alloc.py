@@ -4,8 +4,9 @@ Plugins run by an engine that owns every device allocation, and serving loops wh
 pool is fixed at start-up, have no way to hand this library a workspace.  This entry point
 keeps its routing scratch in a static device array inside the library instead.  The test
 calls it through the C ABI twice in a row (the array keeps the first call's contents) and
-checks both results against moe_debug_route, the workspace-based entry point: integers
-bit-exact, routing weights within the 1e-6 relative tolerance of the routing parity tests.
+checks both results against moe_debug_route, the workspace-based entry point, and against the
+CPU oracle's routing: integers bit-exact, routing weights within the 1e-6 relative tolerance of
+the routing parity tests.
 
 This file is named to be collected last, so that a run stopping at the first failure has
 already run every other test.
@@ -56,15 +57,23 @@ def _same(a, b):
             assert torch.equal(x, y), i
 
 
-def test_noalloc_route_matches_workspace_route_twice():
+def test_noalloc_route_matches_workspace_route_twice(orc):
     cases = [(2048, 128, 8, 1.1), (37, 16, 4, None)]  # the maximum size, then a small ragged one
     for n, (T, E, k, zipf) in enumerate(cases):
-        logits = torch.from_numpy(synth.gen_logits(T, E, seed=100 + n, zipf_alpha=zipf)).cuda()
+        lg = synth.gen_logits(T, E, seed=100 + n, zipf_alpha=zipf)
+        logits = torch.from_numpy(lg).cuda()
         st, got = _noalloc(logits, k)
         assert st == 0, M.moe_status_string(st)
         want = _with_workspace(logits, k)
         torch.cuda.synchronize()
         _same(got, want)
+        # and against the CPU oracle's routing and permutation
+        ridx, rw = orc.route(lg, k)
+        roff, rperm, rinv = orc.permute(ridx, E)
+        idx, w, off, perm, inv = (t.cpu().numpy() for t in got)
+        assert np.array_equal(idx, ridx) and np.array_equal(off, roff)
+        assert np.array_equal(perm, rperm) and np.array_equal(inv, rinv)
+        np.testing.assert_allclose(w, rw, rtol=1e-6, atol=0)
 
 
 def test_noalloc_route_rejects_too_many_tokens():
