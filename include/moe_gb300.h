@@ -84,12 +84,14 @@ typedef enum {
  *          D_A  = weight_packed u8 [E, H, I/2]  D_B = weight_scale E4M3 [E, H, I/16]
  *          GU_GS / D_GS = weight_global_scale f32 [E] (the quantize multiplier 2688/amax)
  *   BF16:  GU_A = bf16 [E, 2I, H]               D_A = bf16 [E, H, I]  (the weights as given)
- *   NVFP4 W4A4 with H and I multiples of 256 also carries a copy of each weight_scale tensor
- *   re-tiled for the block-scaled tensor-core path, every (128-row tile, 256-column chunk) one
- *   contiguous 2 KB block:
- *          GU_BT = E4M3 [E, 2I/128, H/256, 128, 16]   D_BT = E4M3 [E, H/128, I/256, 128, 16]
- *          (element [e, t, c, r, j] = weight_scale[e, 128 t + r, 16 c + j]); written by
- *          moe_pack_experts next to the canonical tensors, not part of the checkpoint format.
+ *   NVFP4 W4A4 also carries a copy of each weight_scale tensor in the order the block-scaled
+ *   tensor-core MMA reads it, one contiguous 2 KB block per (128-row tile, 256-column chunk)
+ *   (C = ceil(K / 256) chunks; a last half chunk has its upper 1 KB unused):
+ *          GU_BT = E4M3 [E, 2I/128, C(H), 4, 32, 4, 4]   D_BT = E4M3 [E, H/128, C(I), 4, 32, 4, 4]
+ *          (element [e, t, c, s, l, j, i] = weight_scale[e, 128 t + 32 j + l, 16 c + 4 s + i]:
+ *          per K = 64 step s, 32 rows of 16 bytes, row l holding the four scales of tile rows
+ *          l, l + 32, l + 64, l + 96); written by moe_pack_experts next to the canonical tensors,
+ *          not part of the checkpoint format.
  * Every tensor starts on a 256-byte boundary of the packed buffer. */
 enum {
   MOE_T_GU_A = 0,
@@ -169,12 +171,12 @@ moe_status_t moe_layer_forward_static_act(const void* x, const float* router_log
                                           const float* act_gs, void* out, void* workspace, size_t ws_bytes,
                                           moe_stream_t stream);
 
-/* Calibration of those static scales on one batch (W4A4 with H and I multiples of 256, T >= 1):
+/* Calibration of those static scales on one batch (W4A4, T >= 1):
  * act_gs[0] = 2688 / max |x| over the batch; then x is quantized with it, the gate/up GEMM runs,
  * and act_gs[1] = 2688 / max |h| over every routed row (h in bf16); each amax is clamped to
  * >= 1e-12 as in the dynamic rule.  No output is written; the workspace is that of
  * moe_layer_forward.  act_gs (dev) f32 [2], 4-byte aligned, written stream-ordered.
- * MOE_ERR_UNSUPPORTED for W4A4 shapes outside the block-scaled FP4 path. */
+ * MOE_ERR_INVALID_ARG for T < 1, a null act_gs or a format other than MOE_FMT_NVFP4_W4A4. */
 moe_status_t moe_calibrate_act_scales(const void* x, const float* router_logits, int T, const moe_packed_desc_t* desc,
                                       const void* packed, int top_k, float* act_gs, void* workspace,
                                       size_t ws_bytes, moe_stream_t stream);

@@ -269,8 +269,8 @@ def packed_view(desc: PackedDesc, packed, which: int):
     N, K = (2 * I, H) if gu else (H, I)
     if which in (MOE_T_GU_GS, MOE_T_D_GS):
         return raw.view(torch.float32)
-    if which in (MOE_T_GU_BT, MOE_T_D_BT):
-        return raw.view(E, N // 128, K // 256, 128, 16)
+    if which in (MOE_T_GU_BT, MOE_T_D_BT):  # tensor-memory atom order (include/moe_gb300.h)
+        return raw.view(E, N // 128, (K + 255) // 256, 4, 32, 4, 4)
     if fmt == FMT_BF16:
         return raw.view(torch.bfloat16).view(E, N, K)
     if fmt in (FMT_FP8, FMT_FP8_W8A8):

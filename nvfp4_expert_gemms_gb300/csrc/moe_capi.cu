@@ -51,14 +51,15 @@ WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
   const size_t R = (size_t)T * k;
   L.h = take(2 * R * I);
   L.y = take(2 * R * (size_t)H);
+  L.cnt = take(256);
   L.xmax = take(4 * (size_t)T);
   L.hmax = take(4 * R);
   if (fmt == MOE_FMT_NVFP4_W4A4) {  // activation codes per permuted row (first T rows: per token)
     L.xq = take(R * H / 2);
-    L.xs = take((size_t)sf_plane_rows(R) * H / 16);
+    L.xs = take((size_t)sf_plane_rows(R) * nvfp4_chunks(H) * 16);
     L.xg = take(4 * R);
     L.hq = take(R * I / 2);
-    L.hs = take((size_t)sf_plane_rows(R) * I / 16);
+    L.hs = take((size_t)sf_plane_rows(R) * nvfp4_chunks(I) * 16);
     L.hg = take(4 * R);
   }
   if (fmt == MOE_FMT_FP8_B128_W8A8) {  // E4M3 codes per permuted row + group-major 1x128 scales
@@ -104,6 +105,13 @@ moe_status_t device_ok() {
 
 static moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Whether the format's down GEMM combines the k routing-weighted rows of each token itself
+// (else a separate combine launch follows it).
+static int combine_cols(int fmt, int row_block) {
+  (void)row_block;
+  return fmt == MOE_FMT_NVFP4_W4A4 ? 1 : 0;
+}
+
 // act_gs: null, or the static activation scales (dev, [2], W4A4 only).  calibrate: act_gs is
 // the output of the calibration instead (out unused, fp4 shapes only).
 static moe_status_t forward_checked(const void* x, const float* logits, int T, const moe_packed_desc_t* d,
@@ -114,7 +122,6 @@ static moe_status_t forward_checked(const void* x, const float* logits, int T, c
   if (act_gs && (d->fmt != MOE_FMT_NVFP4_W4A4 || !aligned(act_gs, 4))) return MOE_ERR_INVALID_ARG;
   if (calibrate) {
     if (!act_gs || T < 1) return MOE_ERR_INVALID_ARG;
-    if (!fp4_supported(*d)) return MOE_ERR_UNSUPPORTED;
     out = (void*)act_gs;  // checked below like an output; never written as one
   }
   if (T > 0 && (!x || !logits || !packed || !out || !ws)) return MOE_ERR_INVALID_ARG;
@@ -128,9 +135,8 @@ static moe_status_t forward_checked(const void* x, const float* logits, int T, c
   if (dv != MOE_OK) return dv;
   char* w = (char*)ws;
   const int rb = d->fmt == MOE_FMT_FP8_B128_W8A8 ? w8a8_row_block()
-                 : d->fmt != MOE_FMT_NVFP4_W4A4  ? tc_row_block(d->fmt, T, k, d->E)
-                 : fp4_supported(*d)             ? fp4_row_block()
-                                                 : simt_row_block();
+                 : d->fmt == MOE_FMT_NVFP4_W4A4  ? fp4_row_block()
+                                                 : tc_row_block(d->fmt, T, k, d->E);
   RoutePrelude pre;
   if (d->fmt == MOE_FMT_FP8_B128_W8A16 && rb == fp8dec_row_block()) {  // FP8 decode path needs row maxima
     pre.zero_u32 = (unsigned*)(w + L.hmax);
@@ -139,12 +145,17 @@ static moe_status_t forward_checked(const void* x, const float* logits, int T, c
     pre.H = d->H;
     pre.xmax = (float*)(w + L.xmax);
   }
+  const int ccols = combine_cols(d->fmt, rb);
+  if (ccols > 0 && k > 1 && !calibrate) {  // the down GEMM's completion counter starts at zero
+    pre.zero2_u32 = (unsigned*)(w + L.cnt);
+    pre.n2_u32 = 1;
+  }
   if (launch_route(logits, T, d->E, k, rb, L, w, pre, s) != cudaSuccess) return MOE_ERR_CUDA;
   const StepEvents ev = g_pending_events;
   g_pending_events = StepEvents();
   if (calibrate)
-    return cuda_status(launch_experts_fp4(*d, (const char*)packed, (const __nv_bfloat16*)x, T, k, L, w, ev, s, act_gs,
-                                          true));
+    return cuda_status(launch_experts_fp4(*d, (const char*)packed, (const __nv_bfloat16*)x, T, k, L, w, ev, s,
+                                          nullptr, act_gs, true));
   return cuda_status(launch_experts(*d, (const char*)packed, (const __nv_bfloat16*)x, T, k, rb, L, w,
                                     (__nv_bfloat16*)out, ev, s, act_gs));
 }
@@ -190,9 +201,9 @@ moe_status_t moe_packed_size(int fmt, int E, int H, int I, moe_packed_desc_t* d)
       sz[MOE_T_D_B] = e * dn / 16;
       sz[MOE_T_GU_GS] = e * 4;
       sz[MOE_T_D_GS] = e * 4;
-      if (fmt == MOE_FMT_NVFP4_W4A4 && fp4_supported(*d)) {  // re-tiled scales for the FP4 MMA path
-        sz[MOE_T_GU_BT] = sz[MOE_T_GU_B];
-        sz[MOE_T_D_BT] = sz[MOE_T_D_B];
+      if (fmt == MOE_FMT_NVFP4_W4A4) {  // scales again, in the tile atoms the block-scaled MMA reads
+        sz[MOE_T_GU_BT] = e * (2 * (size_t)I / 128) * nvfp4_chunks(H) * 2048;
+        sz[MOE_T_D_BT] = e * ((size_t)H / 128) * nvfp4_chunks(I) * 2048;
       }
       break;
   }
@@ -325,7 +336,7 @@ moe_status_t moe_debug_route(const float* logits, int T, int E, int top_k, int32
   if (dv != MOE_OK) return dv;
   cudaStream_t s = (cudaStream_t)stream;
   char* w = (char*)workspace;
-  if (launch_route(logits, T, E, top_k, simt_row_block(), L, w, RoutePrelude(), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_route(logits, T, E, top_k, kMinRowBlock, L, w, RoutePrelude(), s) != cudaSuccess) return MOE_ERR_CUDA;
   const size_t R = (size_t)T * top_k;
   cudaError_t e = cudaMemcpyAsync(offsets, w + L.offsets, 4 * (size_t)(E + 1), cudaMemcpyDeviceToDevice, s);
   if (R) {

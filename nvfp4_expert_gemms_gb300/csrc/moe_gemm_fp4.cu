@@ -16,21 +16,32 @@
 // output features.  An N = 256 block-scaled MMA costs the tensor pipe the same issue time as
 // N = 64 or 128, so one instruction per K step covers what two N = 128 ones did.  Codes arrive
 // by TMA tiles in the 128-byte swizzle (x is quantized straight into permuted row order, one copy
-// per routed token slot, so the gate/up GEMM needs no row gather).  The block scales come in
-// layouts where the 128 rows of one 256-column chunk are one contiguous 2 KB block (the packed
-// re-tiled weight-scale copy; the quantizer writes activation scales chunk-major), each one bulk
-// copy next to its codes rather than 128 strided 16-byte pieces; the four scale warps place
-// both in tensor memory in the layout the MMA reads (per K = 64 step: row r of the operand in lane
-// r % 32 of column r / 32, four scales per word, repeated in every lane quarter).
+// per routed token slot, so the gate/up GEMM needs no row gather).  The block scales of a
+// (128-row tile, 256-column chunk) are one contiguous 2 KB block each: the packed weight copy
+// keeps them in the order tensor memory wants them (per K = 64 step a 512-byte atom whose row l
+// holds the four scales of tile rows l, l + 32, l + 64, l + 96), the activation quantizer writes
+// them chunk-major ([chunk][row][16]); each arrives by one bulk copy next to its codes, and four
+// scale warps move both into tensor memory with tcgen05.st (measured faster than tcgen05.cp
+// issued by the MMA thread, which shares the tensor pipe with the MMAs).  K need not be a
+// multiple of 256: a last half chunk (128 columns) issues two K steps, its upper half being TMA
+// fill that no MMA reads.
 //
-// Warps (448 threads): 0-3 stage scale factors, 4-11 run the epilogue (thread = token row, 64
-// or 128 contiguous output features), 12 issues TMA, 13 owns TMEM and issues the MMAs.
+// The down GEMM also combines, deterministically: its epilogue stores the routing-weighted bf16
+// row of (token t, slot j) at row t * k + j of a slot-ordered buffer, a signal warp publishes
+// each finished item and counts it, and after the GEMM items the work queue hands out combine
+// items (kCombTokens tokens each): once every GEMM item is counted, the producer bulk-copies
+// each token's k contiguous rows into the (now idle) stage memory and the epilogue warps sum
+// them in slot order in fp32 and write out[t] in bf16.
+//
+// Warps: 0-7 epilogue (thread = token row, 64 or 128 contiguous output features), 8-11 scale
+// warps, (down) 12 signal warp, then the TMA producer and the MMA issuer (which owns TMEM).
 // Persistent CTAs walk (routing tile, column block) work items.
 #include <cudaTypedefs.h>
 
 #include "moe_formats.cuh"
 #include "moe_nvfp4.cuh"
 #include "moe_tc.cuh"
+
 
 namespace moe {
 
@@ -40,24 +51,36 @@ using namespace tc;
 
 constexpr int kKC = 256;                  // K per chunk: 128 bytes of codes per row
 constexpr int kRows = 128;                // activation rows per item (MMA M): the routing row block
-constexpr int kStagesW = 4, kStagesX = 4, kStagesS = 4;
-constexpr int kRing = 8;                  // work items handed from the producer to the other warps
-constexpr int kSfWarps = 4, kEpiWarp0 = 4, kEpiWarps = 8, kProdWarp = 12, kMmaWarp = 13;
-constexpr int kThreads = 14 * 32;
+constexpr int kStages = 4;                // weight / activation chunks in flight
+constexpr int kRing = 16;                 // work items handed from the producer to the other warps
+constexpr int kCombRing = 4;              // down: items whose stored rows await the signal warp
 constexpr int kWCodes = 128 * 128;        // one 128-row weight tile, 128-byte swizzle
-constexpr int kWSf = 128 * 16;            // its 128 rows x 16 scales
-constexpr int kWStage = 2 * kWCodes + 2 * kWSf;  // two tiles = the 256 B rows of one item
+constexpr int kSfBlock = 2048;            // scales of one (128-row tile, chunk): four 512-byte atoms
+constexpr int kWStage = 2 * kWCodes + 2 * kSfBlock;  // two tiles = the 256 B rows of one item
 constexpr int kXCodes = kRows * 128;      // activation codes, 128-byte swizzle
-constexpr int kXStage = kXCodes + kRows * 16;  // then their 128 rows x 16 scales
-constexpr size_t kSmem = 1024 + (size_t)kStagesW * kWStage + (size_t)kStagesX * kXStage;
-constexpr uint32_t kSfCol = 256;          // TMEM: [0, 256) accumulator, then 4 x 48 scale-factor columns
-constexpr uint32_t kSfStageCols = 48;     // A (activation) scales 4 x 4 columns, B (weight) scales 4 x 8
+constexpr int kXStage = kXCodes + kSfBlock;
+constexpr size_t kSmem = 1024 + (size_t)kStages * (kWStage + kXStage);
+constexpr uint32_t kSfCol = 256;          // TMEM: [0, 256) accumulator, then 4 x 48 scale columns
+constexpr uint32_t kSfStageCols = 48;     // per K step: A (activation) scales 4 columns, B (weight) 8
+constexpr int kCombTokens = 24;           // tokens per combine item of the down GEMM
+constexpr int kCombBuf = 96 * 1024;       // combine: two buffers of partial rows in the stage memory
+
+// Warp roles: 0-7 epilogue (warp w reads TMEM lane quarter w % 4), 8-11 scale warps (quarter
+// w % 4), then (down only) a signal warp, the TMA producer and the MMA issuer.
+constexpr int kEpiWarps = 8, kSfWarp0 = 8, kSfWarps = 4, kSigWarp = 12;
+template <int MODE>
+struct Roles {
+  static constexpr int kSigWarps = MODE == 1 ? 1 : 0;
+  static constexpr int kProdWarp = kSigWarp + kSigWarps, kMmaWarp = kProdWarp + 1;
+  static constexpr int kThreads = (kMmaWarp + 1) * 32;
+};
+static_assert(2 * kCombBuf <= kStages * (kWStage + kXStage), "combine buffers live in the stage memory");
 
 struct Fp4Args {
   CUtensorMap wcode;        // weight codes [E*N, K/2]
   CUtensorMap xcode;        // activation codes [R, K/2], permuted row order
-  const uint8_t* wsft;      // weight block scales re-tiled [E, N/128, K/256, 128, 16]
-  const uint8_t* asft;      // activation block scales chunk-major [K/256][sf_rows][16]
+  const uint8_t* wsft;      // weight block scales in tile atoms [E, N/128, C, 2048]
+  const uint8_t* asft;      // activation block scales chunk-major [C][sf_rows][16]
   int sf_rows;
   const float* wgs;         // weight global scales [E]
   const float* ags;         // activation global scales [R]
@@ -67,9 +90,12 @@ struct Fp4Args {
   uint16_t* h_out;          // MODE 0 output [R, I] bf16 (dynamic activation scales)
   const float* hgs_static;  // MODE 2 (gate/up, static activation scales): h's global scale (dev); h
   uint8_t* hq_out;          //   leaves NVFP4-quantized instead: codes [R, I/2], chunk-major block
-  uint8_t* hsf_out;         //   scales [I/256][sf_rows][16] and the global scale per row [R]
+  uint8_t* hsf_out;         //   scales [C(I)][sf_rows][16] and the global scale per row [R]
   float* hg_out;
-  uint16_t* y_out;          // MODE 1 output: routing-weighted rows [R, H] bf16, permuted order
+  uint16_t* comb;           // MODE 1: routing-weighted rows [T*k, H] bf16, row t*k + j = (token t, slot j)
+  int* done;                // MODE 1: GEMM items finished (their rows published), zero on entry
+  uint16_t* out;            // MODE 1 output [T, H] bf16
+  int T;
   int* err;
   int* work_ctr;            // items handed out past each CTA's first (zeroed by routing)
   int k, N, K, I, H;
@@ -98,22 +124,51 @@ __device__ __forceinline__ void tmem_st_32x16(uint32_t taddr, const uint32_t* v)
       : "memory");
 }
 
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Orders global data acquired by generic loads before later bulk (async-proxy) copies of it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// The routing-weighted partial rows stream through L2 once each (written by the epilogue, read
+// back by the combine much later), so they are written evict-first.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void st_global_v8_hint(void* p, const uint32_t* v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "l"(pol)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)bf16_bits(lo) | ((uint32_t)bf16_bits(hi) << 16);
 }
 
-// MODE 0: gate/up (h in bf16), 1: down, 2: gate/up with static activation scales (h leaves as
-// NVFP4 codes, block scales and global scales).
+// MODE 0: gate/up (h in bf16), 1: down + combine, 2: gate/up with static activation scales (h
+// leaves as NVFP4 codes, block scales and global scales).
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant__ Fp4Args a) {
+__global__ void __launch_bounds__(Roles<MODE>::kThreads, 1) fp4_kernel(const __grid_constant__ Fp4Args a) {
   constexpr bool kGateUp = MODE != 1, kFuseH = MODE == 2;
+  constexpr int kSigWarps = Roles<MODE>::kSigWarps, kProdWarp = Roles<MODE>::kProdWarp,
+                kMmaWarp = Roles<MODE>::kMmaWarp;
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = (char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   char* sW = smem;
-  char* sX = sW + kStagesW * kWStage;
-  __shared__ uint64_t w_full[kStagesW], w_empty[kStagesW], x_full[kStagesX], x_empty[kStagesX], s_full[kStagesS],
-      s_empty[kStagesS], acc_full, acc_empty, drain;
+  char* sX = sW + kStages * kWStage;
+  __shared__ uint64_t w_full[kStages], w_empty[kStages], x_full[kStages], x_empty[kStages], s_full[kStages],
+      s_empty[kStages], acc_full, acc_empty, drain;
   __shared__ uint64_t work_full[kRing], work_empty[kRing];
+  __shared__ uint64_t rows_stored[kCombRing], rows_taken[kCombRing], c_full[2], c_empty[2];
   __shared__ int s_work[kRing];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -122,28 +177,40 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
   // was final before the gate/up GEMM passed its own pdl_wait(), so only the h codes need the wait
   if (kGateUp) pdl_wait();
   const int ntiles = load_tile(a.tiles).expert;
-  const int ncb = kGateUp ? a.I / 128 : a.H / 256;
-  const int nwork = ntiles * ncb;
+  const int ncb = kGateUp ? a.I / 128 : (a.H + 255) / 256;
+  // down: after the ngemm GEMM items, one combine item per kCombTokens tokens
+  const int ngemm = ntiles * ncb;
+  const int nslices = kGateUp || a.k == 1 ? 0 : (a.T + kCombTokens - 1) / kCombTokens;
+  const int nwork = ngemm + nslices;
+  // combine items move partial rows in segments of (token, cseg columns) -- each one contiguous
+  // run of k rows when cseg = H -- packed nseg to a buffer
+  const int cseg = !kGateUp && a.k * a.H * 2 > kCombBuf ? kCombBuf / (a.k * 2) / 256 * 256 : a.H;
+  const int nsegc = (a.H + cseg - 1) / cseg, nseg = max(1, kCombBuf / (a.k * cseg * 2));
   if ((int)blockIdx.x >= nwork) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nK = a.K / kKC;
+  const int nK = (a.K + kKC - 1) / kKC;           // chunks; the last is a half chunk when K % 256 = 128
+  const int last_ks = (a.K % kKC) ? 2 : 4;        // K = 64 steps of the last chunk
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStagesW; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&w_full[i], 1);
       mbar_init(&w_empty[i], 1);
-    }
-    for (int i = 0; i < kStagesX; ++i) {
       mbar_init(&x_full[i], 1);
       mbar_init(&x_empty[i], 1);
-    }
-    for (int i = 0; i < kStagesS; ++i) {
       mbar_init(&s_full[i], kSfWarps);
       mbar_init(&s_empty[i], 1);
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&work_full[i], 1);
-      mbar_init(&work_empty[i], kSfWarps + 1 + kEpiWarps);  // every consuming warp
+      mbar_init(&work_empty[i], 1 + kEpiWarps + kSfWarps + kSigWarps);  // every consuming warp
+    }
+    for (int i = 0; i < kCombRing; ++i) {
+      mbar_init(&rows_stored[i], kEpiWarps);
+      mbar_init(&rows_taken[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c_full[i], 1);
+      mbar_init(&c_empty[i], kEpiWarps);
     }
     mbar_init(&acc_full, 1);
     mbar_init(&acc_empty, kEpiWarps);
@@ -178,19 +245,24 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
     if (lane == 0) mbar_arrive(&work_empty[slot]);
     return wk;
   };
-  // item wk: routing tile wk / ncb; weight rows w0 .. w0+127 and w1 .. w1+127 of its expert
-  auto item = [&](int wk, TileEntry& te, int& w0, int& w1) {
-    te = load_tile(a.tiles + 1 + wk / ncb);
+  // Item wk: a combine item (down, wk >= ngemm; returns false), or routing tile `tile`, weight
+  // rows w0 .. w0+127 and w1 .. w1+127 of its expert.  GEMM items run tile by tile, so a tile's
+  // activations are reused by its column blocks while in L2.
+  auto item = [&](int wk, TileEntry& te, int& tile, int& w0, int& w1) -> bool {
+    if (!kGateUp && wk >= ngemm) return false;
+    tile = wk / ncb;
     const int cb = wk % ncb;
+    te = load_tile(a.tiles + 1 + tile);
     w0 = kGateUp ? cb * 128 : cb * 256;
     w1 = kGateUp ? a.I + w0 : w0 + 128;
+    return true;
   };
 
   if (warp == kProdWarp) {
     // ---------------- TMA producer (whole warp walks the loop, lane 0 issues) ----------------
-    int it = 0;
-    bool ok = true;
-    int armed_w[kStagesW] = {0}, armed_x[kStagesX] = {0};
+    int it = 0, cg = 0;  // chunks, combine buffer groups
+    bool ok = true, comb_ready = false;
+    int armed_w[kStages] = {0}, armed_x[kStages] = {0}, armed_c[2] = {0};
     for (int n = 0; ok; ++n) {
       int wk = -1;
       if (lane == 0) {
@@ -207,33 +279,72 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok || wk < 0) break;
       TileEntry te;
-      int w0, w1;
-      item(wk, te, w0, w1);
-      for (int kc = 0; kc < nK; ++kc, ++it) {
-        const int sw = it % kStagesW, sx = it % kStagesX;
+      int tile, w0, w1;
+      if (!item(wk, te, tile, w0, w1)) {
+        // combine item: stream its tokens' partial rows into the two buffers.  The first one waits
+        // until every GEMM item of the grid is done -- then also this CTA's stage memory is free.
         if (lane == 0) {
-          ok = mbar_wait(&w_empty[sw], ((it / kStagesW) & 1) ^ 1, &s_abort);
+          if (!comb_ready) {
+            const long long t0 = clock64();
+            while (ok && ld_acquire_gpu(a.done) < ngemm) {
+              if (*(volatile int*)&s_abort || clock64() - t0 > kWaitLimitCycles) {
+                *(volatile int*)&s_abort = 1;
+                ok = false;
+              }
+            }
+            fence_proxy_async_global();  // the rows acquired above, read next by bulk copies
+            comb_ready = true;
+          }
+          const int tb = (wk - ngemm) * kCombTokens, te_ = min(a.T, tb + kCombTokens);
+          for (int g0 = 0; ok && g0 < (te_ - tb) * nsegc; g0 += nseg, ++cg) {
+            const int b = cg & 1, ng_ = min(nseg, (te_ - tb) * nsegc - g0);
+            ok = mbar_wait(&c_empty[b], ((cg >> 1) & 1) ^ 1, &s_abort);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&c_full[b], (uint32_t)(ng_ * a.k * min(cseg, a.H) * 2));
+            ++armed_c[b];
+            for (int u = 0; u < ng_; ++u) {
+              const int sg = g0 + u, t = tb + sg / nsegc, c0 = (sg % nsegc) * cseg, cw = min(cseg, a.H - c0);
+              char* dst = smem + (size_t)b * kCombBuf + (size_t)u * a.k * cseg * 2;
+              const uint16_t* src = a.comb + (size_t)t * a.k * a.H + c0;
+              if (cw == a.H)
+                bulk_load(dst, src, (uint32_t)(a.k * a.H * 2), &c_full[b]);
+              else
+                for (int j = 0; j < a.k; ++j)
+                  bulk_load(dst + (size_t)j * cw * 2, src + (size_t)j * a.H, (uint32_t)(cw * 2), &c_full[b]);
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        continue;
+      }
+      for (int kc = 0; kc < nK; ++kc, ++it) {
+        const int st = it % kStages;
+        if (lane == 0) {
+          ok = mbar_wait(&w_empty[st], ((it / kStages) & 1) ^ 1, &s_abort);
           if (ok) {
-            char* ws = sW + sw * kWStage;
-            mbar_arrive_expect_tx(&w_full[sw], 2 * (kWCodes + kWSf));
-            ++armed_w[sw];
+            char* ws = sW + st * kWStage;
+            mbar_arrive_expect_tx(&w_full[st], 2 * (kWCodes + kSfBlock));
+            ++armed_w[st];
             for (int g = 0; g < 2; ++g) {
               const int wr = g == 0 ? w0 : w1;
-              tma_load_2d(ws + g * kWCodes, &a.wcode, &w_full[sw], kc * (kKC / 2), te.expert * a.N + wr);
-              // the 128 rows' scales of this chunk: one contiguous 2 KB block of the re-tiled copy
-              const size_t blk = ((size_t)te.expert * (a.N / 128) + wr / 128) * nK + kc;
-              bulk_load(ws + 2 * kWCodes + g * kWSf, a.wsft + blk * kWSf, kWSf, &w_full[sw]);
+              tma_load_2d(ws + g * kWCodes, &a.wcode, &w_full[st], kc * (kKC / 2), te.expert * a.N + wr);
+              // the 128 rows' scales of this chunk (a second tile past N -- the last down column
+              // block when H % 256 = 128 -- computes columns nobody stores: any finite scales do)
+              const int sr = wr < a.N ? wr : w0;
+              const size_t blk = ((size_t)te.expert * (a.N / 128) + sr / 128) * nK + kc;
+              bulk_load(ws + 2 * kWCodes + g * kSfBlock, a.wsft + blk * kSfBlock, kSfBlock, &w_full[st]);
             }
           }
           if (ok) {
-            ok = mbar_wait(&x_empty[sx], ((it / kStagesX) & 1) ^ 1, &s_abort);
+            ok = mbar_wait(&x_empty[st], ((it / kStages) & 1) ^ 1, &s_abort);
             if (MODE == 1 && it == 0) pdl_wait();
             if (ok) {
-              mbar_arrive_expect_tx(&x_full[sx], kXStage);
-              ++armed_x[sx];
-              tma_load_2d(sX + sx * kXStage, &a.xcode, &x_full[sx], kc * (kKC / 2), te.row0);
-              bulk_load(sX + sx * kXStage + kXCodes, a.asft + ((size_t)kc * a.sf_rows + te.row0) * 16, kRows * 16,
-                        &x_full[sx]);
+              mbar_arrive_expect_tx(&x_full[st], kXStage);
+              ++armed_x[st];
+              tma_load_2d(sX + st * kXStage, &a.xcode, &x_full[st], kc * (kKC / 2), te.row0);
+              // the 128 rows' scales of this chunk: one contiguous 2 KB block of the chunk plane
+              bulk_load(sX + st * kXStage + kXCodes, a.asft + ((size_t)kc * a.sf_rows + te.row0) * 16, kRows * 16,
+                        &x_full[st]);
             }
           }
         }
@@ -243,41 +354,46 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
     }
     if (lane == 0 && s_abort) {  // let every issued copy land before shared memory goes away
       volatile int no_abort = 0;
-      for (int i = 0; i < kStagesW; ++i)
+      for (int i = 0; i < kStages; ++i) {
         if (armed_w[i]) mbar_wait(&w_full[i], (armed_w[i] - 1) & 1, &no_abort);
-      for (int i = 0; i < kStagesX; ++i)
         if (armed_x[i]) mbar_wait(&x_full[i], (armed_x[i] - 1) & 1, &no_abort);
+      }
+      for (int i = 0; i < 2; ++i)
+        if (armed_c[i]) mbar_wait(&c_full[i], (armed_c[i] - 1) & 1, &no_abort);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer (whole warp waits, lane 0 issues) ----------------
     const uint32_t idesc = idesc_nvf4(kRows, 256);
-    int it = 0;
+    int it = 0, ng = 0;  // chunks and GEMM items so far
     bool ok = true;
-    for (int nitem = 0; ok; ++nitem) {
-      if (next_item(nitem, ok) < 0) break;
+    for (int n = 0; ok; ++n) {
+      const int wk = next_item(n, ok);
+      if (wk < 0) break;
+      if (!kGateUp && wk >= ngemm) continue;  // a combine item
+      const int nitem = ng++;
       ok = mbar_wait(&acc_empty, (nitem & 1) ^ 1, &s_abort);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       fence_after_sync();
       for (int kc = 0; kc < nK; ++kc, ++it) {
-        const int sw = it % kStagesW, sx = it % kStagesX, ss = it % kStagesS;
-        ok = mbar_wait(&w_full[sw], (it / kStagesW) & 1, &s_abort) &&
-             mbar_wait(&x_full[sx], (it / kStagesX) & 1, &s_abort) &&
-             mbar_wait(&s_full[ss], (it / kStagesS) & 1, &s_abort);
+        const int st = it % kStages;
+        ok = mbar_wait(&w_full[st], (it / kStages) & 1, &s_abort) &&
+             mbar_wait(&x_full[st], (it / kStages) & 1, &s_abort) &&
+             mbar_wait(&s_full[st], (it / kStages) & 1, &s_abort);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         fence_after_sync();
         if (lane == 0) {
-          const uint32_t xa = smem_u32(sX + sx * kXStage), wa = smem_u32(sW + sw * kWStage);
-          const uint32_t sfa = tmem + kSfCol + ss * kSfStageCols, sfb = sfa + 16;
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
+          const uint32_t xa = smem_u32(sX + st * kXStage), wa = smem_u32(sW + st * kWStage);
+          const uint32_t sfa = tmem + kSfCol + st * kSfStageCols, sfb = sfa + 16;
+          const int nks = kc == nK - 1 ? last_ks : 4;
+          for (int ks = 0; ks < nks; ++ks)
             mma_nvf4(tmem, sdesc_k_sw128(xa + ks * 32), sdesc_k_sw128(wa + ks * 32), idesc, sfa + 4 * ks,
                      sfb + 8 * ks, (kc | ks) != 0);
-          mma_commit(&w_empty[sw]);
-          mma_commit(&x_empty[sx]);
-          mma_commit(&s_empty[ss]);
+          mma_commit(&w_empty[st]);
+          mma_commit(&x_empty[st]);
+          mma_commit(&s_empty[st]);
         }
         __syncwarp();
       }
@@ -286,85 +402,145 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
     }
     if (lane == 0) mma_commit(&drain);
     __syncwarp();
-  } else if (warp < kSfWarps) {
-    // ---------------- scale factors -> tensor memory ----------------
-    const int q = warp, l = lane;
+  } else if (warp >= kSfWarp0 && warp < kSfWarp0 + kSfWarps) {
+    // ---------------- scale warps: block scales -> tensor memory (warp = lane quarter) -------
+    // TMEM lane l, column 4 ks + j: K step ks's four scales of activation row l + 32 j (from the
+    // row's 16 chunk bytes); column 16 + 8 ks + 4 g + j: those of weight row l + 32 j of tile g
+    // (atom row l of the packed copy).  Every lane quarter gets a copy.
+    const int q = warp & 3;
     int it = 0;
     bool ok = true;
     for (int n = 0; ok; ++n) {
       const int wk = next_item(n, ok);
       if (wk < 0) break;
       TileEntry te;
-      int w0, w1;
-      item(wk, te, w0, w1);
+      int tile, w0, w1;
+      if (!item(wk, te, tile, w0, w1)) continue;  // a combine item
       for (int kc = 0; kc < nK; ++kc, ++it) {
-        const int sw = it % kStagesW, sx = it % kStagesX, ss = it % kStagesS;
-        ok = __all_sync(0xffffffffu, mbar_wait(&w_full[sw], (it / kStagesW) & 1, &s_abort) &&
-                                         mbar_wait(&x_full[sx], (it / kStagesX) & 1, &s_abort) &&
-                                         mbar_wait(&s_empty[ss], ((it / kStagesS) & 1) ^ 1, &s_abort));
+        const int st = it % kStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(&w_full[st], (it / kStages) & 1, &s_abort) &&
+                                         mbar_wait(&x_full[st], (it / kStages) & 1, &s_abort) &&
+                                         mbar_wait(&s_empty[st], ((it / kStages) & 1) ^ 1, &s_abort));
         if (!ok) break;
         fence_after_sync();
-        const uint32_t col = kSfCol + ss * kSfStageCols;
-        // A: column 4 ks + j holds the K-step-ks word of activation row l + 32 j (rows past the
-        // tile scale by 0)
-        const char* xsf = sX + sx * kXStage + kXCodes;
-        uint4 x4[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          x4[j] = l + 32 * j < te.rows ? *(const uint4*)(xsf + (l + 32 * j) * 16) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t col = kSfCol + st * kSfStageCols;
+        const char* xsf = sX + st * kXStage + kXCodes + 16 * lane;
+        const char* wsf = sW + st * kWStage + 2 * kWCodes + 16 * lane;
         uint32_t v[16];
+        uint4 x4[4];  // activations: row l + 32 j's 16 scales (word = K step)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x4[j] = *(const uint4*)(xsf + 512 * j);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          v[0 + j] = x4[j].x;
+          v[j] = x4[j].x;
           v[4 + j] = x4[j].y;
           v[8 + j] = x4[j].z;
           v[12 + j] = x4[j].w;
         }
         tmem_st_32x16(taddr(tmem, q * 32, col), v);
-        // B: column 16 + 8 ks + j holds the K-step-ks word of weight row l + 32 j (j < 4: first
-        // 128-row tile, j >= 4: second)
-        uint4 w[8];
-        const char* wsf = sW + sw * kWStage + 2 * kWCodes;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) w[j] = *(const uint4*)(wsf + (j >> 2) * kWSf + (l + 32 * (j & 3)) * 16);
+        for (int h = 0; h < 2; ++h) {  // weight columns of K steps 2h, 2h + 1
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          v[0 + j] = w[j].x;
-          v[8 + j] = w[j].y;
+          for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              const uint4 u = *(const uint4*)(wsf + g * kSfBlock + (2 * h + kk) * 512);
+              v[8 * kk + 4 * g] = u.x;
+              v[8 * kk + 4 * g + 1] = u.y;
+              v[8 * kk + 4 * g + 2] = u.z;
+              v[8 * kk + 4 * g + 3] = u.w;
+            }
+          tmem_st_32x16(taddr(tmem, q * 32, col + 16 + 16 * h), v);
         }
-        tmem_st_32x16(taddr(tmem, q * 32, col + 16), v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          v[0 + j] = w[j].z;
-          v[8 + j] = w[j].w;
-        }
-        tmem_st_32x16(taddr(tmem, q * 32, col + 32), v);
         tmem_st_wait();
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_full[ss]);
+        if (lane == 0) mbar_arrive(&s_full[st]);
       }
     }
-  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
-    // ---------------- epilogue: thread = token row of the tile ----------------
-    const int q = warp & 3, half = (warp - kEpiWarp0) >> 2, r = q * 32 + lane;
+  } else if (warp == kSigWarp) {
+    // ---------------- signal warp (down): per GEMM item, take the epilogue's stored rows
+    // (freeing the ring slot), publish them at GPU scope and count the item done ----------------
+    int ng = 0;
     bool ok = true;
-    for (int nitem = 0; ok; ++nitem) {
-      const int wk = next_item(nitem, ok);
+    for (int n = 0; ok; ++n) {
+      const int wk = next_item(n, ok);
+      if (!ok || wk < 0) break;
+      if (wk >= ngemm) continue;
+      const int nitem = ng++, rs = nitem % kCombRing;
+      ok = __all_sync(0xffffffffu, mbar_wait(&rows_stored[rs], (nitem / kCombRing) & 1, &s_abort));
+      if (!ok) break;
+      if (a.k > 1 && lane == 0) {
+        fence_acq_rel_gpu();  // the epilogue's stores (observed through the barrier) before the count
+        atomicAdd(a.done, 1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rows_taken[rs]);
+    }
+  } else {
+    // ---------------- epilogue: thread = token row of the tile ----------------
+    const int q = warp & 3, half = warp >> 2, r = q * 32 + lane;
+    bool ok = true;
+    int ng = 0, cg = 0;  // GEMM items, combine buffer groups so far
+    for (int n = 0; ok; ++n) {
+      const int wk = next_item(n, ok);
       // the epilogue warps leave together (they meet in a named barrier every item)
       if (!named_bar_and(1, kEpiWarps * 32, ok && wk >= 0)) break;
       TileEntry te;
-      int w0, w1;
-      item(wk, te, w0, w1);
-      // the row's scale (1 / (gs_w gs_a), times the routing weight for the down GEMM), read
-      // while the MMAs run
+      int tile, w0, w1;
+      if (!item(wk, te, tile, w0, w1)) {
+        // combine item: per buffer group, each (token, column segment): out = bf16 of the sum of
+        // the token's k routing-weighted rows in slot order (thread: 8 columns at a time)
+        bool cok = true;
+        const int tb = (wk - ngemm) * kCombTokens, te_ = min(a.T, tb + kCombTokens);
+        for (int g0 = 0; g0 < (te_ - tb) * nsegc; g0 += nseg, ++cg) {
+          const int b = cg & 1, ng_ = min(nseg, (te_ - tb) * nsegc - g0);
+          cok = cok && mbar_wait(&c_full[b], (cg >> 1) & 1, &s_abort);
+          if (cok) {
+            for (int u = 0; u < ng_; ++u) {
+              const int sg = g0 + u, t = tb + sg / nsegc, c0 = (sg % nsegc) * cseg, cw = min(cseg, a.H - c0);
+              const char* seg = smem + (size_t)b * kCombBuf + (size_t)u * a.k * cseg * 2;
+              for (int c = 8 * (int)threadIdx.x; c < cw; c += 8 * kEpiWarps * 32) {
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // slot order
+                for (int j = 0; j < a.k; ++j) {
+                  const uint4 v = *(const uint4*)(seg + ((size_t)j * cw + c) * 2);
+                  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    acc[2 * e] += __uint_as_float(w[e] << 16);
+                    acc[2 * e + 1] += __uint_as_float(w[e] & 0xFFFF0000u);
+                  }
+                }
+                *(uint4*)(a.out + (size_t)t * a.H + c0 + c) =
+                    make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                               pack_bf16x2(acc[6], acc[7]));
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&c_empty[b]);
+        }
+        if (!named_bar_and(1, kEpiWarps * 32, cok)) break;  // the epilogue warps leave together
+        continue;
+      }
+      const int nitem = ng++;
+      // the row's scale (1 / (gs_w gs_a), times the routing weight for the down GEMM) and, for
+      // the down GEMM, its (token, slot) entry, read while the MMAs run
       const bool live = r < te.rows;
       float cs = 0.f;
+      int p = 0;
       if (live) {
         const float g = a.wgs[te.expert] * a.ags[te.row0 + r];
-        cs = kGateUp ? 1.0f / g : a.topk_w[a.perm[te.row0 + r]] / g;
+        if (kGateUp) {
+          cs = 1.0f / g;
+        } else {
+          p = a.perm[te.row0 + r];
+          cs = a.topk_w[p] / g;
+        }
       }
       ok = mbar_wait(&acc_full, nitem & 1, &s_abort);
+      if (MODE == 1 && ok && nitem >= kCombRing)  // the signal warp has taken this ring slot's rows
+        ok = mbar_wait(&rows_taken[nitem % kCombRing], ((nitem / kCombRing) & 1) ^ 1, &s_abort);
       // every epilogue thread takes the same branch
       ok = named_bar_and(1, kEpiWarps * 32, ok);
       if (!ok) break;
@@ -432,33 +608,45 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
         }
         if (kFuseH && live) {
           const size_t row = (size_t)te.row0 + r;
-          const int f0 = w0 + 64 * half;  // four whole blocks of one 256-column chunk
+          const int f0 = w0 + 64 * half;  // four whole blocks = one K step of one 256-column chunk
           st_global_v8(a.hq_out + row * (a.I / 2) + f0 / 2, hc);
           *(uint32_t*)(a.hsf_out + ((size_t)(f0 >> 8) * a.sf_rows + row) * 16 + ((f0 & 255) >> 4)) = hs4;
           if (f0 == 0) a.hg_out[row] = ghs;
         }
       } else {
-        // output features w0 + 128 half .. + 127 of the routing-weighted row
-        uint16_t* dst = a.y_out + (size_t)(te.row0 + r) * a.H + w0 + 128 * half;
+        // output features fb .. fb + 127 of the routing-weighted row of (token t, slot p % k): to
+        // the slot-ordered buffer (the combine items sum the k rows), or with one slot straight
+        // to the output
+        const int fb = w0 + 128 * half;
+        const bool mine = live && fb < a.H;
+        const uint64_t stream = policy_evict_first();
+        uint16_t* dst = a.k == 1 ? a.out + (size_t)(p / a.k) * a.H + fb : a.comb + (size_t)p * a.H + fb;
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const int c = 128 * half + 64 * b;
-          uint32_t Y[64];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) tmem_ld_32x16(taddr(tmem, q * 32, c + 16 * i), Y + 16 * i);
+        for (int b = 0; b < 4; ++b) {
+          uint32_t Y[32];
+          tmem_ld_32x16(taddr(tmem, q * 32, 128 * half + 32 * b), Y);
+          tmem_ld_32x16(taddr(tmem, q * 32, 128 * half + 32 * b + 16), Y + 16);
           tmem_ld_wait();
-          if (b == 1) {
+          if (b == 3) {
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty);
           }
 #pragma unroll
-          for (int j = 0; j < 32; ++j)  // in place: word j reads words 2j, 2j+1 >= j
+          for (int j = 0; j < 16; ++j)  // in place: word j reads words 2j, 2j+1 >= j
             Y[j] = pack_bf16x2(__uint_as_float(Y[2 * j]) * cs, __uint_as_float(Y[2 * j + 1]) * cs);
-          if (live)
+          if (mine) {
+            if (a.k > 1)  // 32-byte stores of whole sectors
 #pragma unroll
-            for (int v = 0; v < 4; ++v) st_global_v8(dst + 64 * b + 16 * v, Y + 8 * v);
+              for (int v = 0; v < 2; ++v) st_global_v8_hint(dst + 32 * b + 16 * v, Y + 8 * v, stream);
+            else  // one slot: the row is the output (16-byte aligned)
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                *(uint4*)(dst + 32 * b + 8 * v) = make_uint4(Y[4 * v], Y[4 * v + 1], Y[4 * v + 2], Y[4 * v + 3]);
+          }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rows_stored[nitem % kCombRing]);  // release: the stores above
       }
     }
   }
@@ -476,8 +664,6 @@ __global__ void __launch_bounds__(kThreads, 1) fp4_kernel(const __grid_constant_
 
 }  // namespace
 
-// The FP4 path needs whole 256-element K chunks in both GEMMs.
-bool fp4_supported(const moe_packed_desc_t& d) { return d.H % 256 == 0 && d.I % 256 == 0; }
 int fp4_row_block() { return kRows; }
 
 template <int MODE>
@@ -488,18 +674,18 @@ static cudaError_t launch_fp4(const Fp4Args& a, int work, cudaStream_t s) {
     attr = true;
   }
   const int sms = tc_num_sms();
-  return launch_pdl(fp4_kernel<MODE>, dim3(work < sms ? work : sms), dim3(kThreads), kSmem, s, a);
+  return launch_pdl(fp4_kernel<MODE>, dim3(work < sms ? work : sms), dim3(Roles<MODE>::kThreads), kSmem, s, a);
 }
 
 cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
-                               const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, const float* act_gs,
-                               bool calibrate) {
+                               const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, uint16_t* out,
+                               const float* act_gs, bool calibrate) {
   const int E = d.E, H = d.H, I = d.I;
   const size_t R = (size_t)T * k;
   const MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
   uint8_t* xq = (uint8_t*)(ws + L.xq);
-  uint8_t* xsf = (uint8_t*)(ws + L.xs);
   uint8_t* hq = (uint8_t*)(ws + L.hq);
+  uint8_t* xsf = (uint8_t*)(ws + L.xs);
   uint8_t* hsf = (uint8_t*)(ws + L.hs);
   const int sf_rows = sf_plane_rows(R);
   float* cal = calibrate ? const_cast<float*>(act_gs) : nullptr;  // calibration writes the two scales
@@ -515,13 +701,16 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   a.hgs_static = act_gs && !calibrate ? act_gs + 1 : nullptr;
   a.hq_out = hq;
   a.hsf_out = hsf;
+  a.sf_rows = sf_rows;
   a.hg_out = (float*)(ws + L.hg);
-  a.y_out = (uint16_t*)(ws + L.y);
+  a.comb = (uint16_t*)(ws + L.y);
+  a.done = (int*)(ws + L.cnt);
+  a.T = T;
+  a.out = out;
   a.err = (int*)(ws + L.err);
   a.k = k;
   a.I = I;
   a.H = H;
-  a.sf_rows = sf_rows;
   a.work_ctr = (int*)(ws + L.err) + 1;
   const int max_tiles = (int)(R / kRows + (R < (size_t)E ? R : (size_t)E) + 1);
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -543,7 +732,7 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
 
   if (cal) return launch_act_scale((const uint16_t*)(ws + L.h), R * I, cal + 1, s);  // h's scale; no down GEMM
   // h -> NVFP4 per permuted row (its own global scale; with static scales the gate/up epilogue
-  // has already quantized it), then down: A = h rows, B = [H, I] weights
+  // has already quantized it), then down: A = h rows, B = [H, I] weights; the epilogue combines
   if (!act_gs)
     launch_quant_rows((const __nv_bfloat16*)(ws + L.h), nullptr, 1, (int)R, I, hq, hsf, (float*)(ws + L.hg), s, false,
                       sf_rows);
@@ -558,7 +747,8 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   a.K = I;
   a.work_ctr = (int*)(ws + L.err) + 2;
   record_event(ev.start[1], s);
-  err = launch_fp4<1>(a, max_tiles * (H / 256), s);
+  const int slices = k > 1 ? (T + kCombTokens - 1) / kCombTokens : 0;
+  err = launch_fp4<1>(a, max_tiles * ((H + 255) / 256) + slices, s);
   record_event(ev.stop[1], s);
   note_launches(2);
   return err;

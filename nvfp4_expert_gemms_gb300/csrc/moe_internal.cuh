@@ -72,7 +72,8 @@ __device__ __forceinline__ TileEntry load_tile(const TileEntry* p) {
 // ---- workspace layout ----------------------------------------------------------------------
 struct WsLayout {
   size_t err, topk_idx, topk_w, blkcnt, blkbase, offsets, perm, inv, tiles;
-  size_t h, y, xq, xs, xg, hq, hs, hg;  // y: routing-weighted down rows [R, H] bf16 (permuted order)
+  size_t h, y, xq, xs, xg, hq, hs, hg;  // y: routing-weighted down rows [R, H] bf16
+  size_t cnt;         // the down GEMM's completion counter (zeroed by routing)
   size_t xp;          // expert-permuted bf16 copy of x (tensor-core path, row blocks >= 64)
   size_t xmax, hmax;  // per-row max |activation| (FP8 decode path)
   size_t x_stage, lg_stage, out_stage;
@@ -95,6 +96,8 @@ moe_status_t device_ok();
 struct RoutePrelude {
   unsigned* zero_u32 = nullptr;
   size_t n_u32 = 0;
+  unsigned* zero2_u32 = nullptr;  // a second range (the combine counters)
+  size_t n2_u32 = 0;
   const uint16_t* x = nullptr;  // bf16 [T, H] or null
   int H = 0;
   float* xmax = nullptr;
@@ -105,10 +108,22 @@ cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, co
                         char* packed, cudaStream_t s);
 cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e, int which, float* out,
                            cudaStream_t s);
+// ---- NVFP4 weight block scales in the order the block-scaled MMA reads them ------------------
+// The MMA takes the E4M3 block scales from tensor memory, where for one K = 64 step of a 128-row
+// tile lane l (of every lane quarter), column j holds the four scales of tile row l + 32 j.  The
+// packed weight copy keeps them in that order -- per K step a 512-byte "atom", byte
+// 16 l + 4 j + i = scale i of row l + 32 j -- four atoms (2 KB) per (128-row tile, 256-column
+// chunk), contiguous per (tile, chunk): byte index of 16-block b of slot s (tile s / 128, row
+// s % 128):
+__host__ __device__ inline int nvfp4_chunks(int K) { return (K + 255) / 256; }
+__host__ __device__ inline size_t sf_atom_byte(size_t slot, int b, int nchunks) {
+  return ((slot >> 7) * (size_t)nchunks + (size_t)(b >> 4)) * 2048 + (size_t)((b & 15) >> 2) * 512 +
+         16 * (slot & 31) + 4 * ((slot & 127) >> 5) + (size_t)(b & 3);
+}
 // NVFP4 quantization of bf16 rows; row r's codes go to output row r, or (scatter != null) to
 // rows scatter[r*k .. r*k+k-1].  early: x was final before the preceding kernel of the stream
 // passed its pdl_wait() (true only right after routing), so x is read before this launch's wait.
-// sf_rows = 0: scales row-major [rows, K/16]; else chunk-major [K/256][sf_rows][16].
+// sf_rows = 0: scales row-major [rows, K/16]; else chunk-major [C][sf_rows][16], C = ceil(K/256).
 // static_gs (dev, one float) != null: that global scale for every row instead of each row's own.
 // gs may be null (the per-row scales are then not stored).
 cudaError_t launch_quant_rows(const __nv_bfloat16* x, const int32_t* scatter, int k, int rows, int K, uint8_t* q,
@@ -167,7 +182,6 @@ inline void record_event(cudaEvent_t ev, cudaStream_t s) {
 }
 // Running count of kernels enqueued by the library (moe_kernel_launch_count).
 void note_launches(int n);
-int simt_row_block();
 // Tensor-core path (FP8 W8A16, INT4 W4A16, NVFP4 W4A16, BF16): row block per tile, and the two GEMMs.
 int tc_row_block(int fmt, int T, int k, int E);
 bool tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1, uint64_t pitch,
@@ -177,13 +191,14 @@ int tc_num_sms();
 int fp8dec_row_block();
 cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,
                                   int k, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);
-// NVFP4 W4A4 path on block-scaled FP4 MMAs (H and I multiples of 256; 128-row routing tiles).
-bool fp4_supported(const moe_packed_desc_t& d);
+// NVFP4 W4A4 path on block-scaled FP4 MMAs (128-row routing tiles; any H, I multiples of 128).
 int fp4_row_block();
-// act_gs: static activation scales (dev, [2]) or null; calibrate: instead of the layer, write the
-// static scales of this batch into act_gs (x's from x, then h's from the gate/up output).
+// The down GEMM combines each token's k routing-weighted rows in its epilogue and writes out
+// (bf16 [T, H]).  act_gs: static activation scales (dev, [2]) or null; calibrate: instead of the
+// layer, write the static scales of this batch into act_gs (x's from x, then h's from the gate/up
+// output; out unused).
 cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
-                               const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s,
+                               const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, uint16_t* out,
                                const float* act_gs = nullptr, bool calibrate = false);
 cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
                               int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);

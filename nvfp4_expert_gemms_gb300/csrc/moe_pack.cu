@@ -113,17 +113,15 @@ __global__ void __launch_bounds__(256) nvfp4_pack_kernel(const uint16_t* __restr
   nvfp4_block(v, gs, (uint2*)(packed + (size_t)e * N * K / 2 + i * 8), scales + (size_t)e * nblk + i);
 }
 
-// Re-tile NVFP4 block scales [E, N, K/16] into [E, N/128, K/256, 128, 16]: thread = one
-// 16-byte (row, 256-column chunk) piece.
-__global__ void __launch_bounds__(256) nvfp4_retile_kernel(const uint4* __restrict__ src, int E, int N, int K,
-                                                           uint4* __restrict__ dst) {
+// Copy NVFP4 block scales [E, N, K/16] into tile atoms for the block-scaled MMA (every
+// 128-row tile of an expert matrix is one tile, so row n of expert e has slot e * N + n):
+// thread = one scale byte.
+__global__ void __launch_bounds__(256) nvfp4_retile_kernel(const uint8_t* __restrict__ src, int E, int N, int K,
+                                                           uint8_t* __restrict__ dst) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int nc = K / 256;
-  if (i >= (size_t)E * N * nc) return;
-  const size_t row = i / nc;  // e * N + n
-  const int c = (int)(i % nc), n = (int)(row % N);
-  const size_t e = row / N;
-  dst[((e * (N / 128) + n / 128) * nc + c) * 128 + n % 128] = src[i];
+  const int nb = K / 16;
+  if (i >= (size_t)E * N * nb) return;
+  dst[sf_atom_byte(i / nb, (int)(i % nb), nvfp4_chunks(K))] = src[i];
 }
 
 __global__ void nvfp4_finish_kernel(unsigned* slot, int E) {
@@ -136,8 +134,9 @@ __global__ void nvfp4_finish_kernel(unsigned* slot, int E) {
 }
 
 // Byte offset of the block scale of 16-block b of row d: row-major [rows, K/16], or with
-// sf_rows > 0 chunk-major [K/256][sf_rows][16] (every 256-column chunk of a run of rows is
-// one contiguous block, as the block-scaled MMA path loads it).
+// sf_rows > 0 chunk-major [C][sf_rows][16] (C = ceil(K/256); every 256-column chunk of a run of
+// rows is one contiguous block, as the block-scaled MMA path loads it; a last half chunk fills
+// 8 of its row's 16 bytes).
 __device__ __forceinline__ size_t sf_index(size_t d, int b, int K, int sf_rows) {
   return sf_rows ? ((size_t)(b >> 4) * sf_rows + d) * 16 + (b & 15) : d * (K / 16) + b;
 }
@@ -339,9 +338,8 @@ cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, co
       note_launches(2);
       const int bt = which == 0 ? MOE_T_GU_BT : MOE_T_D_BT;
       if (d.size[bt]) {
-        const size_t pieces = (size_t)E * N * (K / 256);
-        nvfp4_retile_kernel<<<(unsigned)((pieces + 255) / 256), 256, 0, s>>>((const uint4*)b, E, N, K,
-                                                                             (uint4*)(packed + d.offset[bt]));
+        const size_t n = (size_t)E * N * (K / 16);
+        nvfp4_retile_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(b, E, N, K, (uint8_t*)(packed + d.offset[bt]));
         note_launches(1);
       }
     }

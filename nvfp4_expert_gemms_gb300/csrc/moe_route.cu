@@ -26,6 +26,7 @@ struct Cand {
 __device__ __forceinline__ void zero_prelude(const RoutePrelude& pre) {
   const size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x, stride = (size_t)gridDim.x * blockDim.x;
   for (size_t i = g; i < pre.n_u32; i += stride) pre.zero_u32[i] = 0u;
+  for (size_t i = g; i < pre.n2_u32; i += stride) pre.zero2_u32[i] = 0u;
 }
 
 // max |x| of token t's activation row (one warp); all loads are issued before use.

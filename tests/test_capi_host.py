@@ -48,6 +48,11 @@ def test_packed_sizes_match_canonical_shapes(orc):
     assert int(d.size[M.MOE_T_GU_BT]) == int(d.size[M.MOE_T_GU_B]) and int(d.size[M.MOE_T_D_BT]) == int(
         d.size[M.MOE_T_D_B])
     assert int(M.moe_packed_size("nvfp4_w4a16", E, H, I).size[M.MOE_T_GU_BT]) == 0
+    # K not a multiple of 256: the copies hold whole 2 KB blocks per (128-row tile, 256-column
+    # chunk), the last chunk half used
+    d = M.moe_packed_size("nvfp4_w4a4", 3, 384, 640)
+    assert int(d.size[M.MOE_T_GU_BT]) == 3 * (2 * 640 // 128) * 2 * 2048
+    assert int(d.size[M.MOE_T_D_BT]) == 3 * (384 // 128) * 3 * 2048
 
 
 def test_packed_tensor_sizes_equal_oracle_outputs(orc):

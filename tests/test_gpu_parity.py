@@ -96,10 +96,13 @@ def test_bf16_pack_and_dequant_are_the_weights():
             assert got.tobytes() == synth.bf16_bits_to_f32(w[e]).tobytes()
 
 
-def test_w4a4_retiled_scales(orc):
-    """The W4A4 buffer's re-tiled scale copies are the canonical weight_scale tensors (bit-exact
-    with the oracle's packing) rearranged to [E, N/128, K/256, 128, 16]."""
-    E, H, I = 3, 512, 256
+@pytest.mark.parametrize("H,I", [(512, 256), (384, 640)])
+def test_w4a4_retiled_scales(orc, H, I):
+    """The W4A4 buffer's scale copies are the canonical weight_scale tensors (bit-exact with the
+    oracle's packing) in the tensor-memory atom order [E, N/128, C, 4, 32, 4, 4]: element
+    [e, t, c, s, l, j, i] = weight_scale[e, 128 t + 32 j + l, 16 c + 4 s + i] (C = ceil(K/256);
+    the unused upper half of a last half chunk is not compared)."""
+    E = 3
     wgu, wd = synth.gen_expert_weights(E, H, I, seed=6)
     layer = M.MoELayer("nvfp4_w4a4", dev_bf16(wgu), dev_bf16(wd))
     torch.cuda.synchronize()
@@ -109,9 +112,15 @@ def test_w4a4_retiled_scales(orc):
                                        (M.MOE_T_D_B, M.MOE_T_D_BT, "d", (H, I))):
         sc = M.packed_view(d, layer.packed, canon).cpu().numpy()
         assert sc.tobytes() == np.ascontiguousarray(ref[name][1]).tobytes()
-        want = sc.reshape(E, N // 128, 128, K // 256, 16).transpose(0, 1, 3, 2, 4)
+        C = (K + 255) // 256
         got = M.packed_view(d, layer.packed, tiled).cpu().numpy()
-        assert np.array_equal(got, want), name
+        assert got.shape == (E, N // 128, C, 4, 32, 4, 4)
+        for e in range(E):
+            for n in range(N):
+                t, j, l = n // 128, (n % 128) // 32, n % 32
+                for b in range(K // 16):
+                    c, st, i = b // 16, (b % 16) // 4, b % 4
+                    assert got[e, t, c, st, l, j, i] == sc[e, n, b], (name, e, n, b)
 
 
 @pytest.mark.parametrize("fmt", ["fp8", "int4", "nvfp4_w4a16"])
