@@ -105,12 +105,7 @@ moe_status_t device_ok() {
 
 static moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// Whether the format's down GEMM combines the k routing-weighted rows of each token itself
-// (else a separate combine launch follows it).
-static int combine_cols(int fmt, int row_block) {
-  (void)row_block;
-  return fmt == MOE_FMT_NVFP4_W4A4 ? 1 : 0;
-}
+
 
 // act_gs: null, or the static activation scales (dev, [2], W4A4 only).  calibrate: act_gs is
 // the output of the calibration instead (out unused, fp4 shapes only).
@@ -145,8 +140,7 @@ static moe_status_t forward_checked(const void* x, const float* logits, int T, c
     pre.H = d->H;
     pre.xmax = (float*)(w + L.xmax);
   }
-  const int ccols = combine_cols(d->fmt, rb);
-  if (ccols > 0 && k > 1 && !calibrate) {  // the down GEMM's completion counter starts at zero
+  if (!calibrate) {  // the down GEMM's completion counter (its combine waits on it) starts at zero
     pre.zero2_u32 = (unsigned*)(w + L.cnt);
     pre.n2_u32 = 1;
   }

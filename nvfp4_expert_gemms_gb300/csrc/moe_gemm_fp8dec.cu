@@ -30,6 +30,7 @@
 
 #include "moe_dec.cuh"
 #include "moe_formats.cuh"
+#include "moe_combine.cuh"
 #include "moe_tc.cuh"
 
 namespace moe {
@@ -60,6 +61,7 @@ struct Fp8Args {
   uint16_t* h_out;         // MODE 0 output [R, I] bf16
   unsigned* h_rowmax;      // MODE 0: running max |h| per permuted row (fp32 bits)
   uint16_t* y_out;         // MODE 1 output: routing-weighted rows [R, H] bf16, permuted order
+  CombineTail ct;        // MODE 1: the combine that follows the GEMM items
   int* err;
   int k, N, K, I, H;
 };
@@ -421,6 +423,11 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
   fence_after_sync();
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0 && s_abort) set_dev_error(a.err, kDevTimeout);
+  if (MODE == 1) {  // the routing-weighted combine, once every working CTA is done
+    __shared__ int s_flag;
+    if (!combine_tail(a.ct, min((int)gridDim.x, nwork), &s_flag) && threadIdx.x == 0)
+      set_dev_error(a.err, kDevTimeout);
+  }
 }
 
 }  // namespace
@@ -429,7 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1) fp8dec_kernel(const __grid_consta
 int fp8dec_row_block() { return kRows; }
 
 cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,
-                                  int k, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s) {
+                                  int k, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s,
+                                  uint16_t* out) {
   const int E = d.E, H = d.H, I = d.I;
   const size_t R = (size_t)T * k;
   const MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
@@ -447,6 +455,7 @@ cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed
   a.h_out = (uint16_t*)(ws + L.h);
   a.h_rowmax = (unsigned*)(ws + L.hmax);
   a.y_out = (uint16_t*)(ws + L.y);
+  combine_tail_args(a.ct, L, ws, T, k, H, out);
   a.err = (int*)(ws + L.err);
   a.k = k;
   a.I = I;

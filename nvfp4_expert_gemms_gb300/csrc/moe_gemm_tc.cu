@@ -30,6 +30,7 @@
 #include <unordered_map>
 
 #include "moe_formats.cuh"
+#include "moe_combine.cuh"
 #include "moe_tc.cuh"
 
 namespace moe {
@@ -100,6 +101,7 @@ struct TcArgs {
   const TileEntry* tiles;
   uint16_t* h_out;
   uint16_t* y_out;  // down: routing-weighted rows [R, H] bf16, permuted order
+  CombineTail ct;        // MODE 1: the combine that follows the GEMM items
   int* err;
   int* work_ctr;  // items handed out past each CTA's first (zeroed by routing)
   int k, N, K, I, H;
@@ -659,6 +661,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   fence_after_sync();
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0 && s_abort) set_dev_error(a.err, kDevTimeout);
+  if (MODE == 1) {  // the routing-weighted combine, once every working CTA is done
+    __shared__ int s_flag;
+    if (!combine_tail(a.ct, min((int)gridDim.x, nwork), &s_flag) && threadIdx.x == 0)
+      set_dev_error(a.err, kDevTimeout);
+  }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -768,7 +775,7 @@ int tc_row_block(int fmt, int T, int k, int E) {
 }
 
 cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
-                              int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s) {
+                              int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, uint16_t* out) {
   const int E = d.E, H = d.H, I = d.I;
   const size_t R = (size_t)T * k;
   const MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
@@ -779,6 +786,7 @@ cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, co
   a.tiles = (const TileEntry*)(ws + L.tiles);
   a.h_out = (uint16_t*)(ws + L.h);
   a.y_out = (uint16_t*)(ws + L.y);
+  combine_tail_args(a.ct, L, ws, T, k, H, out);
   a.err = (int*)(ws + L.err);
   a.k = k;
   a.I = I;

@@ -29,6 +29,7 @@
 
 #include "moe_dec.cuh"
 #include "moe_formats.cuh"
+#include "moe_combine.cuh"
 #include "moe_tc.cuh"
 #include "moe_w8a8.cuh"
 
@@ -105,6 +106,7 @@ struct W8Args {
   const TileEntry* tiles;
   uint16_t* h_out;       // MODE 0 output [R, I] bf16
   uint16_t* y_out;       // MODE 1 output: routing-weighted rows [R, H] bf16, permuted order
+  CombineTail ct;        // MODE 1: the combine that follows the GEMM items
   int* err;
   int* work_ctr;         // items handed out past each CTA's first (zeroed by routing)
   int k, N, K, I, H;
@@ -376,6 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const __grid_constant
   fence_after_sync();
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
   if (threadIdx.x == 0 && s_abort) set_dev_error(a.err, kDevTimeout);
+  if (MODE == 1) {  // the routing-weighted combine, once every working CTA is done
+    __shared__ int s_flag;
+    if (!combine_tail(a.ct, min((int)gridDim.x, nwork), &s_flag) && threadIdx.x == 0)
+      set_dev_error(a.err, kDevTimeout);
+  }
 }
 
 template <int MODE>
@@ -406,7 +413,7 @@ cudaError_t launch_quant_fp8_rows(const __nv_bfloat16* x, const int32_t* scatter
 }
 
 cudaError_t launch_experts_w8a8(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
-                                const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s) {
+                                const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, uint16_t* out) {
   const int E = d.E, H = d.H, I = d.I;
   const size_t R = (size_t)T * k;
   const MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
@@ -425,6 +432,7 @@ cudaError_t launch_experts_w8a8(const moe_packed_desc_t& d, const char* packed, 
   a.tiles = (const TileEntry*)(ws + L.tiles);
   a.h_out = (uint16_t*)(ws + L.h);
   a.y_out = (uint16_t*)(ws + L.y);
+  combine_tail_args(a.ct, L, ws, T, k, H, out);
   a.err = (int*)(ws + L.err);
   a.k = k;
   a.I = I;

@@ -189,8 +189,10 @@ bool tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
 int tc_num_sms();
 // FP8 decode path (16-row tiles, weights straight into kind::f8f6f4 MMAs).
 int fp8dec_row_block();
+// Each down GEMM ends with the deterministic routing-weighted combine into out (bf16 [T, H]).
 cudaError_t launch_experts_fp8dec(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,
-                                  int k, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);
+                                  int k, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s,
+                                  uint16_t* out);
 // NVFP4 W4A4 path on block-scaled FP4 MMAs (128-row routing tiles; any H, I multiples of 128).
 int fp4_row_block();
 // The down GEMM combines each token's k routing-weighted rows in its epilogue and writes out
@@ -201,6 +203,7 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
                                const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, uint16_t* out,
                                const float* act_gs = nullptr, bool calibrate = false);
 cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
-                              int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);
+                              int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, uint16_t* out);
+
 
 }  // namespace moe

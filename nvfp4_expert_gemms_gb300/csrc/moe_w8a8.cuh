@@ -21,8 +21,8 @@ cudaError_t launch_quant_fp8_rows(const __nv_bfloat16* x, const int32_t* scatter
 size_t w8a8_act_bytes(size_t R, int K);
 
 // The layer's two GEMMs (after routing): x -> FP8 per permuted row, gate/up (h in bf16),
-// h -> FP8, down (routing-weighted rows y).  The finalize step is the caller's.
+// h -> FP8, down (routing-weighted rows y), which ends with the combine into out (bf16 [T, H]).
 cudaError_t launch_experts_w8a8(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
-                                const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s);
+                                const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, uint16_t* out);
 
 }  // namespace moe
