@@ -104,7 +104,9 @@ struct W8Args {
   const int32_t* perm;
   const float* topk_w;
   const TileEntry* tiles;
-  uint16_t* h_out;       // MODE 0 output [R, I] bf16
+  uint16_t* h_out;
+  uint8_t* hq_out;       // MODE 2 output: h's E4M3 codes [R, I] and scale_inv group-major
+  float* hs_out;         //   [I/128][sf_rows] (h rounded to bf16, then quantized per 1x128 group)       // MODE 0 output [R, I] bf16
   uint16_t* y_out;       // MODE 1 output: routing-weighted rows [R, H] bf16, permuted order
   CombineTail ct;        // MODE 1: the combine that follows the GEMM items
   int* err;
@@ -124,10 +126,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)bf16_bits(lo) | ((uint32_t)bf16_bits(hi) << 16);
 }
 
-// MODE 0: gate/up (h in bf16), 1: down.
+// MODE 0: gate/up (h in bf16), 1: down, 2: gate/up with h quantized to FP8 in the epilogue.
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const __grid_constant__ W8Args a) {
-  constexpr bool kGateUp = MODE == 0;
+  constexpr bool kGateUp = MODE != 1, kFuseH = MODE == 2;
+  __shared__ uint32_t s_hmax[kFuseH ? 4 : 1][kFuseH ? kRows : 1];  // MODE 2: each column group's max |h| bits
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = (char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   char* sW = smem;
@@ -339,6 +342,50 @@ __global__ void __launch_bounds__(kThreads, 1) w8a8_kernel(const __grid_constant
         if (lane == 0) mbar_arrive(&p_empty[b]);
       }
       if (!named_bar_and(1, kPromWarps * 32, ok)) break;
+      if (kFuseH) {
+        // The item's 128 features of a row are exactly one 1x128 group of h, spread over the four
+        // column groups of lane quarter q (warps q, q + 4, q + 8, q + 12): h -> bf16, the group's
+        // max |h| through shared memory, then E4M3 codes with s = 448 / amax, as the activation
+        // quantizer does.  Every thread takes part (the rows past the tile too); only live rows
+        // are stored.
+        uint32_t hw[16], m = 0u;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float hv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float gv = acc[2 * j + e], uv = acc[32 + 2 * j + e];
+            hv[e] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+          }
+          hw[j] = pack_bf16x2(hv[0], hv[1]);
+          // max |h| on the bf16 bit patterns, NaN left out (as in quant_fp8_rows_kernel)
+          const uint32_t lo = hw[j] & 0x7FFFu, hi = (hw[j] >> 16) & 0x7FFFu;
+          m = max(m, max(lo <= 0x7F80u ? lo : 0u, hi <= 0x7F80u ? hi : 0u));
+        }
+        s_hmax[grp][r] = m;
+        named_bar_sync(2 + q, 4 * 32);
+        m = max(max(s_hmax[0][r], s_hmax[1][r]), max(s_hmax[2][r], s_hmax[3][r]));
+        named_bar_sync(2 + q, 4 * 32);  // s_hmax is rewritten for the next item
+        float amax = __uint_as_float(m << 16);
+        if (amax < 1e-12f) amax = 1e-12f;
+        const float sc = __fdiv_rn(448.0f, amax);
+        uint32_t cw[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t u0 = hw[2 * j], u1 = hw[2 * j + 1];
+          const uint32_t c01 = dec::e4m3x2(__fmul_rn(__uint_as_float(u0 << 16), sc),
+                                           __fmul_rn(__uint_as_float(u0 & 0xFFFF0000u), sc));
+          const uint32_t c23 = dec::e4m3x2(__fmul_rn(__uint_as_float(u1 << 16), sc),
+                                           __fmul_rn(__uint_as_float(u1 & 0xFFFF0000u), sc));
+          cw[j] = c01 | (c23 << 16);
+        }
+        if (live) {
+          const size_t row = (size_t)te.row0 + r;
+          st_global_v8(a.hq_out + row * a.I + w0 + 32 * grp, cw);
+          if (grp == 0) a.hs_out[(size_t)(w0 / 128) * a.sf_rows + row] = __fdiv_rn(1.0f, sc);
+        }
+        continue;
+      }
       if (!live) continue;
       if (kGateUp) {
         // features w0 + 32 grp .. + 31: gate in acc[j], up in acc[32 + j]
@@ -438,6 +485,8 @@ cudaError_t launch_experts_w8a8(const moe_packed_desc_t& d, const char* packed, 
   a.I = I;
   a.H = H;
   a.sf_rows = sf_rows;
+  a.hq_out = hq;
+  a.hs_out = hs;
   a.work_ctr = (int*)(ws + L.err) + 1;
   const int max_tiles = (int)(R / kRows + (R < (size_t)E ? R : (size_t)E) + 1);
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -451,13 +500,11 @@ cudaError_t launch_experts_w8a8(const moe_packed_desc_t& d, const char* packed, 
   a.N = 2 * I;
   a.K = H;
   record_event(ev.start[0], s);
-  err = launch_w8a8<0>(a, max_tiles * (I / 128), s);
+  err = launch_w8a8<2>(a, max_tiles * (I / 128), s);  // h leaves the epilogue as FP8 codes and scales
   record_event(ev.stop[0], s);
   if (err != cudaSuccess) return err;
 
-  // h -> FP8 per permuted row, then down: A = h rows, B = [H, I] weights
-  err = launch_quant_fp8_rows((const __nv_bfloat16*)(ws + L.h), nullptr, 1, (int)R, I, hq, hs, sf_rows, s);
-  if (err != cudaSuccess) return err;
+  // down: A = h rows (quantized by the gate/up epilogue), B = [H, I] weights
   if (!tc_make_map(&a.wcode, u8, dn.a, I, (uint64_t)E * H, I, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tc_make_map(&a.xcode, u8, hq, I, (uint64_t)R, I, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
