@@ -84,14 +84,18 @@ typedef enum {
  *          D_A  = weight_packed u8 [E, H, I/2]  D_B = weight_scale E4M3 [E, H, I/16]
  *          GU_GS / D_GS = weight_global_scale f32 [E] (the quantize multiplier 2688/amax)
  *   BF16:  GU_A = bf16 [E, 2I, H]               D_A = bf16 [E, H, I]  (the weights as given)
- *   NVFP4 W4A4 also carries a copy of each weight_scale tensor in the order the block-scaled
- *   tensor-core MMA reads it, one contiguous 2 KB block per (128-row tile, 256-column chunk)
- *   (C = ceil(K / 256) chunks; a last half chunk has its upper 1 KB unused):
- *          GU_BT = E4M3 [E, 2I/128, C(H), 4, 32, 4, 4]   D_BT = E4M3 [E, H/128, C(I), 4, 32, 4, 4]
- *          (element [e, t, c, s, l, j, i] = weight_scale[e, 128 t + 32 j + l, 16 c + 4 s + i]:
- *          per K = 64 step s, 32 rows of 16 bytes, row l holding the four scales of tile rows
- *          l, l + 32, l + 64, l + 96); written by moe_pack_experts next to the canonical tensors,
- *          not part of the checkpoint format.
+ *   NVFP4 W4A4 also carries both matrices as a tensor-core operand image: the same codes and
+ *   scales rearranged into the exact shared-memory image that one block-scaled MMA step reads,
+ *   so that each (pair of 128-row tiles, 256-column chunk) arrives in one bulk copy:
+ *          GU_IMG = u8 [E, I/128, C(H), 36864]   D_IMG = u8 [E, ceil(H/256), C(I), 36864]
+ *   (C(K) = ceil(K/256) chunks).  Block [e, p, c]: tile 0 = rows r0 .. r0+127, tile 1 = rows
+ *   r1 .. r1+127 (gate/up: r0 = 128p gate rows, r1 = I + 128p the matching up rows; down:
+ *   r0 = 256p, r1 = 256p + 128, a tile past H all zero); bytes [16384 g, 16384 g + 16384) hold
+ *   tile g's codes of columns 256c .. 256c+255, row l's 128 bytes at 128 l with 16-byte piece j
+ *   stored at piece j ^ (l % 8) (the 128-byte swizzle); bytes [32768 + 2048 g, + 2048) hold
+ *   tile g's scales in the order tensor memory takes them: byte 512 s + 16 l + 4 j + i = the
+ *   scale of row 32 j + l, 16-block 16c + 4s + i.  Columns past K (a last half chunk) are zero.
+ *   Written by moe_pack_experts next to the canonical tensors; not part of the checkpoint format.
  * Every tensor starts on a 256-byte boundary of the packed buffer. */
 enum {
   MOE_T_GU_A = 0,
@@ -100,8 +104,8 @@ enum {
   MOE_T_D_B = 3,
   MOE_T_GU_GS = 4,
   MOE_T_D_GS = 5,
-  MOE_T_GU_BT = 6,
-  MOE_T_D_BT = 7,
+  MOE_T_GU_IMG = 6,
+  MOE_T_D_IMG = 7,
   MOE_T_COUNT = 8
 };
 

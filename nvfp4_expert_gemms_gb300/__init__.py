@@ -25,7 +25,7 @@ FMT_FP8_W8A8 = 6
 FORMATS = {"fp8": FMT_FP8, "int4": FMT_INT4, "nvfp4_w4a16": FMT_NVFP4_W4A16, "nvfp4_w4a4": FMT_NVFP4_W4A4,
            "bf16": FMT_BF16, "fp8_w8a8": FMT_FP8_W8A8}
 
-MOE_T_GU_A, MOE_T_GU_B, MOE_T_D_A, MOE_T_D_B, MOE_T_GU_GS, MOE_T_D_GS, MOE_T_GU_BT, MOE_T_D_BT = range(8)
+MOE_T_GU_A, MOE_T_GU_B, MOE_T_D_A, MOE_T_D_B, MOE_T_GU_GS, MOE_T_D_GS, MOE_T_GU_IMG, MOE_T_D_IMG = range(8)
 
 EXPORTS = ("moe_packed_size", "moe_pack_experts", "moe_workspace_size", "moe_layer_forward",
            "moe_workspace_size_host_io", "moe_layer_forward_host", "moe_get_device_error", "moe_status_string",
@@ -265,12 +265,12 @@ def packed_view(desc: PackedDesc, packed, which: int):
     o, n = int(desc.offset[which]), int(desc.size[which])
     raw = packed[o:o + n]
     fmt = desc.fmt
-    gu = which in (MOE_T_GU_A, MOE_T_GU_B, MOE_T_GU_BT)
+    gu = which in (MOE_T_GU_A, MOE_T_GU_B, MOE_T_GU_IMG)
     N, K = (2 * I, H) if gu else (H, I)
     if which in (MOE_T_GU_GS, MOE_T_D_GS):
         return raw.view(torch.float32)
-    if which in (MOE_T_GU_BT, MOE_T_D_BT):  # tensor-memory atom order (include/moe_gb300.h)
-        return raw.view(E, N // 128, (K + 255) // 256, 4, 32, 4, 4)
+    if which in (MOE_T_GU_IMG, MOE_T_D_IMG):  # tensor-core operand image (include/moe_gb300.h)
+        return raw.view(E, N // 256 if gu else (N + 255) // 256, (K + 255) // 256, 36864)
     if fmt == FMT_BF16:
         return raw.view(torch.bfloat16).view(E, N, K)
     if fmt in (FMT_FP8, FMT_FP8_W8A8):

@@ -33,6 +33,7 @@ WsLayout route_layout(int E, int T, int k) {
   L.blkcnt = take(4 * (size_t)L.nb * E);
   L.blkbase = take(4 * (size_t)L.nb * E);
   L.offsets = take(4 * (size_t)(E + 1));
+  L.toff = take(4 * (size_t)(E + 1));
   L.perm = take(4 * R);
   L.inv = take(4 * R);
   L.tiles = take(sizeof(TileEntry) * (size_t)(L.max_tiles + 1));
@@ -54,12 +55,11 @@ WsLayout ws_layout(int fmt, int E, int H, int I, int T, int k, bool host_io) {
   L.cnt = take(256);
   L.xmax = take(4 * (size_t)T);
   L.hmax = take(4 * R);
-  if (fmt == MOE_FMT_NVFP4_W4A4) {  // activation codes per permuted row (first T rows: per token)
-    L.xq = take(R * H / 2);
-    L.xs = take((size_t)sf_plane_rows(R) * nvfp4_chunks(H) * 16);
+  if (fmt == MOE_FMT_NVFP4_W4A4) {  // x and h as operand images per 128-row routing tile + row scales
+    const size_t tiles = R / 128 + (R < (size_t)E ? R : (size_t)E) + 1;
+    L.xi = take(tiles * nvfp4_chunks(H) * kAImgBlock);
     L.xg = take(4 * R);
-    L.hq = take(R * I / 2);
-    L.hs = take((size_t)sf_plane_rows(R) * nvfp4_chunks(I) * 16);
+    L.hi = take(tiles * nvfp4_chunks(I) * kAImgBlock);
     L.hg = take(4 * R);
   }
   if (fmt == MOE_FMT_FP8_B128_W8A8) {  // E4M3 codes per permuted row + group-major 1x128 scales
@@ -195,9 +195,9 @@ moe_status_t moe_packed_size(int fmt, int E, int H, int I, moe_packed_desc_t* d)
       sz[MOE_T_D_B] = e * dn / 16;
       sz[MOE_T_GU_GS] = e * 4;
       sz[MOE_T_D_GS] = e * 4;
-      if (fmt == MOE_FMT_NVFP4_W4A4) {  // scales again, in the tile atoms the block-scaled MMA reads
-        sz[MOE_T_GU_BT] = e * (2 * (size_t)I / 128) * nvfp4_chunks(H) * 2048;
-        sz[MOE_T_D_BT] = e * ((size_t)H / 128) * nvfp4_chunks(I) * 2048;
+      if (fmt == MOE_FMT_NVFP4_W4A4) {  // codes and scales again, as the tensor-core operand image
+        sz[MOE_T_GU_IMG] = e * ((size_t)I / 128) * nvfp4_chunks(H) * kWImgBlock;
+        sz[MOE_T_D_IMG] = e * (((size_t)H + 255) / 256) * nvfp4_chunks(I) * kWImgBlock;
       }
       break;
   }

@@ -14,17 +14,20 @@
 // gate/up: the 256 weight rows are 128 gate rows over the 128 matching up rows, so a thread
 // of the epilogue holds gate and up of the same features of its token; down: 256 consecutive
 // output features.  An N = 256 block-scaled MMA costs the tensor pipe the same issue time as
-// N = 64 or 128, so one instruction per K step covers what two N = 128 ones did.  Codes arrive
-// by TMA tiles in the 128-byte swizzle (x is quantized straight into permuted row order, one copy
-// per routed token slot, so the gate/up GEMM needs no row gather).  The block scales of a
-// (128-row tile, 256-column chunk) are one contiguous 2 KB block each: the packed weight copy
-// keeps them in the order tensor memory wants them (per K = 64 step a 512-byte atom whose row l
-// holds the four scales of tile rows l, l + 32, l + 64, l + 96), the activation quantizer writes
-// them chunk-major ([chunk][row][16]); each arrives by one bulk copy next to its codes, and four
-// scale warps move both into tensor memory with tcgen05.st (measured faster than tcgen05.cp
-// issued by the MMA thread, which shares the tensor pipe with the MMAs).  K need not be a
-// multiple of 256: a last half chunk (128 columns) issues two K steps, its upper half being TMA
-// fill that no MMA reads.
+// N = 64 or 128, so one instruction per K step covers what two N = 128 ones did.
+// Both operands are read from operand images (moe_internal.cuh, ActImage): the packed weights
+// and the quantized activations are laid out in global memory exactly as one K chunk of an item
+// sits in shared memory -- codes in the 128-byte swizzle, block scales in the order the scale
+// warps move them -- so a chunk of each operand arrives by ONE bulk copy.  (A TMA unit's cost
+// is per copy and nearly independent of its size up to tens of KB: three 16 KB tensor tiles and
+// three 2 KB scale copies per chunk took ~1.07 us, the two image copies ~0.94 us.)  x is
+// quantized straight into its image (one copy per routed token slot, at its routing tile's row),
+// so the gate/up GEMM needs no row gather; h likewise.  The weight scale image keeps, per K = 64
+// step, a 512-byte atom whose row l holds the four scales of tile rows l, l + 32, l + 64, l + 96;
+// the activation scales are 16 bytes per row; four scale warps move both into tensor memory
+// with tcgen05.st (measured faster than tcgen05.cp issued by the MMA thread, which shares the
+// tensor pipe with the MMAs).  K need not be a multiple of 256: a last half chunk (128 columns)
+// issues two K steps, its upper half (zero in the images) unread.
 //
 // The down GEMM also combines, deterministically: its epilogue stores the routing-weighted bf16
 // row of (token t, slot j) at row t * k + j of a slot-ordered buffer, a signal warp publishes
@@ -77,11 +80,9 @@ struct Roles {
 static_assert(2 * kCombBuf <= kStages * (kWStage + kXStage), "combine buffers live in the stage memory");
 
 struct Fp4Args {
-  CUtensorMap wcode;        // weight codes [E*N, K/2]
-  CUtensorMap xcode;        // activation codes [R, K/2], permuted row order
-  const uint8_t* wsft;      // weight block scales in tile atoms [E, N/128, C, 2048]
-  const uint8_t* asft;      // activation block scales chunk-major [C][sf_rows][16]
-  int sf_rows;
+  const uint8_t* wimg;      // weight operand image [E, P, C, kWImgBlock] (P = tile pairs per expert)
+  const uint8_t* aimg;      // activation operand image [tiles, C, kAImgBlock]
+  int C, P;                 // K chunks, weight tile pairs
   const float* wgs;         // weight global scales [E]
   const float* ags;         // activation global scales [R]
   const int32_t* perm;
@@ -89,8 +90,8 @@ struct Fp4Args {
   const TileEntry* tiles;
   uint16_t* h_out;          // MODE 0 output [R, I] bf16 (dynamic activation scales)
   const float* hgs_static;  // MODE 2 (gate/up, static activation scales): h's global scale (dev); h
-  uint8_t* hq_out;          //   leaves NVFP4-quantized instead: codes [R, I/2], chunk-major block
-  uint8_t* hsf_out;         //   scales [C(I)][sf_rows][16] and the global scale per row [R]
+  uint8_t* hq_out;          //   leaves NVFP4-quantized instead, into its operand image [tiles, C(I), ..]
+  int hC;                   //   (C(I) chunks), with the global scale per routed row [R]
   float* hg_out;
   uint16_t* comb;           // MODE 1: routing-weighted rows [T*k, H] bf16, row t*k + j = (token t, slot j)
   int* done;                // MODE 1: GEMM items finished (their rows published), zero on entry
@@ -222,10 +223,6 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1) fp4_kernel(const __g
     tmem_alloc(&s_tmem, 512);
     tmem_relinquish();
   }
-  if (warp == kProdWarp && lane == 0) {
-    prefetch_tmap(&a.wcode);
-    prefetch_tmap(&a.xcode);
-  }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -321,30 +318,20 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1) fp4_kernel(const __g
         const int st = it % kStages;
         if (lane == 0) {
           ok = mbar_wait(&w_empty[st], ((it / kStages) & 1) ^ 1, &s_abort);
-          if (ok) {
-            char* ws = sW + st * kWStage;
-            mbar_arrive_expect_tx(&w_full[st], 2 * (kWCodes + kSfBlock));
+          if (ok) {  // one bulk copy: both weight tiles' codes and scales of this chunk
+            mbar_arrive_expect_tx(&w_full[st], kWImgBlock);
             ++armed_w[st];
-            for (int g = 0; g < 2; ++g) {
-              const int wr = g == 0 ? w0 : w1;
-              tma_load_2d(ws + g * kWCodes, &a.wcode, &w_full[st], kc * (kKC / 2), te.expert * a.N + wr);
-              // the 128 rows' scales of this chunk (a second tile past N -- the last down column
-              // block when H % 256 = 128 -- computes columns nobody stores: any finite scales do)
-              const int sr = wr < a.N ? wr : w0;
-              const size_t blk = ((size_t)te.expert * (a.N / 128) + sr / 128) * nK + kc;
-              bulk_load(ws + 2 * kWCodes + g * kSfBlock, a.wsft + blk * kSfBlock, kSfBlock, &w_full[st]);
-            }
+            const int pair = kGateUp ? w0 / 128 : w0 / 256;
+            bulk_load(sW + st * kWStage, a.wimg + (((size_t)te.expert * a.P + pair) * a.C + kc) * kWImgBlock,
+                      kWImgBlock, &w_full[st]);
           }
           if (ok) {
             ok = mbar_wait(&x_empty[st], ((it / kStages) & 1) ^ 1, &s_abort);
             if (MODE == 1 && it == 0) pdl_wait();
-            if (ok) {
-              mbar_arrive_expect_tx(&x_full[st], kXStage);
+            if (ok) {  // one bulk copy: the routing tile's codes and scales of this chunk
+              mbar_arrive_expect_tx(&x_full[st], kAImgBlock);
               ++armed_x[st];
-              tma_load_2d(sX + st * kXStage, &a.xcode, &x_full[st], kc * (kKC / 2), te.row0);
-              // the 128 rows' scales of this chunk: one contiguous 2 KB block of the chunk plane
-              bulk_load(sX + st * kXStage + kXCodes, a.asft + ((size_t)kc * a.sf_rows + te.row0) * 16, kRows * 16,
-                        &x_full[st]);
+              bulk_load(sX + st * kXStage, a.aimg + ((size_t)tile * a.C + kc) * kAImgBlock, kAImgBlock, &x_full[st]);
             }
           }
         }
@@ -606,12 +593,14 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1) fp4_kernel(const __g
             hs4 |= (uint32_t)sc << (8 * blk);
           }
         }
-        if (kFuseH && live) {
-          const size_t row = (size_t)te.row0 + r;
+        if (kFuseH && live) {  // into h's operand image: row r of routing tile `tile`
           const int f0 = w0 + 64 * half;  // four whole blocks = one K step of one 256-column chunk
-          st_global_v8(a.hq_out + row * (a.I / 2) + f0 / 2, hc);
-          *(uint32_t*)(a.hsf_out + ((size_t)(f0 >> 8) * a.sf_rows + row) * 16 + ((f0 & 255) >> 4)) = hs4;
-          if (f0 == 0) a.hg_out[row] = ghs;
+          const int b0 = (f0 & 255) >> 4;
+          uint8_t* blk = a.hq_out + ((size_t)tile * a.hC + (f0 >> 8)) * kAImgBlock;
+          *(uint4*)(blk + img_code_byte(r, b0)) = make_uint4(hc[0], hc[1], hc[2], hc[3]);
+          *(uint4*)(blk + img_code_byte(r, b0 + 2)) = make_uint4(hc[4], hc[5], hc[6], hc[7]);
+          *(uint32_t*)(blk + kImgTile + 16 * r + b0) = hs4;
+          if (f0 == 0) a.hg_out[te.row0 + r] = ghs;
         }
       } else {
         // output features fb .. fb + 127 of the routing-weighted row of (token t, slot p % k): to
@@ -683,14 +672,21 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   const int E = d.E, H = d.H, I = d.I;
   const size_t R = (size_t)T * k;
   const MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
-  uint8_t* xq = (uint8_t*)(ws + L.xq);
-  uint8_t* hq = (uint8_t*)(ws + L.hq);
-  uint8_t* xsf = (uint8_t*)(ws + L.xs);
-  uint8_t* hsf = (uint8_t*)(ws + L.hs);
-  const int sf_rows = sf_plane_rows(R);
+  // x and h go straight into their operand images (slot of routed row p: 128 toff[e] + p - off[e])
+  ActImage xim, him;
+  xim.img = (uint8_t*)(ws + L.xi);
+  xim.chunks = nvfp4_chunks(H);
+  xim.topk_idx = (const int32_t*)(ws + L.topk_idx);
+  xim.perm = (const int32_t*)(ws + L.perm);
+  xim.offsets = (const int32_t*)(ws + L.offsets);
+  xim.toff = (const int32_t*)(ws + L.toff);
+  him = xim;
+  him.img = (uint8_t*)(ws + L.hi);
+  him.chunks = nvfp4_chunks(I);
   float* cal = calibrate ? const_cast<float*>(act_gs) : nullptr;  // calibration writes the two scales
   if (cal && launch_act_scale((const uint16_t*)x, (size_t)T * H, cal, s) != cudaSuccess) return cudaGetLastError();
-  launch_quant_rows(x, (const int32_t*)(ws + L.inv), k, T, H, xq, xsf, (float*)(ws + L.xg), s, !cal, sf_rows, act_gs);
+  launch_quant_rows(x, (const int32_t*)(ws + L.inv), k, T, H, nullptr, nullptr, (float*)(ws + L.xg), s, !cal, 0, act_gs,
+                    &xim);
 
   Fp4Args a;
   memset(&a, 0, sizeof(a));
@@ -699,9 +695,8 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   a.tiles = (const TileEntry*)(ws + L.tiles);
   a.h_out = (uint16_t*)(ws + L.h);
   a.hgs_static = act_gs && !calibrate ? act_gs + 1 : nullptr;
-  a.hq_out = hq;
-  a.hsf_out = hsf;
-  a.sf_rows = sf_rows;
+  a.hq_out = him.img;
+  a.hC = him.chunks;
   a.hg_out = (float*)(ws + L.hg);
   a.comb = (uint16_t*)(ws + L.y);
   a.done = (int*)(ws + L.cnt);
@@ -713,14 +708,12 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   a.H = H;
   a.work_ctr = (int*)(ws + L.err) + 1;
   const int max_tiles = (int)(R / kRows + (R < (size_t)E ? R : (size_t)E) + 1);
-  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 
-  // gate/up: A = quantized x in permuted row order, B = fused [2I, H] NVFP4 weights
-  if (!tc_make_map(&a.wcode, u8, gu.a, H / 2, (uint64_t)E * 2 * I, H / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc_make_map(&a.xcode, u8, xq, H / 2, (uint64_t)R, H / 2, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
-  a.wsft = (const uint8_t*)packed + d.offset[MOE_T_GU_BT];
-  a.asft = xsf;
+  // gate/up: A = x's image (routing tiles), B = the fused [2I, H] weights' image (gate/up tile pairs)
+  a.wimg = (const uint8_t*)packed + d.offset[MOE_T_GU_IMG];
+  a.aimg = xim.img;
+  a.C = xim.chunks;
+  a.P = I / 128;
   a.wgs = gu.gs;
   a.ags = (const float*)(ws + L.xg);
   a.N = 2 * I;
@@ -731,16 +724,15 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
   if (err != cudaSuccess) return err;
 
   if (cal) return launch_act_scale((const uint16_t*)(ws + L.h), R * I, cal + 1, s);  // h's scale; no down GEMM
-  // h -> NVFP4 per permuted row (its own global scale; with static scales the gate/up epilogue
-  // has already quantized it), then down: A = h rows, B = [H, I] weights; the epilogue combines
+  // h -> NVFP4 per routed row (its own global scale; with static scales the gate/up epilogue has
+  // already quantized it), then down: A = h's image, B = the [H, I] weights' image; the epilogue combines
   if (!act_gs)
-    launch_quant_rows((const __nv_bfloat16*)(ws + L.h), nullptr, 1, (int)R, I, hq, hsf, (float*)(ws + L.hg), s, false,
-                      sf_rows);
-  if (!tc_make_map(&a.wcode, u8, dn.a, I / 2, (uint64_t)E * H, I / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc_make_map(&a.xcode, u8, hq, I / 2, (uint64_t)R, I / 2, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
-  a.wsft = (const uint8_t*)packed + d.offset[MOE_T_D_BT];
-  a.asft = hsf;
+    launch_quant_rows((const __nv_bfloat16*)(ws + L.h), nullptr, 1, (int)R, I, nullptr, nullptr, (float*)(ws + L.hg),
+                      s, false, 0, nullptr, &him);
+  a.wimg = (const uint8_t*)packed + d.offset[MOE_T_D_IMG];
+  a.aimg = him.img;
+  a.C = him.chunks;
+  a.P = (H + 255) / 256;
   a.wgs = dn.gs;
   a.ags = (const float*)(ws + L.hg);
   a.N = H;

@@ -72,7 +72,9 @@ __device__ __forceinline__ TileEntry load_tile(const TileEntry* p) {
 // ---- workspace layout ----------------------------------------------------------------------
 struct WsLayout {
   size_t err, topk_idx, topk_w, blkcnt, blkbase, offsets, perm, inv, tiles;
+  size_t toff;  // first routing tile of each expert [E + 1]
   size_t h, y, xq, xs, xg, hq, hs, hg;  // y: routing-weighted down rows [R, H] bf16
+  size_t xi, hi;  // W4A4: x and h as tensor-core operand images (ActImage)
   size_t cnt;         // the down GEMM's completion counter (zeroed by routing)
   size_t xp;          // expert-permuted bf16 copy of x (tensor-core path, row blocks >= 64)
   size_t xmax, hmax;  // per-row max |activation| (FP8 decode path)
@@ -108,27 +110,51 @@ cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, co
                         char* packed, cudaStream_t s);
 cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e, int which, float* out,
                            cudaStream_t s);
-// ---- NVFP4 weight block scales in the order the block-scaled MMA reads them ------------------
-// The MMA takes the E4M3 block scales from tensor memory, where for one K = 64 step of a 128-row
-// tile lane l (of every lane quarter), column j holds the four scales of tile row l + 32 j.  The
-// packed weight copy keeps them in that order -- per K step a 512-byte "atom", byte
-// 16 l + 4 j + i = scale i of row l + 32 j -- four atoms (2 KB) per (128-row tile, 256-column
-// chunk), contiguous per (tile, chunk): byte index of 16-block b of slot s (tile s / 128, row
-// s % 128):
+// ---- NVFP4 W4A4 tensor-core operand images --------------------------------------------------
+// One block-scaled MMA step reads, per 128-row tile and 256-column chunk, 16 KB of E2M1 codes in
+// the 128-byte swizzle layout and 2 KB of E4M3 block scales.  The W4A4 path keeps both operands
+// in exactly that shape in global memory, so each stage of the GEMMs is one bulk copy per
+// operand (a TMA unit's cost is per copy, nearly independent of its size):
+//   weights     (packed buffer)  [E, pairs, C, kWImgBlock]: two 128-row tiles (gate/up: a gate
+//               tile and the matching up tile; down: 256 consecutive output rows) -> codes of
+//               tile 0, codes of tile 1, scales of tile 0, scales of tile 1, the scales in the
+//               order tensor memory takes them (per K = 64 step a 512-byte atom whose 16-byte
+//               row l holds the four scales of tile rows l, l + 32, l + 64, l + 96);
+//   activations (workspace)      [tiles, C, kAImgBlock]: one routing tile -> codes, then the
+//               scales row by row (16 bytes per row).
+// C = ceil(K / 256); a last half chunk leaves its upper 64 bytes per row unused.
+constexpr int kImgTile = 16384, kImgSf = 2048;
+constexpr int kWImgBlock = 2 * kImgTile + 2 * kImgSf, kAImgBlock = kImgTile + kImgSf;
 __host__ __device__ inline int nvfp4_chunks(int K) { return (K + 255) / 256; }
-__host__ __device__ inline size_t sf_atom_byte(size_t slot, int b, int nchunks) {
-  return ((slot >> 7) * (size_t)nchunks + (size_t)(b >> 4)) * 2048 + (size_t)((b & 15) >> 2) * 512 +
-         16 * (slot & 31) + 4 * ((slot & 127) >> 5) + (size_t)(b & 3);
+// Byte of the 8 codes of 16-block b (0..15 of the chunk) of tile row l within a tile's codes.
+__host__ __device__ inline int img_code_byte(int l, int b) { return 128 * l + (((b >> 1) ^ (l & 7)) << 4) + 8 * (b & 1); }
+// Weight scale of tile row l, 16-block b (0..15 of the chunk), within a tile's scale atoms.
+__host__ __device__ inline int img_wsf_byte(int l, int b) { return 512 * (b >> 2) + 16 * (l & 31) + 4 * (l >> 5) + (b & 3); }
+// Routed row p of expert e is row slot % 128 of routing tile slot / 128 (128-row tiles).
+__device__ __forceinline__ int img_slot(int p, int e, const int32_t* offsets, const int32_t* toff) {
+  return 128 * toff[e] + p - offsets[e];
 }
+// Where a quantizer puts NVFP4 activation rows instead of row-major codes: the operand image.
+// Rows are routed (permuted) rows; a row's expert comes from topk_idx at its (token, slot) index
+// (the scatter index for x, perm[row] for h).
+struct ActImage {
+  uint8_t* img = nullptr;
+  int chunks = 0;
+  const int32_t* topk_idx = nullptr;
+  const int32_t* perm = nullptr;
+  const int32_t* offsets = nullptr;
+  const int32_t* toff = nullptr;
+};
 // NVFP4 quantization of bf16 rows; row r's codes go to output row r, or (scatter != null) to
 // rows scatter[r*k .. r*k+k-1].  early: x was final before the preceding kernel of the stream
 // passed its pdl_wait() (true only right after routing), so x is read before this launch's wait.
 // sf_rows = 0: scales row-major [rows, K/16]; else chunk-major [C][sf_rows][16], C = ceil(K/256).
 // static_gs (dev, one float) != null: that global scale for every row instead of each row's own.
 // gs may be null (the per-row scales are then not stored).
+// img != null: codes and scales go to the operand image instead (q, sf unused).
 cudaError_t launch_quant_rows(const __nv_bfloat16* x, const int32_t* scatter, int k, int rows, int K, uint8_t* q,
                               uint8_t* sf, float* gs, cudaStream_t s, bool early = false, int sf_rows = 0,
-                              const float* static_gs = nullptr);
+                              const float* static_gs = nullptr, const ActImage* img = nullptr);
 // Rows of one chunk plane of chunk-major activation scales for R routed rows: a 128-row tile
 // starting at any row below R stays inside its plane.
 inline int sf_plane_rows(size_t R) { return (int)R + 128; }

@@ -113,15 +113,34 @@ __global__ void __launch_bounds__(256) nvfp4_pack_kernel(const uint16_t* __restr
   nvfp4_block(v, gs, (uint2*)(packed + (size_t)e * N * K / 2 + i * 8), scales + (size_t)e * nblk + i);
 }
 
-// Copy NVFP4 block scales [E, N, K/16] into tile atoms for the block-scaled MMA (every
-// 128-row tile of an expert matrix is one tile, so row n of expert e has slot e * N + n):
-// thread = one scale byte.
-__global__ void __launch_bounds__(256) nvfp4_retile_kernel(const uint8_t* __restrict__ src, int E, int N, int K,
-                                                           uint8_t* __restrict__ dst) {
+// The W4A4 operand image of one expert matrix [E, N, K] (canonical codes [E, N, K/2] and block
+// scales [E, N, K/16] in, ActImage layout out): thread = one row of one (tile pair, chunk) block,
+// writing its 128 code bytes (16-byte pieces swizzled) and its 16 scales.  gate/up (gu): pair p
+// = gate rows 128p.. over up rows I + 128p..; down: rows 256p .. 256p + 255 (rows past N zero).
+// Columns past K (a last half chunk) are zero.
+__global__ void __launch_bounds__(256) nvfp4_image_kernel(const uint8_t* __restrict__ codes,
+                                                          const uint8_t* __restrict__ scales, int E, int N, int K,
+                                                          bool gu, uint8_t* __restrict__ img) {
+  const int C = nvfp4_chunks(K), P = gu ? N / 256 : (N + 255) / 256;
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int nb = K / 16;
-  if (i >= (size_t)E * N * nb) return;
-  dst[sf_atom_byte(i / nb, (int)(i % nb), nvfp4_chunks(K))] = src[i];
+  if (i >= (size_t)E * P * C * 256) return;
+  const int nl = (int)(i % 256), c = (int)((i / 256) % C), p = (int)((i / 256 / C) % P), e = (int)(i / 256 / C / P);
+  const int g = nl >> 7, l = nl & 127;
+  const int n = gu ? (g == 0 ? 128 * p + l : N / 2 + 128 * p + l) : 256 * p + nl;
+  uint8_t* blk = img + (((size_t)e * P + p) * C + c) * kWImgBlock;
+  uint8_t* tcodes = blk + g * kImgTile;
+  uint8_t* tsf = blk + 2 * kImgTile + g * kImgSf;
+  const int kb = min(128, K / 2 - 128 * c);  // code bytes of this row in the chunk (64 for a half chunk)
+  const bool row_ok = n < N;
+  const uint8_t* src = codes + ((size_t)e * N + (row_ok ? n : 0)) * (K / 2) + 128 * c;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (row_ok && 16 * j < kb) v = *(const uint4*)(src + 16 * j);
+    *(uint4*)(tcodes + 128 * l + ((j ^ (l & 7)) << 4)) = v;
+  }
+  const uint8_t* ssrc = scales + ((size_t)e * N + (row_ok ? n : 0)) * (K / 16) + 16 * c;
+  for (int b = 0; b < 16; ++b) tsf[img_wsf_byte(l, b)] = row_ok && 8 * b < kb ? ssrc[b] : (uint8_t)0;
 }
 
 __global__ void nvfp4_finish_kernel(unsigned* slot, int E) {
@@ -149,7 +168,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
                                                          const int32_t* __restrict__ scatter, int k, int rows, int K,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                          float* __restrict__ gs_out, int sf_rows,
-                                                         const float* __restrict__ static_gs) {
+                                                         const float* __restrict__ static_gs, ActImage im) {
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   pdl_wait();
@@ -184,9 +203,18 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
     uint8_t scale;
     nvfp4_block(v, gs, &code, &scale);
     for (int c = 0; c < ncopy; ++c) {
-      const size_t d = scatter ? (size_t)scatter[(size_t)r * k + c] : (size_t)r;
-      *(uint2*)(q + d * (K / 2) + b * 8) = code;
-      sf[sf_index(d, b, K, sf_rows)] = scale;
+      const size_t src = scatter ? (size_t)r * k + c : 0;
+      const size_t d = scatter ? (size_t)scatter[src] : (size_t)r;
+      if (im.img) {
+        const int e = im.topk_idx[scatter ? src : (size_t)im.perm[d]];
+        const int slot = img_slot((int)d, e, im.offsets, im.toff);
+        uint8_t* blk = im.img + ((size_t)(slot >> 7) * im.chunks + (b >> 4)) * kAImgBlock;
+        *(uint2*)(blk + img_code_byte(slot & 127, b & 15)) = code;
+        blk[kImgTile + 16 * (slot & 127) + (b & 15)] = scale;
+      } else {
+        *(uint2*)(q + d * (K / 2) + b * 8) = code;
+        sf[sf_index(d, b, K, sf_rows)] = scale;
+      }
     }
   }
 }
@@ -203,7 +231,7 @@ __global__ void __launch_bounds__(256) quant_rows_flat_kernel(const uint16_t* __
                                                               const int32_t* __restrict__ scatter, int k, int rows,
                                                               uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                               float* __restrict__ gs_out, int sf_rows,
-                                                              const float* __restrict__ static_gs) {
+                                                              const float* __restrict__ static_gs, ActImage im) {
   constexpr int K = 16 * NBLK, kFlat = NBLK * RPW, NB = (kFlat + 31) / 32;
   static_assert(NB <= 8 && RPW * kMaxTopK <= 32, "flat quantizer shape");
   const int lane = threadIdx.x & 31;
@@ -247,11 +275,16 @@ __global__ void __launch_bounds__(256) quant_rows_flat_kernel(const uint16_t* __
   }
   // destinations: lane rr*k + c holds row rr's copy c (scatter), else row r0 + rr
   const int ncopy = scatter ? k : 1;
-  int my_dst = 0;
+  int my_dst = 0, my_slot = 0;  // permuted row, and with an image its slot there
   if (scatter) {
-    if (lane < RPW * k && r0 + lane / k < rows) my_dst = scatter[(size_t)(r0 + lane / k) * k + lane % k];
+    if (lane < RPW * k && r0 + lane / k < rows) {
+      const size_t src = (size_t)(r0 + lane / k) * k + lane % k;
+      my_dst = scatter[src];
+      if (im.img) my_slot = img_slot(my_dst, im.topk_idx[src], im.offsets, im.toff);
+    }
   } else {
     my_dst = r0 + lane;
+    if (im.img && lane < RPW && my_dst < rows) my_slot = img_slot(my_dst, im.topk_idx[im.perm[my_dst]], im.offsets, im.toff);
   }
 #pragma unroll
   for (int rr = 0; rr < RPW; ++rr)
@@ -275,10 +308,18 @@ __global__ void __launch_bounds__(256) quant_rows_flat_kernel(const uint16_t* __
     uint8_t scale;
     nvfp4_encode(v, __uint_as_float(bmax[j] << 16), g, &code, &scale);
     for (int c = 0; c < ncopy; ++c) {  // warp-uniform trip count: the shuffle sees every lane
-      const int d = __shfl_sync(0xffffffffu, my_dst, (row < RPW ? row : 0) * ncopy + c);
+      const int from = (row < RPW ? row : 0) * ncopy + c;
+      const int d = __shfl_sync(0xffffffffu, my_dst, from);
+      const int slot = __shfl_sync(0xffffffffu, my_slot, from);
       if (live) {
-        *(uint2*)(q + (size_t)d * (K / 2) + b * 8) = code;
-        sf[sf_index((size_t)d, b, K, sf_rows)] = scale;
+        if (im.img) {
+          uint8_t* blk = im.img + ((size_t)(slot >> 7) * im.chunks + (b >> 4)) * kAImgBlock;
+          *(uint2*)(blk + img_code_byte(slot & 127, b & 15)) = code;
+          blk[kImgTile + 16 * (slot & 127) + (b & 15)] = scale;
+        } else {
+          *(uint2*)(q + (size_t)d * (K / 2) + b * 8) = code;
+          sf[sf_index((size_t)d, b, K, sf_rows)] = scale;
+        }
       }
     }
   }
@@ -336,10 +377,11 @@ cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, co
       nvfp4_pack_kernel<<<dim3((unsigned)((nblk + 255) / 256), E), 256, 0, s>>>(w, N, K, slot, a, b);
       nvfp4_finish_kernel<<<(E + 127) / 128, 128, 0, s>>>(slot, E);
       note_launches(2);
-      const int bt = which == 0 ? MOE_T_GU_BT : MOE_T_D_BT;
-      if (d.size[bt]) {
-        const size_t n = (size_t)E * N * (K / 16);
-        nvfp4_retile_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(b, E, N, K, (uint8_t*)(packed + d.offset[bt]));
+      const int it = which == 0 ? MOE_T_GU_IMG : MOE_T_D_IMG;
+      if (d.size[it]) {
+        const size_t n = d.size[it] / kWImgBlock * 256;
+        nvfp4_image_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, b, E, N, K, which == 0,
+                                                                        (uint8_t*)(packed + d.offset[it]));
         note_launches(1);
       }
     }
@@ -374,34 +416,35 @@ cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e
 template <int NBLK, int RPW>
 static cudaError_t launch_quant_flat(bool early, const __nv_bfloat16* x, const int32_t* scatter, int k, int rows,
                                      uint8_t* q, uint8_t* sf, float* gs, int sf_rows, const float* static_gs,
-                                     cudaStream_t s) {
+                                     const ActImage& im, cudaStream_t s) {
   const dim3 grid((rows + 8 * RPW - 1) / (8 * RPW));
   if (early)
     return launch_pdl(quant_rows_flat_kernel<NBLK, RPW, true>, grid, dim3(256), 0, s, (const uint16_t*)x, scatter, k,
-                      rows, q, sf, gs, sf_rows, static_gs);
+                      rows, q, sf, gs, sf_rows, static_gs, im);
   return launch_pdl(quant_rows_flat_kernel<NBLK, RPW, false>, grid, dim3(256), 0, s, (const uint16_t*)x, scatter, k,
-                    rows, q, sf, gs, sf_rows, static_gs);
+                    rows, q, sf, gs, sf_rows, static_gs, im);
 }
 
 cudaError_t launch_quant_rows(const __nv_bfloat16* x, const int32_t* scatter, int k, int rows, int K, uint8_t* q,
                               uint8_t* sf, float* gs, cudaStream_t s, bool early, int sf_rows,
-                              const float* static_gs) {
+                              const float* static_gs, const ActImage* img) {
   if (rows <= 0) return cudaGetLastError();
+  const ActImage im = img ? *img : ActImage();
   note_launches(1);
   switch (K) {  // register-resident shapes: RPW rows fill whole 32-lane passes of 16-blocks
-    case 128: return launch_quant_flat<8, 4>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
-    case 256: return launch_quant_flat<16, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
-    case 512: return launch_quant_flat<32, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
-    case 768: return launch_quant_flat<48, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
-    case 1024: return launch_quant_flat<64, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
-    case 1280: return launch_quant_flat<80, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
-    case 1536: return launch_quant_flat<96, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
-    case 2048: return launch_quant_flat<128, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
-    case 3072: return launch_quant_flat<192, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
-    case 4096: return launch_quant_flat<256, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, s);
+    case 128: return launch_quant_flat<8, 4>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, im, s);
+    case 256: return launch_quant_flat<16, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, im, s);
+    case 512: return launch_quant_flat<32, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, im, s);
+    case 768: return launch_quant_flat<48, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, im, s);
+    case 1024: return launch_quant_flat<64, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, im, s);
+    case 1280: return launch_quant_flat<80, 2>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, im, s);
+    case 1536: return launch_quant_flat<96, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, im, s);
+    case 2048: return launch_quant_flat<128, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, im, s);
+    case 3072: return launch_quant_flat<192, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, im, s);
+    case 4096: return launch_quant_flat<256, 1>(early, x, scatter, k, rows, q, sf, gs, sf_rows, static_gs, im, s);
     default:
       return launch_pdl(quant_rows_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, (const uint16_t*)x, scatter, k, rows,
-                        K, q, sf, gs, sf_rows, static_gs);
+                        K, q, sf, gs, sf_rows, static_gs, im);
   }
 }
 

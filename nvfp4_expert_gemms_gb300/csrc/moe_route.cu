@@ -177,6 +177,7 @@ __global__ void __launch_bounds__(1024) route_topk_kernel(const float* __restric
 __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restrict__ blkcnt, int nb, int E,
                                                           int row_block, int max_tiles,
                                                           int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ toffsets,
                                                           int32_t* __restrict__ blkbase,
                                                           TileEntry* __restrict__ tiles, int* err) {
   __shared__ int tot[kMaxE], ntl[kMaxE], off_s[kMaxE + 1], toff_s[kMaxE + 1];
@@ -202,7 +203,10 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(const int32_t* __restr
   __syncthreads();
   if (e < 32) expert_scan(tot, E, row_block, max_tiles, off_s, toff_s, tiles, e);
   __syncthreads();
-  if (e <= E) offsets[e] = off_s[e];
+  if (e <= E) {
+    offsets[e] = off_s[e];
+    toffsets[e] = toff_s[e];
+  }
   if (pp < parts) {  // each part's blocks start after the earlier parts' rows of the expert
     int run = off_s[pe];
     for (int p = 0; p < pp; ++p) run += psum[p * E + pe];
@@ -269,6 +273,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
                                                            int row_block, int max_tiles,
                                                            int32_t* __restrict__ topk_idx,
                                                            float* __restrict__ topk_w, int32_t* __restrict__ offsets,
+                                                           int32_t* __restrict__ toffsets,
                                                            int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                                                            TileEntry* __restrict__ tiles, int* err, RoutePrelude pre) {
   __shared__ int cnt[kMaxE], off_s[kMaxE + 1], toff_s[kMaxE + 1];
@@ -294,7 +299,10 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
   __syncthreads();
   if (warp == 0) expert_scan(cnt, E, row_block, max_tiles, off_s, toff_s, tiles, lane);
   __syncthreads();
-  if (tid <= E) offsets[tid] = off_s[tid];
+  if (tid <= E) {
+    offsets[tid] = off_s[tid];
+    toffsets[tid] = toff_s[tid];
+  }
   if (tid < E) {
     const int ntl = (cnt[tid] + row_block - 1) / row_block, t0 = toff_s[tid];
     for (int i = 0; i < ntl; ++i) {
@@ -334,6 +342,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int row_block
   int32_t* blkcnt = (int32_t*)(ws + L.blkcnt);
   int32_t* blkbase = (int32_t*)(ws + L.blkbase);
   int32_t* off = (int32_t*)(ws + L.offsets);
+  int32_t* toff = (int32_t*)(ws + L.toff);
   int32_t* perm = (int32_t*)(ws + L.perm);
   int32_t* inv = (int32_t*)(ws + L.inv);
   TileEntry* tiles = (TileEntry*)(ws + L.tiles);
@@ -341,14 +350,14 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int row_block
   if (T > 0 && T <= kRouteTB) {
     note_launches(1);
     return launch_pdl(route_small_kernel, dim3(1), dim3(1024), 0, s, logits, T, E, k, row_block, L.max_tiles, idx,
-                      w, off, perm, inv, tiles, err, pre);
+                      w, off, toff, perm, inv, tiles, err, pre);
   }
   cudaError_t e = cudaSuccess;
   if (T > 0) e = launch_pdl(route_topk_kernel, dim3(nb), dim3(1024), 0, s, logits, T, E, k, idx, w, blkcnt, err, pre);
   else e = cudaMemsetAsync(err, 0, sizeof(int), s);
   if (e == cudaSuccess)
     e = launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)blkcnt, T > 0 ? nb : 0, E, row_block,
-                   L.max_tiles, off, blkbase, tiles, err);
+                   L.max_tiles, off, toff, blkbase, tiles, err);
   if (e == cudaSuccess && T > 0)
     e = launch_pdl(route_scatter_kernel, dim3(nb), dim3(kRouteTB), 0, s, (const int32_t*)idx, T, E, k,
                    (const int32_t*)blkbase, perm, inv);

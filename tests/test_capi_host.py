@@ -42,17 +42,17 @@ def test_packed_sizes_match_canonical_shapes(orc):
         assert all(int(d.offset[i]) % 256 == 0 for i in range(8))
         assert d.bytes >= got
     # the NVFP4 layer is the 0.32 GiB the page quotes (canonical tensors; the W4A4 buffer adds
-    # its re-tiled copy of the two scale tensors)
+    # the two matrices' tensor-core operand images, the same codes and scales rearranged)
     d = M.moe_packed_size("nvfp4_w4a4", E, H, I)
     assert round(sum(int(d.size[i]) for i in range(6)) / 2 ** 30, 2) == 0.32
-    assert int(d.size[M.MOE_T_GU_BT]) == int(d.size[M.MOE_T_GU_B]) and int(d.size[M.MOE_T_D_BT]) == int(
-        d.size[M.MOE_T_D_B])
-    assert int(M.moe_packed_size("nvfp4_w4a16", E, H, I).size[M.MOE_T_GU_BT]) == 0
-    # K not a multiple of 256: the copies hold whole 2 KB blocks per (128-row tile, 256-column
-    # chunk), the last chunk half used
+    assert int(d.size[M.MOE_T_GU_IMG]) == int(d.size[M.MOE_T_GU_A]) + int(d.size[M.MOE_T_GU_B])
+    assert int(d.size[M.MOE_T_D_IMG]) == int(d.size[M.MOE_T_D_A]) + int(d.size[M.MOE_T_D_B])
+    assert int(M.moe_packed_size("nvfp4_w4a16", E, H, I).size[M.MOE_T_GU_IMG]) == 0
+    # K not a multiple of 256 and H not of 256: whole 36 KB blocks per (tile pair, 256-column
+    # chunk), the last chunk half used, the last down pair's second tile empty
     d = M.moe_packed_size("nvfp4_w4a4", 3, 384, 640)
-    assert int(d.size[M.MOE_T_GU_BT]) == 3 * (2 * 640 // 128) * 2 * 2048
-    assert int(d.size[M.MOE_T_D_BT]) == 3 * (384 // 128) * 3 * 2048
+    assert int(d.size[M.MOE_T_GU_IMG]) == 3 * (640 // 128) * 2 * 36864
+    assert int(d.size[M.MOE_T_D_IMG]) == 3 * 2 * 3 * 36864
 
 
 def test_packed_tensor_sizes_equal_oracle_outputs(orc):

@@ -96,31 +96,56 @@ def test_bf16_pack_and_dequant_are_the_weights():
             assert got.tobytes() == synth.bf16_bits_to_f32(w[e]).tobytes()
 
 
+def _operand_image(codes, scales, N, K, gu):
+    """The W4A4 weight operand image as the header defines it, built from canonical codes
+    [E, N, K/2] and scales [E, N, K/16]: block [e, p, c] = codes of tile 0 and tile 1 (128 rows x
+    128 bytes, 16-byte piece j of row l at piece j ^ (l % 8)), then their scales (byte
+    512 s + 16 (l % 32) + 4 (l // 32) + i = scale of row l, block 16c + 4s + i); zero past N, K."""
+    E = codes.shape[0]
+    C, P = (K + 255) // 256, (N // 256 if gu else (N + 255) // 256)
+    img = np.zeros((E, P, C, 36864), np.uint8)
+    ln = np.arange(128)
+    for p in range(P):
+        for g in range(2):
+            rows = (128 * p + ln if g == 0 else N // 2 + 128 * p + ln) if gu else 256 * p + 128 * g + ln
+            ok = rows < N
+            for c in range(C):
+                kb = min(128, K // 2 - 128 * c)
+                lines = np.zeros((E, 128, 128), np.uint8)
+                lines[:, ok, :kb] = codes[:, rows[ok], 128 * c:128 * c + kb]
+                sw = np.zeros((E, 128, 8, 16), np.uint8)
+                pieces = lines.reshape(E, 128, 8, 16)
+                for j in range(8):
+                    sw[:, ln, j ^ (ln & 7)] = pieces[:, :, j]
+                img[:, p, c, 16384 * g:16384 * (g + 1)] = sw.reshape(E, 16384)
+                sb = np.zeros((E, 128, 16), np.uint8)
+                sb[:, ok, :kb // 8] = scales[:, rows[ok], 16 * c:16 * c + kb // 8]
+                atoms = sb.reshape(E, 4, 32, 4, 4).transpose(0, 3, 2, 1, 4)
+                img[:, p, c, 32768 + 2048 * g:32768 + 2048 * (g + 1)] = atoms.reshape(E, 2048)
+    return img
+
+
 @pytest.mark.parametrize("H,I", [(512, 256), (384, 640)])
-def test_w4a4_retiled_scales(orc, H, I):
-    """The W4A4 buffer's scale copies are the canonical weight_scale tensors (bit-exact with the
-    oracle's packing) in the tensor-memory atom order [E, N/128, C, 4, 32, 4, 4]: element
-    [e, t, c, s, l, j, i] = weight_scale[e, 128 t + 32 j + l, 16 c + 4 s + i] (C = ceil(K/256);
-    the unused upper half of a last half chunk is not compared)."""
+def test_w4a4_weight_image(orc, H, I):
+    """The W4A4 buffer's operand images hold exactly the canonical codes and scales (bit-exact
+    with the oracle's packing), rearranged as the header's layout says -- including a last half
+    chunk (K % 256 = 128) and a down tile pair whose second tile lies past H."""
     E = 3
     wgu, wd = synth.gen_expert_weights(E, H, I, seed=6)
     layer = M.MoELayer("nvfp4_w4a4", dev_bf16(wgu), dev_bf16(wd))
     torch.cuda.synchronize()
     ref = orc.pack_experts(FID["nvfp4_w4a4"], wgu, wd)
     d = layer.desc
-    for canon, tiled, name, (N, K) in ((M.MOE_T_GU_B, M.MOE_T_GU_BT, "gu", (2 * I, H)),
-                                       (M.MOE_T_D_B, M.MOE_T_D_BT, "d", (H, I))):
-        sc = M.packed_view(d, layer.packed, canon).cpu().numpy()
+    for ca, cb, im, name, (N, K), gu in ((M.MOE_T_GU_A, M.MOE_T_GU_B, M.MOE_T_GU_IMG, "gu", (2 * I, H), True),
+                                         (M.MOE_T_D_A, M.MOE_T_D_B, M.MOE_T_D_IMG, "d", (H, I), False)):
+        codes = M.packed_view(d, layer.packed, ca).cpu().numpy()
+        sc = M.packed_view(d, layer.packed, cb).cpu().numpy()
+        assert codes.tobytes() == np.ascontiguousarray(ref[name][0]).tobytes()
         assert sc.tobytes() == np.ascontiguousarray(ref[name][1]).tobytes()
-        C = (K + 255) // 256
-        got = M.packed_view(d, layer.packed, tiled).cpu().numpy()
-        assert got.shape == (E, N // 128, C, 4, 32, 4, 4)
-        for e in range(E):
-            for n in range(N):
-                t, j, l = n // 128, (n % 128) // 32, n % 32
-                for b in range(K // 16):
-                    c, st, i = b // 16, (b % 16) // 4, b % 4
-                    assert got[e, t, c, st, l, j, i] == sc[e, n, b], (name, e, n, b)
+        got = M.packed_view(d, layer.packed, im).cpu().numpy()
+        want = _operand_image(codes.reshape(E, N, K // 2), sc.reshape(E, N, K // 16), N, K, gu)
+        assert got.shape == want.shape
+        assert got.tobytes() == want.tobytes(), name
 
 
 @pytest.mark.parametrize("fmt", ["fp8", "int4", "nvfp4_w4a16"])
