@@ -54,17 +54,22 @@ using namespace tc;
 
 constexpr int kKC = 256;                  // K per chunk: 128 bytes of codes per row
 constexpr int kRows = 128;                // activation rows per item (MMA M): the routing row block
-constexpr int kStages = 4;                // weight / activation chunks in flight
+constexpr int kCPS = 2;                   // K chunks per stage: one bulk copy per operand covers them
+constexpr int kStages = 4 / kCPS;         // stages in flight
 constexpr int kRing = 16;                 // work items handed from the producer to the other warps
 constexpr int kCombRing = 4;              // down: items whose stored rows await the signal warp
 constexpr int kWCodes = 128 * 128;        // one 128-row weight tile, 128-byte swizzle
 constexpr int kSfBlock = 2048;            // scales of one (128-row tile, chunk): four 512-byte atoms
-constexpr int kWStage = 2 * kWCodes + 2 * kSfBlock;  // two tiles = the 256 B rows of one item
+constexpr int kWChunk = 2 * kWCodes + 2 * kSfBlock;  // two tiles = the 256 B rows of one item
 constexpr int kXCodes = kRows * 128;      // activation codes, 128-byte swizzle
-constexpr int kXStage = kXCodes + kSfBlock;
+constexpr int kXChunk = kXCodes + kSfBlock;
+constexpr int kWStage = kCPS * kWChunk, kXStage = kCPS * kXChunk;
 constexpr size_t kSmem = 1024 + (size_t)kStages * (kWStage + kXStage);
-constexpr uint32_t kSfCol = 256;          // TMEM: [0, 256) accumulator, then 4 x 48 scale columns
-constexpr uint32_t kSfStageCols = 48;     // per K step: A (activation) scales 4 columns, B (weight) 8
+constexpr uint32_t kSfCol = 256;          // TMEM: [0, 256) accumulator, then the stages' scale columns
+constexpr uint32_t kSfChunkCols = 48;     // per K step: A (activation) scales 4 columns, B (weight) 8
+constexpr uint32_t kSfStageCols = kCPS * kSfChunkCols;
+static_assert(kWChunk == kWImgBlock && kXChunk == kAImgBlock, "a stage holds whole image blocks");
+static_assert(kSfCol + kStages * kSfStageCols <= 512, "tensor memory columns");
 constexpr int kCombTokens = 24;           // tokens per combine item of the down GEMM
 constexpr int kCombBuf = 96 * 1024;       // combine: two buffers of partial rows in the stage memory
 
@@ -191,6 +196,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1) fp4_kernel(const __g
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nK = (a.K + kKC - 1) / kKC;           // chunks; the last is a half chunk when K % 256 = 128
   const int last_ks = (a.K % kKC) ? 2 : 4;        // K = 64 steps of the last chunk
+  const int nKP = (nK + kCPS - 1) / kCPS;         // stages per item
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -314,24 +320,25 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1) fp4_kernel(const __g
         ok = __shfl_sync(0xffffffffu, ok, 0);
         continue;
       }
-      for (int kc = 0; kc < nK; ++kc, ++it) {
-        const int st = it % kStages;
+      for (int kp = 0; kp < nKP; ++kp, ++it) {
+        const int st = it % kStages, kc0 = kp * kCPS, nch = min(kCPS, nK - kc0);
         if (lane == 0) {
           ok = mbar_wait(&w_empty[st], ((it / kStages) & 1) ^ 1, &s_abort);
-          if (ok) {  // one bulk copy: both weight tiles' codes and scales of this chunk
-            mbar_arrive_expect_tx(&w_full[st], kWImgBlock);
+          if (ok) {  // one bulk copy: both weight tiles' codes and scales of the stage's chunks
+            mbar_arrive_expect_tx(&w_full[st], (uint32_t)(nch * kWChunk));
             ++armed_w[st];
             const int pair = kGateUp ? w0 / 128 : w0 / 256;
-            bulk_load(sW + st * kWStage, a.wimg + (((size_t)te.expert * a.P + pair) * a.C + kc) * kWImgBlock,
-                      kWImgBlock, &w_full[st]);
+            bulk_load(sW + st * kWStage, a.wimg + (((size_t)te.expert * a.P + pair) * a.C + kc0) * kWChunk,
+                      (uint32_t)(nch * kWChunk), &w_full[st]);
           }
           if (ok) {
             ok = mbar_wait(&x_empty[st], ((it / kStages) & 1) ^ 1, &s_abort);
             if (MODE == 1 && it == 0) pdl_wait();
-            if (ok) {  // one bulk copy: the routing tile's codes and scales of this chunk
-              mbar_arrive_expect_tx(&x_full[st], kAImgBlock);
+            if (ok) {  // one bulk copy: the routing tile's codes and scales of the stage's chunks
+              mbar_arrive_expect_tx(&x_full[st], (uint32_t)(nch * kXChunk));
               ++armed_x[st];
-              bulk_load(sX + st * kXStage, a.aimg + ((size_t)tile * a.C + kc) * kAImgBlock, kAImgBlock, &x_full[st]);
+              bulk_load(sX + st * kXStage, a.aimg + ((size_t)tile * a.C + kc0) * kXChunk, (uint32_t)(nch * kXChunk),
+                        &x_full[st]);
             }
           }
         }
@@ -363,8 +370,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1) fp4_kernel(const __g
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       fence_after_sync();
-      for (int kc = 0; kc < nK; ++kc, ++it) {
-        const int st = it % kStages;
+      for (int kp = 0; kp < nKP; ++kp, ++it) {
+        const int st = it % kStages, kc0 = kp * kCPS, nch = min(kCPS, nK - kc0);
         ok = mbar_wait(&w_full[st], (it / kStages) & 1, &s_abort) &&
              mbar_wait(&x_full[st], (it / kStages) & 1, &s_abort) &&
              mbar_wait(&s_full[st], (it / kStages) & 1, &s_abort);
@@ -372,12 +379,15 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1) fp4_kernel(const __g
         if (!ok) break;
         fence_after_sync();
         if (lane == 0) {
-          const uint32_t xa = smem_u32(sX + st * kXStage), wa = smem_u32(sW + st * kWStage);
-          const uint32_t sfa = tmem + kSfCol + st * kSfStageCols, sfb = sfa + 16;
-          const int nks = kc == nK - 1 ? last_ks : 4;
-          for (int ks = 0; ks < nks; ++ks)
-            mma_nvf4(tmem, sdesc_k_sw128(xa + ks * 32), sdesc_k_sw128(wa + ks * 32), idesc, sfa + 4 * ks,
-                     sfb + 8 * ks, (kc | ks) != 0);
+          for (int j = 0; j < nch; ++j) {
+            const int kc = kc0 + j;
+            const uint32_t xa = smem_u32(sX + st * kXStage + j * kXChunk), wa = smem_u32(sW + st * kWStage + j * kWChunk);
+            const uint32_t sfa = tmem + kSfCol + st * kSfStageCols + j * kSfChunkCols, sfb = sfa + 16;
+            const int nks = kc == nK - 1 ? last_ks : 4;
+            for (int ks = 0; ks < nks; ++ks)
+              mma_nvf4(tmem, sdesc_k_sw128(xa + ks * 32), sdesc_k_sw128(wa + ks * 32), idesc, sfa + 4 * ks,
+                       sfb + 8 * ks, (kc | ks) != 0);
+          }
           mma_commit(&w_empty[st]);
           mma_commit(&x_empty[st]);
           mma_commit(&s_empty[st]);
@@ -403,16 +413,17 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1) fp4_kernel(const __g
       TileEntry te;
       int tile, w0, w1;
       if (!item(wk, te, tile, w0, w1)) continue;  // a combine item
-      for (int kc = 0; kc < nK; ++kc, ++it) {
-        const int st = it % kStages;
+      for (int kp = 0; kp < nKP; ++kp, ++it) {
+        const int st = it % kStages, nch = min(kCPS, nK - kp * kCPS);
         ok = __all_sync(0xffffffffu, mbar_wait(&w_full[st], (it / kStages) & 1, &s_abort) &&
                                          mbar_wait(&x_full[st], (it / kStages) & 1, &s_abort) &&
                                          mbar_wait(&s_empty[st], ((it / kStages) & 1) ^ 1, &s_abort));
         if (!ok) break;
         fence_after_sync();
-        const uint32_t col = kSfCol + st * kSfStageCols;
-        const char* xsf = sX + st * kXStage + kXCodes + 16 * lane;
-        const char* wsf = sW + st * kWStage + 2 * kWCodes + 16 * lane;
+        for (int jc = 0; jc < nch; ++jc) {
+        const uint32_t col = kSfCol + st * kSfStageCols + jc * kSfChunkCols;
+        const char* xsf = sX + st * kXStage + jc * kXChunk + kXCodes + 16 * lane;
+        const char* wsf = sW + st * kWStage + jc * kWChunk + 2 * kWCodes + 16 * lane;
         uint32_t v[16];
         uint4 x4[4];  // activations: row l + 32 j's 16 scales (word = K step)
 #pragma unroll
@@ -438,6 +449,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1) fp4_kernel(const __g
               v[8 * kk + 4 * g + 3] = u.w;
             }
           tmem_st_32x16(taddr(tmem, q * 32, col + 16 + 16 * h), v);
+        }
         }
         tmem_st_wait();
         fence_before_sync();
