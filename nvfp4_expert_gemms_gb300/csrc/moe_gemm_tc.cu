@@ -43,7 +43,7 @@ constexpr int kKC = 128;          // K elements per pipeline chunk
 constexpr int kConvWarps = 16;    // warps 0-15: converters + epilogue
 constexpr int kProdWarp = 16;     // TMA producer
 constexpr int kMmaWarp = 17;      // TMEM owner and MMA issuer
-constexpr int kGathWarp0 = 18, kGathWarps = 2;  // activation row gather (gate/up)
+constexpr int kGathWarp0 = 18, kGathWarps = 2;  // activations: row gather (small BN) or warp 18 issues TMA tiles
 constexpr int kRing = 8;           // work items handed from the producer to the other warps
 constexpr int kThreads = 20 * 32;
 constexpr uint32_t kTmemCols = 512;
@@ -112,6 +112,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
   return d;
+}
+
+// An empty asm that claims to read and rewrite the 32 converted words: the conversion is then
+// finished before the barrier waits that follow it (register-only arithmetic may otherwise be
+// scheduled after them, serialising it behind the tensor-memory slot's release).
+__device__ __forceinline__ void reg_fence(uint32_t* v) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 8)
+    asm volatile("" : "+r"(v[i]), "+r"(v[i + 1]), "+r"(v[i + 2]), "+r"(v[i + 3]), "+r"(v[i + 4]), "+r"(v[i + 5]),
+                 "+r"(v[i + 6]), "+r"(v[i + 7]));
 }
 
 // ---- converters: half a chunk (64 K) of one weight row -> 32 bf16x2 words -------------------
@@ -197,41 +207,41 @@ __device__ __forceinline__ void conv_int4(const char* sub, int r, int kh, float 
   }
 }
 
-// NVFP4: four E2M1 codes at a time become bf16 through byte-permute lookups of the bf16 bytes of
-// {0, .5, 1, 1.5, 2, 3, 4, 6}, the sign bits are merged, and one packed multiply by the E4M3 block
-// scale (exact: the product has at most 6 significant bits).  The global scale is applied in the
-// epilogue.
-__device__ __forceinline__ void e2m1x4_to_bf16x2(uint32_t w16, uint32_t& p0, uint32_t& p1) {
-  const uint32_t sel = w16 & 0x7777u;
-  const uint32_t lo = prmt(0xC0800000u, 0xC0804000u, sel);  // low bytes of the bf16 values
-  const uint32_t hi = prmt(0x3F3F3F00u, 0x40404040u, sel);  // high bytes
-  p0 = prmt(lo, hi, 0x5140u) | ((w16 << 12) & 0x8000u) | ((w16 << 24) & 0x80000000u);
-  p1 = prmt(lo, hi, 0x7362u) | ((w16 << 4) & 0x8000u) | ((w16 << 16) & 0x80000000u);
-}
-
+// NVFP4: the weights come as the converter's image (nvfp4_w4a16_image_kernel): in each 32-bit
+// word of eight E2M1 codes the bits sit where one shift (or rotate) and mask puts a pair of codes
+// under the exponent of a bf16 pair -- code bits (e1 e0 m) at bf16 bits 8..6 and the sign at bit
+// 15 give the bf16 value code * 2^-126, E2M1 subnormals on bf16 subnormals.  One packed multiply
+// by bf16(block scale * 2^116) then gives w * 2^-10 exactly (at most 6 significant bits); the
+// epilogue applies 2^10 / global scale.  The scale's E4M3 bits go under bf16's exponent plus 236
+// (2^-120 to 2^116), or, when a block scale of the half chunk is zero or subnormal, through fp32.
 __device__ __forceinline__ void conv_nvfp4(const char* sub, int r, int kh, uint32_t bs4, uint32_t* out) {
+  constexpr uint32_t kPair = 0x81C081C0u;  // bf16 pair bits: sign, exponent bits 1..0, mantissa bit 6
   uint4 q[2];
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) q[cc] = *(const uint4*)(sub + r * 64 + (((kh * 2 + cc) ^ ((r >> 1) & 3)) * 16));
   uint32_t bs2[4];
+  const uint32_t ex = bs4 & 0x78787878u;
+  if ((((ex - 0x08080808u) & ~ex) & 0x80808080u) == 0u) {  // four normal scales
+    const uint32_t m = bs4 & 0x7F7F7F7Fu;
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const float f = e4m3_to_f32((bs4 >> (8 * b)) & 0xFF);
-    bs2[b] = pack_bf16x2(f, f);
+    for (int b = 0; b < 4; ++b) bs2[b] = prmt(m, 0u, 0x4040u | (uint32_t)b | ((uint32_t)b << 8)) * 16u + 0x76007600u;
+  } else {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float f = e4m3_to_f32((bs4 >> (8 * b)) & 0xFF) * 0x1p116f;
+      bs2[b] = pack_bf16x2(f, f);
+    }
   }
 #pragma unroll
-  for (int cc = 0; cc < 2; ++cc) {  // 16-byte chunk = 32 codes = two 16-element blocks
+  for (int cc = 0; cc < 2; ++cc) {  // 16-byte piece = 32 codes = two 16-element blocks
     const uint32_t w[4] = {q[cc].x, q[cc].y, q[cc].z, q[cc].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t bs = bs2[cc * 2 + (i >> 1)];
-      uint32_t p0, p1, p2, p3;
-      e2m1x4_to_bf16x2(w[i] & 0xFFFFu, p0, p1);
-      e2m1x4_to_bf16x2(w[i] >> 16, p2, p3);
-      out[cc * 16 + i * 4 + 0] = bmul2(p0, bs);
-      out[cc * 16 + i * 4 + 1] = bmul2(p1, bs);
-      out[cc * 16 + i * 4 + 2] = bmul2(p2, bs);
-      out[cc * 16 + i * 4 + 3] = bmul2(p3, bs);
+      const uint32_t bs = bs2[cc * 2 + (i >> 1)], x = w[i];
+      out[cc * 16 + i * 4 + 0] = bmul2((x << 6) & kPair, bs);
+      out[cc * 16 + i * 4 + 1] = bmul2((x << 2) & kPair, bs);
+      out[cc * 16 + i * 4 + 2] = bmul2(__funnelshift_r(x, x, 4) & kPair, bs);
+      out[cc * 16 + i * 4 + 3] = bmul2((x & 0x81808180u) | ((x >> 8) & 0x00400040u), bs);
     }
   }
 }
@@ -308,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&work_full[i], 1);
-      mbar_init(&work_empty[i], (kGather ? kGathWarps : 0) + 1 + kConvWarps);  // every consuming warp
+      mbar_init(&work_empty[i], (kGather ? kGathWarps : 1) + 1 + kConvWarps);  // every consuming warp
     }
     mbar_init(&acc_full, 1);
     mbar_init(&drain, 1);
@@ -327,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = s_tmem;
-  if (MODE == 1 && warp != kProdWarp) pdl_wait();  // the producer waits before its first h tile
+  if (MODE == 1 && warp != kProdWarp) pdl_wait();  // the weight producer needs nothing from the gate/up GEMM
   pdl_trigger();
 
   // Work items are handed out dynamically (SMs do not all stream at the same rate): the
@@ -360,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   if (warp == kProdWarp) {
     // ---------------- TMA producer (the whole warp walks the loop, lane 0 issues) ----------------
     int it = 0;
-    int armed_w[kStagesW] = {0}, armed_b[SB] = {0};
+    int armed_w[kStagesW] = {0};
     for (int n = 0;; ++n) {
       int wk = -1;
       bool ok = true;
@@ -381,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       int nb0, nb1, nsub;
       item(wk, te, nb0, nb1, nsub);
       for (int kc = 0; kc < nK; ++kc, ++it) {
-        const int sw = it % kStagesW, sb = it % SB;
+        const int sw = it % kStagesW;
         if (lane == 0) {
           ok = mbar_wait(&w_empty[sw], ((it / kStagesW) & 1) ^ 1, &s_abort);
           if (ok) {
@@ -399,17 +409,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
                 tma_load_2d(dst, &a.wmap, &w_full[sw], nb, te.expert * (a.K / 8) + kc * 16);
               else
                 tma_load_2d(dst, &a.wmap, &w_full[sw], kc * (kKC / 2), te.expert * a.N + nb);
-            }
-          }
-          if (ok && !kGather) {
-            ok = mbar_wait(&b_empty[sb], ((it / SB) & 1) ^ 1, &s_abort);
-            if (MODE == 1 && it == 0) pdl_wait();
-            if (ok) {
-              char* bd = sB + sb * BSTAGE;
-              mbar_arrive_expect_tx(&b_full[sb], BSTAGE);
-              ++armed_b[sb];
-              tma_load_2d(bd, &a.bmap, &b_full[sb], kc * kKC, te.row0);
-              tma_load_2d(bd + BN * 128, &a.bmap, &b_full[sb], kc * kKC + 64, te.row0);
             }
           }
         }
@@ -449,6 +448,38 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       volatile int no_abort = 0;
       for (int i = 0; i < kStagesW; ++i)
         if (armed_w[i]) mbar_wait(&w_full[i], (armed_w[i] - 1) & 1, &no_abort);
+    }
+    __syncwarp();
+  } else if (!kGather && warp == kGathWarp0) {
+    // ---------------- activation tiles by TMA (a warp of their own, so that the weight stream
+    // runs as far ahead as its stages allow instead of at the pace of the activation ring) -------
+    int it = 0;
+    int armed_b[SB] = {0};
+    bool ok = true;
+    for (int nitem = 0; ok; ++nitem) {
+      const int wk = next_item(nitem, ok);
+      if (wk < 0) break;
+      TileEntry te;
+      int nb0, nb1, nsub;
+      item(wk, te, nb0, nb1, nsub);
+      for (int kc = 0; kc < nK; ++kc, ++it) {
+        const int sb = it % SB;
+        if (lane == 0) {
+          ok = mbar_wait(&b_empty[sb], ((it / SB) & 1) ^ 1, &s_abort);
+          if (ok) {
+            char* bd = sB + sb * BSTAGE;
+            mbar_arrive_expect_tx(&b_full[sb], BSTAGE);
+            ++armed_b[sb];
+            tma_load_2d(bd, &a.bmap, &b_full[sb], kc * kKC, te.row0);
+            tma_load_2d(bd + BN * 128, &a.bmap, &b_full[sb], kc * kKC + 64, te.row0);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+    }
+    if (lane == 0 && s_abort) {  // let every issued copy land before shared memory goes away
+      volatile int no_abort = 0;
       for (int i = 0; i < SB; ++i)
         if (armed_b[i]) mbar_wait(&b_full[i], (armed_b[i] - 1) & 1, &no_abort);
     }
@@ -562,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       const bool active = g < nsub;
       const int nb = g == 0 ? nb0 : nb1;
       const int buf = nitem & 1;
-      const float inv_gs = FMT == MOE_FMT_NVFP4_W4A16 ? 1.0f / a.wgs[e] : 1.f;
+      const float inv_gs = FMT == MOE_FMT_NVFP4_W4A16 ? 0x1p10f / a.wgs[e] : 1.f;  // see conv_nvfp4
       if (MODE == 1 && threadIdx.x < BN) {  // column table of the down epilogue
         const int col = threadIdx.x;
         int ct = 0;
@@ -596,6 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
           else if (FMT == MOE_FMT_FP8_B128_W8A16) conv_fp8(sub, r, kh, sc, v);
           else if (FMT == MOE_FMT_INT4_G128_W4A16) conv_int4(sub, r, kh, sc, v);
           else conv_nvfp4(sub, r, kh, bs4, v);
+          reg_fence(v);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&w_empty[sw]);
@@ -778,7 +810,12 @@ cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, co
                               int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, uint16_t* out) {
   const int E = d.E, H = d.H, I = d.I;
   const size_t R = (size_t)T * k;
-  const MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
+  MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
+  if (d.fmt == MOE_FMT_NVFP4_W4A16) {  // NVFP4 codes in the converter's bit order (conv_nvfp4)
+    if (!d.size[MOE_T_GU_IMG] || !d.size[MOE_T_D_IMG]) return cudaErrorInvalidValue;
+    gu.a = (const uint8_t*)(packed + d.offset[MOE_T_GU_IMG]);
+    dn.a = (const uint8_t*)(packed + d.offset[MOE_T_D_IMG]);
+  }
   TcArgs a;
   memset(&a, 0, sizeof(a));
   a.perm = (const int32_t*)(ws + L.perm);

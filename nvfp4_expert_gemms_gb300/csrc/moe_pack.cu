@@ -143,6 +143,28 @@ __global__ void __launch_bounds__(256) nvfp4_image_kernel(const uint8_t* __restr
   for (int b = 0; b < 16; ++b) tsf[img_wsf_byte(l, b)] = row_ok && 8 * b < kb ? ssrc[b] : (uint8_t)0;
 }
 
+// The NVFP4 W4A16 weights in the bf16 converter's bit order (conv_nvfp4 in moe_gemm_tc.cu): the
+// canonical codes' shape and byte positions, each 32-bit word of eight E2M1 codes (element k =
+// nibble k; code bits m, e0, e1, s = bits 0..3) with its bits moved so that element pair j comes
+// out of one shift-and-mask of the word: pair 0 by << 6, pair 1 by << 2, pair 2 by a rotate right
+// by 4, pair 3 in place except the two mantissa bits (>> 8).
+__device__ __forceinline__ uint32_t w4a16_image_word(uint32_t c) {
+  constexpr uint8_t kDst[8][4] = {{0, 1, 2, 9},     {16, 17, 18, 25}, {4, 5, 6, 13},  {20, 21, 22, 29},
+                                  {10, 11, 12, 19}, {26, 27, 28, 3},  {14, 7, 8, 15}, {30, 23, 24, 31}};
+  uint32_t o = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) o |= ((c >> (4 * k + b)) & 1u) << kDst[k][b];
+  return o;
+}
+
+__global__ void __launch_bounds__(256) nvfp4_w4a16_image_kernel(const uint32_t* __restrict__ codes, size_t words,
+                                                                uint32_t* __restrict__ img) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < words) img[i] = w4a16_image_word(codes[i]);
+}
+
 __global__ void nvfp4_finish_kernel(unsigned* slot, int E) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e < E) {
@@ -378,7 +400,12 @@ cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, co
       nvfp4_finish_kernel<<<(E + 127) / 128, 128, 0, s>>>(slot, E);
       note_launches(2);
       const int it = which == 0 ? MOE_T_GU_IMG : MOE_T_D_IMG;
-      if (d.size[it]) {
+      if (d.size[it] && d.fmt == MOE_FMT_NVFP4_W4A16) {
+        const size_t words = d.size[it] / 4;
+        nvfp4_w4a16_image_kernel<<<(unsigned)((words + 255) / 256), 256, 0, s>>>(
+            (const uint32_t*)a, words, (uint32_t*)(packed + d.offset[it]));
+        note_launches(1);
+      } else if (d.size[it]) {
         const size_t n = d.size[it] / kWImgBlock * 256;
         nvfp4_image_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, b, E, N, K, which == 0,
                                                                         (uint8_t*)(packed + d.offset[it]));

@@ -37,7 +37,7 @@ def test_packed_sizes_match_canonical_shapes(orc):
     per_expert = {"fp8": 4_719_744, "int4": 2_433_024, "nvfp4_w4a16": 2_654_216}
     for fmt, want in per_expert.items():
         d = M.moe_packed_size(fmt, E, H, I)
-        got = sum(int(d.size[i]) for i in range(8))
+        got = sum(int(d.size[i]) for i in range(6))  # the canonical tensors (no images)
         assert got == E * want, (fmt, got)
         assert all(int(d.offset[i]) % 256 == 0 for i in range(8))
         assert d.bytes >= got
@@ -47,7 +47,10 @@ def test_packed_sizes_match_canonical_shapes(orc):
     assert round(sum(int(d.size[i]) for i in range(6)) / 2 ** 30, 2) == 0.32
     assert int(d.size[M.MOE_T_GU_IMG]) == int(d.size[M.MOE_T_GU_A]) + int(d.size[M.MOE_T_GU_B])
     assert int(d.size[M.MOE_T_D_IMG]) == int(d.size[M.MOE_T_D_A]) + int(d.size[M.MOE_T_D_B])
-    assert int(M.moe_packed_size("nvfp4_w4a16", E, H, I).size[M.MOE_T_GU_IMG]) == 0
+    # W4A16 repeats only the codes, in the bf16 converter's bit order (same shape as GU_A / D_A)
+    d = M.moe_packed_size("nvfp4_w4a16", E, H, I)
+    assert int(d.size[M.MOE_T_GU_IMG]) == int(d.size[M.MOE_T_GU_A])
+    assert int(d.size[M.MOE_T_D_IMG]) == int(d.size[M.MOE_T_D_A])
     # K not a multiple of 256 and H not of 256: whole 36 KB blocks per (tile pair, 256-column
     # chunk), the last chunk half used, the last down pair's second tile empty
     d = M.moe_packed_size("nvfp4_w4a4", 3, 384, 640)
@@ -118,3 +121,38 @@ def test_w8a8_layout_and_workspace():
                                C.c_void_p(512), C.c_void_p(1024), n.value, None)
     assert st == 2  # MOE_ERR_UNSUPPORTED: H = 384 is not a multiple of 256
     assert lib.moe_debug_quant_act_fp8(C.c_void_p(256), 4, 200, C.c_void_p(512), C.c_void_p(1024), None) == 1
+
+
+def test_w4a16_converter_bit_order():
+    """The header's W4A16 bit order uses every bit of a word once, and the converter's four
+    shift-and-mask steps (pair 0: << 6, pair 1: << 2, pair 2: rotate right 4, pair 3: in place
+    plus the mantissa bits >> 8, each masked to a bf16 pair's sign, low exponent bits and top
+    mantissa bit) give, for every pair of codes, bf16 values equal to code * 2^-126 with the
+    code's sign; and every normal E4M3 block scale, its 7 magnitude bits times 16 plus 0x7600,
+    is bf16(scale * 2^116).  Their product is the weight * 2^-10, which the epilogue undoes."""
+    import w4a16_bits
+
+    assert sorted(b for d in w4a16_bits.DST for b in d) == list(range(32))
+    e2m1 = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6])
+    c = np.arange(2 ** 16, dtype=np.uint64)
+    canon = (c | (c << np.uint64(16))).astype("<u4")  # every (byte 0, byte 1) pair; bytes 2, 3 repeat them
+    x = w4a16_bits.words(canon.view(np.uint8)).astype(np.uint64)
+    m32, pair = np.uint64(0xFFFFFFFF), np.uint64(0x81C081C0)
+    steps = [((x << np.uint64(6)) & m32) & pair, ((x << np.uint64(2)) & m32) & pair,
+             (((x >> np.uint64(4)) | (x << np.uint64(28))) & m32) & pair,
+             (x & np.uint64(0x81808180)) | ((x >> np.uint64(8)) & np.uint64(0x00400040))]
+    for j, o in enumerate(steps):
+        o = o.astype(np.uint32)
+        for half in (0, 1):
+            h = (o >> np.uint32(16 * half)) & np.uint32(0xFFFF)
+            val = (h << np.uint32(16)).view(np.float32).astype(np.float64) * 2.0 ** 126
+            code = ((canon.astype(np.uint64) >> np.uint64(8 * j + 4 * half)) & np.uint64(15)).astype(np.int64)
+            assert np.array_equal(val, e2m1[code]), (j, half)
+            assert np.array_equal(h >> np.uint32(15), (code >> 3).astype(np.uint32)), (j, half)  # signed zeros too
+    for byte in range(1, 0x7F):
+        e, m = byte >> 3, byte & 7
+        if e == 0:
+            continue  # zero and subnormal scales take the fp32 route
+        want = 2.0 ** (e - 7) * (1 + m / 8) * 2.0 ** 116
+        bits = np.array([(byte * 16 + 0x7600) << 16], np.uint32)
+        assert float(bits.view(np.float32)[0]) == want, hex(byte)

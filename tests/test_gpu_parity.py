@@ -11,6 +11,7 @@ import torch
 
 import nvfp4_expert_gemms_gb300 as M
 import synth
+import w4a16_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -123,6 +124,21 @@ def _operand_image(codes, scales, N, K, gu):
                 atoms = sb.reshape(E, 4, 32, 4, 4).transpose(0, 3, 2, 1, 4)
                 img[:, p, c, 32768 + 2048 * g:32768 + 2048 * (g + 1)] = atoms.reshape(E, 2048)
     return img
+
+
+def test_w4a16_converter_image():
+    """The W4A16 buffer's second copy of the codes is the canonical codes with each 32-bit
+    word's bits moved as the header's table says."""
+    E, H, I = 3, 384, 256
+    wgu, wd = synth.gen_expert_weights(E, H, I, seed=9)
+    layer = M.MoELayer("nvfp4_w4a16", dev_bf16(wgu), dev_bf16(wd))
+    torch.cuda.synchronize()
+    d = layer.desc
+    for ca, im in ((M.MOE_T_GU_A, M.MOE_T_GU_IMG), (M.MOE_T_D_A, M.MOE_T_D_IMG)):
+        codes = M.packed_view(d, layer.packed, ca).cpu().numpy()
+        got = M.packed_view(d, layer.packed, im).cpu().numpy()
+        assert got.shape == codes.shape
+        assert got.tobytes() == w4a16_bits.words(codes).tobytes()
 
 
 @pytest.mark.parametrize("H,I", [(512, 256), (384, 640)])
