@@ -96,13 +96,17 @@ typedef enum {
  *   tile g's scales in the order tensor memory takes them: byte 512 s + 16 l + 4 j + i = the
  *   scale of row 32 j + l, 16-block 16c + 4s + i.  Columns past K (a last half chunk) are zero.
  *   Written by moe_pack_experts next to the canonical tensors; not part of the checkpoint format.
- *   NVFP4 W4A16 carries its codes again in the bf16 converter's bit order: GU_IMG = u8 [E, 2I,
- *   H/2], D_IMG = u8 [E, H, I/2], the shape and byte positions of GU_A / D_A, each little-endian
- *   32-bit word of eight codes (element k = nibble k of the canonical word, code bits m, e0, e1,
- *   s) re-ordered so that bits (m, e0, e1, s) of element k sit at bits
+ *   NVFP4 W4A16 carries its codes and scales again as the bf16 converter's weight image:
+ *          GU_IMG = u8 [E, H/128, 2I/128, 9216]   D_IMG = u8 [E, I/128, H/128, 9216]
+ *   Block [e, c, b] = one 128-row tile (gate/up: gate rows 64b .. 64b+63, then up rows
+ *   I+64b .. I+64b+63; down: rows 128b .. 128b+127) of columns 128c .. 128c+127: row l's 64 code
+ *   bytes at 64 l with 16-byte piece p stored at piece p ^ ((l / 2) % 4), then at 8192 + 8 l the
+ *   row's 8 E4M3 scales.  Each little-endian 32-bit code word (eight codes; element k = nibble k
+ *   of the canonical word, code bits m, e0, e1, s) is re-ordered so that bits (m, e0, e1, s) of
+ *   element k sit at bits
  *   k=0: 0,1,2,9  k=1: 16,17,18,25  k=2: 4,5,6,13  k=3: 20,21,22,29
  *   k=4: 10,11,12,19  k=5: 26,27,28,3  k=6: 14,7,8,15  k=7: 30,23,24,31.
- *   Also written by moe_pack_experts; the scales stay in GU_B / D_B.
+ *   Also written by moe_pack_experts.
  * Every tensor starts on a 256-byte boundary of the packed buffer. */
 enum {
   MOE_T_GU_A = 0,

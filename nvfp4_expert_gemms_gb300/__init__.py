@@ -269,8 +269,8 @@ def packed_view(desc: PackedDesc, packed, which: int):
     N, K = (2 * I, H) if gu else (H, I)
     if which in (MOE_T_GU_GS, MOE_T_D_GS):
         return raw.view(torch.float32)
-    if which in (MOE_T_GU_IMG, MOE_T_D_IMG) and fmt == FMT_NVFP4_W4A16:  # codes in the converter's bit order
-        return raw.view(E, N, K // 2)
+    if which in (MOE_T_GU_IMG, MOE_T_D_IMG) and fmt == FMT_NVFP4_W4A16:  # the bf16 converter's weight image
+        return raw.view(E, K // 128, N // 128, 9216)
     if which in (MOE_T_GU_IMG, MOE_T_D_IMG):  # tensor-core operand image (include/moe_gb300.h)
         return raw.view(E, N // 256 if gu else (N + 255) // 256, (K + 255) // 256, 36864)
     if fmt == FMT_BF16:

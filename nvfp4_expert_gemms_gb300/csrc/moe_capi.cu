@@ -198,9 +198,9 @@ moe_status_t moe_packed_size(int fmt, int E, int H, int I, moe_packed_desc_t* d)
       if (fmt == MOE_FMT_NVFP4_W4A4) {  // codes and scales again, as the tensor-core operand image
         sz[MOE_T_GU_IMG] = e * ((size_t)I / 128) * nvfp4_chunks(H) * kWImgBlock;
         sz[MOE_T_D_IMG] = e * (((size_t)H + 255) / 256) * nvfp4_chunks(I) * kWImgBlock;
-      } else {  // W4A16: the codes again, each word's bits in the bf16 converter's order
-        sz[MOE_T_GU_IMG] = e * gu / 2;
-        sz[MOE_T_D_IMG] = e * dn / 2;
+      } else {  // W4A16: codes (in the bf16 converter's bit order) and scales again, per tile and chunk
+        sz[MOE_T_GU_IMG] = e * ((size_t)H / 128) * ((size_t)2 * I / 128) * kW16Block;
+        sz[MOE_T_D_IMG] = e * ((size_t)I / 128) * ((size_t)H / 128) * kW16Block;
       }
       break;
   }

@@ -63,7 +63,7 @@ struct WFmt<MOE_FMT_INT4_G128_W4A16> {
 };
 template <>
 struct WFmt<MOE_FMT_NVFP4_W4A16> {
-  static constexpr int kSubBytes = 128 * 64;  // 128 rows x 64 bytes (128 codes), 64-byte swizzle
+  static constexpr int kSubBytes = kW16Block;  // one image block (128 rows' codes, then their scales)
 };
 template <>
 struct WFmt<MOE_FMT_BF16> {
@@ -80,19 +80,20 @@ struct TcCfg {
   static constexpr int kBStage = BN * 256;
   static constexpr int SB = BN <= 32 ? 4 : (BN == 64 ? 4 : (FMT == MOE_FMT_BF16 ? 2 : 3));  // BF16: 32 KB weight sub-tiles
   static constexpr int kWFree = 220 * 1024 - 1024 - SB * kBStage;
-  static constexpr int kStagesWFit = kWFree / (2 * kWSub + (FMT == MOE_FMT_BF16 ? 0 : 2048));
+  // per weight stage, the chunk's scales (copied by the producer warp next to the TMA tile):
+  // FP8 one fp32 per sub-tile, INT4 128 fp16 per sub-tile; NVFP4's are in its image blocks, BF16 has none
+  static constexpr int kScaleSlot = FMT == MOE_FMT_BF16 || FMT == MOE_FMT_NVFP4_W4A16 ? 0 : 2048;
+  static constexpr int kStagesWFit = kWFree / (2 * kWSub + kScaleSlot);
   static constexpr int kStagesW = kStagesWFit > 12 ? 12 : (kStagesWFit < 2 ? 2 : kStagesWFit);
   static constexpr int LAG = SB - 2;
-  // per weight stage, the chunk's scales (copied by the producer warp next to the TMA tile):
-  // FP8 one fp32 per sub-tile, INT4 128 fp16 per sub-tile, NVFP4 8 E4M3 bytes per row, BF16 none
-  static constexpr int kScaleSlot = FMT == MOE_FMT_BF16 ? 0 : 2048;
   static constexpr size_t kSmem = 1024 + (size_t)kStagesW * 2 * kWSub + (size_t)SB * kBStage +
                                   (size_t)kStagesW * kScaleSlot;
 };
 
 struct TcArgs {
   CUtensorMap wmap;  // packed weight codes of the matrix
-  CUtensorMap bmap;  // activation rows in permuted order (BN-row box): x copy or h
+  CUtensorMap bmap;  // activation rows in permuted order as [K/64 atoms][rows][64], boxes of BN rows x 2 atoms
+  const uint8_t* wimg;  // NVFP4: the weight image [E, K/128, N/128, kW16Block]
   const __nv_bfloat16* x;  // activations of the gate/up GEMM [T, K], gathered by token (small row blocks)
   const void* wscale;
   const float* wgs;
@@ -305,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStagesW; ++i) {
-      mbar_init(&w_full[i], 1 + 32);  // the TMA issue plus one cp.async arrival per producer lane
+      // the TMA issue, plus (scales by cp.async) one arrival per producer lane
+      mbar_init(&w_full[i], FMT == MOE_FMT_NVFP4_W4A16 ? 1 : 1 + 32);
       mbar_init(&w_empty[i], kConvWarps);
     }
     for (int i = 0; i < kStagesA; ++i) {
@@ -330,8 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     tmem_relinquish();
   }
   if (warp == kProdWarp && lane == 0) {
-    prefetch_tmap(&a.wmap);
-    prefetch_tmap(&a.bmap);
+    if (FMT != MOE_FMT_NVFP4_W4A16) prefetch_tmap(&a.wmap);
+    if (!kGather) prefetch_tmap(&a.bmap);
   }
   fence_before_sync();
   __syncthreads();
@@ -397,6 +399,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
           if (ok) {
             mbar_arrive_expect_tx(&w_full[sw], nsub * WSUB);
             ++armed_w[sw];
+            if (FMT == MOE_FMT_NVFP4_W4A16)  // the item's (one or) two adjacent image blocks
+              bulk_load(sW + sw * WSTAGE,
+                        a.wimg + (((size_t)te.expert * nK + kc) * (a.N / 128) + 2 * (wk % ncb)) * kW16Block,
+                        nsub * kW16Block, &w_full[sw]);
+            else
             for (int g = 0; g < nsub; ++g) {
               char* dst = sW + sw * WSTAGE + g * WSUB;
               const int nb = g == 0 ? nb0 : nb1;
@@ -405,10 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
                 tma_load_2d(dst + 128 * 128, &a.wmap, &w_full[sw], kc * kKC + 64, te.expert * a.N + nb);
               } else if (FMT == MOE_FMT_FP8_B128_W8A16)
                 tma_load_2d(dst, &a.wmap, &w_full[sw], kc * kKC, te.expert * a.N + nb);
-              else if (FMT == MOE_FMT_INT4_G128_W4A16)
-                tma_load_2d(dst, &a.wmap, &w_full[sw], nb, te.expert * (a.K / 8) + kc * 16);
               else
-                tma_load_2d(dst, &a.wmap, &w_full[sw], kc * (kKC / 2), te.expert * a.N + nb);
+                tma_load_2d(dst, &a.wmap, &w_full[sw], nb, te.expert * (a.K / 8) + kc * 16);
             }
           }
         }
@@ -417,7 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         {  // this chunk's weight scales into the stage's slot, completing on the same barrier
           char* ss = sS + sw * kScaleSlot;
           const int e = te.expert;
-          if (FMT == MOE_FMT_BF16) {
+          if (FMT == MOE_FMT_NVFP4_W4A16) {
+            // in the image blocks
+          } else if (FMT == MOE_FMT_BF16) {
             // no scales: the arrival below still completes this lane's share of the barrier
           } else if (FMT == MOE_FMT_FP8_B128_W8A16) {
             if (lane < nsub)
@@ -429,17 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
               cp_async_16(smem_u32(ss + g * 256 + piece * 16),
                           (const char*)a.wscale + (((size_t)e * (a.K / 128) + kc) * a.N + (g == 0 ? nb0 : nb1)) * 2 +
                               piece * 16);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int row = lane + 32 * i, g = row >> 7;
-              if (g < nsub)
-                cp_async_8(smem_u32(ss + row * 8), (const uint8_t*)a.wscale +
-                                                       ((size_t)e * a.N + (g == 0 ? nb0 : nb1) + (row & 127)) * (a.K / 16) +
-                                                       kc * 8);
-            }
           }
-          cp_async_mbar_arrive_noinc(&w_full[sw]);
+          if (FMT != MOE_FMT_NVFP4_W4A16) cp_async_mbar_arrive_noinc(&w_full[sw]);
         }
       }
       if (!ok) break;
@@ -470,8 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
             char* bd = sB + sb * BSTAGE;
             mbar_arrive_expect_tx(&b_full[sb], BSTAGE);
             ++armed_b[sb];
-            tma_load_2d(bd, &a.bmap, &b_full[sb], kc * kKC, te.row0);
-            tma_load_2d(bd + BN * 128, &a.bmap, &b_full[sb], kc * kKC + 64, te.row0);
+            tma_load_3d(bd, &a.bmap, &b_full[sb], 0, te.row0, kc * 2);  // both 64-K atoms
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -543,7 +540,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     // ---------------- MMA issuer ----------------
     // The whole warp walks the loop and waits together (lane 0 issues): a lane left idling in a
     // barrier wait would hold the diverged warp, and with it the issuing lane, asleep.
-    const uint32_t idesc = idesc_bf16_f32(128, BN);
     int it = 0;
     bool ok = true;
     for (int nitem = 0; ok; ++nitem) {
@@ -552,6 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       TileEntry te;
       int nb0, nb1, nsub;
       item(wk, te, nb0, nb1, nsub);
+      // the MMA's N: the item's rows rounded up to 16 (a routing tile of a small expert is mostly
+      // padding, and the tensor pipe's time per MMA scales with N)
+      const int nmma = ((te.rows + 15) & ~15) < BN ? ((te.rows + 15) & ~15) : BN;
+      const uint32_t idesc = idesc_bf16_f32(128, nmma);
       for (int kc = 0; kc < nK; ++kc, ++it) {
         const int sa = it % kStagesA, sb = it % SB;
         ok = mbar_wait(&a_full[sa], (it / kStagesA) & 1, &s_abort) &&
@@ -616,17 +616,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         if (active && FMT != MOE_FMT_BF16) {
           if (FMT == MOE_FMT_FP8_B128_W8A16) sc_raw = *(const uint32_t*)(ss + g * 4);
           else if (FMT == MOE_FMT_INT4_G128_W4A16) sc_raw = __float_as_uint(__half2float(*(const __half*)(ss + g * 256 + r * 2)));
-          else sc_raw = *(const uint32_t*)(ss + (g * 128 + r) * 8 + kh * 4);
         }
         const float sc = __uint_as_float(sc_raw);
-        const uint32_t bs4 = sc_raw;
         uint32_t v[32];
         if (active) {
           const char* sub = sW + sw * WSTAGE + g * WSUB;
           if (FMT == MOE_FMT_BF16) conv_bf16(sub, r, kh, v);
           else if (FMT == MOE_FMT_FP8_B128_W8A16) conv_fp8(sub, r, kh, sc, v);
           else if (FMT == MOE_FMT_INT4_G128_W4A16) conv_int4(sub, r, kh, sc, v);
-          else conv_nvfp4(sub, r, kh, bs4, v);
+          else {  // image block of this row: gate/up blocks hold 64 gate rows, then the up rows
+            const int blk = MODE == 0 ? r >> 6 : g, row = MODE == 0 ? 64 * g + (r & 63) : r;
+            const char* b = sW + sw * WSTAGE + blk * WSUB;
+            conv_nvfp4(b, row, kh, *(const uint32_t*)(b + kW16Codes + row * 8 + kh * 4), v);
+          }
           reg_fence(v);
         }
         __syncwarp();
@@ -650,7 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       if (MODE == 0) {
         const int part = warp >> 2;  // 0..3: 16-column chunks part, part+4, ...
         const int n = nb0 + r;
-        for (int c0 = part * 16; c0 < BN; c0 += 64) {
+        const int cend = te.rows < BN ? te.rows : BN;  // warp-uniform: no column group past the rows
+        for (int c0 = part * 16; c0 < cend; c0 += 64) {
           uint32_t G[16], U[16];
           tmem_ld_32x16(taddr(tmem, q * 32, c0), G);
           tmem_ld_32x16(taddr(tmem, q * 32, BN + c0), U);
@@ -669,7 +672,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
         const int c = nb + r;
         const int* ct = s_ct[buf];
         const float* cw = s_cw[buf];
-        for (int c0 = kh * 16; c0 < BN; c0 += 32) {
+        const int cend = te.rows < BN ? te.rows : BN;
+        for (int c0 = kh * 16; c0 < cend; c0 += 32) {
           uint32_t Y[16];
           tmem_ld_32x16(taddr(tmem, q * 32, g * BN + c0), Y);
           tmem_ld_wait();
@@ -748,8 +752,21 @@ bool weight_map(CUtensorMap* m, int fmt, const MatView& v, int E) {
   if (fmt == MOE_FMT_INT4_G128_W4A16)
     return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, v.a, v.N, (uint64_t)E * (v.K / 8), (uint64_t)v.N * 4, 128, 16,
                     CU_TENSOR_MAP_SWIZZLE_NONE);
-  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, v.a, v.K / 2, (uint64_t)E * v.N, v.K / 2, 64, 128,
-                  CU_TENSOR_MAP_SWIZZLE_64B);
+  return true;  // NVFP4: image blocks by bulk copy
+}
+
+// Activation rows [R, K] bf16 viewed as [K/64 atoms][R rows][64]: one copy brings BN rows x
+// 128 K as two 128-byte swizzle atoms.
+bool act_map(CUtensorMap* m, const void* base, uint64_t R, int K, int bn) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, R, (cuuint64_t)K / 64};
+  cuuint64_t strides[2] = {(cuuint64_t)K * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)bn, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int FMT, int MODE, int BN>
@@ -810,12 +827,9 @@ cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, co
                               int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, uint16_t* out) {
   const int E = d.E, H = d.H, I = d.I;
   const size_t R = (size_t)T * k;
-  MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
-  if (d.fmt == MOE_FMT_NVFP4_W4A16) {  // NVFP4 codes in the converter's bit order (conv_nvfp4)
-    if (!d.size[MOE_T_GU_IMG] || !d.size[MOE_T_D_IMG]) return cudaErrorInvalidValue;
-    gu.a = (const uint8_t*)(packed + d.offset[MOE_T_GU_IMG]);
-    dn.a = (const uint8_t*)(packed + d.offset[MOE_T_D_IMG]);
-  }
+  const MatView gu = mat_view(d, packed, 0), dn = mat_view(d, packed, 1);
+  // NVFP4: weight image blocks (codes in the converter's bit order, then scales)
+  if (d.fmt == MOE_FMT_NVFP4_W4A16 && (!d.size[MOE_T_GU_IMG] || !d.size[MOE_T_D_IMG])) return cudaErrorInvalidValue;
   TcArgs a;
   memset(&a, 0, sizeof(a));
   a.perm = (const int32_t*)(ws + L.perm);
@@ -832,12 +846,11 @@ cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, co
 
   // gate/up: A = fused [2I, H] weights, B = gathered rows of x
   if (!weight_map(&a.wmap, d.fmt, gu, E)) return cudaErrorInvalidValue;
+  a.wimg = (const uint8_t*)(packed + d.offset[MOE_T_GU_IMG]);
   a.x = x;
   if (bn >= kTcPermuteFromRows) {
     __nv_bfloat16* xp = (__nv_bfloat16*)(ws + L.xp);
-    if (launch_gather_rows(x, a.perm, k, (int)R, H, xp, s) != cudaSuccess ||
-        !make_map(&a.bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xp, H, (uint64_t)R, (uint64_t)H * 2, 64, bn,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
+    if (launch_gather_rows(x, a.perm, k, (int)R, H, xp, s) != cudaSuccess || !act_map(&a.bmap, xp, R, H, bn))
       return cudaErrorInvalidValue;
   }
   a.wscale = gu.b;
@@ -851,10 +864,8 @@ cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, co
   if (err != cudaSuccess) return err;
 
   // down: A = [H, I] weights, B = rows of h (already in permuted order)
-  if (!weight_map(&a.wmap, d.fmt, dn, E) ||
-      !make_map(&a.bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws + L.h, I, (uint64_t)R, (uint64_t)I * 2, 64, bn,
-                CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
+  if (!weight_map(&a.wmap, d.fmt, dn, E) || !act_map(&a.bmap, ws + L.h, R, I, bn)) return cudaErrorInvalidValue;
+  a.wimg = (const uint8_t*)(packed + d.offset[MOE_T_D_IMG]);
   a.wscale = dn.b;
   a.wgs = dn.gs;
   a.N = H;

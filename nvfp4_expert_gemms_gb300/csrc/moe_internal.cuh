@@ -124,6 +124,10 @@ cudaError_t launch_dequant(const moe_packed_desc_t& d, const char* packed, int e
 //               scales row by row (16 bytes per row).
 // C = ceil(K / 256); a last half chunk leaves its upper 64 bytes per row unused.
 constexpr int kImgTile = 16384, kImgSf = 2048;
+// NVFP4 W4A16 weight image block ([E, K/128, N/128] of them): one 128-row tile (gate/up: 64 gate
+// rows, then the same features' up rows) of one 128-column chunk -- 64 code bytes per row in the bf16 converter's bit
+// order, 16-byte piece p of row l at piece p ^ ((l / 2) % 4), then 8 E4M3 scales per row.
+constexpr int kW16Codes = 128 * 64, kW16Block = kW16Codes + 128 * 8;
 constexpr int kWImgBlock = 2 * kImgTile + 2 * kImgSf, kAImgBlock = kImgTile + kImgSf;
 __host__ __device__ inline int nvfp4_chunks(int K) { return (K + 255) / 256; }
 // Byte of the 8 codes of 16-block b (0..15 of the chunk) of tile row l within a tile's codes.

@@ -143,11 +143,11 @@ __global__ void __launch_bounds__(256) nvfp4_image_kernel(const uint8_t* __restr
   for (int b = 0; b < 16; ++b) tsf[img_wsf_byte(l, b)] = row_ok && 8 * b < kb ? ssrc[b] : (uint8_t)0;
 }
 
-// The NVFP4 W4A16 weights in the bf16 converter's bit order (conv_nvfp4 in moe_gemm_tc.cu): the
-// canonical codes' shape and byte positions, each 32-bit word of eight E2M1 codes (element k =
-// nibble k; code bits m, e0, e1, s = bits 0..3) with its bits moved so that element pair j comes
-// out of one shift-and-mask of the word: pair 0 by << 6, pair 1 by << 2, pair 2 by a rotate right
-// by 4, pair 3 in place except the two mantissa bits (>> 8).
+// One 32-bit word of eight E2M1 codes in the bf16 converter's bit order (conv_nvfp4 in
+// moe_gemm_tc.cu): element k = nibble k of the canonical word (code bits m, e0, e1, s = bits
+// 0..3), its bits moved so that element pair j comes out of one shift-and-mask of the word: pair
+// 0 by << 6, pair 1 by << 2, pair 2 by a rotate right by 4, pair 3 in place except the two
+// mantissa bits (>> 8).
 __device__ __forceinline__ uint32_t w4a16_image_word(uint32_t c) {
   constexpr uint8_t kDst[8][4] = {{0, 1, 2, 9},     {16, 17, 18, 25}, {4, 5, 6, 13},  {20, 21, 22, 29},
                                   {10, 11, 12, 19}, {26, 27, 28, 3},  {14, 7, 8, 15}, {30, 23, 24, 31}};
@@ -159,10 +159,27 @@ __device__ __forceinline__ uint32_t w4a16_image_word(uint32_t c) {
   return o;
 }
 
-__global__ void __launch_bounds__(256) nvfp4_w4a16_image_kernel(const uint32_t* __restrict__ codes, size_t words,
-                                                                uint32_t* __restrict__ img) {
+// The W4A16 weight image of one expert matrix (canonical codes [E, N, K/2], scales [E, N, K/16]),
+// blocks [E, K/128, N/128]: thread = one row l of one (expert, 128-column chunk c, 128-row tile b)
+// block; gate/up (gu) tile b = gate rows 64b.. then up rows N/2 + 64b..; down tile b = rows 128b...
+__global__ void __launch_bounds__(256) nvfp4_w4a16_image_kernel(const uint8_t* __restrict__ codes,
+                                                                const uint8_t* __restrict__ scales, int E, int N,
+                                                                int K, bool gu, uint8_t* __restrict__ img) {
+  const int C = K / 128, NB = N / 128;
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < words) img[i] = w4a16_image_word(codes[i]);
+  if (i >= (size_t)E * NB * C * 128) return;
+  const int l = (int)(i % 128), b = (int)((i / 128) % NB), c = (int)((i / 128 / NB) % C), e = (int)(i / 128 / NB / C);
+  const int n = gu ? (l < 64 ? 64 * b + l : N / 2 + 64 * b + l - 64) : 128 * b + l;
+  uint8_t* blk = img + (((size_t)e * C + c) * NB + b) * kW16Block;
+  const uint8_t* src = codes + ((size_t)e * N + n) * (K / 2) + 64 * c;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint4 v = *(const uint4*)(src + 16 * p);
+    const uint4 o = make_uint4(w4a16_image_word(v.x), w4a16_image_word(v.y), w4a16_image_word(v.z),
+                               w4a16_image_word(v.w));
+    *(uint4*)(blk + 64 * l + ((p ^ ((l >> 1) & 3)) << 4)) = o;
+  }
+  *(uint2*)(blk + kW16Codes + 8 * l) = *(const uint2*)(scales + ((size_t)e * N + n) * (K / 16) + 8 * c);
 }
 
 __global__ void nvfp4_finish_kernel(unsigned* slot, int E) {
@@ -401,9 +418,9 @@ cudaError_t launch_pack(const moe_packed_desc_t& d, const __nv_bfloat16* wgu, co
       note_launches(2);
       const int it = which == 0 ? MOE_T_GU_IMG : MOE_T_D_IMG;
       if (d.size[it] && d.fmt == MOE_FMT_NVFP4_W4A16) {
-        const size_t words = d.size[it] / 4;
-        nvfp4_w4a16_image_kernel<<<(unsigned)((words + 255) / 256), 256, 0, s>>>(
-            (const uint32_t*)a, words, (uint32_t*)(packed + d.offset[it]));
+        const size_t n = d.size[it] / kW16Block * 128;
+        nvfp4_w4a16_image_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, b, E, N, K, which == 0,
+                                                                              (uint8_t*)(packed + d.offset[it]));
         note_launches(1);
       } else if (d.size[it]) {
         const size_t n = d.size[it] / kWImgBlock * 256;

@@ -47,10 +47,11 @@ def test_packed_sizes_match_canonical_shapes(orc):
     assert round(sum(int(d.size[i]) for i in range(6)) / 2 ** 30, 2) == 0.32
     assert int(d.size[M.MOE_T_GU_IMG]) == int(d.size[M.MOE_T_GU_A]) + int(d.size[M.MOE_T_GU_B])
     assert int(d.size[M.MOE_T_D_IMG]) == int(d.size[M.MOE_T_D_A]) + int(d.size[M.MOE_T_D_B])
-    # W4A16 repeats only the codes, in the bf16 converter's bit order (same shape as GU_A / D_A)
+    # W4A16 repeats codes and scales as the bf16 converter's image: 9 KB per 128-row tile and chunk
     d = M.moe_packed_size("nvfp4_w4a16", E, H, I)
-    assert int(d.size[M.MOE_T_GU_IMG]) == int(d.size[M.MOE_T_GU_A])
-    assert int(d.size[M.MOE_T_D_IMG]) == int(d.size[M.MOE_T_D_A])
+    assert int(d.size[M.MOE_T_GU_IMG]) == int(d.size[M.MOE_T_GU_A]) + int(d.size[M.MOE_T_GU_B])
+    assert int(d.size[M.MOE_T_D_IMG]) == int(d.size[M.MOE_T_D_A]) + int(d.size[M.MOE_T_D_B])
+    assert int(d.size[M.MOE_T_GU_IMG]) == E * (2 * I // 128) * (H // 128) * 9216
     # K not a multiple of 256 and H not of 256: whole 36 KB blocks per (tile pair, 256-column
     # chunk), the last chunk half used, the last down pair's second tile empty
     d = M.moe_packed_size("nvfp4_w4a4", 3, 384, 640)

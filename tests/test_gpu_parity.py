@@ -127,18 +127,22 @@ def _operand_image(codes, scales, N, K, gu):
 
 
 def test_w4a16_converter_image():
-    """The W4A16 buffer's second copy of the codes is the canonical codes with each 32-bit
-    word's bits moved as the header's table says."""
+    """The W4A16 buffer's weight image holds the canonical codes (each 32-bit word's bits moved
+    as the header's table says, pieces swizzled) and scales, per 128-row tile and 128-column
+    chunk; gate/up tiles pair 64 gate rows with the same features' up rows."""
     E, H, I = 3, 384, 256
     wgu, wd = synth.gen_expert_weights(E, H, I, seed=9)
     layer = M.MoELayer("nvfp4_w4a16", dev_bf16(wgu), dev_bf16(wd))
     torch.cuda.synchronize()
     d = layer.desc
-    for ca, im in ((M.MOE_T_GU_A, M.MOE_T_GU_IMG), (M.MOE_T_D_A, M.MOE_T_D_IMG)):
-        codes = M.packed_view(d, layer.packed, ca).cpu().numpy()
+    for ca, cb, im, (N, K), gu in ((M.MOE_T_GU_A, M.MOE_T_GU_B, M.MOE_T_GU_IMG, (2 * I, H), True),
+                                   (M.MOE_T_D_A, M.MOE_T_D_B, M.MOE_T_D_IMG, (H, I), False)):
+        codes = M.packed_view(d, layer.packed, ca).cpu().numpy().reshape(E, N, K // 2)
+        sc = M.packed_view(d, layer.packed, cb).cpu().numpy().reshape(E, N, K // 16)
         got = M.packed_view(d, layer.packed, im).cpu().numpy()
-        assert got.shape == codes.shape
-        assert got.tobytes() == w4a16_bits.words(codes).tobytes()
+        want = w4a16_bits.image(codes, sc, gu)
+        assert got.shape == want.shape
+        assert got.tobytes() == want.tobytes(), gu
 
 
 @pytest.mark.parametrize("H,I", [(512, 256), (384, 640)])
