@@ -18,6 +18,8 @@ cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const
   if (d.fmt == MOE_FMT_FP8_B128_W8A8) return launch_experts_w8a8(d, packed, x, T, k, L, ws, ev, s, o);
   if (d.fmt == MOE_FMT_FP8_B128_W8A16 && row_block == fp8dec_row_block())
     return launch_experts_fp8dec(d, packed, x, T, k, L, ws, ev, s, o);
+  if (d.fmt == MOE_FMT_NVFP4_W4A16 && row_block == tcw_row_block())
+    return launch_experts_tcw(d, packed, x, T, k, L, ws, ev, s, o);
   return launch_experts_tc(d, packed, x, T, k, row_block, L, ws, ev, s, o);
 }
 

@@ -217,6 +217,9 @@ int tc_row_block(int fmt, int T, int k, int E);
 bool tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1, uint64_t pitch,
                  uint32_t b0, uint32_t b1, CUtensorMapSwizzle sw);
 int tc_num_sms();
+// Activation rows [R, K] bf16 as a 3-D map ([K/64 atoms][R rows][64]) whose box brings bn rows x
+// 128 K, both 128-byte swizzle atoms, in one copy.
+bool tc_act_map(CUtensorMap* m, const void* base, uint64_t R, int K, int bn);
 // FP8 decode path (16-row tiles, weights straight into kind::f8f6f4 MMAs).
 int fp8dec_row_block();
 // Each down GEMM ends with the deterministic routing-weighted combine into out (bf16 [T, H]).
@@ -234,6 +237,10 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
                                const float* act_gs = nullptr, bool calibrate = false);
 cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
                               int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, uint16_t* out);
+// NVFP4 W4A16 with 256-row routing tiles (tc_row_block's choice at prefill sizes).
+int tcw_row_block();
+cudaError_t launch_experts_tcw(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
+                               const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, uint16_t* out);
 
 
 }  // namespace moe

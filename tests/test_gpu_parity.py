@@ -419,6 +419,14 @@ def test_layer_edge_cases(orc, fmt, T, E, k):
     check_close(synth.bf16_bits_to_f32(c.run()), c.oracle(orc), fmt)
 
 
+@pytest.mark.parametrize("T,H,I,E,k", [(1100, 256, 128, 8, 2), (1500, 384, 256, 16, 4), (530, 512, 384, 2, 1)])
+def test_w4a16_wide_tiles(orc, T, H, I, E, k):
+    """NVFP4 W4A16 at prefill sizes (more than 64 rows per active expert) takes 256-row routing
+    tiles: full and ragged tiles, K of one to four chunks (fewer than the A ring's four stages)."""
+    c = Case("nvfp4_w4a16", T, H, I, E, k, seed=T)
+    check_close(synth.bf16_bits_to_f32(c.run()), c.oracle(orc), f"T={T}")
+
+
 def test_layer_zero_tokens_is_a_no_op():
     c = Case("fp8", 4, 256, 128, 8, 2)
     x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
