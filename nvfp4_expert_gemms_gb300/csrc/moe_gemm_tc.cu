@@ -209,6 +209,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   constexpr int SB = Cfg::SB;  // activation stages
   constexpr int kStagesA = BN <= 64 ? 3 : 2;
   constexpr uint32_t kACol = BN <= 64 ? 128 : 256;
+  // Row blocks of 32 or fewer: two accumulators (one per item in flight) fit below the A ring, so
+  // the next item's first chunks are converted and multiplied while the previous item's epilogue
+  // runs; larger row blocks keep one accumulator, drained before the next item's conversion.
+  constexpr bool kDB = BN <= 32;
+  static_assert(!kDB || 4 * BN <= (int)kACol, "two accumulators fit below the A ring");
   constexpr int WSUB = WFmt<FMT>::kSubBytes;
   constexpr int WSTAGE = 2 * WSUB;
   constexpr int BSTAGE = Cfg::kBStage;  // BN rows x 128 K bf16, two 128-byte swizzle atoms
@@ -219,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   char* sS = sB + SB * BSTAGE;  // scale slots, one per weight stage
   constexpr int kScaleSlot = Cfg::kScaleSlot;
   __shared__ uint64_t w_full[kStagesW], w_empty[kStagesW], a_full[kStagesA], a_empty[kStagesA], b_full[SB],
-      b_empty[SB], acc_full, drain;
+      b_empty[SB], acc_full[2], acc_empty[2], drain;
   __shared__ uint64_t work_full[kRing], work_empty[kRing];
   __shared__ int s_work[kRing];
   __shared__ uint32_t s_tmem;
@@ -256,7 +261,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       mbar_init(&work_full[i], 1);
       mbar_init(&work_empty[i], (kGather ? kGathWarps : 1) + 1 + kConvWarps);  // every consuming warp
     }
-    mbar_init(&acc_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kConvWarps);
+    }
     mbar_init(&drain, 1);
     s_abort = 0;
     fence_barrier_init();
@@ -486,10 +494,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       // padding, and the tensor pipe's time per MMA scales with N)
       const int nmma = ((te.rows + 15) & ~15) < BN ? ((te.rows + 15) & ~15) : BN;
       const uint32_t idesc = idesc_bf16_f32(128, nmma);
+      const int ab = kDB ? nitem & 1 : 0;
+      const uint32_t acc = tmem + ab * 2 * BN;
       for (int kc = 0; kc < nK; ++kc, ++it) {
         const int sa = it % kStagesA, sb = it % SB;
         ok = mbar_wait(&a_full[sa], (it / kStagesA) & 1, &s_abort) &&
-             mbar_wait(&b_full[sb], (it / SB) & 1, &s_abort);
+             mbar_wait(&b_full[sb], (it / SB) & 1, &s_abort) &&
+             (!kDB || kc != 0 || mbar_wait(&acc_empty[ab], ((nitem >> 1) & 1) ^ 1, &s_abort));
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         fence_after_sync();
@@ -499,14 +510,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint64_t bdsc = sdesc_k_sw128(b0 + (ks >> 2) * BN * 128 + (ks & 3) * 32);
-              mma_f16_ts(tmem + g * BN, tmem + kACol + sa * 128 + g * 64 + ks * 8, bdsc, idesc, (kc | ks) != 0);
+              mma_f16_ts(acc + g * BN, tmem + kACol + sa * 128 + g * 64 + ks * 8, bdsc, idesc, (kc | ks) != 0);
             }
           mma_commit(&a_empty[sa]);
           mma_commit(&b_empty[sb]);
         }
         __syncwarp();
       }
-      if (ok && lane == 0) mma_commit(&acc_full);
+      if (ok && lane == 0) mma_commit(&acc_full[ab]);
       __syncwarp();
     }
     if (lane == 0) mma_commit(&drain);  // completes once every MMA issued by this thread has finished
@@ -516,109 +527,162 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
     const int g = (warp >> 2) & 1, kh = warp >> 3, q = warp & 3, r = q * 32 + lane;
     int it = 0;
     bool ok = true;
-    for (int nitem = 0;; ++nitem) {
-      const int wk = next_item(nitem, ok);
-      // the converter warps leave together (they meet in a named barrier every item)
-      if (!named_bar_and(1, kConvWarps * 32, ok && wk >= 0)) break;
-      TileEntry te;
-      int nb0, nb1, nsub;
-      item(wk, te, nb0, nb1, nsub);
-      const int e = te.expert;
+    // one K chunk of the item into the A ring: this thread's row of sub-tile g, K half kh
+    auto convert = [&](int nsub) -> bool {
       const bool active = g < nsub;
-      const int nb = g == 0 ? nb0 : nb1;
-      const int buf = nitem & 1;
-      const float inv_gs = FMT == MOE_FMT_NVFP4_W4A16 ? 0x1p10f / a.wgs[e] : 1.f;  // see conv_nvfp4
-      if (MODE == 1 && threadIdx.x < BN) {  // column table of the down epilogue
-        const int col = threadIdx.x;
-        int ct = 0;
-        float cw = 0.f;
-        if (col < te.rows) {
-          const int p = a.perm[te.row0 + col];
-          ct = p / a.k;
-          cw = a.topk_w[p] * inv_gs;
-        }
-        s_ct[buf][col] = ct;
-        s_cw[buf][col] = cw;
+      const int sw = it % kStagesW, sa = it % kStagesA;
+      if (!__all_sync(0xffffffffu, mbar_wait(&w_full[sw], (it / kStagesW) & 1, &s_abort))) return false;
+      // the chunk's scale for this thread's row (or sub-tile), from the stage's scale slot
+      const char* ss = sS + sw * kScaleSlot;
+      uint32_t sc_raw = 0u;
+      if (active && FMT != MOE_FMT_BF16) {
+        if (FMT == MOE_FMT_FP8_B128_W8A16) sc_raw = *(const uint32_t*)(ss + g * 4);
+        else if (FMT == MOE_FMT_INT4_G128_W4A16) sc_raw = __float_as_uint(__half2float(*(const __half*)(ss + g * 256 + r * 2)));
       }
-      for (int kc = 0; kc < nK; ++kc, ++it) {
-        const int sw = it % kStagesW, sa = it % kStagesA;
-        ok = __all_sync(0xffffffffu, mbar_wait(&w_full[sw], (it / kStagesW) & 1, &s_abort));
-        if (!ok) break;
-        // the chunk's scale for this thread's row (or sub-tile), from the stage's scale slot
-        const char* ss = sS + sw * kScaleSlot;
-        uint32_t sc_raw = 0u;
-        if (active && FMT != MOE_FMT_BF16) {
-          if (FMT == MOE_FMT_FP8_B128_W8A16) sc_raw = *(const uint32_t*)(ss + g * 4);
-          else if (FMT == MOE_FMT_INT4_G128_W4A16) sc_raw = __float_as_uint(__half2float(*(const __half*)(ss + g * 256 + r * 2)));
+      const float sc = __uint_as_float(sc_raw);
+      uint32_t v[32];
+      if (active) {
+        const char* sub = sW + sw * WSTAGE + g * WSUB;
+        if (FMT == MOE_FMT_BF16) conv_bf16(sub, r, kh, v);
+        else if (FMT == MOE_FMT_FP8_B128_W8A16) conv_fp8(sub, r, kh, sc, v);
+        else if (FMT == MOE_FMT_INT4_G128_W4A16) conv_int4(sub, r, kh, sc, v);
+        else {  // image block of this row: gate/up blocks hold 64 gate rows, then the up rows
+          const int blk = MODE == 0 ? r >> 6 : g, row = MODE == 0 ? 64 * g + (r & 63) : r;
+          const char* b = sW + sw * WSTAGE + blk * WSUB;
+          conv_nvfp4(b, row, kh, *(const uint32_t*)(b + kW16Codes + row * 8 + kh * 4), v);
         }
-        const float sc = __uint_as_float(sc_raw);
-        uint32_t v[32];
-        if (active) {
-          const char* sub = sW + sw * WSTAGE + g * WSUB;
-          if (FMT == MOE_FMT_BF16) conv_bf16(sub, r, kh, v);
-          else if (FMT == MOE_FMT_FP8_B128_W8A16) conv_fp8(sub, r, kh, sc, v);
-          else if (FMT == MOE_FMT_INT4_G128_W4A16) conv_int4(sub, r, kh, sc, v);
-          else {  // image block of this row: gate/up blocks hold 64 gate rows, then the up rows
-            const int blk = MODE == 0 ? r >> 6 : g, row = MODE == 0 ? 64 * g + (r & 63) : r;
-            const char* b = sW + sw * WSTAGE + blk * WSUB;
-            conv_nvfp4(b, row, kh, *(const uint32_t*)(b + kW16Codes + row * 8 + kh * 4), v);
-          }
-          reg_fence(v);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&w_empty[sw]);
-        ok = __all_sync(0xffffffffu, mbar_wait(&a_empty[sa], ((it / kStagesA) & 1) ^ 1, &s_abort));
-        if (!ok) break;
-        fence_after_sync();
-        if (active) {
-          tmem_st_32x32(taddr(tmem, q * 32, kACol + sa * 128 + g * 64 + kh * 32), v);
-          tmem_st_wait();
-        }
-        fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[sa]);
+        reg_fence(v);
       }
-      // epilogue of this item; every converter thread takes the same branch here
-      if (ok) ok = mbar_wait(&acc_full, nitem & 1, &s_abort);
-      ok = named_bar_and(1, kConvWarps * 32, ok);
-      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&w_empty[sw]);
+      if (!__all_sync(0xffffffffu, mbar_wait(&a_empty[sa], ((it / kStagesA) & 1) ^ 1, &s_abort))) return false;
       fence_after_sync();
+      if (active) {
+        tmem_st_32x32(taddr(tmem, q * 32, kACol + sa * 128 + g * 64 + kh * 32), v);
+        tmem_st_wait();
+      }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_full[sa]);
+      return true;
+    };
+    // epilogue of item n from accumulator buffer ab (the caller has waited for acc_full); with
+    // two accumulators the buffer is released as soon as this warp has read its columns
+    auto epilogue = [&](int n, int ab, const TileEntry& te, int nb0, int nb1, int nsub, float inv_gs) {
+      const uint32_t acc = tmem + ab * 2 * BN;
+      const int cend = te.rows < BN ? te.rows : BN;  // warp-uniform: no column group past the rows
+      auto release = [&]() {
+        if (kDB) {
+          fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[ab]);
+        }
+      };
       if (MODE == 0) {
         const int part = warp >> 2;  // 0..3: 16-column chunks part, part+4, ...
-        const int n = nb0 + r;
-        const int cend = te.rows < BN ? te.rows : BN;  // warp-uniform: no column group past the rows
+        const int n_out = nb0 + r;
+        bool released = false;
         for (int c0 = part * 16; c0 < cend; c0 += 64) {
           uint32_t G[16], U[16];
-          tmem_ld_32x16(taddr(tmem, q * 32, c0), G);
-          tmem_ld_32x16(taddr(tmem, q * 32, BN + c0), U);
+          tmem_ld_32x16(taddr(acc, q * 32, c0), G);
+          tmem_ld_32x16(taddr(acc, q * 32, BN + c0), U);
           tmem_ld_wait();
+          if (c0 + 64 >= cend) {  // this warp's last read of the accumulator
+            release();
+            released = true;
+          }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c0 + j;
             if (col < te.rows) {
               const float gv = __uint_as_float(G[j]) * inv_gs, uv = __uint_as_float(U[j]) * inv_gs;
               const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
-              a.h_out[(size_t)(te.row0 + col) * a.I + n] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+              a.h_out[(size_t)(te.row0 + col) * a.I + n_out] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
             }
           }
         }
-      } else if (active) {
-        const int c = nb + r;
-        const int* ct = s_ct[buf];
-        const float* cw = s_cw[buf];
-        const int cend = te.rows < BN ? te.rows : BN;
-        for (int c0 = kh * 16; c0 < cend; c0 += 32) {
+        if (!released) release();
+      } else {
+        const bool active = g < nsub;
+        const int c = (g == 0 ? nb0 : nb1) + r;
+        const float* cw = s_cw[n & 1];
+        bool released = false;
+        for (int c0 = kh * 16; active && c0 < cend; c0 += 32) {
           uint32_t Y[16];
-          tmem_ld_32x16(taddr(tmem, q * 32, g * BN + c0), Y);
+          tmem_ld_32x16(taddr(acc, q * 32, g * BN + c0), Y);
           tmem_ld_wait();
+          if (c0 + 32 >= cend) {
+            release();
+            released = true;
+          }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c0 + j;
             if (col < te.rows) a.y_out[(size_t)(te.row0 + col) * a.H + c] = bf16_bits(cw[col] * __uint_as_float(Y[j]));
           }
         }
+        if (!released) release();
       }
-      fence_before_sync();  // accumulator reads are ordered before the next item's MMAs
+    };
+    bool have_prev = false;
+    TileEntry te_p;
+    int nb0_p = 0, nb1_p = 0, nsub_p = 0;
+    float igs_p = 1.f;
+    for (int nitem = 0;; ++nitem) {
+      const int wk = next_item(nitem, ok);
+      // the converter warps leave together (they meet in a named barrier every item)
+      const bool live = named_bar_and(1, kConvWarps * 32, ok && wk >= 0);
+      if (!kDB && !live) break;
+      TileEntry te;
+      int nb0 = 0, nb1 = 0, nsub = 0, d = 0;
+      float inv_gs = 1.f;
+      if (live) {
+        item(wk, te, nb0, nb1, nsub);
+        inv_gs = FMT == MOE_FMT_NVFP4_W4A16 ? 0x1p10f / a.wgs[te.expert] : 1.f;  // see conv_nvfp4
+        if (MODE == 1 && threadIdx.x < BN) {  // column table of the down epilogue
+          const int col = threadIdx.x;
+          int ct = 0;
+          float cw = 0.f;
+          if (col < te.rows) {
+            const int p = a.perm[te.row0 + col];
+            ct = p / a.k;
+            cw = a.topk_w[p] * inv_gs;
+          }
+          s_ct[nitem & 1][col] = ct;
+          s_cw[nitem & 1][col] = cw;
+        }
+        if (kDB) {  // the item's first chunks go into the A ring before the previous item's epilogue
+          d = nK < kStagesA ? nK : kStagesA;
+          for (int kc = 0; kc < d && ok; ++kc, ++it) ok = convert(nsub);
+        }
+      }
+      if (kDB) {
+        if (have_prev && ok) {
+          const int n = nitem - 1, ab = n & 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[ab], (n >> 1) & 1, &s_abort));
+          if (ok) {
+            fence_after_sync();
+            epilogue(n, ab, te_p, nb0_p, nb1_p, nsub_p, igs_p);
+          }
+        }
+        if (!live) break;  // (a warp whose wait failed skips its work but still meets the barrier)
+        for (int kc = d; kc < nK && ok; ++kc, ++it) ok = convert(nsub);
+        te_p = te;
+        nb0_p = nb0;
+        nb1_p = nb1;
+        nsub_p = nsub;
+        igs_p = inv_gs;
+        have_prev = true;
+      } else {
+        for (int kc = 0; kc < nK && ok; ++kc, ++it) ok = convert(nsub);
+        // epilogue of this item; every converter thread takes the same branch here
+        if (ok) ok = mbar_wait(&acc_full[0], nitem & 1, &s_abort);
+        ok = named_bar_and(1, kConvWarps * 32, ok);
+        if (!ok) break;
+        fence_after_sync();
+        epilogue(nitem, 0, te, nb0, nb1, nsub, inv_gs);
+        fence_before_sync();  // accumulator reads are ordered before the next item's MMAs
+      }
     }
   }
 
