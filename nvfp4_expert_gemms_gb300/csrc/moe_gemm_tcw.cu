@@ -263,53 +263,69 @@ __global__ void __launch_bounds__(kThreads, 1) tcw_expert_gemm_kernel(const __gr
       if (lane == 0) mbar_arrive(&a_full[sa]);
       return true;
     };
-    // epilogue of item n: this warp's accumulator columns part*16 + 64 i, i = 0..3, in two
-    // halves (registers); the accumulator is released once the second half is read
+    // epilogue of item n: this warp's accumulator columns part*16 + 64 i, i = 0..3, read in two
+    // halves (registers) and turned into packed bf16 results; the accumulator is released once
+    // the second half is read, and the stores follow
     auto epilogue = [&](int n, const TileEntry& te, int nb, float inv_gs) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(&acc_full, n & 1, &s_abort))) return false;
       fence_after_sync();
       const int cend = te.rows < kBN ? te.rows : kBN;  // warp-uniform
+      const bool gl = lane < 16;
+      uint32_t P[4][8];  // bf16 pairs: gate/up 8 results per group (4 words), down 16 (8 words)
+      const int ngr = cend > part * 16 ? (cend - part * 16 + 63) / 64 : 0;  // this warp's groups
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t X[2][16];
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-          if (part * 16 + 64 * (2 * h + i) < cend) tmem_ld_32x16(taddr(tmem, q * 32, part * 16 + 64 * (2 * h + i)), X[i]);
-        tmem_ld_wait();
-        if (h == 1) {
+      for (int gi = 0; gi < 4; ++gi) {  // one group at a time: load, (last one: release), compute
+        const int c0 = part * 16 + 64 * gi;
+        uint32_t X[16];
+        if (gi < ngr) {
+          tmem_ld_32x16(taddr(tmem, q * 32, c0), X);
+          tmem_ld_wait();
+        }
+        if (gi == (ngr > 0 ? ngr - 1 : 0)) {
           fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty);
         }
+        if (gi >= ngr) continue;
+        if (MODE == 0) {
+          // lanes 0-15 hold gate values of feature nb + 16q + lane, lanes 16-31 the same
+          // features' up values; the low half computes columns c0..c0+7, the high half c0+8..
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int c0 = part * 16 + 64 * (2 * h + i);
-          if (c0 >= cend) continue;
-          if (MODE == 0) {
-            // lanes 0-15 hold gate values of feature nb + 16q + lane, lanes 16-31 the same
-            // features' up values; the low half computes columns c0..c0+7, the high half c0+8..
-            const bool gl = lane < 16;
-            const int n_out = nb + 16 * q + (lane & 15);
+          for (int j = 0; j < 8; j += 2) {
+            float hv[2];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t recv = __shfl_xor_sync(0xffffffffu, gl ? X[i][8 + j] : X[i][j], 16);
-              const float gv = __uint_as_float(gl ? X[i][j] : recv) * inv_gs;
-              const float uv = __uint_as_float(gl ? recv : X[i][8 + j]) * inv_gs;
-              const int col = c0 + (gl ? 0 : 8) + j;
-              if (col < te.rows) {
-                const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
-                a.h_out[(size_t)(te.row0 + col) * a.I + n_out] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
-              }
+            for (int u = 0; u < 2; ++u) {
+              const uint32_t recv = __shfl_xor_sync(0xffffffffu, gl ? X[8 + j + u] : X[j + u], 16);
+              const float gv = __uint_as_float(gl ? X[j + u] : recv) * inv_gs;
+              const float uv = __uint_as_float(gl ? recv : X[8 + j + u]) * inv_gs;
+              hv[u] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
             }
-          } else {
-            const int c = nb + 32 * q + lane;
-            const float* cw = s_cw[n & 1];
+            P[gi][j >> 1] = pack_bf16x2(hv[0], hv[1]);
+          }
+        } else {
+          const float* cw = s_cw[n & 1];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int col = c0 + j;
-              if (col < te.rows)
-                a.y_out[(size_t)(te.row0 + col) * a.H + c] = bf16_bits(cw[col] * __uint_as_float(X[i][j]));
-            }
+          for (int j = 0; j < 16; j += 2)
+            P[gi][j >> 1] = pack_bf16x2(cw[c0 + j] * __uint_as_float(X[j]), cw[c0 + j + 1] * __uint_as_float(X[j + 1]));
+        }
+      }
+#pragma unroll
+      for (int gi = 0; gi < 4; ++gi) {
+        const int c0 = part * 16 + 64 * gi;
+        if (c0 >= cend) continue;
+        if (MODE == 0) {
+          const int n_out = nb + 16 * q + (lane & 15);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int col = c0 + (gl ? 0 : 8) + j;
+            if (col < te.rows) a.h_out[(size_t)(te.row0 + col) * a.I + n_out] = (uint16_t)(P[gi][j >> 1] >> (16 * (j & 1)));
+          }
+        } else {
+          const int c = nb + 32 * q + lane;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            if (col < te.rows) a.y_out[(size_t)(te.row0 + col) * a.H + c] = (uint16_t)(P[gi][j >> 1] >> (16 * (j & 1)));
           }
         }
       }
