@@ -16,8 +16,10 @@ cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const
   uint16_t* o = (uint16_t*)out;
   if (d.fmt == MOE_FMT_NVFP4_W4A4) return launch_experts_fp4(d, packed, x, T, k, L, ws, ev, s, o, act_gs);
   if (d.fmt == MOE_FMT_FP8_B128_W8A8) return launch_experts_w8a8(d, packed, x, T, k, L, ws, ev, s, o);
-  if (d.fmt == MOE_FMT_FP8_B128_W8A16 && row_block == fp8dec_row_block())
+  if (d.fmt == MOE_FMT_FP8_B128_W8A16 && row_block == fp8dec_row_block()) {
+    if (fp8gemv_preferred(T, k, d.E, d.I)) return launch_experts_fp8gemv(d, packed, x, T, k, row_block, L, ws, ev, s, o);
     return launch_experts_fp8dec(d, packed, x, T, k, L, ws, ev, s, o);
+  }
   if (d.fmt == MOE_FMT_NVFP4_W4A16 && row_block == tcw_row_block())
     return launch_experts_tcw(d, packed, x, T, k, L, ws, ev, s, o);
   return launch_experts_tc(d, packed, x, T, k, row_block, L, ws, ev, s, o);

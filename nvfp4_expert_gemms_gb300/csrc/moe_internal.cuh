@@ -237,6 +237,11 @@ cudaError_t launch_experts_fp4(const moe_packed_desc_t& d, const char* packed, c
                                const float* act_gs = nullptr, bool calibrate = false);
 cudaError_t launch_experts_tc(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,
                               int bn, const WsLayout& L, char* ws, const StepEvents& ev, cudaStream_t s, uint16_t* out);
+// FP8 W8A16 decode steps whose active experts average at most two rows: CUDA-core GEMVs.
+cudaError_t launch_experts_fp8gemv(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,
+                                   int k, int row_block, const WsLayout& L, char* ws, const StepEvents& ev,
+                                   cudaStream_t s, uint16_t* out);
+bool fp8gemv_preferred(int T, int k, int E, int I);
 // NVFP4 W4A16 with 256-row routing tiles (tc_row_block's choice at prefill sizes).
 int tcw_row_block();
 cudaError_t launch_experts_tcw(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,

@@ -427,6 +427,16 @@ def test_w4a16_wide_tiles(orc, T, H, I, E, k):
     check_close(synth.bf16_bits_to_f32(c.run()), c.oracle(orc), f"T={T}")
 
 
+@pytest.mark.parametrize("T,E,k,zipf", [(64, 64, 2, 1.1), (3, 16, 4, None), (40, 128, 8, None)])
+def test_fp8_decode_gemv(orc, T, E, k, zipf):
+    """FP8 W8A16 decode steps with few active experts averaging at most two rows go through the
+    CUDA-core GEMVs (the first two cases; the third takes the tensor-core decode kernel):
+    Zipf-skewed routing gives tiles of up to 16 rows (several passes of four rows over the
+    weights), K of 256 and 128 (a last partial 512-byte segment)."""
+    c = Case("fp8", T, 256, 128, E, k, seed=T + E, zipf=zipf)
+    check_close(synth.bf16_bits_to_f32(c.run()), c.oracle(orc), f"T={T}")
+
+
 def test_layer_zero_tokens_is_a_no_op():
     c = Case("fp8", 4, 256, 128, 8, 2)
     x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
