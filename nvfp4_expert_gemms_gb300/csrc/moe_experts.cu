@@ -20,6 +20,8 @@ cudaError_t launch_experts(const moe_packed_desc_t& d, const char* packed, const
     if (fp8gemv_preferred(T, k, d.E, d.I)) return launch_experts_fp8gemv(d, packed, x, T, k, row_block, L, ws, ev, s, o);
     return launch_experts_fp8dec(d, packed, x, T, k, L, ws, ev, s, o);
   }
+  if (d.fmt == MOE_FMT_INT4_G128_W4A16 && int4gemv_preferred(T, k, d.E, d.H, d.I))
+    return launch_experts_int4gemv(d, packed, x, T, k, row_block, L, ws, ev, s, o);
   if (d.fmt == MOE_FMT_NVFP4_W4A16 && row_block == tcw_row_block())
     return launch_experts_tcw(d, packed, x, T, k, L, ws, ev, s, o);
   return launch_experts_tc(d, packed, x, T, k, row_block, L, ws, ev, s, o);

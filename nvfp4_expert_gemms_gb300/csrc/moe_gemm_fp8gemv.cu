@@ -177,11 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1) fp8gemv_kernel(const GemvArgs a) 
 // Measured on one GB300 at H = 2048, I = 768, top-8 (FP8 decode, tokens/s of one layer): T = 1
 // 34.1k here against 29.4k on the tensor-core decode kernel, whose 48 gate/up items then leave
 // most SMs idle; T = 4 57.4k against 73.9k and T = 16 80.7k against 157k once that kernel has
-// an item for every SM.  So the GEMVs take the steps whose active experts average at most two
-// rows and give the tensor-core kernel fewer gate/up items (128 rows each) than there are SMs.
+// an item for every SM (and the INT4 GEMVs lose already at T = 2, 96 items).  So the GEMVs take
+// the steps whose active experts average at most two rows and give the tensor-core kernel fewer
+// gate/up items (128 rows each) than half the SMs.
 bool fp8gemv_preferred(int T, int k, int E, int I) {
   const long R = (long)T * k, active = R < E ? (R > 0 ? R : 1) : E;
-  return (R + active - 1) / active <= 2 && active * (I / 128) < tc_num_sms();
+  return (R + active - 1) / active <= 2 && 2 * active * (I / 128) < tc_num_sms();
 }
 
 cudaError_t launch_experts_fp8gemv(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,

@@ -242,6 +242,11 @@ cudaError_t launch_experts_fp8gemv(const moe_packed_desc_t& d, const char* packe
                                    int k, int row_block, const WsLayout& L, char* ws, const StepEvents& ev,
                                    cudaStream_t s, uint16_t* out);
 bool fp8gemv_preferred(int T, int k, int E, int I);
+// INT4 W4A16 decode steps, the same way (moe_gemm_int4gemv.cu).
+cudaError_t launch_experts_int4gemv(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T,
+                                    int k, int row_block, const WsLayout& L, char* ws, const StepEvents& ev,
+                                    cudaStream_t s, uint16_t* out);
+bool int4gemv_preferred(int T, int k, int E, int H, int I);
 // NVFP4 W4A16 with 256-row routing tiles (tc_row_block's choice at prefill sizes).
 int tcw_row_block();
 cudaError_t launch_experts_tcw(const moe_packed_desc_t& d, const char* packed, const __nv_bfloat16* x, int T, int k,

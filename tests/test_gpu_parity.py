@@ -427,13 +427,14 @@ def test_w4a16_wide_tiles(orc, T, H, I, E, k):
     check_close(synth.bf16_bits_to_f32(c.run()), c.oracle(orc), f"T={T}")
 
 
+@pytest.mark.parametrize("fmt", ["fp8", "int4"])
 @pytest.mark.parametrize("T,E,k,zipf", [(64, 64, 2, 1.1), (3, 16, 4, None), (40, 128, 8, None)])
-def test_fp8_decode_gemv(orc, T, E, k, zipf):
-    """FP8 W8A16 decode steps with few active experts averaging at most two rows go through the
-    CUDA-core GEMVs (the first two cases; the third takes the tensor-core decode kernel):
+def test_decode_gemv(orc, fmt, T, E, k, zipf):
+    """FP8 and INT4 W4A16 decode steps with few active experts averaging at most two rows go
+    through the CUDA-core GEMVs (the first two cases; the third takes the tensor-core kernels):
     Zipf-skewed routing gives tiles of up to 16 rows (several passes of four rows over the
-    weights), K of 256 and 128 (a last partial 512-byte segment)."""
-    c = Case("fp8", T, 256, 128, E, k, seed=T + E, zipf=zipf)
+    weights), K of 256 and 128 (FP8: a last partial 512-byte segment; INT4: 2 and 1 K groups)."""
+    c = Case(fmt, T, 256, 128, E, k, seed=T + E, zipf=zipf)
     check_close(synth.bf16_bits_to_f32(c.run()), c.oracle(orc), f"T={T}")
 
 
