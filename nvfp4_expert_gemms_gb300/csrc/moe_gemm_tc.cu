@@ -230,7 +230,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_tok[2][BN];     // gather: token of each row of the item (double-buffered)
-  __shared__ int s_ct[2][BN];      // down epilogue: token of each column
   __shared__ float s_cw[2][BN];    // down epilogue: routing weight / global scale of each column
 
   // gate/up: the tile table may come from the launch right before this one; down: it was final
@@ -639,17 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_gemm_kernel(const __gri
       if (live) {
         item(wk, te, nb0, nb1, nsub);
         inv_gs = FMT == MOE_FMT_NVFP4_W4A16 ? 0x1p10f / a.wgs[te.expert] : 1.f;  // see conv_nvfp4
-        if (MODE == 1 && threadIdx.x < BN) {  // column table of the down epilogue
+        if (MODE == 1 && threadIdx.x < BN) {  // column table of the down epilogue: routing weights
           const int col = threadIdx.x;
-          int ct = 0;
-          float cw = 0.f;
-          if (col < te.rows) {
-            const int p = a.perm[te.row0 + col];
-            ct = p / a.k;
-            cw = a.topk_w[p] * inv_gs;
-          }
-          s_ct[nitem & 1][col] = ct;
-          s_cw[nitem & 1][col] = cw;
+          s_cw[nitem & 1][col] = col < te.rows ? a.topk_w[a.perm[te.row0 + col]] * inv_gs : 0.f;
         }
         if (kDB) {  // the item's first chunks go into the A ring before the previous item's epilogue
           d = nK < kStagesA ? nK : kStagesA;
